@@ -1,0 +1,262 @@
+"""CPU oracle for NVFP4 block-scaled quantisation and the scale-learning STE.
+
+TEST INFRASTRUCTURE, not product code. Only ``tests/``, ``__graft_entry__.smoke()``
+and the CPU-baseline leg of ``bench.py`` may import this package. The CUDA
+library never loads it and shares no code with it.
+
+The arithmetic lives in ``nvfp4_oracle.c`` (plain single-threaded C, fp32
+round-to-nearest, no contraction); this module only compiles it with gcc and
+marshals numpy arrays through ctypes.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "nvfp4_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+ST_NONFINITE_INPUT = 1
+ST_BAD_SCALE = 2
+ST_BAD_AMAX = 4
+
+CFLAGS = ["-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/liboracle.so`` (skipped when up to date)."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", *CFLAGS, _SRC, "-o", tmp, "-lm"], check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def lib() -> C.CDLL:
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = C.CDLL(build())
+            _declare(_lib)
+    return _lib
+
+
+_u8p = C.POINTER(C.c_uint8)
+_u16p = C.POINTER(C.c_uint16)
+_u32p = C.POINTER(C.c_uint32)
+_f32p = C.POINTER(C.c_float)
+_i64 = C.c_int64
+
+
+def _declare(L):
+    L.orc_bf16_to_f32.restype = C.c_float
+    L.orc_bf16_to_f32.argtypes = [C.c_uint16]
+    L.orc_f32_to_bf16.restype = C.c_uint16
+    L.orc_f32_to_bf16.argtypes = [C.c_float]
+    L.orc_f32_to_bf16_array.argtypes = [_f32p, _i64, _u16p]
+    for name in ("orc_e2m1_value", "orc_e4m3_value", "orc_ue5m3_value"):
+        getattr(L, name).restype = C.c_float
+        getattr(L, name).argtypes = [C.c_uint8]
+    L.orc_scale_value.restype = C.c_float
+    L.orc_scale_value.argtypes = [C.c_int, C.c_uint8]
+    L.orc_e2m1_rne.restype = C.c_uint8
+    L.orc_e2m1_rne.argtypes = [C.c_float]
+    L.orc_scale_encode.restype = C.c_uint8
+    L.orc_scale_encode.argtypes = [C.c_int, C.c_float]
+    L.orc_e2m1_sr.restype = C.c_uint8
+    L.orc_e2m1_sr.argtypes = [C.c_float, C.c_uint32]
+    L.orc_philox4x32_10.argtypes = [_u32p, _u32p, _u32p]
+    L.orc_sr_bits.restype = C.c_uint32
+    L.orc_sr_bits.argtypes = [C.c_uint32, C.c_uint32, C.c_uint32, C.c_uint64]
+    L.orc_e2m1_rne_array.argtypes = [_f32p, _i64, _u8p]
+    L.orc_scale_encode_array.argtypes = [C.c_int, _f32p, _i64, _u8p]
+    L.orc_e2m1_sr_array.argtypes = [_f32p, _u32p, _i64, _u8p]
+    L.orc_sr_bits_array.argtypes = [C.c_uint32, C.c_uint32, C.c_uint32, C.c_uint64, _i64, _u32p]
+    L.orc_encode_block.argtypes = [_f32p, C.c_float, C.c_int, C.c_int, C.c_int,
+                                   C.c_uint32, C.c_uint32, C.c_uint32, C.c_uint64,
+                                   _u8p, _u8p, _u8p, _u16p, _f32p, _f32p]
+    L.orc_global_amax.restype = C.c_int
+    L.orc_global_amax.argtypes = [_u16p, _i64, _i64, _f32p]
+    L.orc_quantize.restype = C.c_int
+    L.orc_quantize.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int, C.c_float,
+                               C.c_uint32, C.c_uint32, _u16p, _i64, _i64, _i64, _f32p,
+                               _u8p, _u8p, _u32p, _u16p, _u8p, _u8p, _u32p, _u16p]
+    L.orc_fakequant_fwd.restype = C.c_int
+    L.orc_fakequant_fwd.argtypes = [_u16p, _i64, _i64, _f32p, _f32p, _u16p]
+    L.orc_scale_grad_bwd.restype = C.c_int
+    L.orc_scale_grad_bwd.argtypes = [_u16p, _u16p, _i64, _i64, _f32p, _f32p, _u16p,
+                                     _f32p, _f32p]
+
+
+def _c(a, dtype) -> np.ndarray:
+    """C-contiguous array of dtype that keeps the shape (0-d included)."""
+    a = np.asarray(a, dtype=dtype)
+    return a if a.flags["C_CONTIGUOUS"] else np.ascontiguousarray(a)
+
+
+def _p(a, ptype):
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(ptype)
+
+
+# ---------------------------------------------------------------- codecs --
+
+def bf16_to_f32(h) -> np.ndarray:
+    h = np.ascontiguousarray(h, dtype=np.uint16)
+    return (h.astype(np.uint32) << 16).view(np.float32)
+
+
+def f32_to_bf16(f) -> np.ndarray:
+    f = _c(f, np.float32)
+    out = np.empty(f.shape, np.uint16)
+    lib().orc_f32_to_bf16_array(_p(f, _f32p), f.size, _p(out, _u16p))
+    return out
+
+
+def e2m1_value(codes) -> np.ndarray:
+    L = lib()
+    c = np.asarray(codes, dtype=np.uint8)
+    return np.array([L.orc_e2m1_value(int(v)) for v in c.ravel()], np.float32).reshape(c.shape)
+
+
+def scale_value(fmt: int, codes) -> np.ndarray:
+    L = lib()
+    c = np.asarray(codes, dtype=np.uint8)
+    return np.array([L.orc_scale_value(fmt, int(v)) for v in c.ravel()], np.float32).reshape(c.shape)
+
+
+def e2m1_rne(y) -> np.ndarray:
+    y = _c(y, np.float32)
+    out = np.empty(y.shape, np.uint8)
+    lib().orc_e2m1_rne_array(_p(y, _f32p), y.size, _p(out, _u8p))
+    return out
+
+
+def scale_encode(fmt: int, t) -> np.ndarray:
+    t = _c(t, np.float32)
+    out = np.empty(t.shape, np.uint8)
+    lib().orc_scale_encode_array(int(fmt), _p(t, _f32p), t.size, _p(out, _u8p))
+    return out
+
+
+def e2m1_sr(y, v16) -> np.ndarray:
+    y = _c(y, np.float32)
+    v = np.ascontiguousarray(np.broadcast_to(np.asarray(v16, np.uint32), y.shape))
+    out = np.empty(y.shape, np.uint8)
+    lib().orc_e2m1_sr_array(_p(y, _f32p), _p(v, _u32p), y.size, _p(out, _u8p))
+    return out
+
+
+def philox(ctr, key) -> np.ndarray:
+    c = np.ascontiguousarray(ctr, dtype=np.uint32)
+    k = np.ascontiguousarray(key, dtype=np.uint32)
+    out = np.empty(4, np.uint32)
+    lib().orc_philox4x32_10(_p(c, _u32p), _p(k, _u32p), _p(out, _u32p))
+    return out
+
+
+def sr_bits(seed: int, step: int, direction: int, idx0: int, n: int) -> np.ndarray:
+    out = np.empty(n, np.uint32)
+    lib().orc_sr_bits_array(seed, step, direction, idx0, n, _p(out, _u32p))
+    return out
+
+
+# ---------------------------------------------------------- block level --
+
+def encode_block(x16, g: float, fmt: int = 0, rounding: int = 0, fos: int = 0,
+                 seed: int = 0, step: int = 0, direction: int = 0, idx0: int = 0) -> dict:
+    x = np.ascontiguousarray(x16, dtype=np.float32)
+    assert x.shape == (16,)
+    codes = np.empty(16, np.uint8)
+    scale = np.empty(1, np.uint8)
+    choice = np.empty(1, np.uint8)
+    dq = np.empty(16, np.uint16)
+    dqf = np.empty(16, np.float32)
+    sse = np.empty(2, np.float32)
+    lib().orc_encode_block(_p(x, _f32p), g, fmt, rounding, fos, seed, step, direction, idx0,
+                           _p(codes, _u8p), _p(scale, _u8p), _p(choice, _u8p),
+                           _p(dq, _u16p), _p(dqf, _f32p), _p(sse, _f32p))
+    return dict(codes=codes, scale=int(scale[0]), choice=int(choice[0]), dq=dq, dqf=dqf,
+                sse6=float(sse[0]), sse4=float(sse[1]))
+
+
+# ----------------------------------------------------------- whole path --
+
+def global_amax(x_bf16: np.ndarray, slices: int = 1):
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16).reshape(-1)
+    n = x.size // slices if slices else 0
+    out = np.zeros(max(slices, 1), np.float32)[:slices]
+    st = lib().orc_global_amax(_p(x, _u16p), slices, n, _p(out, _f32p))
+    return out, st
+
+
+def quantize(x_bf16: np.ndarray, gamax: np.ndarray, *, blocks: int = 1, scale_fmt: int = 0,
+             rounding: int = 0, four_over_six: int = 0, scale_max: float = 0.0,
+             seed: int = 0, step: int = 0, dequant: bool = True) -> dict:
+    """x_bf16: uint16 array shaped [S, R, C] (or [R, C]); gamax: float32 [S]."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    if x.ndim == 2:
+        x = x[None]
+    S, R, Cc = x.shape
+    gam = np.ascontiguousarray(gamax, dtype=np.float32).reshape(-1)
+    assert gam.size == S
+    out = {}
+    B = R * Cc // 16
+    W = (B + 31) // 32
+
+    def alloc(tag, mr, mc):
+        out[tag + "codes"] = np.zeros((S, mr, mc // 2), np.uint8)
+        out[tag + "scales"] = np.zeros((S, mr, mc // 16), np.uint8)
+        out[tag + "choice"] = np.zeros((S, W), np.uint32)
+        out[tag + "dq"] = np.zeros((S, mr, mc), np.uint16) if dequant else None
+
+    if blocks & 1:
+        alloc("row_", R, Cc)
+    if blocks & 2:
+        alloc("col_", Cc, R)
+    g = out.get
+    st = lib().orc_quantize(blocks, scale_fmt, rounding, four_over_six, scale_max, seed, step,
+                            _p(x, _u16p), S, R, Cc, _p(gam, _f32p),
+                            _p(g("row_codes"), _u8p), _p(g("row_scales"), _u8p),
+                            _p(g("row_choice"), _u32p), _p(g("row_dq"), _u16p),
+                            _p(g("col_codes"), _u8p), _p(g("col_scales"), _u8p),
+                            _p(g("col_choice"), _u32p), _p(g("col_dq"), _u16p))
+    out["status"] = st
+    return out
+
+
+def fakequant_fwd(x_bf16, s_pre, s_post=None):
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    R, Cc = x.shape
+    sp = np.ascontiguousarray(s_pre, dtype=np.float32)
+    so = None if s_post is None else np.ascontiguousarray(s_post, dtype=np.float32)
+    xq = np.empty_like(x)
+    st = lib().orc_fakequant_fwd(_p(x, _u16p), R, Cc, _p(sp, _f32p), _p(so, _f32p),
+                                 _p(xq, _u16p))
+    return xq, st
+
+
+def scale_grad_bwd(x_bf16, gq_bf16, s_pre, s_post=None, want_gx: bool = True):
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    gq = np.ascontiguousarray(gq_bf16, dtype=np.uint16)
+    R, Cc = x.shape
+    sp = np.ascontiguousarray(s_pre, dtype=np.float32)
+    so = None if s_post is None else np.ascontiguousarray(s_post, dtype=np.float32)
+    gx = np.empty_like(x) if want_gx else None
+    gs_pre = np.empty(sp.shape, np.float32)
+    gs_post = None if so is None else np.empty(sp.shape, np.float32)
+    st = lib().orc_scale_grad_bwd(_p(x, _u16p), _p(gq, _u16p), R, Cc, _p(sp, _f32p),
+                                  _p(so, _f32p), _p(gx, _u16p), _p(gs_pre, _f32p),
+                                  _p(gs_post, _f32p))
+    return dict(gx=gx, gs_pre=gs_pre, gs_post=gs_post, status=st)

@@ -1,0 +1,279 @@
+"""Pins of the oracle's block encoder, 4/6 selector and stochastic rounder:
+worked examples the pages print, exact probabilities, an independent float64
+brute force over both 4/6 candidates, and invariants of the method."""
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from conftest import golden
+from test_oracle_formats import textbook_minifloat
+
+GRID = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6], np.float64)
+W = golden("worked_examples.json")
+
+
+def _block(vals, n=16):
+    x = np.zeros(n, np.float32)
+    x[: len(vals)] = vals
+    return x
+
+
+# ------------------------------------------------------- worked examples --
+
+def test_scale9_example(orc):
+    ex = W["scale9_block"]
+    r = orc.encode_block(_block([ex["block_max"]]), ex["global_scale"])
+    assert orc.scale_value(0, r["scale"]) == ex["scale"]
+    assert orc.e2m1_value(r["codes"][0]) == ex["code_value"]
+    assert r["dqf"][0] == ex["block_max"]
+
+
+def test_requant_forward_example(orc):
+    ex = W["requant_example"]
+    # a block with scale 9 (largest value 54), holding 5.4
+    r = orc.encode_block(_block([54.0, ex["x"]]), 1.0)
+    assert orc.scale_value(0, r["scale"]) == ex["scale"]
+    assert orc.e2m1_value(r["codes"][1]) == ex["code_value"]
+    assert r["dqf"][1] == ex["value"]
+
+
+def test_widget_576(orc):
+    ex = W["widget_576"]
+    r = orc.encode_block(_block([ex["x_inferred"]]), 1.0)
+    assert orc.scale_value(0, r["scale"]) == ex["scale"]
+    assert orc.e2m1_value(r["codes"][0]) == ex["code_value"]
+    assert r["dqf"][0] == ex["value"]
+    assert round(float(r["dqf"][0]) - ex["x_inferred"], 1) == ex["error"]
+
+
+def test_representable_range_and_outer_scale_shift(orc):
+    ex = W["range"]
+    for g, (lo, hi) in ((1.0, ex["g1"]), (2.0, ex["g2"])):
+        # smallest: E2M1 0.5 under the smallest E4M3 scale; largest: 6 x 448
+        r = orc.encode_block(_block([6 * lo * 2, lo]), g)
+        assert r["dqf"][1] == lo and orc.scale_value(0, r["scale"]) == 2.0 ** -9
+        r = orc.encode_block(_block([hi]), g)
+        assert r["dqf"][0] == hi and orc.scale_value(0, r["scale"]) == 448.0
+
+
+def test_four_over_six_vignettes(orc):
+    e1, e2 = W["four_over_six_1"], W["four_over_six_2"]
+    r = orc.encode_block(_block(e1["block"]), 1.0, fos=1)
+    assert round(r["sse6"] / 4, 2) == e1["mse6"] and r["sse4"] / 4 == e1["mse4"]
+    assert r["choice"] == 1 and e1["choice"] == 4
+    r = orc.encode_block(_block(e2["block"]), 1.0, fos=1)
+    assert r["sse6"] / 4 == e2["mse6"]
+    assert r["choice"] == 0 and e2["choice"] == 6
+    assert r["sse4"] > r["sse6"]
+
+
+def test_four_over_six_mapping_claim(orc):
+    m = W["four_over_six_mapping"]
+    amax = 48.0  # amax/6 = 8 and amax/4 = 12 are both exact E4M3 values
+    r4 = orc.encode_block(_block([amax, m["frac_code3_under_4"] * amax]), 1.0, fos=1)
+    assert r4["choice"] == 1 and orc.e2m1_value(r4["codes"][1]) == 3.0
+    assert r4["dqf"][1] == 36.0
+    r6 = orc.encode_block(_block([amax, 32.0]), 1.0)
+    assert orc.e2m1_value(r6["codes"][1]) == 4.0
+    assert round(r6["dqf"][1] / amax, 4) == m["frac_code4_under_6"]
+
+
+def test_global_scale_uses_fp8_max_256_under_four_over_six(orc):
+    x = np.array([[1536.0] + [0.0] * 15], np.float32)
+    xb = orc.f32_to_bf16(x)
+    q6 = orc.quantize(xb, np.array([1536.0], np.float32), four_over_six=0)
+    q46 = orc.quantize(xb, np.array([1536.0], np.float32), four_over_six=1)
+    # M = 448: g = 1536/2688, block scale 448; M = 256: g = 1, block scale 256 (x6)
+    assert orc.scale_value(0, q6["row_scales"][0, 0, 0]) == 448.0
+    assert orc.scale_value(0, q46["row_scales"][0, 0, 0]) in (256.0, 384.0)
+
+
+# ------------------------------------------------------ 4/6 brute force --
+
+def _candidate64(x: np.ndarray, g: float, k: float):
+    """Independent float64 reconstruction of one candidate: the block scale
+    comes from the textbook E4M3 rounding of amax/(k g) (taken in fp32 as the
+    method does), the elements from the textbook E2M1 rounding of x/d."""
+    f32 = np.float32
+    amax = np.max(np.abs(x))
+    t = f32(amax) * (f32(1.0) / (f32(k) * f32(g)))
+    s = textbook_minifloat(np.array([t]), mbits=3, emin=-6, vmax=448.0)[0]
+    d = f32(f32(s) * f32(g))
+    inv = f32(1.0) / d if d > 0 else f32(0.0)
+    y = (x.astype(np.float32) * inv).astype(np.float32)
+    v = textbook_minifloat(np.abs(y), mbits=1, emin=0, vmax=6.0) * np.where(np.signbit(y), -1, 1)
+    err = x.astype(np.float64) - v * np.float64(d)
+    return float(np.sum(err * err)), v, float(d)
+
+
+@pytest.mark.parametrize("dist", ["normal", "t3", "uniform", "spiky"])
+def test_four_over_six_picks_lower_error_candidate(orc, dist):
+    rng = np.random.default_rng(11)
+    picked = [0, 0]
+    for _ in range(400):
+        if dist == "normal":
+            x = rng.standard_normal(16)
+        elif dist == "t3":
+            x = rng.standard_t(3, 16)
+        elif dist == "uniform":
+            x = rng.uniform(-1, 1, 16)
+        else:
+            x = rng.standard_normal(16) * 0.1
+            x[rng.integers(16)] = 5.0
+        x = x.astype(np.float32)
+        g = float(np.float32(np.exp(rng.uniform(-3, 3))) / np.float32(2688.0))
+        r = orc.encode_block(x, g, fos=1)
+        s6, v6, d6 = _candidate64(x, g, 6.0)
+        s4, v4, d4 = _candidate64(x, g, 4.0)
+        if abs(s4 - s6) <= 1e-5 * max(s4, s6, 1e-30):
+            continue  # too close for an fp32 sum to decide the same way
+        want = 1 if s4 < s6 else 0
+        assert r["choice"] == want
+        picked[want] += 1
+        v, d = (v4, d4) if want else (v6, d6)
+        assert np.array_equal(orc.e2m1_value(r["codes"]).astype(np.float64), v)
+        assert np.array_equal(r["dqf"], (v * d).astype(np.float32))
+    assert picked[0] > 0 and picked[1] > 0
+
+
+def test_four_over_six_never_increases_tensor_error(orc):
+    rng = np.random.default_rng(5)
+    x = (rng.standard_t(3, (64, 256)) * 0.5).astype(np.float32)
+    xb = orc.f32_to_bf16(x)
+    xf = (xb.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    gam = np.array([np.abs(xf).max()], np.float32)
+    e = {}
+    for fos in (0, 1):
+        q = orc.quantize(xb, gam, four_over_six=fos, scale_max=256.0)
+        dq = (q["row_dq"][0].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        e[fos] = np.sum((dq - xf) ** 2)
+    assert e[1] < e[0]
+
+
+# ------------------------------------------------------ stochastic round --
+
+def _exact_p(y: float):
+    a = Fraction(abs(float(y)))
+    for lo, hi in zip(GRID[:-1], GRID[1:]):
+        if Fraction(lo) <= a < Fraction(hi):
+            return lo, hi, (a - Fraction(lo)) / (Fraction(hi) - Fraction(lo))
+    return 6.0, 6.0, Fraction(0)
+
+
+def test_sr_probability_is_exact_over_all_random_values(orc):
+    rng = np.random.default_rng(3)
+    ys = [2.25, 0.1, 0.3, 1.0 / 3.0, 5.999, 4.0, 0.0, 7.5, 1e-30, 2.9999998]
+    ys += list(rng.uniform(0, 6, 20))
+    v = np.arange(65536, dtype=np.uint32)
+    for y in np.array(ys, np.float32):
+        lo, hi, p = _exact_p(y)
+        codes = orc.e2m1_sr(np.full(65536, y, np.float32), v)
+        vals = orc.e2m1_value(codes).astype(np.float64)
+        assert set(np.unique(vals)) <= {lo, hi}
+        ups = int(np.sum(vals == hi)) if hi != lo else 0
+        # u = V / 2^16 < p  <=>  V < p * 2^16: ceil(p * 2^16) values of V
+        want = -((-p * 65536).numerator // (p * 65536).denominator) if p else 0
+        assert ups == want, (y, ups, want)
+        neg = orc.e2m1_sr(np.full(65536, -y, np.float32), v)
+        assert np.array_equal(neg, codes | 8)
+
+
+def test_sr_example_from_the_pages(orc):
+    ex = W["sr_example"]
+    y = np.float32(ex["value"] / ex["scale"])
+    vals = orc.e2m1_value(orc.e2m1_sr(np.full(65536, y, np.float32),
+                                      np.arange(65536, dtype=np.uint32))).astype(np.float64)
+    assert np.mean(vals == ex["lo"]) == ex["p_lo"] and np.mean(vals == ex["hi"]) == ex["p_hi"]
+    assert np.mean(vals) * ex["scale"] == ex["expectation"]
+
+
+def test_sr_is_unbiased_with_philox_bits(orc):
+    n = 1 << 20
+    rng = np.random.default_rng(9)
+    y = rng.uniform(-6, 6, n).astype(np.float32)
+    bits = orc.sr_bits(1234, 7, 0, 0, n)
+    assert bits.max() < 65536 and abs(bits.mean() / 65535 - 0.5) < 2e-3
+    q = orc.e2m1_value(orc.e2m1_sr(y, bits)).astype(np.float64)
+    err = q - y.astype(np.float64)
+    assert abs(err.mean()) < 4 * err.std() / np.sqrt(n)
+    # RNE of the same values is biased for this distribution only by ties; SR
+    # must never move a value by more than one grid step
+    assert np.max(np.abs(err)) <= 2.0
+
+
+def test_sr_bits_layout(orc):
+    seed, step = 77, 5
+    bits = orc.sr_bits(seed, step, 1, 64, 32)
+    for i in range(32):
+        idx = 64 + i
+        j = idx >> 3
+        w = orc.philox([j & 0xFFFFFFFF, j >> 32, 1, 0], [seed, step])[(idx & 7) >> 1]
+        assert bits[i] == ((int(w) >> 16) if idx & 1 else (int(w) & 0xFFFF))
+
+
+# ------------------------------------------------------------ invariants --
+
+def test_zero_block_and_signed_zero(orc):
+    x = _block([0.0, -0.0])
+    r = orc.encode_block(x, 1.0)
+    assert r["scale"] == 0 and r["codes"][0] == 0 and r["codes"][1] == 8
+    assert np.all(r["dqf"] == 0)
+
+
+def test_column_blocks_are_row_blocks_of_the_transpose(orc):
+    rng = np.random.default_rng(2)
+    x = orc.f32_to_bf16(rng.standard_normal((2, 48, 32)).astype(np.float32))
+    gam = np.array([3.0, 5.0], np.float32)
+    both = orc.quantize(x, gam, blocks=3, four_over_six=1)
+    rowT = orc.quantize(np.ascontiguousarray(x.transpose(0, 2, 1)), gam, blocks=1,
+                        four_over_six=1)
+    for k in ("codes", "scales", "choice", "dq"):
+        assert np.array_equal(both["col_" + k], rowT["row_" + k])
+
+
+def test_current_scaling_is_periodic_with_period_one(orc):
+    """Periodic scaling reuses a global amax taken T steps ago; with T = 1 the
+    amax is always the current one, so both policies give the same bytes."""
+    rng = np.random.default_rng(4)
+    xs = [orc.f32_to_bf16((rng.standard_normal((8, 64)) * 1.05 ** t).astype(np.float32))
+          for t in range(3)]
+    stale = None
+    for t, x in enumerate(xs):
+        cur, _ = orc.global_amax(x)
+        if t % 1 == 0:
+            stale = cur
+        a = orc.quantize(x, cur, scale_fmt=1, rounding=1, seed=3, step=t)
+        b = orc.quantize(x, stale, scale_fmt=1, rounding=1, seed=3, step=t)
+        assert all(np.array_equal(a[k], b[k]) for k in ("row_codes", "row_scales", "row_dq"))
+
+
+def test_ue5m3_absorbs_a_stale_amax_where_e4m3_saturates(orc):
+    """UE5M3 blog: with periodic tensor scaling the wider scale format keeps
+    blocks representable while the data drift away from the cached amax."""
+    rng = np.random.default_rng(8)
+    base = rng.standard_normal((64, 256)).astype(np.float32)
+    base *= np.exp(rng.standard_normal((64, 1)) * 2.0).astype(np.float32)
+    x0 = orc.f32_to_bf16(base)
+    stale, _ = orc.global_amax(x0)
+    x15 = orc.f32_to_bf16(base * np.float32(1.05 ** 15))
+    xf = (x15.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    res = {}
+    for fmt in (0, 1):
+        q = orc.quantize(x15, stale, scale_fmt=fmt, scale_max=448.0)
+        top = 0x7E if fmt == 0 else 0xFF
+        dq = (q["row_dq"][0].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        res[fmt] = (int(np.sum(q["row_scales"] == top)), float(np.sum((dq - xf) ** 2)))
+    assert res[0][0] > 0 and res[1][0] == 0
+    assert res[1][1] < res[0][1]
+
+
+def test_nonfinite_input_and_bad_amax_are_flagged(orc):
+    x = orc.f32_to_bf16(np.ones((1, 32), np.float32))
+    x[0, 3] = 0x7F80
+    assert orc.quantize(x, np.array([1.0], np.float32))["status"] & orc.ST_NONFINITE_INPUT
+    _, st = orc.global_amax(x)
+    assert st & orc.ST_NONFINITE_INPUT
+    y = orc.f32_to_bf16(np.ones((1, 32), np.float32))
+    assert orc.quantize(y, np.array([np.nan], np.float32))["status"] & orc.ST_BAD_AMAX
+    assert orc.quantize(y, np.array([1.0], np.float32))["status"] == 0
