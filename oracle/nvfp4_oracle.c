@@ -40,7 +40,7 @@
  *  R3 Global decode scale g = gamax / (6 M) (M = 448, or 256 with 4/6);
  *     g = 1 when gamax == 0.
  *  R4 Block scale for a target k (6, or 4 under 4/6): den = k g,
- *     rden = 1/den (per slice), t = amax_b * rden, code = Q(t),
+ *     rden = 1/den (per slice, clamped to FLT_MAX), t = amax_b * rden, code = Q(t),
  *     d = dec(code) * g, inv = 1/d (clamped to FLT_MAX; 0 when d == 0),
  *     y_i = x_i * inv. Every step is one fp32 operation rounded to nearest.
  *  R5 Stochastic rounding: a = |y|; lo <= a < hi are the grid neighbours,
@@ -250,6 +250,7 @@ static void encode_candidate(const float* x, float amax, float g, float k, int f
                              int rounding, const uint32_t* v16, cand_t* c) {
   float den = k * g;
   float rden = 1.0f / den;
+  if (rden > FLT_MAX) rden = FLT_MAX; /* g so small that 1/(k g) overflows */
   float t = amax * rden;
   c->scale = orc_scale_encode(fmt, t);
   c->d = orc_scale_value(fmt, c->scale) * g;
