@@ -1,0 +1,186 @@
+/*
+ * nvfp4.h -- C ABI of the GB300 (sm_103a) NVFP4 block-scaled quantisation
+ * library: bf16 -> NVFP4 encoding and the scale-learning STE backward.
+ *
+ * Conventions shared by every entry point
+ * ----------------------------------------
+ *  - Every pointer argument except `stream` is a DEVICE pointer owned by the
+ *    caller. The library allocates nothing and never synchronises: all work is
+ *    enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream)
+ *    and the call returns as soon as it is enqueued.
+ *  - Tensors are row-major and C-contiguous. bf16 data is passed as `void*`
+ *    holding IEEE bfloat16 bit patterns.
+ *  - Alignment: every tensor pointer (x, codes, scales, choice, dequant,
+ *    gradients) must be 16-byte aligned; fp32 scalars and scale arrays
+ *    4-byte aligned.
+ *  - Argument errors are returned synchronously BEFORE anything is enqueued.
+ *  - Data errors (NaN/Inf inputs, unusable scales or amax values) are found
+ *    by the kernels and OR-ed into `*status` (a device int32, may be NULL) as
+ *    NVFP4_DEV_* bits. The caller clears it; it accumulates over calls. When a
+ *    bit is set the outputs of that call are unspecified.
+ *  - Empty inputs (a zero dimension) return NVFP4_OK and enqueue nothing.
+ *  - NVFP4_ERR_CUDA means a launch failed; earlier work on the stream is not
+ *    affected by the call.
+ *
+ * Number formats (End-to-End 4-Bit Training, "Low-precision formats on
+ * Blackwell"; UE5M3 blog, math derivation):
+ *  - element: E2M1, magnitudes {0, 0.5, 1, 1.5, 2, 3, 4, 6}, bit 3 = sign;
+ *  - block scale: E4M3 (bias 7, max 448) or unsigned UE5M3 (bias 15, max
+ *    122880, all 256 codes finite), one per 16 values;
+ *  - outer scale: FP32 decode scale g = gamax / (6 * M) per slice, with
+ *    M = scale_max (448, or 256 under Four-Over-Six: "Four Over Six",
+ *    implementation details), g = 1 when gamax = 0.
+ *  A value is reconstructed as e2m1(code) * scale(block) * g.
+ */
+#ifndef NVFP4_H
+#define NVFP4_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define NVFP4_API __attribute__((visibility("default")))
+#else
+#define NVFP4_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  NVFP4_OK = 0,
+  NVFP4_ERR_NULL = 1,  /* a required pointer is NULL                          */
+  NVFP4_ERR_SHAPE = 2, /* negative size, or a blocked dim not a multiple of 16 */
+  NVFP4_ERR_ALIGN = 3, /* a pointer is not aligned as required                 */
+  NVFP4_ERR_ENUM = 4,  /* a configuration field is out of range                */
+  NVFP4_ERR_CUDA = 6   /* a CUDA launch or memset failed                       */
+} nvfp4_status;
+
+/* Bits of the device status word. */
+#define NVFP4_DEV_NONFINITE_INPUT 1 /* an input element is NaN or Inf        */
+#define NVFP4_DEV_BAD_SCALE 2       /* s_pre not in [FLT_MIN, FLT_MAX] or a   */
+                                    /* non-finite s_post                       */
+#define NVFP4_DEV_BAD_AMAX 4        /* a global amax is NaN, Inf or negative  */
+
+/* nvfp4_config.blocks */
+#define NVFP4_BLOCKS_ROW 1  /* 1x16 blocks along the last dimension            */
+#define NVFP4_BLOCKS_COL 2  /* 16x1 blocks along rows: the row encoding of X^T */
+#define NVFP4_BLOCKS_BOTH 3 /* both encodings from one read of X               */
+/* nvfp4_config.scale_fmt */
+#define NVFP4_SCALE_E4M3 0
+#define NVFP4_SCALE_UE5M3 1
+/* nvfp4_config.rounding */
+#define NVFP4_ROUND_RNE 0 /* E2M1 round to nearest, ties to the even code    */
+#define NVFP4_ROUND_SR 1  /* stochastic rounding, Philox4x32-10 bits         */
+
+typedef struct {
+  int32_t blocks;        /* NVFP4_BLOCKS_*                                     */
+  int32_t scale_fmt;     /* NVFP4_SCALE_*                                      */
+  int32_t rounding;      /* NVFP4_ROUND_*                                      */
+  int32_t four_over_six; /* 0 or 1: per block keep the lower-error of max->6   */
+                         /* and max->4 (sum of squared errors; ties keep 6)    */
+  float scale_max;       /* M of the outer scale; 0 = 256 with 4/6, else 448   */
+  uint32_t seed;         /* stochastic rounding key word 0                     */
+  uint32_t step;         /* stochastic rounding key word 1 (training step)     */
+} nvfp4_config;
+
+/* Outputs of one encoding (row or column). Shapes for an input [S][R][C]:
+ *   row encoding: codes [S][R][C/2], scales [S][R][C/16], dequant [S][R][C]
+ *   col encoding: codes [S][C][R/2], scales [S][C][R/16], dequant [S][C][R]
+ *   choice: [S][W] 32-bit words, W = ceil(R*C/16/32); bit b%32 of word b/32
+ *           of slice s is block b of that slice (blocks in output order);
+ *           1 = the block was encoded with its max scaled to 4.
+ * codes: two E2M1 codes per byte, the even element in the low nibble.
+ * scales: one scale byte per block, no swizzle. */
+typedef struct {
+  uint8_t* codes;   /* required                                              */
+  uint8_t* scales;  /* required                                              */
+  uint32_t* choice; /* required when four_over_six = 1, ignored otherwise    */
+  void* dequant;    /* bf16 of code * scale * g (each product rounded to     */
+                    /* fp32, then to bf16); NULL = not written               */
+} nvfp4_out;
+
+/* Global amax (End-to-End 4-Bit Training, "Low-precision formats on
+ * Blackwell": the FP32 outer scale is set per tensor; UE5M3 blog: current
+ * tensor scaling recomputes it every step, periodic scaling every T steps).
+ * x: bf16 [slices][rows][cols]; amax: fp32 [slices], overwritten with the
+ * largest |x| of each slice. A caller doing periodic scaling calls this on
+ * refresh steps only and passes the same buffer to nvfp4_quantize in between.
+ * Errors: NULL x/amax, negative sizes, misaligned x. */
+NVFP4_API nvfp4_status nvfp4_amax(const void* x, int64_t slices, int64_t rows, int64_t cols,
+                        float* amax, int32_t* status, void* stream);
+
+/* NVFP4 quantisation of x: bf16 [slices][rows][cols] (End-to-End 4-Bit
+ * Training, "Low-precision formats on Blackwell" and "Block-scaled backward
+ * passes"; UE5M3 blog, math derivation and stochastic rounding; "Four Over
+ * Six", method). Per block of 16: block amax, block-scale code
+ * Q(amax * (1 / (k * g))) for k = 6 (and k = 4 under 4/6), element codes
+ * E2M1(x * (1 / (scale * g))) by RNE or stochastic rounding, 4/6 selection,
+ * packing, optional dequant.
+ * global_amax: fp32 [slices], current (from nvfp4_amax) or stale (periodic).
+ * row: outputs of the row encoding, required iff blocks has the ROW bit.
+ * col: outputs of the column encoding, required iff blocks has the COL bit.
+ * Stochastic rounding: the 16 random bits of the element at flat index idx of
+ * an encoding's output layout come from Philox4x32-10 with key (seed, step),
+ * counter (idx/8 low word, idx/8 high word, 0 for rows / 1 for columns, 0),
+ * 16-bit half idx%2 of word (idx%8)/2; the value rounds up iff
+ * bits/65536 < (|y| - lo) / (hi - lo).
+ * Errors: NULL required pointers, ROW with cols % 16, COL with rows % 16,
+ * enum fields out of range, scale_max < 0, misaligned buffers. */
+NVFP4_API nvfp4_status nvfp4_quantize(const nvfp4_config* cfg, const void* x, int64_t slices,
+                            int64_t rows, int64_t cols, const float* global_amax,
+                            const nvfp4_out* row, const nvfp4_out* col, int32_t* status,
+                            void* stream);
+
+/* Fake quantisation for scale learning (Scale Learning blog, "How Scale
+ * Learning Works", first and dual-scale equations):
+ *   xq = bf16(s_post * clamp(round(x * (1 / s_pre)), -6, 6))
+ * with round the E2M1 RNE rounding. x, xq: bf16 [rows][cols], cols % 16 == 0;
+ * s_pre, s_post: fp32 [rows][cols/16] per-block scales; s_post = NULL for a
+ * single (tied) scale. Errors: NULL pointers, cols % 16, misalignment. */
+NVFP4_API nvfp4_status nvfp4_fakequant_fwd(const void* x, int64_t rows, int64_t cols,
+                                 const float* s_pre, const float* s_post, void* xq,
+                                 int32_t* status, void* stream);
+
+/* STE backward of nvfp4_fakequant_fwd (Scale Learning blog, "How Scale
+ * Learning Works": derivative of x~ w.r.t. s, s_post and s_pre, with the
+ * derivative of round taken as 1). gq = dL/dx~ (bf16 [rows][cols]).
+ * With r = x * (1/s_pre), q = clamp(round(r)), in = (-6 <= r <= 6):
+ *   gx      = bf16(in ? gq * a : 0), a = s_post * (1/s_pre) (dual), 1 (tied)
+ *   dual:   gs_post = sum gq * q,   gs_pre = -a * sum gq * (in ? r : 0)
+ *   tied:   gs_pre  = sum gq * (in ? q - r : q)      (gs_post must be NULL)
+ * Block sums are fp32 in a fixed order: per half of 8, even and odd positions
+ * accumulate separately with fma from +0; half = even + odd; block = half0 +
+ * half1. gx may be NULL (scale-only learning). gs_pre is required; gs_post is
+ * required for dual scales. Outputs: fp32 [rows][cols/16].
+ * Errors: NULL pointers, cols % 16, misalignment, gs_post without s_post. */
+NVFP4_API nvfp4_status nvfp4_scale_grad_bwd(const void* x, const void* gq, int64_t rows, int64_t cols,
+                                  const float* s_pre, const float* s_post, void* gx,
+                                  float* gs_pre, float* gs_post, int32_t* status,
+                                  void* stream);
+
+/* ---- diagnostics: the device codecs element by element -------------------
+ * For exhaustive checks of the conversions the kernels use. op:
+ *   0: out[i] = E2M1 RNE code of in[i]         (n even: pairs share a byte)
+ *   1: out[i] = E4M3 code of in[i] >= 0        (block-scale encoder)
+ *   2: out[i] = UE5M3 code of in[i] >= 0       (block-scale encoder)
+ *   3: out[i] = E2M1 stochastic code of in[i] with random bits aux[i] & 0xFFFF
+ * in, aux (op 3 only): device arrays of n elements; out: device uint8 [n].
+ * This entry point has no counterpart on the pages; it exists for testing. */
+NVFP4_API nvfp4_status nvfp4_codec_probe(int32_t op, const float* in, const uint32_t* aux, int64_t n,
+                               uint8_t* out, void* stream);
+
+/* The 16 random bits the stochastic rounder draws for elements idx0 ..
+ * idx0 + n - 1 of an encoding (direction 0 = rows, 1 = columns), written to
+ * out (device uint32 [n]). Diagnostics; no counterpart on the pages. */
+NVFP4_API nvfp4_status nvfp4_sr_bits(uint32_t seed, uint32_t step, uint32_t direction, uint64_t idx0,
+                           int64_t n, uint32_t* out, void* stream);
+
+/* Short text for a status code. */
+NVFP4_API const char* nvfp4_status_string(nvfp4_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_H */

@@ -1,0 +1,275 @@
+"""GB300 (sm_103a) NVFP4 block-scaled quantisation and scale-learning STE.
+
+The compute lives in ``libnvfp4.so`` (hand-written CUDA behind the C ABI of
+``include/nvfp4.h``). This module only marshals arguments: it passes device
+pointers of torch tensors and the current CUDA stream to the C entry points,
+which have the same names. There is no CPU fallback: every call raises if the
+library is not built or no CUDA device is present.
+
+    from nvfp4_block_scaled_02_gb300 import nvfp4_amax, nvfp4_quantize, Config
+    amax = nvfp4_amax(x)                           # current tensor scaling
+    out = nvfp4_quantize(x, amax, Config(four_over_six=1))
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import threading
+from dataclasses import dataclass
+
+import torch
+
+__all__ = [
+    "Config", "Nvfp4Error", "build", "lib", "nvfp4_amax", "nvfp4_quantize",
+    "nvfp4_fakequant_fwd", "nvfp4_scale_grad_bwd", "nvfp4_codec_probe", "nvfp4_sr_bits",
+    "alloc_encoding", "PeriodicAmax", "BLOCKS_ROW", "BLOCKS_COL", "BLOCKS_BOTH",
+    "SCALE_E4M3", "SCALE_UE5M3", "ROUND_RNE", "ROUND_SR",
+    "DEV_NONFINITE_INPUT", "DEV_BAD_SCALE", "DEV_BAD_AMAX",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libnvfp4.so")
+
+BLOCKS_ROW, BLOCKS_COL, BLOCKS_BOTH = 1, 2, 3
+SCALE_E4M3, SCALE_UE5M3 = 0, 1
+ROUND_RNE, ROUND_SR = 0, 1
+DEV_NONFINITE_INPUT, DEV_BAD_SCALE, DEV_BAD_AMAX = 1, 2, 4
+
+_STATUS = {0: "ok", 1: "null pointer", 2: "shape", 3: "alignment", 4: "enum", 6: "cuda"}
+
+
+class Nvfp4Error(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed: status {code} ({_STATUS.get(code, '?')})")
+        self.code = code
+
+
+class _Config(C.Structure):
+    _fields_ = [("blocks", C.c_int32), ("scale_fmt", C.c_int32), ("rounding", C.c_int32),
+                ("four_over_six", C.c_int32), ("scale_max", C.c_float), ("seed", C.c_uint32),
+                ("step", C.c_uint32)]
+
+
+class _Out(C.Structure):
+    _fields_ = [("codes", C.c_void_p), ("scales", C.c_void_p), ("choice", C.c_void_p),
+                ("dequant", C.c_void_p)]
+
+
+@dataclass
+class Config:
+    blocks: int = BLOCKS_ROW
+    scale_fmt: int = SCALE_E4M3
+    rounding: int = ROUND_RNE
+    four_over_six: int = 0
+    scale_max: float = 0.0
+    seed: int = 0
+    step: int = 0
+
+    def c(self) -> _Config:
+        return _Config(self.blocks, self.scale_fmt, self.rounding, self.four_over_six,
+                       self.scale_max, self.seed & 0xFFFFFFFF, self.step & 0xFFFFFFFF)
+
+
+_lock = threading.Lock()
+_lib = None
+
+_i64, _vp, _u32, _i32 = C.c_int64, C.c_void_p, C.c_uint32, C.c_int32
+
+
+def build(force: bool = False) -> str:
+    """Compile libnvfp4.so for sm_103a (no-op when up to date)."""
+    from . import buildlib
+    return buildlib.build(force=force)
+
+
+def lib() -> C.CDLL:
+    """The loaded CUDA library. Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build the CUDA library first "
+                    "(python -m nvfp4_block_scaled_02_gb300.buildlib)")
+            L = C.CDLL(LIB_PATH)
+            L.nvfp4_amax.argtypes = [_vp, _i64, _i64, _i64, _vp, _vp, _vp]
+            L.nvfp4_quantize.argtypes = [C.POINTER(_Config), _vp, _i64, _i64, _i64, _vp,
+                                         C.POINTER(_Out), C.POINTER(_Out), _vp, _vp]
+            L.nvfp4_fakequant_fwd.argtypes = [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp]
+            L.nvfp4_scale_grad_bwd.argtypes = [_vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp,
+                                               _vp, _vp]
+            L.nvfp4_codec_probe.argtypes = [_i32, _vp, _vp, _i64, _vp, _vp]
+            L.nvfp4_sr_bits.argtypes = [_u32, _u32, _u32, C.c_uint64, _i64, _vp, _vp]
+            L.nvfp4_status_string.restype = C.c_char_p
+            L.nvfp4_status_string.argtypes = [C.c_int]
+            for name in ("nvfp4_amax", "nvfp4_quantize", "nvfp4_fakequant_fwd",
+                         "nvfp4_scale_grad_bwd", "nvfp4_codec_probe", "nvfp4_sr_bits"):
+                getattr(L, name).restype = C.c_int
+            _lib = L
+    return _lib
+
+
+# ------------------------------------------------------------- marshalling --
+
+def _dev(t: torch.Tensor | None, name: str) -> int | None:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (this library has no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _bf16(t: torch.Tensor, name: str) -> int:
+    if t.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+        raise TypeError(f"{name} must hold bf16 data, got {t.dtype}")
+    return _dev(t, name)
+
+
+def _stream(device: torch.device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _check(fn: str, code: int) -> None:
+    if code != 0:
+        raise Nvfp4Error(fn, code)
+
+
+def _shape3(x: torch.Tensor):
+    if x.dim() == 2:
+        return 1, x.shape[0], x.shape[1]
+    if x.dim() == 3:
+        return x.shape[0], x.shape[1], x.shape[2]
+    raise ValueError("x must be [rows, cols] or [slices, rows, cols]")
+
+
+# ---------------------------------------------------------------- entries --
+
+def nvfp4_amax(x: torch.Tensor, amax: torch.Tensor | None = None,
+               status: torch.Tensor | None = None) -> torch.Tensor:
+    """Per-slice max |x| of a bf16 [rows, cols] or [slices, rows, cols] tensor."""
+    S, R, Cc = _shape3(x)
+    if amax is None:
+        amax = torch.empty(S, dtype=torch.float32, device=x.device)
+    _check("nvfp4_amax", lib().nvfp4_amax(_bf16(x, "x"), S, R, Cc, _dev(amax, "amax"),
+                                          _dev(status, "status"), _stream(x.device)))
+    return amax
+
+
+def alloc_encoding(slices: int, rows: int, cols: int, device, four_over_six: bool,
+                   dequant: bool = True) -> dict:
+    """Output tensors of one encoding of a [slices, rows, cols] input, for blocks
+    of 16 along `cols` (pass the transposed dims for the column encoding)."""
+    nb = rows * cols // 16
+    w = (nb + 31) // 32
+    return {
+        "codes": torch.empty((slices, rows, cols // 2), dtype=torch.uint8, device=device),
+        "scales": torch.empty((slices, rows, cols // 16), dtype=torch.uint8, device=device),
+        "choice": (torch.empty((slices, w), dtype=torch.int32, device=device)
+                   if four_over_six else None),
+        "dequant": (torch.empty((slices, rows, cols), dtype=torch.bfloat16, device=device)
+                    if dequant else None),
+    }
+
+
+def _out(enc: dict | None) -> _Out | None:
+    if enc is None:
+        return None
+    return _Out(_dev(enc["codes"], "codes"), _dev(enc["scales"], "scales"),
+                _dev(enc.get("choice"), "choice"), _dev(enc.get("dequant"), "dequant"))
+
+
+def nvfp4_quantize(x: torch.Tensor, global_amax: torch.Tensor, cfg: Config | None = None,
+                   row: dict | None = None, col: dict | None = None,
+                   status: torch.Tensor | None = None, dequant: bool = True) -> dict:
+    """NVFP4-encode a bf16 tensor. Returns {"row": {...}, "col": {...}} with the
+    encodings the config asks for (allocated here unless passed in)."""
+    cfg = cfg or Config()
+    S, R, Cc = _shape3(x)
+    fos = bool(cfg.four_over_six)
+    if cfg.blocks & 1 and row is None:
+        row = alloc_encoding(S, R, Cc, x.device, fos, dequant)
+    if cfg.blocks & 2 and col is None:
+        col = alloc_encoding(S, Cc, R, x.device, fos, dequant)
+    ro, co = _out(row if cfg.blocks & 1 else None), _out(col if cfg.blocks & 2 else None)
+    c = cfg.c()
+    _check("nvfp4_quantize", lib().nvfp4_quantize(
+        C.byref(c), _bf16(x, "x"), S, R, Cc, _dev(global_amax, "global_amax"),
+        C.byref(ro) if ro is not None else None, C.byref(co) if co is not None else None,
+        _dev(status, "status"), _stream(x.device)))
+    return {"row": row if cfg.blocks & 1 else None, "col": col if cfg.blocks & 2 else None}
+
+
+def nvfp4_fakequant_fwd(x: torch.Tensor, s_pre: torch.Tensor, s_post: torch.Tensor | None = None,
+                        out: torch.Tensor | None = None,
+                        status: torch.Tensor | None = None) -> torch.Tensor:
+    R, Cc = x.shape
+    out = torch.empty_like(x) if out is None else out
+    _check("nvfp4_fakequant_fwd", lib().nvfp4_fakequant_fwd(
+        _bf16(x, "x"), R, Cc, _dev(s_pre, "s_pre"), _dev(s_post, "s_post"), _bf16(out, "out"),
+        _dev(status, "status"), _stream(x.device)))
+    return out
+
+
+def nvfp4_scale_grad_bwd(x: torch.Tensor, gq: torch.Tensor, s_pre: torch.Tensor,
+                         s_post: torch.Tensor | None = None, want_gx: bool = True,
+                         gx: torch.Tensor | None = None, gs_pre: torch.Tensor | None = None,
+                         gs_post: torch.Tensor | None = None,
+                         status: torch.Tensor | None = None) -> dict:
+    R, Cc = x.shape
+    if want_gx and gx is None:
+        gx = torch.empty_like(x)
+    gs_pre = torch.empty_like(s_pre) if gs_pre is None else gs_pre
+    if s_post is not None and gs_post is None:
+        gs_post = torch.empty_like(s_post)
+    _check("nvfp4_scale_grad_bwd", lib().nvfp4_scale_grad_bwd(
+        _bf16(x, "x"), _bf16(gq, "gq"), R, Cc, _dev(s_pre, "s_pre"), _dev(s_post, "s_post"),
+        _dev(gx if want_gx else None, "gx"), _dev(gs_pre, "gs_pre"),
+        _dev(gs_post if s_post is not None else None, "gs_post"), _dev(status, "status"),
+        _stream(x.device)))
+    return {"gx": gx if want_gx else None, "gs_pre": gs_pre,
+            "gs_post": gs_post if s_post is not None else None}
+
+
+def nvfp4_codec_probe(op: int, inp: torch.Tensor, aux: torch.Tensor | None = None,
+                      out: torch.Tensor | None = None) -> torch.Tensor:
+    out = torch.empty(inp.numel(), dtype=torch.uint8, device=inp.device) if out is None else out
+    _check("nvfp4_codec_probe", lib().nvfp4_codec_probe(
+        op, _dev(inp, "in"), _dev(aux, "aux"), inp.numel(), _dev(out, "out"),
+        _stream(inp.device)))
+    return out
+
+
+def nvfp4_sr_bits(seed: int, step: int, direction: int, idx0: int, n: int,
+                  device="cuda", out: torch.Tensor | None = None) -> torch.Tensor:
+    out = torch.empty(n, dtype=torch.int32, device=device) if out is None else out
+    _check("nvfp4_sr_bits", lib().nvfp4_sr_bits(seed & 0xFFFFFFFF, step & 0xFFFFFFFF, direction,
+                                                idx0, n, _dev(out, "out"),
+                                                _stream(out.device)))
+    return out
+
+
+class PeriodicAmax:
+    """Periodic tensor scaling (UE5M3 blog): the global amax is recomputed on
+    steps where step % period == 0 and reused, stale, in between. period = 1 is
+    current tensor scaling. The cached amax lives in a caller-visible device
+    buffer, so resuming means passing it back."""
+
+    def __init__(self, period: int, slices: int = 1, device="cuda", amax_fn=None,
+                 amax: torch.Tensor | None = None):
+        if period < 1:
+            raise ValueError("period must be >= 1")
+        self.period = period
+        self.valid = amax is not None
+        self.amax = (amax if amax is not None
+                     else torch.zeros(slices, dtype=torch.float32, device=device))
+        self._fn = amax_fn or (lambda x, out: nvfp4_amax(x, out))
+        self.refreshes = 0
+
+    def __call__(self, x: torch.Tensor, step: int) -> torch.Tensor:
+        if step % self.period == 0 or not self.valid:
+            self.valid = True
+            self._fn(x, self.amax)
+            self.refreshes += 1
+        return self.amax

@@ -1,0 +1,78 @@
+// amax.cu -- per-slice global amax of a bf16 tensor (the FP32 outer scale's
+// input; End-to-End 4-Bit Training, "Low-precision formats on Blackwell";
+// current vs periodic tensor scaling in the UE5M3 blog).
+//
+// Pure read stream: 128-bit loads, |x| as the integer bf16 pattern & 0x7FFF
+// (the ordering of non-negative floats is the ordering of their bits), packed
+// u16x2 max, a warp max (redux), a CTA max, and one atomicMax per CTA on the
+// fp32 bit pattern of the result. MAX is exact and order-free, so the result
+// does not depend on the schedule.
+#include "device.cuh"
+#include "launch.h"
+
+namespace nvfp4 {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kUnroll = 4;
+
+__global__ void __launch_bounds__(kThreads) amax_kernel(const uint16_t* __restrict__ x, int64_t n,
+                                                        uint32_t* amax_bits, int32_t* status) {
+  const int64_t s = blockIdx.y;
+  const uint16_t* base = x + s * n;
+  const int64_t head0 = ((16 - ((uintptr_t)base & 15)) & 15) / 2;
+  const int64_t head = head0 < n ? head0 : n;
+  const uint4* v = reinterpret_cast<const uint4*>(base + head);
+  const int64_t nvec = (n - head) / 8;
+  const int64_t tail0 = head + nvec * 8;
+
+  uint32_t m = 0;
+  if (blockIdx.x == 0) {
+    for (int64_t i = threadIdx.x; i < head; i += kThreads) m = max(m, (uint32_t)(base[i] & 0x7FFFu));
+    for (int64_t i = tail0 + threadIdx.x; i < n; i += kThreads)
+      m = max(m, (uint32_t)(base[i] & 0x7FFFu));
+  }
+  const int64_t stride = (int64_t)gridDim.x * kThreads;
+  for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < nvec; i += stride * kUnroll) {
+    uint4 r[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t j = i + u * stride;
+      r[u] = j < nvec ? __ldcs(v + j) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) m = max(m, absmax_bits4(r[u]));
+  }
+  m = __reduce_max_sync(0xFFFFFFFFu, m);
+  __shared__ uint32_t wmax[kThreads / 32];
+  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kThreads / 32; ++w) m = max(m, wmax[w]);
+    if (m >= 0x7F80u) flag(status, NVFP4_DEV_NONFINITE_INPUT_BIT);
+    if (m) atomicMax(amax_bits + s, m << 16);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_amax(const uint16_t* x, int64_t S, int64_t n, float* amax, int32_t* status,
+                        cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(amax, 0, (size_t)S * sizeof(float), st);
+  if (e != cudaSuccess) return e;
+  if (n == 0) return cudaSuccess;
+  const int64_t nvec = n / 8 + 1;
+  const int64_t want = (nvec + kThreads * kUnroll - 1) / (kThreads * kUnroll);
+  const int64_t cap = std::max<int64_t>(1, (int64_t)sm_count() * 8 / std::max<int64_t>(1, S));
+  for (int64_t s0 = 0; s0 < S; s0 += 65535) {
+    dim3 grid((unsigned)std::min(want, cap), (unsigned)std::min<int64_t>(S - s0, 65535));
+    amax_kernel<<<grid, kThreads, 0, st>>>(x + s0 * n, n, reinterpret_cast<uint32_t*>(amax + s0),
+                                           status);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace nvfp4

@@ -1,0 +1,209 @@
+// api.cu -- the C ABI declared in include/nvfp4.h: argument validation (all
+// synchronous, before anything is enqueued), output-buffer preparation on the
+// caller's stream, and dispatch to the kernels.
+#include <cstdint>
+#include <mutex>
+
+#include "launch.h"
+
+namespace nvfp4 {
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+}  // namespace nvfp4
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
+
+nvfp4_status cuda_status(cudaError_t e) { return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA; }
+
+nvfp4_status check_out(const nvfp4_out* o, bool fos) {
+  if (!o || !o->codes || !o->scales) return NVFP4_ERR_NULL;
+  if (fos && !o->choice) return NVFP4_ERR_NULL;
+  if (!aligned(o->codes, 16) || !aligned(o->scales, 16) || !aligned(o->dequant, 16))
+    return NVFP4_ERR_ALIGN;
+  if (fos && !aligned(o->choice, 16)) return NVFP4_ERR_ALIGN;
+  return NVFP4_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* nvfp4_status_string(nvfp4_status s) {
+  switch (s) {
+    case NVFP4_OK: return "ok";
+    case NVFP4_ERR_NULL: return "a required pointer is NULL";
+    case NVFP4_ERR_SHAPE: return "invalid shape (negative, or a blocked dimension not a multiple of 16)";
+    case NVFP4_ERR_ALIGN: return "a pointer is not aligned as required";
+    case NVFP4_ERR_ENUM: return "a configuration field is out of range";
+    case NVFP4_ERR_CUDA: return "a CUDA launch failed";
+  }
+  return "unknown status";
+}
+
+nvfp4_status nvfp4_amax(const void* x, int64_t slices, int64_t rows, int64_t cols, float* amax,
+                        int32_t* status, void* stream) {
+  if (slices < 0 || rows < 0 || cols < 0) return NVFP4_ERR_SHAPE;
+  if (slices == 0) return NVFP4_OK;
+  if (!amax) return NVFP4_ERR_NULL;
+  if (rows * cols != 0 && !x) return NVFP4_ERR_NULL;
+  if (!aligned(x, 16) || !aligned(amax, 4) || !aligned(status, 4)) return NVFP4_ERR_ALIGN;
+  return cuda_status(nvfp4::launch_amax(static_cast<const uint16_t*>(x), slices, rows * cols, amax,
+                                        status, static_cast<cudaStream_t>(stream)));
+}
+
+nvfp4_status nvfp4_quantize(const nvfp4_config* cfg, const void* x, int64_t slices, int64_t rows,
+                            int64_t cols, const float* global_amax, const nvfp4_out* row,
+                            const nvfp4_out* col, int32_t* status, void* stream) {
+  if (!cfg) return NVFP4_ERR_NULL;
+  if (cfg->blocks < 1 || cfg->blocks > 3 || cfg->scale_fmt < 0 || cfg->scale_fmt > 1 ||
+      cfg->rounding < 0 || cfg->rounding > 1 || cfg->four_over_six < 0 || cfg->four_over_six > 1 ||
+      !(cfg->scale_max >= 0.0f) || !(cfg->scale_max <= 3.402823466e+38f))
+    return NVFP4_ERR_ENUM;
+  if (slices < 0 || rows < 0 || cols < 0) return NVFP4_ERR_SHAPE;
+  const bool do_row = cfg->blocks & 1, do_col = cfg->blocks & 2;
+  if (do_row && cols % 16 != 0) return NVFP4_ERR_SHAPE;
+  if (do_col && rows % 16 != 0) return NVFP4_ERR_SHAPE;
+  if (slices == 0 || rows == 0 || cols == 0) return NVFP4_OK;
+  if (!x || !global_amax) return NVFP4_ERR_NULL;
+  if (!aligned(x, 16) || !aligned(global_amax, 4) || !aligned(status, 4)) return NVFP4_ERR_ALIGN;
+  const bool fos = cfg->four_over_six != 0, sr = cfg->rounding == NVFP4_ROUND_SR;
+  if (do_row) {
+    nvfp4_status e = check_out(row, fos);
+    if (e != NVFP4_OK) return e;
+  }
+  if (do_col) {
+    nvfp4_status e = check_out(col, fos);
+    if (e != NVFP4_OK) return e;
+  }
+  const float M = cfg->scale_max > 0.0f ? cfg->scale_max : (fos ? 256.0f : 448.0f);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t Bs = rows * cols / 16, W = (Bs + 31) / 32;
+
+  if (do_row && !do_col) {
+    nvfp4::RowParams p{};
+    p.x = static_cast<const uint4*>(x);
+    p.Bs = Bs;
+    p.W = W;
+    p.gamax = global_amax;
+    p.M = M;
+    p.seed = cfg->seed;
+    p.step = cfg->step;
+    p.codes = reinterpret_cast<uint32_t*>(row->codes);
+    p.scales = row->scales;
+    p.choice = fos ? row->choice : nullptr;
+    p.dq = static_cast<uint4*>(row->dequant);
+    p.status = status;
+    return cuda_status(nvfp4::launch_quant_row(p, slices, cfg->scale_fmt, sr, fos, st));
+  }
+  // column blocks (alone or with row blocks): the bitmaps are OR-ed into
+  if (fos) {
+    const size_t bytes = (size_t)(slices * W) * sizeof(uint32_t);
+    if (do_row && cudaMemsetAsync(row->choice, 0, bytes, st) != cudaSuccess) return NVFP4_ERR_CUDA;
+    if (cudaMemsetAsync(col->choice, 0, bytes, st) != cudaSuccess) return NVFP4_ERR_CUDA;
+  }
+  nvfp4::DualParams p{};
+  p.x = static_cast<const uint16_t*>(x);
+  p.R = rows;
+  p.C = cols;
+  p.gamax = global_amax;
+  p.M = M;
+  p.seed = cfg->seed;
+  p.step = cfg->step;
+  if (do_row) {
+    p.r_codes = row->codes;
+    p.r_scales = row->scales;
+    p.r_choice = fos ? row->choice : nullptr;
+    p.r_dq = static_cast<uint16_t*>(row->dequant);
+  }
+  p.c_codes = col->codes;
+  p.c_scales = col->scales;
+  p.c_choice = fos ? col->choice : nullptr;
+  p.c_dq = static_cast<uint16_t*>(col->dequant);
+  p.status = status;
+  return cuda_status(nvfp4::launch_quant_dual(p, slices, do_row, cfg->scale_fmt, sr, fos, st));
+}
+
+static nvfp4_status ste_common(const void* x, int64_t rows, int64_t cols, const float* s_pre) {
+  if (rows < 0 || cols < 0 || cols % 16 != 0) return NVFP4_ERR_SHAPE;
+  if (rows == 0 || cols == 0) return NVFP4_OK;
+  if (!x || !s_pre) return NVFP4_ERR_NULL;
+  if (!aligned(x, 16) || !aligned(s_pre, 4)) return NVFP4_ERR_ALIGN;
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_fakequant_fwd(const void* x, int64_t rows, int64_t cols, const float* s_pre,
+                                 const float* s_post, void* xq, int32_t* status, void* stream) {
+  nvfp4_status e = ste_common(x, rows, cols, s_pre);
+  if (e != NVFP4_OK || rows == 0 || cols == 0) return e;
+  if (!xq) return NVFP4_ERR_NULL;
+  if (!aligned(xq, 16) || !aligned(s_post, 4) || !aligned(status, 4)) return NVFP4_ERR_ALIGN;
+  nvfp4::SteParams p{};
+  p.x = static_cast<const uint4*>(x);
+  p.nblocks = rows * cols / 16;
+  p.s_pre = s_pre;
+  p.s_post = s_post;
+  p.out = static_cast<uint4*>(xq);
+  p.status = status;
+  return cuda_status(nvfp4::launch_fakequant_fwd(p, static_cast<cudaStream_t>(stream)));
+}
+
+nvfp4_status nvfp4_scale_grad_bwd(const void* x, const void* gq, int64_t rows, int64_t cols,
+                                  const float* s_pre, const float* s_post, void* gx,
+                                  float* gs_pre, float* gs_post, int32_t* status, void* stream) {
+  nvfp4_status e = ste_common(x, rows, cols, s_pre);
+  if (e != NVFP4_OK || rows == 0 || cols == 0) return e;
+  if (!gq || !gs_pre) return NVFP4_ERR_NULL;
+  if (s_post && !gs_post) return NVFP4_ERR_NULL;
+  if (!s_post && gs_post) return NVFP4_ERR_NULL;
+  if (!aligned(gq, 16) || !aligned(gx, 16) || !aligned(gs_pre, 4) || !aligned(gs_post, 4) ||
+      !aligned(s_post, 4) || !aligned(status, 4))
+    return NVFP4_ERR_ALIGN;
+  nvfp4::SteParams p{};
+  p.x = static_cast<const uint4*>(x);
+  p.gq = static_cast<const uint4*>(gq);
+  p.nblocks = rows * cols / 16;
+  p.s_pre = s_pre;
+  p.s_post = s_post;
+  p.out = static_cast<uint4*>(gx);
+  p.gs_pre = gs_pre;
+  p.gs_post = gs_post;
+  p.status = status;
+  return cuda_status(nvfp4::launch_scale_grad_bwd(p, static_cast<cudaStream_t>(stream)));
+}
+
+nvfp4_status nvfp4_codec_probe(int32_t op, const float* in, const uint32_t* aux, int64_t n,
+                               uint8_t* out, void* stream) {
+  if (op < 0 || op > 3) return NVFP4_ERR_ENUM;
+  if (n < 0) return NVFP4_ERR_SHAPE;
+  if (n == 0) return NVFP4_OK;
+  if (!in || !out || (op == 3 && !aux)) return NVFP4_ERR_NULL;
+  if (!aligned(in, 4) || !aligned(aux, 4)) return NVFP4_ERR_ALIGN;
+  return cuda_status(
+      nvfp4::launch_codec_probe(op, in, aux, n, out, static_cast<cudaStream_t>(stream)));
+}
+
+nvfp4_status nvfp4_sr_bits(uint32_t seed, uint32_t step, uint32_t direction, uint64_t idx0,
+                           int64_t n, uint32_t* out, void* stream) {
+  if (n < 0) return NVFP4_ERR_SHAPE;
+  if (n == 0) return NVFP4_OK;
+  if (!out) return NVFP4_ERR_NULL;
+  if (!aligned(out, 4)) return NVFP4_ERR_ALIGN;
+  return cuda_status(nvfp4::launch_sr_bits(seed, step, direction, idx0, n, out,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

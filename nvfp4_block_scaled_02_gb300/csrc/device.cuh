@@ -1,0 +1,207 @@
+// device.cuh -- sm_103a device building blocks of the NVFP4 kernels:
+// bf16 unpacking, E2M1 / E4M3 / UE5M3 conversions (Blackwell cvt PTX where
+// the hardware has them), Philox4x32-10, the stochastic E2M1 rounder, packed
+// f32x2 arithmetic and the per-slice block-scale tables.
+//
+// All floating-point arithmetic here is IEEE fp32 round-to-nearest; the
+// library is compiled with --fmad=false so no product/sum pair is fused unless
+// written as an explicit fma.
+#pragma once
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace nvfp4 {
+
+constexpr float kFltMax = 3.402823466e+38f;
+
+// ---------------------------------------------------------------- bf16 ----
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+// Pack two fp32 values to bf16x2 with RNE; `lo` lands in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+// Max of |x| over the bf16 halves of 4 words, as a bf16 bit pattern (0..0x7FFF).
+__device__ __forceinline__ uint32_t absmax_bits4(uint4 v) {
+  uint32_t a = __vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu);
+  uint32_t b = __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu);
+  uint32_t m = __vmaxu2(a, b);
+  return max(m & 0xFFFFu, m >> 16);
+}
+
+// ---------------------------------------------------------- packed f32x2 --
+// Blackwell executes these as one instruction for two lanes of fp32 work.
+struct f2 { float x, y; };
+__device__ __forceinline__ unsigned long long f2_pack(f2 a) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a.x), "f"(a.y));
+  return r;
+}
+__device__ __forceinline__ f2 f2_unpack(unsigned long long r) {
+  f2 a;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a.x), "=f"(a.y) : "l"(r));
+  return a;
+}
+__device__ __forceinline__ f2 f2_mul(f2 a, f2 b) {
+  unsigned long long r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_pack(a)), "l"(f2_pack(b)));
+  return f2_unpack(r);
+}
+__device__ __forceinline__ f2 f2_fma(f2 a, f2 b, f2 c) {
+  unsigned long long r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(f2_pack(a)), "l"(f2_pack(b)), "l"(f2_pack(c)));
+  return f2_unpack(r);
+}
+
+// ----------------------------------------------------------------- E2M1 ---
+// Two fp32 -> two E2M1 codes in one byte, round to nearest even, saturating
+// to +-6 (cvt ... satfinite). `even` goes to the low nibble.
+__device__ __forceinline__ uint32_t e2m1x2_rn(float even, float odd) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+      : "=r"(r) : "f"(odd), "f"(even));
+  return r;
+}
+// Eight fp32 values (4 pairs) -> 8 codes in one word, element 0 in bits 0..3.
+__device__ __forceinline__ uint32_t e2m1x8_rn(const f2 (&y)[4]) {
+  uint32_t b0 = e2m1x2_rn(y[0].x, y[0].y), b1 = e2m1x2_rn(y[1].x, y[1].y);
+  uint32_t b2 = e2m1x2_rn(y[2].x, y[2].y), b3 = e2m1x2_rn(y[3].x, y[3].y);
+  return b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+}
+// Value of one E2M1 code (low 4 bits of c) as fp32.
+__device__ __forceinline__ float e2m1_value(uint32_t c) {
+  // magnitude codes 2..7 are the fp32 patterns 0x3F000000 + (m << 22);
+  // code 1 is 0.5 and code 0 is 0.
+  uint32_t m = c & 7u;
+  uint32_t bits = m >= 2 ? 0x3F000000u + (m << 22) : (m == 1 ? 0x3F000000u : 0u);
+  return __uint_as_float(bits | ((c & 8u) << 28));
+}
+// Decode two codes held in a byte via the hardware E2M1x2 -> f16x2 path.
+__device__ __forceinline__ f2 e2m1x2_to_f2(uint32_t byte) {
+  uint32_t h2;
+  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+      : "=r"(h2) : "r"(byte));
+  f2 r;
+  asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+      : "=f"(r.x), "=f"(r.y) : "r"(h2));
+  return r;
+}
+// Decode the 8 codes of a word into 4 pairs (element 2k in .x of pair k).
+__device__ __forceinline__ void e2m1x8_to_f2(uint32_t w, f2 (&q)[4]) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) q[k] = e2m1x2_to_f2((w >> (8 * k)) & 0xFFu);
+}
+
+// --------------------------------------------------------- block scales ---
+// E4M3 encode of t >= 0: RNE, saturating at 448 (cvt ... satfinite).
+__device__ __forceinline__ uint32_t e4m3_encode(float t) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 t;\n\tcvt.rn.satfinite.e4m3x2.f32 t, %1, %2;\n\tcvt.u32.u16 %0, t;\n\t}"
+      : "=r"(r) : "f"(0.0f), "f"(t));
+  return r & 0xFFu;
+}
+__device__ __forceinline__ float e4m3_value(uint32_t c) {
+  uint32_t e = (c >> 3) & 15u, m = c & 7u;
+  if (e == 0) return (float)m * 0.001953125f;  // m * 2^-9, exact
+  return __uint_as_float(((e + 120u) << 23) | (m << 20));
+}
+// UE5M3 (unsigned, bias 15, exponent field 0 subnormal, all codes finite,
+// max 1.875 * 2^16): RNE encode of t >= 0, saturating. No hardware path.
+__device__ __forceinline__ uint32_t ue5m3_encode(float t) {
+  if (!(t < 122880.0f)) return 255u;
+  if (t < 6.103515625e-05f) return __float2uint_rn(__fmul_rn(t, 131072.0f));  // m * 2^-17
+  uint32_t u = __float_as_uint(t);
+  uint32_t r = u + 0x7FFFFu + ((u >> 20) & 1u);  // round the mantissa at bit 20
+  return min((r >> 20) - (112u << 3), 255u);     // rebias exponent 127 -> 15
+}
+__device__ __forceinline__ float ue5m3_value(uint32_t c) {
+  uint32_t e = (c >> 3) & 31u, m = c & 7u;
+  if (e == 0) return (float)m * 7.62939453125e-06f;  // m * 2^-17, exact
+  return __uint_as_float(((e + 112u) << 23) | (m << 20));
+}
+template <int FMT>
+__device__ __forceinline__ uint32_t scale_encode(float t) {
+  if constexpr (FMT == 0) return e4m3_encode(t); else return ue5m3_encode(t);
+}
+template <int FMT>
+__device__ __forceinline__ float scale_value(uint32_t c) {
+  if constexpr (FMT == 0) return e4m3_value(c); else return ue5m3_value(c);
+}
+
+// Per-slice constants of the two-level scale: g = gamax / (6 M) (g = 1 for a
+// zero amax), and rden_k = 1 / (k g) for the targets k = 6 and k = 4 (clamped
+// to FLT_MAX, so a vanishing g saturates the block scales instead of making
+// 0 * inf).
+struct SliceScale {
+  float g, rden6, rden4;
+  bool bad;
+};
+__device__ __forceinline__ SliceScale slice_scale(float gamax, float M) {
+  SliceScale s;
+  s.bad = !(gamax >= 0.0f) || gamax > kFltMax;
+  float g = 1.0f;
+  if (!s.bad && gamax > 0.0f) g = __fdiv_rn(gamax, __fmul_rn(6.0f, M));
+  s.g = g;
+  s.rden6 = fminf(__frcp_rn(__fmul_rn(6.0f, g)), kFltMax);
+  s.rden4 = fminf(__frcp_rn(__fmul_rn(4.0f, g)), kFltMax);
+  return s;
+}
+// Table entry for a block-scale code: d = dec(code) * g and inv = 1 / d
+// (clamped to FLT_MAX; 0 when d == 0).
+template <int FMT>
+__device__ __forceinline__ void scale_entry(uint32_t code, float g, float& d, float& inv) {
+  d = __fmul_rn(scale_value<FMT>(code), g);
+  inv = 0.0f;
+  if (d > 0.0f) inv = fminf(__frcp_rn(d), kFltMax);
+}
+
+// --------------------------------------------------------------- Philox ---
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of two
+// 32x32 -> 64 multiplies, key bumped by the Weyl constants between rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+    uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return c;
+}
+// The 128 random bits of the group of 8 elements starting at flat index
+// idx0 (idx0 % 8 == 0) of an encoding in direction dir (0 rows, 1 columns).
+__device__ __forceinline__ uint4 sr_group_bits(uint32_t seed, uint32_t step, uint32_t dir,
+                                               uint64_t idx0) {
+  uint64_t j = idx0 >> 3;
+  return philox4x32_10(make_uint4((uint32_t)j, (uint32_t)(j >> 32), dir, 0u), seed, step);
+}
+// Random bits of element k (0..7) of a group.
+__device__ __forceinline__ uint32_t sr_bits_of(const uint4& w, int k) {
+  uint32_t word = (k >> 1) == 0 ? w.x : (k >> 1) == 1 ? w.y : (k >> 1) == 2 ? w.z : w.w;
+  return (k & 1) ? (word >> 16) : (word & 0xFFFFu);
+}
+
+// Stochastic E2M1 rounding with 16 random bits v: round |y| up to the next
+// grid value iff v / 2^16 < p, p = (|y| - lo) / (hi - lo). Implemented as
+// code = (T + 0xFFFF - v) >> 16 with T = code_lo * 2^16 + ceil(p * 2^16):
+// below 2 the grid step is 0.5 and T = ceil(|y| * 2^17) (one fma rounded up
+// against 2^23); from 2 on T is read off the fp32 bits (the E2M1 code and
+// its fraction are the exponent and leading mantissa bits).
+__device__ __forceinline__ uint32_t e2m1_sr(float y, uint32_t v) {
+  float a = fminf(fabsf(y), 6.0f);
+  uint32_t t_small = __float_as_uint(__fmaf_ru(a, 131072.0f, 8388608.0f)) - 0x4B000000u;
+  uint32_t t_big = (__float_as_uint(a) - 0x3F000000u + 63u) >> 6;
+  uint32_t t = a < 2.0f ? t_small : t_big;
+  uint32_t code = (t + (0xFFFFu - v)) >> 16;
+  return code | ((__float_as_uint(y) >> 28) & 8u);
+}
+
+// ---------------------------------------------------------- status word ---
+__device__ __forceinline__ void flag(int32_t* status, int32_t bit) {
+  if (status) atomicOr(status, bit);
+}
+
+}  // namespace nvfp4

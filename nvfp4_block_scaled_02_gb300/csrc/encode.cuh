@@ -1,0 +1,182 @@
+// encode.cuh -- the per-block NVFP4 encoder shared by the row kernel (two
+// lanes per 16-value block, 8 values each) and the column/dual kernel (one
+// lane per block). The block's values are held as 4 or 8 f32x2 pairs in
+// registers; nothing touches memory.
+//
+// Steps for one block (End-to-End 4-Bit Training, "Low-precision formats on
+// Blackwell"; UE5M3 blog, math derivation; "Four Over Six", method):
+//   amax -> t_k = amax * (1/(k g)) -> scale code Q(t_k) -> d_k, inv_k from the
+//   per-slice table -> y = x * inv_k -> E2M1 code (RNE or stochastic) ->
+//   (4/6) block sum of (x - q d_k)^2 for k = 6, 4, keep 4 iff strictly lower.
+#pragma once
+#include "device.cuh"
+
+namespace nvfp4 {
+
+// Round 8 values (4 pairs) scaled by inv to E2M1, nibble k = element k.
+template <bool SR>
+__device__ __forceinline__ uint32_t round8(const f2 (&x)[4], float inv, const uint4& rb) {
+  f2 y[4];
+  const f2 iv{inv, inv};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) y[k] = f2_mul(x[k], iv);
+  if constexpr (!SR) {
+    return e2m1x8_rn(y);
+  } else {
+    uint32_t w = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      w |= e2m1_sr(y[k].x, sr_bits_of(rb, 2 * k)) << (8 * k);
+      w |= e2m1_sr(y[k].y, sr_bits_of(rb, 2 * k + 1)) << (8 * k + 4);
+    }
+    return w;
+  }
+}
+
+// Sum over 8 values of (x - q d)^2 in the fixed order: even and odd positions
+// accumulate separately with fma from +0 (one f32x2 accumulator), then
+// even + odd. Also returns the decoded code values.
+__device__ __forceinline__ float half_sse(const f2 (&x)[4], uint32_t codes, float d, f2 (&q)[4]) {
+  e2m1x8_to_f2(codes, q);
+  const f2 nd{-d, -d};
+  f2 acc{0.0f, 0.0f};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    f2 e = f2_fma(q[k], nd, x[k]);
+    acc = f2_fma(e, e, acc);
+  }
+  return __fadd_rn(acc.x, acc.y);
+}
+
+// Dequantised bf16 of 8 decoded values times d, packed as a uint4.
+__device__ __forceinline__ uint4 dequant8(const f2 (&q)[4], float d) {
+  const f2 dd{d, d};
+  f2 r[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) r[k] = f2_mul(q[k], dd);
+  return make_uint4(pack_bf16x2(r[0].x, r[0].y), pack_bf16x2(r[1].x, r[1].y),
+                    pack_bf16x2(r[2].x, r[2].y), pack_bf16x2(r[3].x, r[3].y));
+}
+
+// Unpack a uint4 of 8 bf16 into 4 pairs.
+__device__ __forceinline__ void unpack8(const uint4& v, f2 (&x)[4]) {
+  x[0] = f2{bf16_lo(v.x), bf16_hi(v.x)};
+  x[1] = f2{bf16_lo(v.y), bf16_hi(v.y)};
+  x[2] = f2{bf16_lo(v.z), bf16_hi(v.z)};
+  x[3] = f2{bf16_lo(v.w), bf16_hi(v.w)};
+}
+
+struct HalfResult {
+  uint32_t codes;  // 8 nibbles
+  uint32_t scale;  // block-scale code
+  bool pick4;      // 4/6 chose target 4
+  uint4 dq;        // 8 bf16
+};
+
+// One lane's half of a row block (8 values); its partner lane (lane ^ 1)
+// holds the other half. amax_bits: the block's amax as bf16 bits (already
+// combined over both halves). Every lane of the warp must call this.
+template <int FMT, bool SR, bool FOS>
+__device__ __forceinline__ HalfResult encode_half(const f2 (&x)[4], uint32_t amax_bits,
+                                                  const SliceScale& ss, const float* s_d,
+                                                  const float* s_inv, const uint4& rb,
+                                                  bool want_dq) {
+  HalfResult r;
+  const float amax = __uint_as_float(amax_bits << 16);
+  const uint32_t c6 = scale_encode<FMT>(__fmul_rn(amax, ss.rden6));
+  const float d6 = s_d[c6], inv6 = s_inv[c6];
+  const uint32_t q6 = round8<SR>(x, inv6, rb);
+  if constexpr (!FOS) {
+    r.codes = q6;
+    r.scale = c6;
+    r.pick4 = false;
+    if (want_dq) {
+      f2 q[4];
+      e2m1x8_to_f2(q6, q);
+      r.dq = dequant8(q, d6);
+    }
+  } else {
+    const uint32_t c4 = scale_encode<FMT>(__fmul_rn(amax, ss.rden4));
+    const float d4 = s_d[c4], inv4 = s_inv[c4];
+    const uint32_t q4 = round8<SR>(x, inv4, rb);
+    f2 v6[4], v4[4];
+    const float h6 = half_sse(x, q6, d6, v6);
+    const float h4 = half_sse(x, q4, d4, v4);
+    const float sse6 = __fadd_rn(h6, __shfl_xor_sync(0xFFFFFFFFu, h6, 1));
+    const float sse4 = __fadd_rn(h4, __shfl_xor_sync(0xFFFFFFFFu, h4, 1));
+    r.pick4 = sse4 < sse6;
+    r.codes = r.pick4 ? q4 : q6;
+    r.scale = r.pick4 ? c4 : c6;
+    if (want_dq) r.dq = r.pick4 ? dequant8(v4, d4) : dequant8(v6, d6);
+  }
+  return r;
+}
+
+// A whole 16-value block held by one lane as two halves (column kernel).
+struct BlockResult {
+  uint32_t codes[2];
+  uint32_t scale;
+  bool pick4;
+  uint4 dq[2];
+};
+
+template <int FMT, bool SR, bool FOS>
+__device__ __forceinline__ BlockResult encode_block(const f2 (&lo)[4], const f2 (&hi)[4],
+                                                    uint32_t amax_bits, const SliceScale& ss,
+                                                    const float* s_d, const float* s_inv,
+                                                    const uint4& rb0, const uint4& rb1,
+                                                    bool want_dq) {
+  BlockResult r;
+  const float amax = __uint_as_float(amax_bits << 16);
+  const uint32_t c6 = scale_encode<FMT>(__fmul_rn(amax, ss.rden6));
+  const float d6 = s_d[c6], inv6 = s_inv[c6];
+  const uint32_t a6 = round8<SR>(lo, inv6, rb0), b6 = round8<SR>(hi, inv6, rb1);
+  if constexpr (!FOS) {
+    r.codes[0] = a6;
+    r.codes[1] = b6;
+    r.scale = c6;
+    r.pick4 = false;
+    if (want_dq) {
+      f2 q[4];
+      e2m1x8_to_f2(a6, q);
+      r.dq[0] = dequant8(q, d6);
+      e2m1x8_to_f2(b6, q);
+      r.dq[1] = dequant8(q, d6);
+    }
+  } else {
+    const uint32_t c4 = scale_encode<FMT>(__fmul_rn(amax, ss.rden4));
+    const float d4 = s_d[c4], inv4 = s_inv[c4];
+    const uint32_t a4 = round8<SR>(lo, inv4, rb0), b4 = round8<SR>(hi, inv4, rb1);
+    f2 va6[4], vb6[4], va4[4], vb4[4];
+    const float sse6 = __fadd_rn(half_sse(lo, a6, d6, va6), half_sse(hi, b6, d6, vb6));
+    const float sse4 = __fadd_rn(half_sse(lo, a4, d4, va4), half_sse(hi, b4, d4, vb4));
+    r.pick4 = sse4 < sse6;
+    r.codes[0] = r.pick4 ? a4 : a6;
+    r.codes[1] = r.pick4 ? b4 : b6;
+    r.scale = r.pick4 ? c4 : c6;
+    if (want_dq) {
+      if (r.pick4) {
+        r.dq[0] = dequant8(va4, d4);
+        r.dq[1] = dequant8(vb4, d4);
+      } else {
+        r.dq[0] = dequant8(va6, d6);
+        r.dq[1] = dequant8(vb6, d6);
+      }
+    }
+  }
+  return r;
+}
+
+// Per-slice block-scale table in shared memory: for every code c of the
+// format, d = dec(c) * g and inv = 1/d. Built by the first 256 threads.
+template <int FMT>
+__device__ __forceinline__ void build_scale_table(float* s_d, float* s_inv, float g) {
+  for (int c = threadIdx.x; c < 256; c += blockDim.x) {
+    float d, inv;
+    scale_entry<FMT>((uint32_t)c, g, d, inv);
+    s_d[c] = d;
+    s_inv[c] = inv;
+  }
+}
+
+}  // namespace nvfp4

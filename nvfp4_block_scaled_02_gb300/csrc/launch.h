@@ -1,0 +1,83 @@
+// launch.h -- internal host-side interface between the C ABI (api.cu) and the
+// kernel translation units. Not installed; the public interface is nvfp4.h.
+#pragma once
+#include <cstdint>
+#include <algorithm>
+#include <cuda_runtime.h>
+
+#include "../../include/nvfp4.h"
+
+#define NVFP4_DEV_NONFINITE_INPUT_BIT NVFP4_DEV_NONFINITE_INPUT
+#define NVFP4_DEV_BAD_SCALE_BIT NVFP4_DEV_BAD_SCALE
+#define NVFP4_DEV_BAD_AMAX_BIT NVFP4_DEV_BAD_AMAX
+
+namespace nvfp4 {
+
+int sm_count();
+
+// Row (1x16) quantiser over a stack of S slices of Bs blocks each.
+struct RowParams {
+  const uint4* x;       // bf16 input, 8 values per uint4
+  int64_t Bs;           // blocks per slice = R * C / 16
+  int64_t W;            // 4/6 bitmap words per slice = ceil(Bs / 32)
+  const float* gamax;   // [S]
+  float M;              // outer-scale FP8 maximum
+  uint32_t seed, step;  // stochastic rounding key
+  uint32_t* codes;      // 8 codes (one uint32) per chunk of 8 values
+  uint8_t* scales;      // one byte per block
+  uint32_t* choice;     // 4/6 bitmap (may be null when 4/6 is off)
+  uint4* dq;            // bf16 dequant, may be null
+  int32_t* status;      // may be null
+  int64_t slice0;       // first slice of this launch (grids cover <= 65535)
+};
+cudaError_t launch_quant_row(const RowParams& p, int64_t S, int fmt, bool sr, bool fos,
+                             cudaStream_t st);
+
+// Column (16x1) and dual (row + column from one read) quantiser.
+struct DualParams {
+  const uint16_t* x;    // bf16 [S][R][C]
+  int64_t R, C;
+  const float* gamax;
+  float M;
+  uint32_t seed, step;
+  // row encoding (used when the kernel writes both)
+  uint8_t* r_codes;
+  uint8_t* r_scales;
+  uint32_t* r_choice;
+  uint16_t* r_dq;
+  // column encoding
+  uint8_t* c_codes;
+  uint8_t* c_scales;
+  uint32_t* c_choice;
+  uint16_t* c_dq;
+  int32_t* status;
+};
+cudaError_t launch_quant_dual(const DualParams& p, int64_t S, bool rows_too, int fmt, bool sr,
+                              bool fos, cudaStream_t st);
+
+// Per-slice global amax.
+cudaError_t launch_amax(const uint16_t* x, int64_t S, int64_t n, float* amax, int32_t* status,
+                        cudaStream_t st);
+
+// Scale-learning fake quantisation and STE backward (row blocks).
+struct SteParams {
+  const uint4* x;
+  const uint4* gq;      // backward only
+  int64_t nblocks;      // R * C / 16
+  const float* s_pre;
+  const float* s_post;  // null = tied
+  uint4* out;           // xq (forward) or gx (backward, may be null)
+  float* gs_pre;
+  float* gs_post;
+  int32_t* status;
+};
+cudaError_t launch_fakequant_fwd(const SteParams& p, cudaStream_t st);
+cudaError_t launch_scale_grad_bwd(const SteParams& p, cudaStream_t st);
+
+// Diagnostics.
+cudaError_t launch_codec_probe(int op, const float* in, const uint32_t* aux, int64_t n,
+                               uint8_t* out, cudaStream_t st);
+cudaError_t launch_sr_bits(uint32_t seed, uint32_t step, uint32_t dir, uint64_t idx0, int64_t n,
+                           uint32_t* out, cudaStream_t st);
+
+}  // namespace nvfp4

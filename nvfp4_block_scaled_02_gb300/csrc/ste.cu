@@ -1,0 +1,143 @@
+// ste.cu -- scale learning: fake quantisation forward and the straight-
+// through-estimator backward for single (tied) and dual (pre/post) per-block
+// scales (Scale Learning blog, "How Scale Learning Works").
+//
+// Both kernels stream 1x16 row blocks with two lanes per block (8 values and
+// one 128-bit load per lane per tensor). Per-block sums are fp32 in the fixed
+// order: within each lane's 8 values, even and odd positions accumulate in
+// the two halves of an f32x2 fma accumulator; half = even + odd; the block
+// sum is the lower half plus the upper half (one shuffle).
+#include "device.cuh"
+#include "encode.cuh"
+#include "launch.h"
+
+namespace nvfp4 {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr float kFltMin = 1.175494351e-38f;
+
+__device__ __forceinline__ bool scale_ok(float sp, float so) {
+  return sp >= kFltMin && sp <= kFltMax && fabsf(so) <= kFltMax;
+}
+
+__device__ __forceinline__ bool finite8(const uint4& v) {
+  return absmax_bits4(v) < 0x7F80u;
+}
+
+__global__ void __launch_bounds__(kThreads) fakequant_fwd_kernel(const SteParams p) {
+  const int64_t nchunks = p.nblocks * 2;
+  const int64_t stride = (int64_t)gridDim.x * kThreads;
+  for (int64_t ch = (int64_t)blockIdx.x * kThreads + threadIdx.x; ch < nchunks; ch += stride) {
+    const int64_t b = ch >> 1;
+    const uint4 v = __ldcs(p.x + ch);
+    const float sp = p.s_pre[b];
+    const float so = p.s_post ? p.s_post[b] : sp;
+    if ((ch & 1) == 0 && !scale_ok(sp, so)) flag(p.status, NVFP4_DEV_BAD_SCALE_BIT);
+    if (!finite8(v)) flag(p.status, NVFP4_DEV_NONFINITE_INPUT_BIT);
+    const float inv = __frcp_rn(sp);
+    f2 x[4], y[4], q[4];
+    unpack8(v, x);
+    const f2 iv{inv, inv};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) y[k] = f2_mul(x[k], iv);
+    e2m1x8_to_f2(e2m1x8_rn(y), q);
+    __stcs(p.out + ch, dequant8(q, so));
+  }
+}
+
+template <bool TIED, bool WANT_GX>
+__global__ void __launch_bounds__(kThreads) scale_grad_bwd_kernel(const SteParams p) {
+  const int64_t nchunks = p.nblocks * 2;
+  const int64_t stride = (int64_t)gridDim.x * kThreads;
+  // all lanes of a warp iterate together (stride and start are warp-aligned),
+  // so the pair shuffle below always has its partner
+  const int64_t start = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+  const int64_t nwarp_iters = (nchunks + stride - 1) / stride;
+  for (int64_t it = 0; it < nwarp_iters; ++it) {
+    const int64_t ch = start + it * stride;
+    const bool ok = ch < nchunks;
+    const int64_t b = ch >> 1;
+    uint4 xv = make_uint4(0, 0, 0, 0), gv = xv;
+    float sp = 1.0f, so = 1.0f;
+    if (ok) {
+      xv = __ldcs(p.x + ch);
+      gv = __ldcs(p.gq + ch);
+      sp = p.s_pre[b];
+      so = TIED ? sp : p.s_post[b];
+      if ((ch & 1) == 0 && !scale_ok(sp, so)) flag(p.status, NVFP4_DEV_BAD_SCALE_BIT);
+      if (!finite8(xv) || !finite8(gv)) flag(p.status, NVFP4_DEV_NONFINITE_INPUT_BIT);
+    }
+    const float inv = __frcp_rn(sp);
+    const float a = TIED ? 1.0f : __fmul_rn(so, inv);
+    f2 x[4], g[4], r[4], q[4];
+    unpack8(xv, x);
+    unpack8(gv, g);
+    const f2 iv{inv, inv};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) r[k] = f2_mul(x[k], iv);
+    e2m1x8_to_f2(e2m1x8_rn(r), q);
+
+    f2 acc0{0.0f, 0.0f}, acc1{0.0f, 0.0f};
+    uint32_t gx[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const bool in_x = r[k].x >= -6.0f && r[k].x <= 6.0f;
+      const bool in_y = r[k].y >= -6.0f && r[k].y <= 6.0f;
+      if constexpr (WANT_GX) {
+        const float gxx = in_x ? (TIED ? g[k].x : __fmul_rn(g[k].x, a)) : 0.0f;
+        const float gxy = in_y ? (TIED ? g[k].y : __fmul_rn(g[k].y, a)) : 0.0f;
+        gx[k] = pack_bf16x2(gxx, gxy);
+      }
+      if constexpr (TIED) {
+        const f2 t{in_x ? __fsub_rn(q[k].x, r[k].x) : q[k].x,
+                   in_y ? __fsub_rn(q[k].y, r[k].y) : q[k].y};
+        acc0 = f2_fma(g[k], t, acc0);
+      } else {
+        acc0 = f2_fma(g[k], q[k], acc0);
+        const f2 rin{in_x ? r[k].x : 0.0f, in_y ? r[k].y : 0.0f};
+        acc1 = f2_fma(g[k], rin, acc1);
+      }
+    }
+    if constexpr (WANT_GX)
+      if (ok) __stcs(p.out + ch, make_uint4(gx[0], gx[1], gx[2], gx[3]));
+    const float h0 = __fadd_rn(acc0.x, acc0.y);
+    const float s0 = __fadd_rn(h0, __shfl_xor_sync(0xFFFFFFFFu, h0, 1));
+    if constexpr (TIED) {
+      if (ok && (ch & 1) == 0) p.gs_pre[b] = s0;
+    } else {
+      const float h1 = __fadd_rn(acc1.x, acc1.y);
+      const float s1 = __fadd_rn(h1, __shfl_xor_sync(0xFFFFFFFFu, h1, 1));
+      if (ok && (ch & 1) == 0) {
+        if (p.gs_post) p.gs_post[b] = s0;
+        p.gs_pre[b] = __fmul_rn(-a, s1);
+      }
+    }
+  }
+}
+
+unsigned grid_for(int64_t nchunks) {
+  const int64_t want = (nchunks + kThreads - 1) / kThreads;
+  const int64_t cap = (int64_t)sm_count() * 8;
+  return (unsigned)std::max<int64_t>(1, std::min(want, cap));
+}
+
+}  // namespace
+
+cudaError_t launch_fakequant_fwd(const SteParams& p, cudaStream_t st) {
+  fakequant_fwd_kernel<<<grid_for(p.nblocks * 2), kThreads, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scale_grad_bwd(const SteParams& p, cudaStream_t st) {
+  const unsigned grid = grid_for(p.nblocks * 2);
+  const bool tied = p.s_post == nullptr, want_gx = p.out != nullptr;
+  if (tied && want_gx) scale_grad_bwd_kernel<true, true><<<grid, kThreads, 0, st>>>(p);
+  else if (tied) scale_grad_bwd_kernel<true, false><<<grid, kThreads, 0, st>>>(p);
+  else if (want_gx) scale_grad_bwd_kernel<false, true><<<grid, kThreads, 0, st>>>(p);
+  else scale_grad_bwd_kernel<false, false><<<grid, kThreads, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace nvfp4

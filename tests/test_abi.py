@@ -1,0 +1,142 @@
+"""The C-ABI library builds, loads, exports every function include/nvfp4.h
+declares, and rejects bad arguments synchronously -- all without a GPU (the
+validation runs before any CUDA call, so nothing here launches a kernel)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "nvfp4.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    import nvfp4_block_scaled_02_gb300 as nv
+    nv.build()
+    return nv.lib()
+
+
+def _declared():
+    text = open(HEADER).read()
+    return re.findall(r"NVFP4_API\s+[\w\s\*]+?\b(nvfp4_\w+)\s*\(", text)
+
+
+def test_header_declares_the_boundary():
+    names = set(_declared())
+    assert {"nvfp4_amax", "nvfp4_quantize", "nvfp4_fakequant_fwd",
+            "nvfp4_scale_grad_bwd"} <= names
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in _declared():
+        assert hasattr(L, name), name
+
+
+def test_library_links_no_oracle_and_no_cpu_path():
+    """The product library and the oracle share nothing: no oracle symbol is in
+    the CUDA library and the package source never imports the oracle."""
+    import nvfp4_block_scaled_02_gb300 as nv
+    lib = nv.lib()
+    for sym in ("orc_quantize", "orc_e2m1_rne", "orc_philox4x32_10"):
+        assert not hasattr(lib, sym)
+    pkg = os.path.dirname(nv.__file__)
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in src and "from oracle" not in src, f
+                assert "nvfp4_oracle" not in src, f
+
+
+def _cfg(**kw):
+    import nvfp4_block_scaled_02_gb300 as nv
+    c = nv.Config(**kw).c()
+    return c
+
+
+FAKE = 0x100000  # a 16-byte aligned, never dereferenced address
+
+
+def _out(codes=FAKE, scales=FAKE, choice=FAKE, dq=FAKE):
+    import nvfp4_block_scaled_02_gb300 as nv
+    return nv._Out(codes, scales, choice, dq)
+
+
+def q(L, cfg, x=FAKE, S=1, R=16, Cc=32, amax=FAKE, row=None, col=None, status=None):
+    return L.nvfp4_quantize(C.byref(cfg) if cfg is not None else None, x, S, R, Cc, amax,
+                            C.byref(row) if row is not None else None,
+                            C.byref(col) if col is not None else None, status, None)
+
+
+def test_quantize_argument_errors(L):
+    assert q(L, None) == 1
+    for bad in (dict(blocks=0), dict(blocks=4), dict(scale_fmt=2), dict(rounding=3),
+                dict(four_over_six=2), dict(scale_max=-1.0), dict(scale_max=float("nan"))):
+        assert q(L, _cfg(**bad), row=_out(), col=_out()) == 4, bad
+    assert q(L, _cfg(blocks=1), Cc=24, row=_out()) == 2      # cols % 16 for row blocks
+    assert q(L, _cfg(blocks=2), R=24, col=_out()) == 2       # rows % 16 for column blocks
+    assert q(L, _cfg(blocks=3), R=24, row=_out(), col=_out()) == 2
+    assert q(L, _cfg(blocks=1), R=-1, row=_out()) == 2
+    assert q(L, _cfg(blocks=1), x=0, row=_out()) == 1
+    assert q(L, _cfg(blocks=1), amax=0, row=_out()) == 1
+    assert q(L, _cfg(blocks=1), row=None) == 1
+    assert q(L, _cfg(blocks=2), col=None) == 1
+    assert q(L, _cfg(blocks=1, four_over_six=1), row=_out(choice=0)) == 1
+    assert q(L, _cfg(blocks=1), x=FAKE + 2, row=_out()) == 3
+    assert q(L, _cfg(blocks=1), row=_out(codes=FAKE + 4)) == 3
+    assert q(L, _cfg(blocks=1), row=_out(dq=FAKE + 8)) == 3
+    assert q(L, _cfg(blocks=1), amax=FAKE + 1, row=_out()) == 3
+
+
+def test_empty_inputs_enqueue_nothing(L):
+    for S, R, Cc in ((0, 16, 32), (1, 0, 32), (1, 16, 0)):
+        assert q(L, _cfg(blocks=3), x=0, S=S, R=R, Cc=Cc, amax=0, row=None, col=None) == 0
+    assert L.nvfp4_amax(None, 0, 4, 4, None, None, None) == 0
+    assert L.nvfp4_fakequant_fwd(None, 0, 16, None, None, None, None, None) == 0
+    assert L.nvfp4_scale_grad_bwd(None, None, 4, 0, None, None, None, None, None, None,
+                                  None) == 0
+
+
+def test_amax_argument_errors(L):
+    assert L.nvfp4_amax(FAKE, -1, 4, 4, FAKE, None, None) == 2
+    assert L.nvfp4_amax(FAKE, 1, 4, 4, None, None, None) == 1
+    assert L.nvfp4_amax(None, 1, 4, 4, FAKE, None, None) == 1
+    assert L.nvfp4_amax(FAKE + 2, 1, 4, 4, FAKE, None, None) == 3
+
+
+def test_ste_argument_errors(L):
+    assert L.nvfp4_fakequant_fwd(FAKE, 4, 24, FAKE, None, FAKE, None, None) == 2
+    assert L.nvfp4_fakequant_fwd(FAKE, 4, 32, None, None, FAKE, None, None) == 1
+    assert L.nvfp4_fakequant_fwd(FAKE, 4, 32, FAKE, None, None, None, None) == 1
+    assert L.nvfp4_fakequant_fwd(FAKE + 8, 4, 32, FAKE, None, FAKE, None, None) == 3
+    bwd = L.nvfp4_scale_grad_bwd
+    assert bwd(FAKE, FAKE, 4, 24, FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == 2
+    assert bwd(FAKE, FAKE, 4, 32, FAKE, FAKE, FAKE, FAKE, None, None, None) == 1  # dual, no gs_post
+    assert bwd(FAKE, FAKE, 4, 32, FAKE, None, FAKE, FAKE, FAKE, None, None) == 1  # tied + gs_post
+    assert bwd(FAKE, FAKE, 4, 32, FAKE, None, FAKE, None, None, None, None) == 1  # no gs_pre
+    assert bwd(FAKE, None, 4, 32, FAKE, None, FAKE, FAKE, None, None, None) == 1
+    assert bwd(FAKE, FAKE + 4, 4, 32, FAKE, None, FAKE, FAKE, None, None, None) == 3
+
+
+def test_diagnostics_argument_errors(L):
+    assert L.nvfp4_codec_probe(7, FAKE, None, 4, FAKE, None) == 4
+    assert L.nvfp4_codec_probe(3, FAKE, None, 4, FAKE, None) == 1
+    assert L.nvfp4_codec_probe(0, FAKE, None, -1, FAKE, None) == 2
+    assert L.nvfp4_sr_bits(0, 0, 0, 0, 4, None, None) == 1
+
+
+def test_status_strings(L):
+    for code in (0, 1, 2, 3, 4, 6):
+        assert L.nvfp4_status_string(code)
+    assert L.nvfp4_status_string(99) == b"unknown status"
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    import nvfp4_block_scaled_02_gb300 as nv
+    x = torch.zeros((16, 32), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        nv.nvfp4_amax(x)
