@@ -1,0 +1,735 @@
+"""Throughput of the NVFP4 hot path on one or more GB300s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5] [--impl ours|reference]
+
+A step is one pass of the hot path over one batch of synthetic input already
+resident in HBM. The default workload is the activation tensor 8192 x 4096 bf16
+(S = 8192 tokens x hidden 4096, 0.5 * Student-t(3) values): current tensor
+scaling (global amax pass), 1x16 row blocks, E4M3 block scales, RNE E2M1,
+Four-Over-Six on, writing codes, scale bytes, the 4/6 bitmap and the dequantised
+tensor. Other --config values time the other workloads (see WORKLOADS).
+
+One JSON line is printed by rank 0. `value` is algorithmic HBM bytes / time
+(GB/s) summed over all ranks; `roofline` relates the dominant kernel's own
+CUDA-event time to the measured HBM copy bandwidth; `e2e` repeats the metric
+through the same C ABI with host buffers (pinned host -> device copy of the
+input and device -> host copy of every output inside the timed region);
+`cpu_baseline` is the plain C oracle on the host cores (a baseline, not the
+target). With --impl reference the oracle itself is the timed arm.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes as C
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import nvfp4_block_scaled_02_gb300 as nv  # noqa: E402
+from nvfp4_block_scaled_02_gb300 import synth  # noqa: E402
+
+METRIC = "NVFP4 quantize/STE-bwd HBM GB/s and Gelem/s; fraction of GB300 HBM peak"
+L2_BYTES = 129 * 2 ** 20
+FALLBACK_HBM_GBS = 6800.0
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ------------------------------------------------------------ workloads --
+
+class Kernel:
+    """A launch of one of our kernels and its algorithmic HBM bytes."""
+
+    def __init__(self, name, nbytes, fn):
+        self.name, self.nbytes, self.fn = name, nbytes, fn
+
+
+class Workload:
+    name = ""
+    elements = 0
+
+    def kernels(self, k: int, bufset: int) -> list:
+        raise NotImplementedError
+
+
+def _alloc_like(shape, dtype, device):
+    return torch.empty(shape, dtype=dtype, device=device)
+
+
+class Activation(Workload):
+    """Activations [S x H] = [8192 x 4096]: amax + row quantise with 4/6."""
+
+    def __init__(self, device, rows=8192, cols=4096, fos=1, seed=1, nsets=None, dist="t3"):
+        self.rows, self.cols, self.fos = rows, cols, fos
+        self.elements = rows * cols
+        xb = (synth.student_t(rows, cols, seed=seed) if dist == "t3"
+              else synth.outlier_normal(rows, cols, seed=seed))
+        self.host_x = xb
+        x0 = torch.from_numpy(xb.view(np.int16)).to(device)
+        self.cfg = nv.Config(four_over_six=fos)
+        out_bytes = self.elements * (0.5 + 1 / 16 + 2) + (self.elements / 16 / 8 if fos else 0)
+        per_set = self.elements * 2 + out_bytes
+        self.nsets = nsets or max(2, int(np.ceil(2.5 * L2_BYTES / per_set)))
+        self.x = [x0] + [x0.clone() for _ in range(self.nsets - 1)]
+        self.amax = [torch.empty(1, dtype=torch.float32, device=device) for _ in range(self.nsets)]
+        self.out = [nv.alloc_encoding(1, rows, cols, device, bool(fos)) for _ in range(self.nsets)]
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.q_bytes = self.elements * (2 + 0.5 + 1 / 16 + 2) + (self.elements / 128 if fos else 0)
+        self.a_bytes = self.elements * 2
+        self.working_set = per_set * self.nsets
+        self._prep(device)
+
+    def _prep(self, device):
+        L = nv.lib()
+        self._c = self.cfg.c()
+        self._outs = [nv._out(o) for o in self.out]
+        st = torch.cuda.current_stream(device).cuda_stream
+        R, Cc = self.rows, self.cols
+
+        def amax(i):
+            return L.nvfp4_amax(self.x[i].data_ptr(), 1, R, Cc, self.amax[i].data_ptr(),
+                                self.status.data_ptr(), st)
+
+        def quant(i):
+            return L.nvfp4_quantize(C.byref(self._c), self.x[i].data_ptr(), 1, R, Cc,
+                                    self.amax[i].data_ptr(), C.byref(self._outs[i]), None,
+                                    self.status.data_ptr(), st)
+        self._amax, self._quant = amax, quant
+
+    def kernels(self, k, i):
+        return [Kernel("amax", self.a_bytes, lambda: self._amax(i)),
+                Kernel("quantize_row", self.q_bytes, lambda: self._quant(i))]
+
+    def e2e_io(self, k):
+        o = self.out[0]
+        outs = [o["codes"], o["scales"], o["dequant"]] + ([o["choice"]] if self.fos else [])
+        return [self.x[0]], outs
+
+    def cpu_sample(self, budget_s):
+        import oracle
+        rows = 64
+        t0 = time.perf_counter()
+        self._cpu_once(oracle, rows)
+        per_row = (time.perf_counter() - t0) / rows
+        rows = int(min(self.rows, max(64, budget_s / max(per_row, 1e-9))))
+        t0 = time.perf_counter()
+        self._cpu_once(oracle, rows)
+        dt = time.perf_counter() - t0
+        return rows * self.cols, dt, f"first {rows} of {self.rows} rows (amax + quantise)"
+
+    def _cpu_once(self, oracle, rows):
+        xb = self.host_x[:rows]
+        a, _ = oracle.global_amax(xb)
+        oracle.quantize(xb, a, four_over_six=self.fos)
+
+    bytes_per_elem = property(lambda self: (self.q_bytes + self.a_bytes) / self.elements)
+    dominant = "quantize_row"
+    workload = property(lambda self: (
+        f"activation {self.rows}x{self.cols} bf16, 0.5*Student-t(nu=3); current scaling "
+        f"(amax pass) + 1x16 row blocks, E4M3 scales, RNE, Four-Over-Six "
+        f"{'on' if self.fos else 'off'}; outputs codes, scales, "
+        f"{'4/6 bitmap, ' if self.fos else ''}dequant"))
+
+
+class SmallNormal(Activation):
+    """1024 x 1024 N(0,1) with 0.1 % x20 outliers, 4/6 off (L2-resident)."""
+
+    def __init__(self, device):
+        super().__init__(device, rows=1024, cols=1024, fos=0, seed=0, dist="normal")
+
+    workload = property(lambda self: (
+        "1024x1024 bf16 N(0,1), 0.1% x20 outliers; amax + 1x16 row blocks, E4M3, RNE, "
+        "4/6 off; outputs codes, scales, dequant"))
+
+
+class ScaleLearning(Workload):
+    """Weight 14336 x 4096: fake-quant forward + STE backward with dual scales."""
+
+    def __init__(self, device, rows=14336, cols=4096, seed=2):
+        wb, gb, s = synth.scale_learning(rows, cols, seed=seed)
+        self.rows, self.cols = rows, cols
+        self.elements = rows * cols
+        self.host = (wb, gb, s)
+        per_set = self.elements * (2 + 2 + 2 + 2) + self.elements / 16 * 16
+        self.nsets = max(2, int(np.ceil(2.5 * L2_BYTES / per_set)))
+        w = torch.from_numpy(wb.view(np.int16)).to(device)
+        g = torch.from_numpy(gb.view(np.int16)).to(device)
+        sp = torch.from_numpy(s).to(device)
+        self.sets = []
+        for _ in range(self.nsets):
+            self.sets.append(dict(w=w.clone(), g=g.clone(), sp=sp.clone(), so=sp.clone(),
+                                  xq=torch.empty_like(w), gx=torch.empty_like(w),
+                                  gsp=torch.empty_like(sp), gso=torch.empty_like(sp)))
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.f_bytes = self.elements * 4.5
+        self.b_bytes = self.elements * 7.0
+        self.working_set = per_set * self.nsets
+        L = nv.lib()
+        st = torch.cuda.current_stream(device).cuda_stream
+        R, Cc = rows, cols
+
+        def fwd(i):
+            d = self.sets[i]
+            return L.nvfp4_fakequant_fwd(d["w"].data_ptr(), R, Cc, d["sp"].data_ptr(),
+                                         d["so"].data_ptr(), d["xq"].data_ptr(),
+                                         self.status.data_ptr(), st)
+
+        def bwd(i):
+            d = self.sets[i]
+            return L.nvfp4_scale_grad_bwd(d["w"].data_ptr(), d["g"].data_ptr(), R, Cc,
+                                          d["sp"].data_ptr(), d["so"].data_ptr(),
+                                          d["gx"].data_ptr(), d["gsp"].data_ptr(),
+                                          d["gso"].data_ptr(), self.status.data_ptr(), st)
+        self._fwd, self._bwd = fwd, bwd
+
+    def kernels(self, k, i):
+        return [Kernel("fakequant_fwd", self.f_bytes, lambda: self._fwd(i)),
+                Kernel("scale_grad_bwd", self.b_bytes, lambda: self._bwd(i))]
+
+    def e2e_io(self, k):
+        d = self.sets[0]
+        return [d["w"], d["g"], d["sp"], d["so"]], [d["xq"], d["gx"], d["gsp"], d["gso"]]
+
+    def cpu_sample(self, budget_s):
+        import oracle
+        wb, gb, s = self.host
+        rows = 256
+        t0 = time.perf_counter()
+        oracle.fakequant_fwd(wb[:rows], s[:rows], s[:rows])
+        oracle.scale_grad_bwd(wb[:rows], gb[:rows], s[:rows], s[:rows])
+        per_row = (time.perf_counter() - t0) / rows
+        rows = int(min(self.rows, max(256, budget_s / max(per_row, 1e-9))))
+        t0 = time.perf_counter()
+        oracle.fakequant_fwd(wb[:rows], s[:rows], s[:rows])
+        oracle.scale_grad_bwd(wb[:rows], gb[:rows], s[:rows], s[:rows])
+        return rows * self.cols, time.perf_counter() - t0, \
+            f"first {rows} of {self.rows} rows (forward + backward)"
+
+    bytes_per_elem = property(lambda self: (self.f_bytes + self.b_bytes) / self.elements)
+    dominant = "scale_grad_bwd"
+    workload = property(lambda self: (
+        f"scale-learning step on weight {self.rows}x{self.cols} bf16 N(0,0.02), dual fp32 "
+        "per-block scales (init amax/6), dL/dx~ N(0,1e-3): fake-quant forward + STE backward "
+        "(dL/dx, dL/ds_pre, dL/ds_post)"))
+
+
+class DriftingGradient(Workload):
+    """Gradients 16384 x 4096, UE5M3, stochastic rounding, periodic scaling
+    (amax refreshed every 16 steps), rows drifting x1.05 per step."""
+
+    def __init__(self, device, rows=16384, cols=4096, seed=3, period=16, nsteps=32):
+        gen = synth.DriftingGradient(rows, cols, seed=seed)
+        self.rows, self.cols, self.period = rows, cols, period
+        self.elements = rows * cols
+        self.host0 = gen.step(0)
+        self.x = [torch.from_numpy(gen.step(t).view(np.int16)).to(device) for t in range(nsteps)]
+        self.nsets = nsteps
+        self.amax = torch.empty(1, dtype=torch.float32, device=device)
+        self.out = [nv.alloc_encoding(1, rows, cols, device, False, dequant=False)
+                    for _ in range(2)]
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.q_bytes = self.elements * (2 + 0.5 + 1 / 16)
+        self.a_bytes = self.elements * 2
+        self.working_set = self.elements * 2 * nsteps
+        L = nv.lib()
+        st = torch.cuda.current_stream(device).cuda_stream
+        self._outs = [nv._out(o) for o in self.out]
+        self._cfgs = [nv.Config(scale_fmt=1, rounding=1, scale_max=448.0, seed=3, step=t).c()
+                      for t in range(nsteps)]
+
+        def amax(t):
+            return L.nvfp4_amax(self.x[t].data_ptr(), 1, rows, cols, self.amax.data_ptr(),
+                                self.status.data_ptr(), st)
+
+        def quant(t):
+            return L.nvfp4_quantize(C.byref(self._cfgs[t]), self.x[t].data_ptr(), 1, rows, cols,
+                                    self.amax.data_ptr(), C.byref(self._outs[t % 2]), None,
+                                    self.status.data_ptr(), st)
+        self._amax, self._quant = amax, quant
+
+    def kernels(self, k, i):
+        t = k % self.nsets
+        ks = []
+        if t % self.period == 0:
+            ks.append(Kernel("amax", self.a_bytes, lambda: self._amax(t)))
+        ks.append(Kernel("quantize_row_sr", self.q_bytes, lambda: self._quant(t)))
+        return ks
+
+    def e2e_io(self, k):
+        t = k % self.nsets
+        o = self.out[t % 2]
+        return [self.x[t]], [o["codes"], o["scales"]]
+
+    def cpu_sample(self, budget_s):
+        import oracle
+        rows = 64
+        xb = self.host0
+        a, _ = oracle.global_amax(xb[:rows])
+        t0 = time.perf_counter()
+        oracle.quantize(xb[:rows], a, scale_fmt=1, rounding=1, seed=3, step=0, dequant=False)
+        per_row = (time.perf_counter() - t0) / rows
+        rows = int(min(self.rows, max(64, budget_s / max(per_row, 1e-9))))
+        t0 = time.perf_counter()
+        oracle.quantize(xb[:rows], a, scale_fmt=1, rounding=1, seed=3, step=0, dequant=False)
+        return rows * self.cols, time.perf_counter() - t0, f"first {rows} of {self.rows} rows"
+
+    bytes_per_elem = property(lambda self: (self.q_bytes + self.a_bytes / self.period)
+                              / self.elements)
+    dominant = "quantize_row_sr"
+    workload = property(lambda self: (
+        f"gradient {self.rows}x{self.cols} bf16 N(0,1) x per-row lognormal(0,2), drifting "
+        f"x1.05/step over {self.nsets} steps; UE5M3 scales, periodic scaling (amax every "
+        f"{self.period} steps), stochastic E2M1 rounding (Philox4x32-10, key seed/step); "
+        "outputs codes, scales"))
+
+
+class MoeExperts(Workload):
+    """64 experts x 2048 x 7168: per-expert amax + one pass emitting row and
+    column NVFP4 encodings with 4/6 and both dequants."""
+
+    def __init__(self, device, experts=64, rows=2048, cols=7168, seed=4):
+        xb = synth.moe_experts(experts, rows, cols, seed=seed)
+        self.S, self.rows, self.cols = experts, rows, cols
+        self.elements = experts * rows * cols
+        self.host_x = xb
+        self.x = torch.from_numpy(xb.view(np.int16)).to(device)
+        del xb
+        self.amax = torch.empty(experts, dtype=torch.float32, device=device)
+        self.row = nv.alloc_encoding(experts, rows, cols, device, True)
+        self.col = nv.alloc_encoding(experts, cols, rows, device, True)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.cfg = nv.Config(blocks=3, four_over_six=1)
+        self._c = self.cfg.c()
+        self._r, self._cc = nv._out(self.row), nv._out(self.col)
+        self.d_bytes = self.elements * (2 + 2 * (0.5 + 1 / 16 + 1 / 128 + 2))
+        self.a_bytes = self.elements * 2
+        self.nsets = 1
+        self.working_set = self.elements * (2 + 2 * 4.57)
+        L = nv.lib()
+        st = torch.cuda.current_stream(device).cuda_stream
+
+        def amax():
+            return L.nvfp4_amax(self.x.data_ptr(), experts, rows, cols, self.amax.data_ptr(),
+                                self.status.data_ptr(), st)
+
+        def dual():
+            return L.nvfp4_quantize(C.byref(self._c), self.x.data_ptr(), experts, rows, cols,
+                                    self.amax.data_ptr(), C.byref(self._r), C.byref(self._cc),
+                                    self.status.data_ptr(), st)
+        self._amax, self._dual = amax, dual
+
+    def kernels(self, k, i):
+        return [Kernel("amax", self.a_bytes, self._amax),
+                Kernel("quantize_dual", self.d_bytes, self._dual)]
+
+    def e2e_io(self, k):
+        names = ("codes", "scales", "choice", "dequant")
+        outs = [self.row[n] for n in names] + [self.col[n] for n in names]
+        return [self.x], outs
+
+    def cpu_sample(self, budget_s):
+        import oracle
+        xb = self.host_x[0]
+        rows = 16
+        a, _ = oracle.global_amax(xb[:rows])
+        t0 = time.perf_counter()
+        oracle.quantize(xb[:rows], a, blocks=3, four_over_six=1)
+        per_row = (time.perf_counter() - t0) / rows
+        rows = int(min(self.rows, max(16, budget_s / max(per_row, 1e-9))))
+        rows -= rows % 16
+        t0 = time.perf_counter()
+        a, _ = oracle.global_amax(xb[:rows])
+        oracle.quantize(xb[:rows], a, blocks=3, four_over_six=1)
+        return rows * self.cols, time.perf_counter() - t0, \
+            f"first {rows} rows of expert 0 (amax + row and column encodings)"
+
+    bytes_per_elem = property(lambda self: (self.d_bytes + self.a_bytes) / self.elements)
+    dominant = "quantize_dual"
+    workload = property(lambda self: (
+        f"MoE expert weights {self.S} x {self.rows}x{self.cols} bf16 N(0,0.02), 0.01% x50 "
+        "outliers; per-expert amax + one pass emitting 1x16 row and 16x1 column encodings, "
+        "E4M3, RNE, Four-Over-Six on, both dequants"))
+
+
+WORKLOADS = {1: SmallNormal, 2: Activation, 3: ScaleLearning, 4: DriftingGradient,
+             5: MoeExperts}
+
+
+# --------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index, period_ms: int = 50):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", f"-lms={period_ms}"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons, n = [], 0.0, set(), 0
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            n += 1
+            for name, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": n}
+
+
+# --------------------------------------------------------------- timing --
+
+def _smi_id(local: int) -> str:
+    """nvidia-smi id of the CUDA device (its PCI bus id when torch exposes it)."""
+    try:
+        p = torch.cuda.get_device_properties(local)
+        dom, bus, devn = p.pci_domain_id, p.pci_bus_id, p.pci_device_id
+        return f"{dom:08X}:{bus:02X}:{devn:02X}.0"
+    except Exception:
+        return str(local)
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_steps(wl, k0, K, events=None):
+    """Launch K steps. With `events`, one pre-created event is recorded before
+    the first kernel and one after every kernel, so the kernels' durations tile
+    the timed region; returns [(kernel, start_event, end_event)]."""
+    out = []
+    j = 0
+    if events is not None:
+        events[0].record()
+    for k in range(k0, k0 + K):
+        i = k % wl.nsets
+        for kern in wl.kernels(k, i):
+            rc = kern.fn()
+            if rc != 0:
+                raise nv.Nvfp4Error(kern.name, rc)
+            if events is not None:
+                events[j + 1].record()
+                out.append((kern, events[j], events[j + 1]))
+                j += 1
+    return out
+
+
+def time_ours(wl, args, world, local):
+    run_steps(wl, 0, args.warmup)
+    torch.cuda.synchronize()
+    nk = sum(len(wl.kernels(k, k % wl.nsets)) for k in range(args.warmup, args.warmup + args.steps))
+    events = [torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(_smi_id(local))
+    time.sleep(0.3)
+    wall0 = time.perf_counter()
+    evs = run_steps(wl, args.warmup, args.steps, events)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    barrier(world)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    total_ms = events[0].elapsed_time(events[nk])
+    per_kernel = {}
+    for kern, a, b in evs:
+        d = per_kernel.setdefault(kern.name, {"ms": 0.0, "n": 0, "bytes": kern.nbytes})
+        d["ms"] += a.elapsed_time(b)
+        d["n"] += 1
+    return total_ms, per_kernel, clk, wall
+
+
+def time_e2e(wl, steps, device):
+    """The same metric through the C ABI with host buffers: every step copies
+    its inputs from pinned host memory to the device, runs the kernels and
+    copies every output back to pinned host memory."""
+    ins0, outs0 = wl.e2e_io(0)
+    h_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in ins0]
+    for h, t in zip(h_in, ins0):
+        h.copy_(t.cpu())
+    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs0]
+    bi = sum(t.numel() * t.element_size() for t in ins0)
+    bo = sum(t.numel() * t.element_size() for t in outs0)
+
+    def step(k):
+        ins, outs = wl.e2e_io(k)
+        for h, t in zip(h_in, ins):
+            t.copy_(h, non_blocking=True)
+        for kern in wl.kernels(k, 0):
+            rc = kern.fn()
+            if rc != 0:
+                raise nv.Nvfp4Error(kern.name, rc)
+        for h, t in zip(h_out, outs):
+            h.copy_(t, non_blocking=True)
+
+    for k in range(2):
+        step(k)
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for k in range(steps):
+        step(k)
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b), bi, bo
+
+
+def cores_used() -> int:
+    return 1
+
+
+def reference_arm(args, world, rank):
+    """The oracle, as it stands, timed on the host cores: each step is a bounded
+    sample of the chosen workload, reported with our arm's metric and unit."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    desc, bpe, sample_text, step = _reference_sample(args)
+    secs, total_e = 0.0, 0
+    for k in range(args.warmup + args.steps):
+        e, dt = step()
+        if k >= args.warmup:
+            secs += dt
+            total_e += e
+    value = total_e * bpe / secs / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * secs / max(1, args.steps), 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": desc, "sample": sample_text},
+        "gelem_per_s": round(total_e / secs / 1e9, 6),
+        "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": cores_used(),
+                         "kind": "oracle", "sample": sample_text},
+        "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _reference_sample(args):
+    """(workload text, algorithmic bytes/elem, sample text, -, step fn) for the
+    reference arm. Each step runs the oracle on the same rows of the workload."""
+    import oracle
+    if args.config in (1, 2):
+        rows, cols = (1024, 1024) if args.config == 1 else (8192, 4096)
+        fos = 0 if args.config == 1 else 1
+        xb = (synth.outlier_normal(rows, cols, seed=0) if args.config == 1
+              else synth.student_t(rows, cols, seed=1))
+        sub = xb[:args.ref_rows]
+        bpe = 2 + 2 + 0.5 + 1 / 16 + (1 / 128 if fos else 0)
+
+        def step():
+            t0 = time.perf_counter()
+            a, _ = oracle.global_amax(sub)
+            oracle.quantize(sub, a, four_over_six=fos)
+            return sub.size, time.perf_counter() - t0
+        wl = "activation 8192x4096 bf16 0.5*Student-t(3), amax + row 4/6" if args.config == 2 \
+            else "1024x1024 bf16 N(0,1) 0.1% x20, amax + row"
+        return wl, bpe, f"first {sub.shape[0]} rows of {rows} per step", step
+    if args.config == 3:
+        wb, gb, s = synth.scale_learning(seed=2)
+        n = args.ref_rows
+
+        def step():
+            t0 = time.perf_counter()
+            oracle.fakequant_fwd(wb[:n], s[:n], s[:n])
+            oracle.scale_grad_bwd(wb[:n], gb[:n], s[:n], s[:n])
+            return n * wb.shape[1], time.perf_counter() - t0
+        return "scale-learning step 14336x4096", 11.5, f"first {n} of 14336 rows per step", step
+    if args.config == 4:
+        xb = synth.DriftingGradient().step(0)
+        sub = xb[:args.ref_rows]
+        a, _ = oracle.global_amax(sub)
+
+        def step():
+            t0 = time.perf_counter()
+            oracle.quantize(sub, a, scale_fmt=1, rounding=1, seed=3, step=0, dequant=False)
+            return sub.size, time.perf_counter() - t0
+        return "gradient 16384x4096 UE5M3 SR periodic", 2.5625 + 2 / 16, \
+            f"first {sub.shape[0]} of 16384 rows per step", step
+    xb = synth.moe_experts(1, 2048, 7168, seed=4)[0]
+    sub = xb[:max(16, args.ref_rows - args.ref_rows % 16)]
+
+    def step():
+        t0 = time.perf_counter()
+        a, _ = oracle.global_amax(sub)
+        oracle.quantize(sub, a, blocks=3, four_over_six=1)
+        return sub.size, time.perf_counter() - t0
+    return "MoE 64x2048x7168 dual 4/6", 2 + 2 + 2 * (0.5 + 1 / 16 + 1 / 128 + 2), \
+        f"first {sub.shape[0]} rows of one expert per step", step
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=2, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-rows", type=int, default=512)
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--experts", type=int, default=64, help="MoE workload: number of experts")
+    ap.add_argument("--sr-steps", type=int, default=32,
+                    help="drifting-gradient workload: distinct step inputs held on the device")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world, rank, local = dist_setup(args) if args.impl == "ours" else (
+        int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), 0)
+    if args.impl == "reference":
+        args.steps = args.steps or 3
+        reference_arm(args, world, rank)
+        return
+
+    device = torch.device("cuda", local)
+    nv.build()
+    extra = {5: dict(experts=args.experts), 4: dict(nsteps=args.sr_steps)}.get(args.config, {})
+    wl = WORKLOADS[args.config](device, **extra)
+    if args.steps is None:
+        # about two seconds of device time, so the clock samples cover the run
+        args.steps = {1: 20000, 2: 40000, 3: 10000, 4: 16000, 5: 150}[args.config]
+    total_ms, per_kernel, clk, wall = time_ours(wl, args, world, local)
+    total_ms = max_over_ranks(total_ms, world)
+    units = wl.elements * args.steps * world
+    alg_bytes = sum(d["bytes"] * d["n"] for d in per_kernel.values()) * world
+    value = alg_bytes / (total_ms * 1e-3) / 1e9
+    st = int(wl.status.item())
+    if st != 0:
+        raise RuntimeError(f"device status {st} during the benchmark")
+
+    peak, peak_kind = measured_peak()
+    dom = per_kernel[wl.dominant]
+    dom_ms = dom["ms"] / dom["n"]
+    achieved = dom["bytes"] / (dom_ms * 1e-3) / 1e9
+    traffic = _committed_traffic(args.config, wl.dominant)
+    kernels = {name: {"launches": d["n"], "avg_us": round(1e3 * d["ms"] / d["n"], 3),
+                      "alg_bytes": int(d["bytes"]),
+                      "gbs": round(d["bytes"] / (d["ms"] / d["n"] * 1e-3) / 1e9, 1),
+                      "frac_of_peak": round(d["bytes"] / (d["ms"] / d["n"] * 1e-3) / 1e9 / peak, 4)}
+               for name, d in per_kernel.items()}
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": wl.workload, "elements_per_step": wl.elements,
+                   "alg_bytes_per_elem": round(wl.bytes_per_elem, 5),
+                   "l2": (f"inputs larger than L2: {wl.nsets} rotating input/output sets, "
+                          f"{wl.working_set / 2 ** 20:.0f} MiB > {L2_BYTES / 2 ** 20:.0f} MiB L2")},
+        "gelem_per_s": round(units / (total_ms * 1e-3) / 1e9, 3),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic, "kernel": wl.dominant,
+                     "peak_source": f"{peak_kind} HBM copy bandwidth"},
+        "kernels": kernels,
+        "gpu_launches": sum(d["n"] for d in per_kernel.values()),
+        "clocks": clk,
+        "host_wall_s": round(wall, 3),
+    }
+    if rank == 0 and not args.no_e2e:
+        ms, bi, bo = time_e2e(wl, args.e2e_steps, device)
+        per_step_bytes = alg_bytes / world / args.steps
+        line["e2e"] = {"value": round(per_step_bytes * args.e2e_steps / (ms * 1e-3) / 1e9, 2),
+                       "unit": "GB/s", "h2d_bytes_per_step": int(bi),
+                       "d2h_bytes_per_step": int(bo)}
+    if rank == 0 and not args.no_cpu:
+        e, dt, sample = wl.cpu_sample(args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(e * wl.bytes_per_elem / dt / 1e9, 5),
+                                "unit": "GB/s", "cores": cores_used(), "kind": "oracle",
+                                "sample": sample, "gelem_per_s": round(e / dt / 1e9, 6)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def _committed_traffic(config: int, kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary of this
+    workload (profiles/traffic.json), or None when not captured."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        v = d.get(str(config), {}).get(kernel)
+        return None if v is None else float(v)
+    except Exception:
+        return None
+
+
+if __name__ == "__main__":
+    main()
