@@ -9,6 +9,7 @@
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 namespace nvfp4 {
@@ -32,28 +33,11 @@ __device__ __forceinline__ uint32_t absmax_bits4(uint4 v) {
 }
 
 // ---------------------------------------------------------- packed f32x2 --
-// Blackwell executes these as one instruction for two lanes of fp32 work.
-struct f2 { float x, y; };
-__device__ __forceinline__ unsigned long long f2_pack(f2 a) {
-  unsigned long long r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a.x), "f"(a.y));
-  return r;
-}
-__device__ __forceinline__ f2 f2_unpack(unsigned long long r) {
-  f2 a;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(a.x), "=f"(a.y) : "l"(r));
-  return a;
-}
-__device__ __forceinline__ f2 f2_mul(f2 a, f2 b) {
-  unsigned long long r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_pack(a)), "l"(f2_pack(b)));
-  return f2_unpack(r);
-}
-__device__ __forceinline__ f2 f2_fma(f2 a, f2 b, f2 c) {
-  unsigned long long r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(f2_pack(a)), "l"(f2_pack(b)), "l"(f2_pack(c)));
-  return f2_unpack(r);
-}
+// Blackwell executes these as one instruction for two lanes of fp32 work
+// (FMUL2 / FFMA2 / FADD2), each lane rounded to nearest like its scalar form.
+using f2 = float2;
+__device__ __forceinline__ f2 f2_mul(f2 a, f2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ f2 f2_fma(f2 a, f2 b, f2 c) { return __ffma2_rn(a, b, c); }
 
 // ----------------------------------------------------------------- E2M1 ---
 // Two fp32 -> two E2M1 codes in one byte, round to nearest even, saturating
@@ -78,15 +62,14 @@ __device__ __forceinline__ float e2m1_value(uint32_t c) {
   uint32_t bits = m >= 2 ? 0x3F000000u + (m << 22) : (m == 1 ? 0x3F000000u : 0u);
   return __uint_as_float(bits | ((c & 8u) << 28));
 }
-// Decode two codes held in a byte via the hardware E2M1x2 -> f16x2 path.
+// Decode two codes held in a byte via the hardware E2M1x2 -> f16x2 path
+// (the low nibble lands in .x), then widen to fp32 (exact).
 __device__ __forceinline__ f2 e2m1x2_to_f2(uint32_t byte) {
   uint32_t h2;
   asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
       : "=r"(h2) : "r"(byte));
-  f2 r;
-  asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
-      : "=f"(r.x), "=f"(r.y) : "r"(h2));
-  return r;
+  __half2 h = *reinterpret_cast<__half2*>(&h2);
+  return __half22float2(h);
 }
 // Decode the 8 codes of a word into 4 pairs (element 2k in .x of pair k).
 __device__ __forceinline__ void e2m1x8_to_f2(uint32_t w, f2 (&q)[4]) {
@@ -197,6 +180,22 @@ __device__ __forceinline__ uint32_t e2m1_sr(float y, uint32_t v) {
   uint32_t t = a < 2.0f ? t_small : t_big;
   uint32_t code = (t + (0xFFFFu - v)) >> 16;
   return code | ((__float_as_uint(y) >> 28) & 8u);
+}
+
+// ------------------------------------------------------------- cp.async ---
+// 16-byte global -> shared copy that bypasses L1 (streamed data), grouped and
+// awaited per thread: a thread only ever reads back the slots it filled, so
+// no block-level barrier is involved.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // ---------------------------------------------------------- status word ---

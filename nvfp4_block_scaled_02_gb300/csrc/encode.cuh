@@ -17,7 +17,7 @@ namespace nvfp4 {
 template <bool SR>
 __device__ __forceinline__ uint32_t round8(const f2 (&x)[4], float inv, const uint4& rb) {
   f2 y[4];
-  const f2 iv{inv, inv};
+  const f2 iv = make_float2(inv, inv);
 #pragma unroll
   for (int k = 0; k < 4; ++k) y[k] = f2_mul(x[k], iv);
   if constexpr (!SR) {
@@ -38,8 +38,8 @@ __device__ __forceinline__ uint32_t round8(const f2 (&x)[4], float inv, const ui
 // even + odd. Also returns the decoded code values.
 __device__ __forceinline__ float half_sse(const f2 (&x)[4], uint32_t codes, float d, f2 (&q)[4]) {
   e2m1x8_to_f2(codes, q);
-  const f2 nd{-d, -d};
-  f2 acc{0.0f, 0.0f};
+  const f2 nd = make_float2(-d, -d);
+  f2 acc = make_float2(0.0f, 0.0f);
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     f2 e = f2_fma(q[k], nd, x[k]);
@@ -50,7 +50,7 @@ __device__ __forceinline__ float half_sse(const f2 (&x)[4], uint32_t codes, floa
 
 // Dequantised bf16 of 8 decoded values times d, packed as a uint4.
 __device__ __forceinline__ uint4 dequant8(const f2 (&q)[4], float d) {
-  const f2 dd{d, d};
+  const f2 dd = make_float2(d, d);
   f2 r[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) r[k] = f2_mul(q[k], dd);
@@ -60,10 +60,10 @@ __device__ __forceinline__ uint4 dequant8(const f2 (&q)[4], float d) {
 
 // Unpack a uint4 of 8 bf16 into 4 pairs.
 __device__ __forceinline__ void unpack8(const uint4& v, f2 (&x)[4]) {
-  x[0] = f2{bf16_lo(v.x), bf16_hi(v.x)};
-  x[1] = f2{bf16_lo(v.y), bf16_hi(v.y)};
-  x[2] = f2{bf16_lo(v.z), bf16_hi(v.z)};
-  x[3] = f2{bf16_lo(v.w), bf16_hi(v.w)};
+  x[0] = make_float2(bf16_lo(v.x), bf16_hi(v.x));
+  x[1] = make_float2(bf16_lo(v.y), bf16_hi(v.y));
+  x[2] = make_float2(bf16_lo(v.z), bf16_hi(v.z));
+  x[3] = make_float2(bf16_lo(v.w), bf16_hi(v.w));
 }
 
 struct HalfResult {
@@ -107,12 +107,19 @@ __device__ __forceinline__ HalfResult encode_half(const f2 (&x)[4], uint32_t ama
     r.pick4 = sse4 < sse6;
     r.codes = r.pick4 ? q4 : q6;
     r.scale = r.pick4 ? c4 : c6;
-    if (want_dq) r.dq = r.pick4 ? dequant8(v4, d4) : dequant8(v6, d6);
+    if (want_dq) {
+      f2 v[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) v[k] = r.pick4 ? v4[k] : v6[k];
+      r.dq = dequant8(v, r.pick4 ? d4 : d6);
+    }
   }
   return r;
 }
 
-// A whole 16-value block held by one lane as two halves (column kernel).
+// A whole 16-value block held by one lane as two halves of 8 (row kernel,
+// column kernel). The decoded values of the candidates are not kept: the
+// chosen codes are decoded again for the dequantised output.
 struct BlockResult {
   uint32_t codes[2];
   uint32_t scale;
@@ -131,38 +138,31 @@ __device__ __forceinline__ BlockResult encode_block(const f2 (&lo)[4], const f2 
   const uint32_t c6 = scale_encode<FMT>(__fmul_rn(amax, ss.rden6));
   const float d6 = s_d[c6], inv6 = s_inv[c6];
   const uint32_t a6 = round8<SR>(lo, inv6, rb0), b6 = round8<SR>(hi, inv6, rb1);
+  float d = d6;
   if constexpr (!FOS) {
     r.codes[0] = a6;
     r.codes[1] = b6;
     r.scale = c6;
     r.pick4 = false;
-    if (want_dq) {
-      f2 q[4];
-      e2m1x8_to_f2(a6, q);
-      r.dq[0] = dequant8(q, d6);
-      e2m1x8_to_f2(b6, q);
-      r.dq[1] = dequant8(q, d6);
-    }
   } else {
     const uint32_t c4 = scale_encode<FMT>(__fmul_rn(amax, ss.rden4));
     const float d4 = s_d[c4], inv4 = s_inv[c4];
     const uint32_t a4 = round8<SR>(lo, inv4, rb0), b4 = round8<SR>(hi, inv4, rb1);
-    f2 va6[4], vb6[4], va4[4], vb4[4];
-    const float sse6 = __fadd_rn(half_sse(lo, a6, d6, va6), half_sse(hi, b6, d6, vb6));
-    const float sse4 = __fadd_rn(half_sse(lo, a4, d4, va4), half_sse(hi, b4, d4, vb4));
+    f2 q[4];
+    const float sse6 = __fadd_rn(half_sse(lo, a6, d6, q), half_sse(hi, b6, d6, q));
+    const float sse4 = __fadd_rn(half_sse(lo, a4, d4, q), half_sse(hi, b4, d4, q));
     r.pick4 = sse4 < sse6;
     r.codes[0] = r.pick4 ? a4 : a6;
     r.codes[1] = r.pick4 ? b4 : b6;
     r.scale = r.pick4 ? c4 : c6;
-    if (want_dq) {
-      if (r.pick4) {
-        r.dq[0] = dequant8(va4, d4);
-        r.dq[1] = dequant8(vb4, d4);
-      } else {
-        r.dq[0] = dequant8(va6, d6);
-        r.dq[1] = dequant8(vb6, d6);
-      }
-    }
+    d = r.pick4 ? d4 : d6;
+  }
+  if (want_dq) {
+    f2 q[4];
+    e2m1x8_to_f2(r.codes[0], q);
+    r.dq[0] = dequant8(q, d);
+    e2m1x8_to_f2(r.codes[1], q);
+    r.dq[1] = dequant8(q, d);
   }
   return r;
 }

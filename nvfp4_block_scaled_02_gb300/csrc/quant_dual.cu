@@ -147,10 +147,10 @@ __global__ void __launch_bounds__(kThreads) quant_dual_kernel(const DualParams p
       f2 lo[4], hi[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        lo[k] = j ? f2{bf16_hi(w[2 * k]), bf16_hi(w[2 * k + 1])}
-                  : f2{bf16_lo(w[2 * k]), bf16_lo(w[2 * k + 1])};
-        hi[k] = j ? f2{bf16_hi(w[8 + 2 * k]), bf16_hi(w[9 + 2 * k])}
-                  : f2{bf16_lo(w[8 + 2 * k]), bf16_lo(w[9 + 2 * k])};
+        lo[k] = j ? make_float2(bf16_hi(w[2 * k]), bf16_hi(w[2 * k + 1]))
+                  : make_float2(bf16_lo(w[2 * k]), bf16_lo(w[2 * k + 1]));
+        hi[k] = j ? make_float2(bf16_hi(w[8 + 2 * k]), bf16_hi(w[9 + 2 * k]))
+                  : make_float2(bf16_lo(w[8 + 2 * k]), bf16_lo(w[9 + 2 * k]));
       }
       const bool okc = c + j < C && r < R;
       if (okc && m >= 0x7F80u) flag(p.status, NVFP4_DEV_NONFINITE_INPUT_BIT);

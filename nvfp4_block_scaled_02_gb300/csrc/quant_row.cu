@@ -2,12 +2,13 @@
 //
 // Row blocks are 16 consecutive elements of a row, and rows are contiguous
 // with C % 16 == 0, so a slice is a flat run of R*C/16 blocks. A warp owns a
-// "tile" of 32 consecutive blocks (1 KiB of bf16): lane l loads chunk l and
-// chunk l + 32 of the tile with 128-bit loads (8 values each), so the two
-// lanes of a pair (l, l^1) hold the two halves of one block. Per tile the warp
-// writes 256 B of codes, 32 scale bytes, one 32-bit 4/6 word (a ballot) and
-// 1 KiB of dequantised bf16 -- all coalesced. U tiles are loaded before any is
-// processed to keep enough bytes in flight per SM.
+// "tile" of 32 consecutive blocks (1 KiB of bf16) and lane l owns block l of
+// it, so every per-block step (amax, both scale candidates, the 4/6 sums and
+// choice) runs once per block with no shuffles. The tile arrives through a
+// cp.async pipeline kStages tiles deep: the warp copies it with two fully
+// coalesced 512 B sweeps into shared memory and each lane then reads its own
+// 32 B block. Per tile the warp writes 256 B of codes, 32 scale bytes, one
+// 32-bit 4/6 word (a ballot) and 1 KiB of dequantised bf16.
 #include "encode.cuh"
 #include "launch.h"
 
@@ -17,19 +18,13 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+constexpr int kStages = 4;  // tiles in flight per warp (cp.async groups)
 
-// Gather the even bits of a ballot (lanes 0, 2, .., 30) into 16 bits.
-__device__ __forceinline__ uint32_t even_bits(uint32_t b) {
-  b &= 0x55555555u;
-  b = (b | (b >> 1)) & 0x33333333u;
-  b = (b | (b >> 2)) & 0x0F0F0F0Fu;
-  b = (b | (b >> 4)) & 0x00FF00FFu;
-  b = (b | (b >> 8)) & 0x0000FFFFu;
-  return b;
-}
-
-template <int FMT, bool SR, bool FOS, int U>
+template <int FMT, bool SR, bool FOS>
 __global__ void __launch_bounds__(kThreads) quant_row_kernel(const RowParams p) {
+  // stage[slot][w][c]: chunk c (0..63) of warp w's tile; chunk c holds values
+  // 8c .. 8c+7 of the tile, i.e. half c%2 of block c/2.
+  __shared__ __align__(16) uint4 stage[kStages][kWarps][64];
   __shared__ float s_d[256], s_inv[256];
   const int64_t s = p.slice0 + blockIdx.y;
   const SliceScale ss = slice_scale(p.gamax[s], p.M);
@@ -37,70 +32,78 @@ __global__ void __launch_bounds__(kThreads) quant_row_kernel(const RowParams p) 
   build_scale_table<FMT>(s_d, s_inv, ss.g);
   __syncthreads();
 
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t ntiles = (p.Bs + 31) / 32;
   const int64_t nwarps = (int64_t)gridDim.x * kWarps;
   const int64_t blk_base = s * p.Bs;  // first block of the slice
   const bool want_dq = p.dq != nullptr;
+  const int64_t t0 = (int64_t)blockIdx.x * kWarps + warp;
 
-  for (int64_t t0 = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); t0 < ntiles;
-       t0 += nwarps * U) {
-    uint4 v[U][2];
-    bool ok[U][2];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t tile = t0 + (int64_t)u * nwarps;
+  // The warp's two coalesced 512 B copies of `tile` into stage slot `slot`.
+  auto issue = [&](int64_t tile, int slot) {
+    if (tile < ntiles) {
+      const int64_t first = tile * 32;  // first block of the tile
+      const int64_t nchunks = 2 * (p.Bs - first);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const int64_t blk = tile * 32 + h * 16 + (lane >> 1);  // block within slice
-        ok[u][h] = tile < ntiles && blk < p.Bs;
-        v[u][h] = ok[u][h] ? __ldcs(p.x + (blk_base + blk) * 2 + (lane & 1))
-                           : make_uint4(0, 0, 0, 0);
+        const int c = h * 32 + lane;
+        if (c < nchunks) cp_async16(&stage[slot][warp][c], p.x + (blk_base + first) * 2 + c);
       }
     }
+    cp_async_commit();
+  };
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t tile = t0 + (int64_t)u * nwarps;
-      if (tile >= ntiles) break;  // warp-uniform
-      uint32_t word = 0;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int64_t blk = tile * 32 + h * 16 + (lane >> 1);
-        const int64_t gblk = blk_base + blk;
-        f2 x[4];
-        unpack8(v[u][h], x);
-        uint32_t m = absmax_bits4(v[u][h]);
-        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-        if (ok[u][h] && m >= 0x7F80u) flag(p.status, NVFP4_DEV_NONFINITE_INPUT_BIT);
-        uint4 rb = make_uint4(0, 0, 0, 0);
-        if constexpr (SR)
-          rb = sr_group_bits(p.seed, p.step, 0u, (uint64_t)(gblk * 16 + (lane & 1) * 8));
-        const HalfResult r = encode_half<FMT, SR, FOS>(x, m, ss, s_d, s_inv, rb, want_dq);
-        if (ok[u][h]) {
-          const int64_t chunk = gblk * 2 + (lane & 1);
-          __stcs(p.codes + chunk, r.codes);
-          if (want_dq) __stcs(p.dq + chunk, r.dq);
-          if ((lane & 1) == 0) p.scales[gblk] = (uint8_t)r.scale;
-        }
-        if constexpr (FOS) word |= even_bits(__ballot_sync(0xFFFFFFFFu, ok[u][h] && r.pick4)) << (16 * h);
-      }
-      if constexpr (FOS)
-        if (lane == 0) p.choice[s * p.W + tile] = word;
+  for (int k = 0; k < kStages - 1; ++k) issue(t0 + k * nwarps, k);
+
+  int slot = 0;
+  for (int64_t tile = t0; tile < ntiles; tile += nwarps) {
+    issue(tile + (kStages - 1) * nwarps, (slot + kStages - 1) % kStages);
+    cp_async_wait<kStages - 1>();  // this lane's copies of the tile have landed
+    __syncwarp();                  // ... and every other lane's
+    const int64_t blk = tile * 32 + lane;
+    const bool ok = blk < p.Bs;
+    const uint4 v0 = ok ? stage[slot][warp][2 * lane] : make_uint4(0, 0, 0, 0);
+    const uint4 v1 = ok ? stage[slot][warp][2 * lane + 1] : make_uint4(0, 0, 0, 0);
+    __syncwarp();  // all reads of this slot done before any lane refills it
+    const int64_t gblk = blk_base + blk;
+    f2 lo[4], hi[4];
+    unpack8(v0, lo);
+    unpack8(v1, hi);
+    const uint32_t m = max(absmax_bits4(v0), absmax_bits4(v1));
+    if (ok && m >= 0x7F80u) flag(p.status, NVFP4_DEV_NONFINITE_INPUT_BIT);
+    uint4 rb0 = make_uint4(0, 0, 0, 0), rb1 = rb0;
+    if constexpr (SR) {
+      rb0 = sr_group_bits(p.seed, p.step, 0u, (uint64_t)gblk * 16);
+      rb1 = sr_group_bits(p.seed, p.step, 0u, (uint64_t)gblk * 16 + 8);
     }
+    const BlockResult r = encode_block<FMT, SR, FOS>(lo, hi, m, ss, s_d, s_inv, rb0, rb1, want_dq);
+    if (ok) {
+      __stcs(reinterpret_cast<uint2*>(p.codes) + gblk, make_uint2(r.codes[0], r.codes[1]));
+      if (want_dq) {
+        __stcs(p.dq + 2 * gblk, r.dq[0]);
+        __stcs(p.dq + 2 * gblk + 1, r.dq[1]);
+      }
+      p.scales[gblk] = (uint8_t)r.scale;
+    }
+    if constexpr (FOS) {
+      const uint32_t word = __ballot_sync(0xFFFFFFFFu, ok && r.pick4);
+      if (lane == 0) p.choice[s * p.W + tile] = word;
+    }
+    slot = (slot + 1) % kStages;
   }
+  cp_async_wait<0>();
 }
 
 template <int FMT, bool SR, bool FOS>
 cudaError_t launch_t(const RowParams& p, int64_t S, cudaStream_t st) {
-  constexpr int U = FOS ? 1 : 2;
   const int64_t ntiles = (p.Bs + 31) / 32;
-  const int64_t want = (ntiles + kWarps * U - 1) / (kWarps * U);
-  const int64_t cap = std::max<int64_t>(1, (int64_t)sm_count() * 8 / std::max<int64_t>(1, S));
+  const int64_t want = (ntiles + kWarps - 1) / kWarps;
+  const int64_t cap = std::max<int64_t>(1, (int64_t)sm_count() * 4 / std::max<int64_t>(1, S));
   RowParams q = p;
   for (int64_t s0 = 0; s0 < S; s0 += 65535) {
     q.slice0 = s0;
     dim3 grid((unsigned)std::min(want, cap), (unsigned)std::min<int64_t>(S - s0, 65535));
-    quant_row_kernel<FMT, SR, FOS, U><<<grid, kThreads, 0, st>>>(q);
+    quant_row_kernel<FMT, SR, FOS><<<grid, kThreads, 0, st>>>(q);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

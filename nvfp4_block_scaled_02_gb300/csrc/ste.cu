@@ -39,7 +39,7 @@ __global__ void __launch_bounds__(kThreads) fakequant_fwd_kernel(const SteParams
     const float inv = __frcp_rn(sp);
     f2 x[4], y[4], q[4];
     unpack8(v, x);
-    const f2 iv{inv, inv};
+    const f2 iv = make_float2(inv, inv);
 #pragma unroll
     for (int k = 0; k < 4; ++k) y[k] = f2_mul(x[k], iv);
     e2m1x8_to_f2(e2m1x8_rn(y), q);
@@ -74,12 +74,12 @@ __global__ void __launch_bounds__(kThreads) scale_grad_bwd_kernel(const SteParam
     f2 x[4], g[4], r[4], q[4];
     unpack8(xv, x);
     unpack8(gv, g);
-    const f2 iv{inv, inv};
+    const f2 iv = make_float2(inv, inv);
 #pragma unroll
     for (int k = 0; k < 4; ++k) r[k] = f2_mul(x[k], iv);
     e2m1x8_to_f2(e2m1x8_rn(r), q);
 
-    f2 acc0{0.0f, 0.0f}, acc1{0.0f, 0.0f};
+    f2 acc0 = make_float2(0.0f, 0.0f), acc1 = acc0;
     uint32_t gx[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -91,12 +91,12 @@ __global__ void __launch_bounds__(kThreads) scale_grad_bwd_kernel(const SteParam
         gx[k] = pack_bf16x2(gxx, gxy);
       }
       if constexpr (TIED) {
-        const f2 t{in_x ? __fsub_rn(q[k].x, r[k].x) : q[k].x,
-                   in_y ? __fsub_rn(q[k].y, r[k].y) : q[k].y};
+        const f2 t = make_float2(in_x ? __fsub_rn(q[k].x, r[k].x) : q[k].x,
+                                 in_y ? __fsub_rn(q[k].y, r[k].y) : q[k].y);
         acc0 = f2_fma(g[k], t, acc0);
       } else {
         acc0 = f2_fma(g[k], q[k], acc0);
-        const f2 rin{in_x ? r[k].x : 0.0f, in_y ? r[k].y : 0.0f};
+        const f2 rin = make_float2(in_x ? r[k].x : 0.0f, in_y ? r[k].y : 0.0f);
         acc1 = f2_fma(g[k], rin, acc1);
       }
     }
