@@ -161,10 +161,11 @@ NVFP4_API nvfp4_status nvfp4_scale_grad_bwd(const void* x, const void* gq, int64
 
 /* ---- diagnostics: the device codecs element by element -------------------
  * For exhaustive checks of the conversions the kernels use. op:
- *   0: out[i] = E2M1 RNE code of in[i]         (n even: pairs share a byte)
+ *   0: out[i] = E2M1 RNE code of in[i]
  *   1: out[i] = E4M3 code of in[i] >= 0        (block-scale encoder)
  *   2: out[i] = UE5M3 code of in[i] >= 0       (block-scale encoder)
  *   3: out[i] = E2M1 stochastic code of in[i] with random bits aux[i] & 0xFFFF
+ * Ops 0 and 3 convert groups of 8 consecutive inputs exactly as the kernels do.
  * in, aux (op 3 only): device arrays of n elements; out: device uint8 [n].
  * This entry point has no counterpart on the pages; it exists for testing. */
 NVFP4_API nvfp4_status nvfp4_codec_probe(int32_t op, const float* in, const uint32_t* aux, int64_t n,

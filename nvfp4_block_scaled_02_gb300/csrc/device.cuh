@@ -48,11 +48,20 @@ __device__ __forceinline__ uint32_t e2m1x2_rn(float even, float odd) {
       : "=r"(r) : "f"(odd), "f"(even));
   return r;
 }
-// Eight fp32 values (4 pairs) -> 8 codes in one word, element 0 in bits 0..3.
+// Eight fp32 values (4 pairs) -> 8 codes in one word, element 0 in bits 0..3:
+// four conversions into byte registers packed by one vector move.
 __device__ __forceinline__ uint32_t e2m1x8_rn(const f2 (&y)[4]) {
-  uint32_t b0 = e2m1x2_rn(y[0].x, y[0].y), b1 = e2m1x2_rn(y[1].x, y[1].y);
-  uint32_t b2 = e2m1x2_rn(y[2].x, y[2].y), b3 = e2m1x2_rn(y[3].x, y[3].y);
-  return b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+  uint32_t w;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(w)
+      : "f"(y[0].x), "f"(y[0].y), "f"(y[1].x), "f"(y[1].y), "f"(y[2].x), "f"(y[2].y),
+        "f"(y[3].x), "f"(y[3].y));
+  return w;
 }
 // Value of one E2M1 code (low 4 bits of c) as fp32.
 __device__ __forceinline__ float e2m1_value(uint32_t c) {
@@ -62,19 +71,23 @@ __device__ __forceinline__ float e2m1_value(uint32_t c) {
   uint32_t bits = m >= 2 ? 0x3F000000u + (m << 22) : (m == 1 ? 0x3F000000u : 0u);
   return __uint_as_float(bits | ((c & 8u) << 28));
 }
-// Decode two codes held in a byte via the hardware E2M1x2 -> f16x2 path
-// (the low nibble lands in .x), then widen to fp32 (exact).
-__device__ __forceinline__ f2 e2m1x2_to_f2(uint32_t byte) {
-  uint32_t h2;
-  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
-      : "=r"(h2) : "r"(byte));
-  __half2 h = *reinterpret_cast<__half2*>(&h2);
-  return __half22float2(h);
-}
-// Decode the 8 codes of a word into 4 pairs (element 2k in .x of pair k).
+// Decode the 8 codes of a word into 4 pairs (element 2k in .x of pair k):
+// one vector move splits the bytes, the hardware E2M1x2 -> f16x2 conversion
+// decodes each (low nibble in the low half), then exact widening to fp32.
 __device__ __forceinline__ void e2m1x8_to_f2(uint32_t w, f2 (&q)[4]) {
-#pragma unroll
-  for (int k = 0; k < 4; ++k) q[k] = e2m1x2_to_f2((w >> (8 * k)) & 0xFFu);
+  uint32_t h0, h1, h2, h3;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3)
+      : "r"(w));
+  q[0] = __half22float2(*reinterpret_cast<__half2*>(&h0));
+  q[1] = __half22float2(*reinterpret_cast<__half2*>(&h1));
+  q[2] = __half22float2(*reinterpret_cast<__half2*>(&h2));
+  q[3] = __half22float2(*reinterpret_cast<__half2*>(&h3));
 }
 
 // --------------------------------------------------------- block scales ---
@@ -167,19 +180,34 @@ __device__ __forceinline__ uint32_t sr_bits_of(const uint4& w, int k) {
   return (k & 1) ? (word >> 16) : (word & 0xFFFFu);
 }
 
-// Stochastic E2M1 rounding with 16 random bits v: round |y| up to the next
-// grid value iff v / 2^16 < p, p = (|y| - lo) / (hi - lo). Implemented as
-// code = (T + 0xFFFF - v) >> 16 with T = code_lo * 2^16 + ceil(p * 2^16):
-// below 2 the grid step is 0.5 and T = ceil(|y| * 2^17) (one fma rounded up
-// against 2^23); from 2 on T is read off the fp32 bits (the E2M1 code and
-// its fraction are the exponent and leading mantissa bits).
-__device__ __forceinline__ uint32_t e2m1_sr(float y, uint32_t v) {
-  float a = fminf(fabsf(y), 6.0f);
-  uint32_t t_small = __float_as_uint(__fmaf_ru(a, 131072.0f, 8388608.0f)) - 0x4B000000u;
-  uint32_t t_big = (__float_as_uint(a) - 0x3F000000u + 63u) >> 6;
-  uint32_t t = a < 2.0f ? t_small : t_big;
-  uint32_t code = (t + (0xFFFFu - v)) >> 16;
-  return code | ((__float_as_uint(y) >> 28) & 8u);
+// Stochastic E2M1 rounding of 8 values (4 pairs) with the group's 128 random
+// bits rb (value k uses the 16-bit half k%2 of word k/2): |y| rounds up to the
+// next grid value iff v / 2^16 < p, p = (|y| - lo) / (hi - lo). Implemented as
+// magnitude code = (T + 0xFFFF - v) >> 16 with T = code_lo * 2^16 + ceil(p * 2^16):
+// below 2 the grid step is 0.5 and T = ceil(|y| * 2^17), one fma rounded up
+// against 2^23; from 2 on T is read off the fp32
+// bits (the code and its fraction are the exponent and leading mantissa bits
+// of |y|). The sign bits are those of the round-to-nearest codes of the same
+// values (both copy the sign of y), taken from one hardware conversion.
+__device__ __forceinline__ uint32_t sr8(const f2 (&y)[4], const uint4& rb) {
+  const uint32_t sign = e2m1x8_rn(y) & 0x88888888u;
+  const uint32_t nw[4] = {~rb.x, ~rb.y, ~rb.z, ~rb.w};  // 0xFFFF - v in each half
+  uint32_t w = sign;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const f2 a = make_float2(fminf(fabsf(y[k].x), 6.0f), fminf(fabsf(y[k].y), 6.0f));
+    const uint32_t sx = __float_as_uint(__fmaf_ru(a.x, 131072.0f, 8388608.0f)) - 0x4B000000u;
+    const uint32_t sy = __float_as_uint(__fmaf_ru(a.y, 131072.0f, 8388608.0f)) - 0x4B000000u;
+    const uint32_t bx = (__float_as_uint(a.x) - 0x3F000000u + 63u) >> 6;
+    const uint32_t by = (__float_as_uint(a.y) - 0x3F000000u + 63u) >> 6;
+    const uint32_t tx = a.x < 2.0f ? sx : bx;
+    const uint32_t ty = a.y < 2.0f ? sy : by;
+    const uint32_t cx = (tx + (nw[k] & 0xFFFFu)) >> 16;
+    const uint32_t cy = (ty + (nw[k] >> 16)) >> 16;
+    w += cx << (8 * k);
+    w += cy << (8 * k + 4);
+  }
+  return w;
 }
 
 // ------------------------------------------------------------- cp.async ---

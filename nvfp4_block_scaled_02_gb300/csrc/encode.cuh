@@ -20,17 +20,8 @@ __device__ __forceinline__ uint32_t round8(const f2 (&x)[4], float inv, const ui
   const f2 iv = make_float2(inv, inv);
 #pragma unroll
   for (int k = 0; k < 4; ++k) y[k] = f2_mul(x[k], iv);
-  if constexpr (!SR) {
-    return e2m1x8_rn(y);
-  } else {
-    uint32_t w = 0;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      w |= e2m1_sr(y[k].x, sr_bits_of(rb, 2 * k)) << (8 * k);
-      w |= e2m1_sr(y[k].y, sr_bits_of(rb, 2 * k + 1)) << (8 * k + 4);
-    }
-    return w;
-  }
+  if constexpr (!SR) return e2m1x8_rn(y);
+  else return sr8(y, rb);
 }
 
 // Sum over 8 values of (x - q d)^2 in the fixed order: even and odd positions

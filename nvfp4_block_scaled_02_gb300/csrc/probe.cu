@@ -8,24 +8,37 @@ namespace nvfp4 {
 
 namespace {
 
+// Ops 0 and 3 run the kernels' own 8-value helpers (e2m1x8_rn, sr8) on
+// groups of 8 consecutive inputs; ops 1 and 2 the block-scale encoders.
 __global__ void codec_probe_kernel(int op, const float* __restrict__ in,
                                    const uint32_t* __restrict__ aux, int64_t n,
                                    uint8_t* __restrict__ out) {
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
-    if (op == 0) {
-      // pairs share one conversion, exactly as in the kernels
-      const int64_t e = i & ~(int64_t)1;
-      const float a = in[e], b = (e + 1 < n) ? in[e + 1] : 0.0f;
-      const uint32_t byte = e2m1x2_rn(a, b);
-      out[i] = (uint8_t)((i & 1) ? (byte >> 4) : (byte & 15u));
-    } else if (op == 1) {
-      out[i] = (uint8_t)e4m3_encode(in[i]);
-    } else if (op == 2) {
-      out[i] = (uint8_t)ue5m3_encode(in[i]);
-    } else {
-      out[i] = (uint8_t)e2m1_sr(in[i], aux[i] & 0xFFFFu);
+  const int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (op == 1 || op == 2) {
+    for (int64_t i = t0; i < n; i += stride)
+      out[i] = (uint8_t)(op == 1 ? e4m3_encode(in[i]) : ue5m3_encode(in[i]));
+    return;
+  }
+  const int64_t ngroups = (n + 7) / 8;
+  for (int64_t gi = t0; gi < ngroups; gi += stride) {
+    const int64_t e0 = gi * 8;
+    float v[8];
+    uint32_t r[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      v[k] = e0 + k < n ? in[e0 + k] : 0.0f;
+      r[k] = (op == 3 && e0 + k < n) ? (aux[e0 + k] & 0xFFFFu) : 0u;
     }
+    f2 y[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) y[k] = make_float2(v[2 * k], v[2 * k + 1]);
+    const uint4 rb = make_uint4(r[0] | (r[1] << 16), r[2] | (r[3] << 16), r[4] | (r[5] << 16),
+                                r[6] | (r[7] << 16));
+    const uint32_t w = op == 0 ? e2m1x8_rn(y) : sr8(y, rb);
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if (e0 + k < n) out[e0 + k] = (uint8_t)((w >> (4 * k)) & 15u);
   }
 }
 
