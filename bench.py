@@ -718,14 +718,31 @@ def main():
         dist.destroy_process_group()
 
 
+def kernel_source_hash() -> str:
+    """sha256 over the CUDA sources, so committed ncu counters can be matched
+    to the kernels they were taken from."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "nvfp4_block_scaled_02_gb300", "csrc")
+    for f in sorted(glob.glob(os.path.join(csrc, "*"))):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(f, "rb") as fh:
+                h.update(os.path.basename(f).encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
 def _committed_traffic(config: int, kernel: str):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary of this
-    workload (profiles/traffic.json), or None when not captured."""
+    """DRAM bytes (read + write) per launch of `kernel` from the committed ncu
+    summary (profiles/traffic.json), or None when absent or taken from other
+    kernel sources than the ones built now."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
             d = json.load(f)
-        v = d.get(str(config), {}).get(kernel)
+        if d.get("source_sha") != kernel_source_hash():
+            return None
+        v = d.get("workloads", {}).get(str(config), {}).get(kernel)
         return None if v is None else float(v)
     except Exception:
         return None
