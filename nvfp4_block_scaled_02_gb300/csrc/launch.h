@@ -36,7 +36,7 @@ cudaError_t launch_quant_row(const RowParams& p, int64_t S, int fmt, bool sr, bo
 // Column (16x1) and dual (row + column from one read) quantiser.
 struct DualParams {
   const uint16_t* x;    // bf16 [S][R][C]
-  int64_t R, C;
+  int64_t S, R, C;
   const float* gamax;
   float M;
   uint32_t seed, step;
