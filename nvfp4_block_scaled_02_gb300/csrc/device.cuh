@@ -159,9 +159,10 @@ __device__ __forceinline__ void scale_entry(uint32_t code, float g, float& d, fl
 __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
-    uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
-    uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
-    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    const uint64_t p0 = (uint64_t)0xD2511F53u * c.x;  // one 32x32 -> 64 multiply
+    const uint64_t p1 = (uint64_t)0xCD9E8D57u * c.z;
+    c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ k0, (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c.w ^ k1,
+                   (uint32_t)p0);
     k0 += 0x9E3779B9u;
     k1 += 0xBB67AE85u;
   }
@@ -180,32 +181,39 @@ __device__ __forceinline__ uint32_t sr_bits_of(const uint4& w, int k) {
   return (k & 1) ? (word >> 16) : (word & 0xFFFFu);
 }
 
+// Three-input fp32 minimum (one instruction on sm_100 and later).
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+  float r;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // Stochastic E2M1 rounding of 8 values (4 pairs) with the group's 128 random
 // bits rb (value k uses the 16-bit half k%2 of word k/2): |y| rounds up to the
-// next grid value iff v / 2^16 < p, p = (|y| - lo) / (hi - lo). Implemented as
-// magnitude code = (T + 0xFFFF - v) >> 16 with T = code_lo * 2^16 + ceil(p * 2^16):
-// below 2 the grid step is 0.5 and T = ceil(|y| * 2^17), one fma rounded up
-// against 2^23; from 2 on T is read off the fp32
-// bits (the code and its fraction are the exponent and leading mantissa bits
-// of |y|). The sign bits are those of the round-to-nearest codes of the same
-// values (both copy the sign of y), taken from one hardware conversion.
+// next grid value iff v / 2^16 < p, p = (|y| - lo) / (hi - lo).
+// On [0, 6] the map u(a) = min(a, 1 + a/2, 2 + a/4) sends the E2M1 grid to the
+// multiples of 1/2 (0..3.5) and is linear inside every grid cell, so with
+// T = ceil(u(|y|) * 2^17) = code_lo * 2^16 + ceil(p * 2^16) the magnitude code
+// is (T + 0xFFFF - v) >> 16. Each line is one fma rounded up against 2^23
+// (exact product, one rounding), and ceil commutes with min; |y| >= 6 (and
+// Inf/NaN) is capped at u = 3.5, code 7. The sign bits are those of the
+// round-to-nearest codes of the same values (both copy the sign of y).
+__device__ __forceinline__ uint32_t sr_mag(float y, uint32_t nv) {
+  const float a = fabsf(y);
+  const float t = fminf(fmin3(__fmaf_ru(a, 131072.0f, 8388608.0f),
+                              __fmaf_ru(a, 65536.0f, 8519680.0f),     // 2^23 + 2^17
+                              __fmaf_ru(a, 32768.0f, 8650752.0f)),    // 2^23 + 2^18
+                        8847360.0f);                                  // 2^23 + 7 * 2^16
+  return (__float_as_uint(t) - 0x4B000000u + nv) >> 16;
+}
 __device__ __forceinline__ uint32_t sr8(const f2 (&y)[4], const uint4& rb) {
   const uint32_t sign = e2m1x8_rn(y) & 0x88888888u;
   const uint32_t nw[4] = {~rb.x, ~rb.y, ~rb.z, ~rb.w};  // 0xFFFF - v in each half
   uint32_t w = sign;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const f2 a = make_float2(fminf(fabsf(y[k].x), 6.0f), fminf(fabsf(y[k].y), 6.0f));
-    const uint32_t sx = __float_as_uint(__fmaf_ru(a.x, 131072.0f, 8388608.0f)) - 0x4B000000u;
-    const uint32_t sy = __float_as_uint(__fmaf_ru(a.y, 131072.0f, 8388608.0f)) - 0x4B000000u;
-    const uint32_t bx = (__float_as_uint(a.x) - 0x3F000000u + 63u) >> 6;
-    const uint32_t by = (__float_as_uint(a.y) - 0x3F000000u + 63u) >> 6;
-    const uint32_t tx = a.x < 2.0f ? sx : bx;
-    const uint32_t ty = a.y < 2.0f ? sy : by;
-    const uint32_t cx = (tx + (nw[k] & 0xFFFFu)) >> 16;
-    const uint32_t cy = (ty + (nw[k] >> 16)) >> 16;
-    w += cx << (8 * k);
-    w += cy << (8 * k + 4);
+    w += sr_mag(y[k].x, nw[k] & 0xFFFFu) << (8 * k);
+    w += sr_mag(y[k].y, nw[k] >> 16) << (8 * k + 4);
   }
   return w;
 }
