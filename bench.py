@@ -369,8 +369,49 @@ class MoeExperts(Workload):
         "E4M3, RNE, Four-Over-Six on, both dequants"))
 
 
+class PerTokenActivation(Activation):
+    """The activation tensor with per-token outer scales: one kernel computes
+    every row's amax and encodes the row (x read from HBM once)."""
+
+    def __init__(self, device):
+        super().__init__(device)
+        L = nv.lib()
+        st = torch.cuda.current_stream(device).cuda_stream
+        R, Cc = self.rows, self.cols
+        self.row_amax = [torch.empty(R, dtype=torch.float32, device=device)
+                         for _ in range(self.nsets)]
+        self.out = [nv.alloc_encoding(R, 1, Cc, device, bool(self.fos)) for _ in range(self.nsets)]
+        self._touts = [nv._out(o) for o in self.out]
+        self.t_bytes = self.q_bytes + R * 4
+
+        def tok(i):
+            return L.nvfp4_quantize_per_token(C.byref(self._c), self.x[i].data_ptr(), R, Cc,
+                                              self.row_amax[i].data_ptr(),
+                                              C.byref(self._touts[i]), self.status.data_ptr(), st)
+        self._tok = tok
+
+    def kernels(self, k, i):
+        return [Kernel("quantize_per_token", self.t_bytes, lambda: self._tok(i))]
+
+    def e2e_io(self, k):
+        o = self.out[0]
+        return [self.x[0]], [o["codes"], o["scales"], o["dequant"], o["choice"], self.row_amax[0]]
+
+    def _cpu_once(self, oracle, rows):
+        xb = self.host_x[:rows].reshape(rows, 1, self.cols)
+        a, _ = oracle.global_amax(xb, rows)
+        oracle.quantize(xb, a, four_over_six=self.fos)
+
+    bytes_per_elem = property(lambda self: self.t_bytes / self.elements)
+    dominant = "quantize_per_token"
+    workload = property(lambda self: (
+        f"activation {self.rows}x{self.cols} bf16, 0.5*Student-t(nu=3); per-token outer scales "
+        "(row amax and encoding in one pass), 1x16 row blocks, E4M3, RNE, Four-Over-Six on; "
+        "outputs codes, scales, 4/6 bitmap, dequant, row amax"))
+
+
 WORKLOADS = {1: SmallNormal, 2: Activation, 3: ScaleLearning, 4: DriftingGradient,
-             5: MoeExperts}
+             5: MoeExperts, 6: PerTokenActivation}
 
 
 # --------------------------------------------------------------- clocks --
@@ -661,7 +702,7 @@ def main():
     wl = WORKLOADS[args.config](device, **extra)
     if args.steps is None:
         # about two seconds of device time, so the clock samples cover the run
-        args.steps = {1: 20000, 2: 40000, 3: 10000, 4: 16000, 5: 150}[args.config]
+        args.steps = {1: 20000, 2: 40000, 3: 10000, 4: 16000, 5: 150, 6: 50000}[args.config]
     total_ms, per_kernel, clk, wall = time_ours(wl, args, world, local)
     total_ms = max_over_ranks(total_ms, world)
     units = wl.elements * args.steps * world

@@ -132,6 +132,21 @@ NVFP4_API nvfp4_status nvfp4_quantize(const nvfp4_config* cfg, const void* x, in
                             const nvfp4_out* row, const nvfp4_out* col, int32_t* status,
                             void* stream);
 
+/* NVFP4 quantisation with per-token outer scales (End-to-End 4-Bit Training,
+ * "Recipe details": activations are quantised with one FP32 outer scale per
+ * token, weights with one per expert). x: bf16 [rows][cols], cols % 16 == 0.
+ * Each row r gets g_r = amax_r / (6 M) from its own amax, computed in the same
+ * kernel, so x is read from HBM once. The outputs are byte for byte those of
+ * nvfp4_amax + nvfp4_quantize with slices = rows and rows = 1: codes
+ * [rows][cols/2], scales [rows][cols/16], dequant [rows][cols], 4/6 bitmap
+ * [rows][ceil(cols/512)] words; row_amax (fp32 [rows]) receives every amax_r.
+ * cfg->blocks must be NVFP4_BLOCKS_ROW. Errors: as nvfp4_quantize, plus NULL
+ * row_amax. */
+NVFP4_API nvfp4_status nvfp4_quantize_per_token(const nvfp4_config* cfg, const void* x,
+                                                int64_t rows, int64_t cols, float* row_amax,
+                                                const nvfp4_out* out, int32_t* status,
+                                                void* stream);
+
 /* Fake quantisation for scale learning (Scale Learning blog, "How Scale
  * Learning Works", first and dual-scale equations):
  *   xq = bf16(s_post * clamp(round(x * (1 / s_pre)), -6, 6))

@@ -22,6 +22,7 @@ import torch
 __all__ = [
     "Config", "Nvfp4Error", "build", "lib", "nvfp4_amax", "nvfp4_quantize",
     "nvfp4_fakequant_fwd", "nvfp4_scale_grad_bwd", "nvfp4_codec_probe", "nvfp4_sr_bits",
+    "nvfp4_quantize_per_token",
     "alloc_encoding", "PeriodicAmax", "BLOCKS_ROW", "BLOCKS_COL", "BLOCKS_BOTH",
     "SCALE_E4M3", "SCALE_UE5M3", "ROUND_RNE", "ROUND_SR",
     "DEV_NONFINITE_INPUT", "DEV_BAD_SCALE", "DEV_BAD_AMAX",
@@ -95,6 +96,8 @@ def lib() -> C.CDLL:
             L.nvfp4_amax.argtypes = [_vp, _i64, _i64, _i64, _vp, _vp, _vp]
             L.nvfp4_quantize.argtypes = [C.POINTER(_Config), _vp, _i64, _i64, _i64, _vp,
                                          C.POINTER(_Out), C.POINTER(_Out), _vp, _vp]
+            L.nvfp4_quantize_per_token.argtypes = [C.POINTER(_Config), _vp, _i64, _i64, _vp,
+                                                   C.POINTER(_Out), _vp, _vp]
             L.nvfp4_fakequant_fwd.argtypes = [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp]
             L.nvfp4_scale_grad_bwd.argtypes = [_vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp,
                                                _vp, _vp]
@@ -102,7 +105,8 @@ def lib() -> C.CDLL:
             L.nvfp4_sr_bits.argtypes = [_u32, _u32, _u32, C.c_uint64, _i64, _vp, _vp]
             L.nvfp4_status_string.restype = C.c_char_p
             L.nvfp4_status_string.argtypes = [C.c_int]
-            for name in ("nvfp4_amax", "nvfp4_quantize", "nvfp4_fakequant_fwd",
+            for name in ("nvfp4_amax", "nvfp4_quantize", "nvfp4_quantize_per_token",
+                         "nvfp4_fakequant_fwd",
                          "nvfp4_scale_grad_bwd", "nvfp4_codec_probe", "nvfp4_sr_bits"):
                 getattr(L, name).restype = C.c_int
             _lib = L
@@ -199,6 +203,30 @@ def nvfp4_quantize(x: torch.Tensor, global_amax: torch.Tensor, cfg: Config | Non
         C.byref(ro) if ro is not None else None, C.byref(co) if co is not None else None,
         _dev(status, "status"), _stream(x.device)))
     return {"row": row if cfg.blocks & 1 else None, "col": col if cfg.blocks & 2 else None}
+
+
+def nvfp4_quantize_per_token(x: torch.Tensor, cfg: Config | None = None, out: dict | None = None,
+                             row_amax: torch.Tensor | None = None,
+                             status: torch.Tensor | None = None, dequant: bool = True) -> dict:
+    """Per-token NVFP4 encoding of a bf16 [rows, cols] tensor (one outer scale per
+    row, from the row's own amax, in one pass). Returns the row encoding plus
+    "row_amax" (fp32 [rows])."""
+    cfg = cfg or Config()
+    if x.dim() != 2:
+        raise ValueError("x must be [rows, cols]")
+    R, Cc = x.shape
+    if out is None:
+        out = alloc_encoding(R, 1, Cc, x.device, bool(cfg.four_over_six), dequant)
+    if row_amax is None:
+        row_amax = torch.empty(R, dtype=torch.float32, device=x.device)
+    o = _out(out)
+    c = cfg.c()
+    _check("nvfp4_quantize_per_token", lib().nvfp4_quantize_per_token(
+        C.byref(c), _bf16(x, "x"), R, Cc, _dev(row_amax, "row_amax"), C.byref(o),
+        _dev(status, "status"), _stream(x.device)))
+    out = dict(out)
+    out["row_amax"] = row_amax
+    return out
 
 
 def nvfp4_fakequant_fwd(x: torch.Tensor, s_pre: torch.Tensor, s_post: torch.Tensor | None = None,

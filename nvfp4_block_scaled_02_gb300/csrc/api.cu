@@ -137,6 +137,38 @@ nvfp4_status nvfp4_quantize(const nvfp4_config* cfg, const void* x, int64_t slic
   return cuda_status(nvfp4::launch_quant_dual(p, slices, do_row, cfg->scale_fmt, sr, fos, st));
 }
 
+nvfp4_status nvfp4_quantize_per_token(const nvfp4_config* cfg, const void* x, int64_t rows,
+                                      int64_t cols, float* row_amax, const nvfp4_out* out,
+                                      int32_t* status, void* stream) {
+  if (!cfg) return NVFP4_ERR_NULL;
+  if (cfg->blocks != NVFP4_BLOCKS_ROW || cfg->scale_fmt < 0 || cfg->scale_fmt > 1 ||
+      cfg->rounding < 0 || cfg->rounding > 1 || cfg->four_over_six < 0 ||
+      cfg->four_over_six > 1 || !(cfg->scale_max >= 0.0f) || !(cfg->scale_max <= 3.402823466e+38f))
+    return NVFP4_ERR_ENUM;
+  if (rows < 0 || cols < 0 || cols % 16 != 0) return NVFP4_ERR_SHAPE;
+  if (rows == 0 || cols == 0) return NVFP4_OK;
+  if (!x || !row_amax) return NVFP4_ERR_NULL;
+  if (!aligned(x, 16) || !aligned(row_amax, 4) || !aligned(status, 4)) return NVFP4_ERR_ALIGN;
+  const bool fos = cfg->four_over_six != 0;
+  nvfp4_status e = check_out(out, fos);
+  if (e != NVFP4_OK) return e;
+  nvfp4::TokenParams p{};
+  p.x = static_cast<const uint4*>(x);
+  p.R = rows;
+  p.C = cols;
+  p.M = cfg->scale_max > 0.0f ? cfg->scale_max : (fos ? 256.0f : 448.0f);
+  p.seed = cfg->seed;
+  p.step = cfg->step;
+  p.row_amax = row_amax;
+  p.codes = reinterpret_cast<uint32_t*>(out->codes);
+  p.scales = out->scales;
+  p.choice = fos ? out->choice : nullptr;
+  p.dq = static_cast<uint4*>(out->dequant);
+  p.status = status;
+  return cuda_status(nvfp4::launch_quant_token(p, cfg->scale_fmt, cfg->rounding == NVFP4_ROUND_SR,
+                                               fos, static_cast<cudaStream_t>(stream)));
+}
+
 static nvfp4_status ste_common(const void* x, int64_t rows, int64_t cols, const float* s_pre) {
   if (rows < 0 || cols < 0 || cols % 16 != 0) return NVFP4_ERR_SHAPE;
   if (rows == 0 || cols == 0) return NVFP4_OK;

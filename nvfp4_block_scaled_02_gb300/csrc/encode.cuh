@@ -118,16 +118,35 @@ struct BlockResult {
   uint4 dq[2];
 };
 
-template <int FMT, bool SR, bool FOS>
+// Where d = dec(code) * g and 1/d come from: a per-slice shared-memory table
+// (one entry per scale code) or, when every row has its own outer scale, the
+// same two fp32 operations done per block.
+struct TableScales {
+  const float* d;
+  const float* inv;
+  __device__ __forceinline__ void operator()(uint32_t code, float& dd, float& ii) const {
+    dd = d[code];
+    ii = inv[code];
+  }
+};
+template <int FMT>
+struct DirectScales {
+  float g;
+  __device__ __forceinline__ void operator()(uint32_t code, float& dd, float& ii) const {
+    scale_entry<FMT>(code, g, dd, ii);
+  }
+};
+
+template <int FMT, bool SR, bool FOS, class Scales>
 __device__ __forceinline__ BlockResult encode_block(const f2 (&lo)[4], const f2 (&hi)[4],
                                                     uint32_t amax_bits, const SliceScale& ss,
-                                                    const float* s_d, const float* s_inv,
-                                                    const uint4& rb0, const uint4& rb1,
-                                                    bool want_dq) {
+                                                    const Scales& scales, const uint4& rb0,
+                                                    const uint4& rb1, bool want_dq) {
   BlockResult r;
   const float amax = __uint_as_float(amax_bits << 16);
   const uint32_t c6 = scale_encode<FMT>(__fmul_rn(amax, ss.rden6));
-  const float d6 = s_d[c6], inv6 = s_inv[c6];
+  float d6, inv6;
+  scales(c6, d6, inv6);
   const uint32_t a6 = round8<SR>(lo, inv6, rb0), b6 = round8<SR>(hi, inv6, rb1);
   float d = d6;
   if constexpr (!FOS) {
@@ -137,7 +156,8 @@ __device__ __forceinline__ BlockResult encode_block(const f2 (&lo)[4], const f2 
     r.pick4 = false;
   } else {
     const uint32_t c4 = scale_encode<FMT>(__fmul_rn(amax, ss.rden4));
-    const float d4 = s_d[c4], inv4 = s_inv[c4];
+    float d4, inv4;
+    scales(c4, d4, inv4);
     const uint32_t a4 = round8<SR>(lo, inv4, rb0), b4 = round8<SR>(hi, inv4, rb1);
     f2 q[4];
     const float sse6 = __fadd_rn(half_sse(lo, a6, d6, q), half_sse(hi, b6, d6, q));

@@ -15,6 +15,18 @@ namespace nvfp4 {
 
 int sm_count();
 
+// CTAs of `kernel` (with `threads` threads and `smem` dynamic shared memory)
+// that fit on one SM at once, at least 1: sizes persistent grids to a single
+// wave.
+template <class Kernel>
+int resident_ctas(Kernel kernel, int threads, size_t smem = 0) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess ||
+      n < 1)
+    n = 1;
+  return n;
+}
+
 // Row (1x16) quantiser over a stack of S slices of Bs blocks each.
 struct RowParams {
   const uint4* x;       // bf16 input, 8 values per uint4
@@ -54,6 +66,21 @@ struct DualParams {
 };
 cudaError_t launch_quant_dual(const DualParams& p, int64_t S, bool rows_too, int fmt, bool sr,
                               bool fos, cudaStream_t st);
+
+// Per-token (per-row outer scale) quantiser, amax and encoding in one pass.
+struct TokenParams {
+  const uint4* x;       // bf16 [R][C], C % 16 == 0
+  int64_t R, C;
+  float M;
+  uint32_t seed, step;
+  float* row_amax;      // [R], written
+  uint32_t* codes;      // as RowParams
+  uint8_t* scales;
+  uint32_t* choice;     // [R][ceil(C/512)] words (may be null when 4/6 is off)
+  uint4* dq;            // may be null
+  int32_t* status;
+};
+cudaError_t launch_quant_token(const TokenParams& p, int fmt, bool sr, bool fos, cudaStream_t st);
 
 // Per-slice global amax.
 cudaError_t launch_amax(const uint16_t* x, int64_t S, int64_t n, float* amax, int32_t* status,

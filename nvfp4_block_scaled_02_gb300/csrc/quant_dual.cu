@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(kThreads) quant_dual_kernel(const DualParams p
         rb1 = sr_group_bits(p.seed, p.step, 1u, (uint64_t)e + 8);
       }
       const BlockResult br =
-          encode_block<FMT, SR, FOS>(lo, hi, m, ss, s_d, s_inv, rb0, rb1, want_dq);
+          encode_block<FMT, SR, FOS>(lo, hi, m, ss, TableScales{s_d, s_inv}, rb0, rb1, want_dq);
       if (okc) {
         *reinterpret_cast<uint2*>(p.c_codes + e / 2) = make_uint2(br.codes[0], br.codes[1]);
         p.c_scales[e / 16] = (uint8_t)br.scale;

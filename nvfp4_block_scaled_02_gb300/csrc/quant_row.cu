@@ -76,7 +76,8 @@ __global__ void __launch_bounds__(kThreads) quant_row_kernel(const RowParams p) 
       rb0 = sr_group_bits(p.seed, p.step, 0u, (uint64_t)gblk * 16);
       rb1 = sr_group_bits(p.seed, p.step, 0u, (uint64_t)gblk * 16 + 8);
     }
-    const BlockResult r = encode_block<FMT, SR, FOS>(lo, hi, m, ss, s_d, s_inv, rb0, rb1, want_dq);
+    const BlockResult r =
+        encode_block<FMT, SR, FOS>(lo, hi, m, ss, TableScales{s_d, s_inv}, rb0, rb1, want_dq);
     if (ok) {
       __stcs(reinterpret_cast<uint2*>(p.codes) + gblk, make_uint2(r.codes[0], r.codes[1]));
       if (want_dq) {
@@ -98,7 +99,9 @@ template <int FMT, bool SR, bool FOS>
 cudaError_t launch_t(const RowParams& p, int64_t S, cudaStream_t st) {
   const int64_t ntiles = (p.Bs + 31) / 32;
   const int64_t want = (ntiles + kWarps - 1) / kWarps;
-  const int64_t cap = std::max<int64_t>(1, (int64_t)sm_count() * 4 / std::max<int64_t>(1, S));
+  static const int per_sm = resident_ctas(quant_row_kernel<FMT, SR, FOS>, kThreads);
+  const int64_t cap =
+      std::max<int64_t>(1, (int64_t)sm_count() * per_sm / std::max<int64_t>(1, S));
   RowParams q = p;
   for (int64_t s0 = 0; s0 < S; s0 += 65535) {
     q.slice0 = s0;

@@ -100,6 +100,17 @@ def test_empty_inputs_enqueue_nothing(L):
                                   None) == 0
 
 
+def test_per_token_argument_errors(L):
+    pt = L.nvfp4_quantize_per_token
+    assert pt(None, FAKE, 4, 32, FAKE, C.byref(_out()), None, None) == 1
+    assert pt(C.byref(_cfg(blocks=3)), FAKE, 4, 32, FAKE, C.byref(_out()), None, None) == 4
+    assert pt(C.byref(_cfg()), FAKE, 4, 24, FAKE, C.byref(_out()), None, None) == 2
+    assert pt(C.byref(_cfg()), FAKE, 4, 32, None, C.byref(_out()), None, None) == 1
+    assert pt(C.byref(_cfg()), FAKE, 4, 32, FAKE, None, None, None) == 1
+    assert pt(C.byref(_cfg()), FAKE + 2, 4, 32, FAKE, C.byref(_out()), None, None) == 3
+    assert pt(C.byref(_cfg()), None, 0, 32, None, None, None, None) == 0
+
+
 def test_amax_argument_errors(L):
     assert L.nvfp4_amax(FAKE, -1, 4, 4, FAKE, None, None) == 2
     assert L.nvfp4_amax(FAKE, 1, 4, 4, None, None, None) == 1
