@@ -69,6 +69,11 @@ typedef enum {
 /* nvfp4_config.scale_fmt */
 #define NVFP4_SCALE_E4M3 0
 #define NVFP4_SCALE_UE5M3 1
+/* nvfp4_config.four_over_six_rule ("Four Over Six": the three selection rules
+ * evaluated; MSE is the adopted one). Sums use the fixed in-block order. */
+#define NVFP4_FOS_MSE 0 /* sum of squared errors                              */
+#define NVFP4_FOS_MAE 1 /* sum of absolute errors                             */
+#define NVFP4_FOS_MAX 2 /* largest absolute error                             */
 /* nvfp4_config.rounding */
 #define NVFP4_ROUND_RNE 0 /* E2M1 round to nearest, ties to the even code    */
 #define NVFP4_ROUND_SR 1  /* stochastic rounding, Philox4x32-10 bits         */
@@ -82,6 +87,7 @@ typedef struct {
   float scale_max;       /* M of the outer scale; 0 = 256 with 4/6, else 448   */
   uint32_t seed;         /* stochastic rounding key word 0                     */
   uint32_t step;         /* stochastic rounding key word 1 (training step)     */
+  int32_t four_over_six_rule; /* NVFP4_FOS_*: the error the 4/6 choice compares */
 } nvfp4_config;
 
 /* Outputs of one encoding (row or column). Shapes for an input [S][R][C]:

@@ -24,7 +24,7 @@ __all__ = [
     "nvfp4_fakequant_fwd", "nvfp4_scale_grad_bwd", "nvfp4_codec_probe", "nvfp4_sr_bits",
     "nvfp4_quantize_per_token",
     "alloc_encoding", "PeriodicAmax", "BLOCKS_ROW", "BLOCKS_COL", "BLOCKS_BOTH",
-    "SCALE_E4M3", "SCALE_UE5M3", "ROUND_RNE", "ROUND_SR",
+    "SCALE_E4M3", "SCALE_UE5M3", "ROUND_RNE", "ROUND_SR", "FOS_MSE", "FOS_MAE", "FOS_MAX",
     "DEV_NONFINITE_INPUT", "DEV_BAD_SCALE", "DEV_BAD_AMAX",
 ]
 
@@ -32,6 +32,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libnvfp4.so")
 
 BLOCKS_ROW, BLOCKS_COL, BLOCKS_BOTH = 1, 2, 3
+FOS_MSE, FOS_MAE, FOS_MAX = 0, 1, 2
 SCALE_E4M3, SCALE_UE5M3 = 0, 1
 ROUND_RNE, ROUND_SR = 0, 1
 DEV_NONFINITE_INPUT, DEV_BAD_SCALE, DEV_BAD_AMAX = 1, 2, 4
@@ -48,7 +49,7 @@ class Nvfp4Error(RuntimeError):
 class _Config(C.Structure):
     _fields_ = [("blocks", C.c_int32), ("scale_fmt", C.c_int32), ("rounding", C.c_int32),
                 ("four_over_six", C.c_int32), ("scale_max", C.c_float), ("seed", C.c_uint32),
-                ("step", C.c_uint32)]
+                ("step", C.c_uint32), ("four_over_six_rule", C.c_int32)]
 
 
 class _Out(C.Structure):
@@ -65,10 +66,12 @@ class Config:
     scale_max: float = 0.0
     seed: int = 0
     step: int = 0
+    four_over_six_rule: int = 0  # FOS_MSE, FOS_MAE or FOS_MAX
 
     def c(self) -> _Config:
         return _Config(self.blocks, self.scale_fmt, self.rounding, self.four_over_six,
-                       self.scale_max, self.seed & 0xFFFFFFFF, self.step & 0xFFFFFFFF)
+                       self.scale_max, self.seed & 0xFFFFFFFF, self.step & 0xFFFFFFFF,
+                       self.four_over_six_rule)
 
 
 _lock = threading.Lock()

@@ -27,6 +27,12 @@ namespace {
 
 bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
 
+// 0 = 4/6 off, 1 = on with the MSE rule (compiled in), 2 = on, rule read at run time
+int fos_mode(const nvfp4_config* cfg) {
+  if (!cfg->four_over_six) return 0;
+  return cfg->four_over_six_rule == NVFP4_FOS_MSE ? 1 : 2;
+}
+
 nvfp4_status cuda_status(cudaError_t e) { return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA; }
 
 nvfp4_status check_out(const nvfp4_out* o, bool fos) {
@@ -69,6 +75,7 @@ nvfp4_status nvfp4_quantize(const nvfp4_config* cfg, const void* x, int64_t slic
                             int64_t cols, const float* global_amax, const nvfp4_out* row,
                             const nvfp4_out* col, int32_t* status, void* stream) {
   if (!cfg) return NVFP4_ERR_NULL;
+  if (cfg->four_over_six_rule < 0 || cfg->four_over_six_rule > 2) return NVFP4_ERR_ENUM;
   if (cfg->blocks < 1 || cfg->blocks > 3 || cfg->scale_fmt < 0 || cfg->scale_fmt > 1 ||
       cfg->rounding < 0 || cfg->rounding > 1 || cfg->four_over_six < 0 || cfg->four_over_six > 1 ||
       !(cfg->scale_max >= 0.0f) || !(cfg->scale_max <= 3.402823466e+38f))
@@ -107,7 +114,8 @@ nvfp4_status nvfp4_quantize(const nvfp4_config* cfg, const void* x, int64_t slic
     p.choice = fos ? row->choice : nullptr;
     p.dq = static_cast<uint4*>(row->dequant);
     p.status = status;
-    return cuda_status(nvfp4::launch_quant_row(p, slices, cfg->scale_fmt, sr, fos, st));
+    p.rule = cfg->four_over_six_rule;
+    return cuda_status(nvfp4::launch_quant_row(p, slices, cfg->scale_fmt, sr, fos_mode(cfg), st));
   }
   // column blocks (alone or with row blocks): the bitmaps are OR-ed into
   if (fos) {
@@ -134,13 +142,16 @@ nvfp4_status nvfp4_quantize(const nvfp4_config* cfg, const void* x, int64_t slic
   p.c_choice = fos ? col->choice : nullptr;
   p.c_dq = static_cast<uint16_t*>(col->dequant);
   p.status = status;
-  return cuda_status(nvfp4::launch_quant_dual(p, slices, do_row, cfg->scale_fmt, sr, fos, st));
+  p.rule = cfg->four_over_six_rule;
+  return cuda_status(
+      nvfp4::launch_quant_dual(p, slices, do_row, cfg->scale_fmt, sr, fos_mode(cfg), st));
 }
 
 nvfp4_status nvfp4_quantize_per_token(const nvfp4_config* cfg, const void* x, int64_t rows,
                                       int64_t cols, float* row_amax, const nvfp4_out* out,
                                       int32_t* status, void* stream) {
   if (!cfg) return NVFP4_ERR_NULL;
+  if (cfg->four_over_six_rule < 0 || cfg->four_over_six_rule > 2) return NVFP4_ERR_ENUM;
   if (cfg->blocks != NVFP4_BLOCKS_ROW || cfg->scale_fmt < 0 || cfg->scale_fmt > 1 ||
       cfg->rounding < 0 || cfg->rounding > 1 || cfg->four_over_six < 0 ||
       cfg->four_over_six > 1 || !(cfg->scale_max >= 0.0f) || !(cfg->scale_max <= 3.402823466e+38f))
@@ -165,8 +176,9 @@ nvfp4_status nvfp4_quantize_per_token(const nvfp4_config* cfg, const void* x, in
   p.choice = fos ? out->choice : nullptr;
   p.dq = static_cast<uint4*>(out->dequant);
   p.status = status;
+  p.rule = cfg->four_over_six_rule;
   return cuda_status(nvfp4::launch_quant_token(p, cfg->scale_fmt, cfg->rounding == NVFP4_ROUND_SR,
-                                               fos, static_cast<cudaStream_t>(stream)));
+                                               fos_mode(cfg), static_cast<cudaStream_t>(stream)));
 }
 
 static nvfp4_status ste_common(const void* x, int64_t rows, int64_t cols, const float* s_pre) {

@@ -39,6 +39,46 @@ __device__ __forceinline__ float half_sse(const f2 (&x)[4], uint32_t codes, floa
   return __fadd_rn(acc.x, acc.y);
 }
 
+// The 4/6 selection metric of 8 values with decoded code values q under
+// `rule`: 0 = sum of squared errors (fma order of half_sse), 1 = sum of |e|
+// (plain adds, same order), 2 = max |e|. Halves combine by + for rules 0 and 1
+// and by max for rule 2.
+__device__ __forceinline__ float half_metric_q(const f2 (&x)[4], const f2 (&q)[4], float d,
+                                               int rule) {
+  const f2 nd = make_float2(-d, -d);
+  f2 acc = make_float2(0.0f, 0.0f);
+  if (rule == 0) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const f2 e = f2_fma(q[k], nd, x[k]);
+      acc = f2_fma(e, e, acc);
+    }
+    return __fadd_rn(acc.x, acc.y);
+  }
+  if (rule == 1) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const f2 e = f2_fma(q[k], nd, x[k]);
+      acc = __fadd2_rn(acc, make_float2(fabsf(e.x), fabsf(e.y)));
+    }
+    return __fadd_rn(acc.x, acc.y);
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const f2 e = f2_fma(q[k], nd, x[k]);
+    acc = make_float2(fmaxf(acc.x, fabsf(e.x)), fmaxf(acc.y, fabsf(e.y)));
+  }
+  return fmaxf(acc.x, acc.y);
+}
+__device__ __forceinline__ float half_metric(const f2 (&x)[4], uint32_t codes, float d, int rule) {
+  f2 q[4];
+  e2m1x8_to_f2(codes, q);
+  return half_metric_q(x, q, d, rule);
+}
+__device__ __forceinline__ float combine_halves(float h0, float h1, int rule) {
+  return rule == 2 ? fmaxf(h0, h1) : __fadd_rn(h0, h1);
+}
+
 // Dequantised bf16 of 8 decoded values times d, packed as a uint4.
 __device__ __forceinline__ uint4 dequant8(const f2 (&q)[4], float d) {
   const f2 dd = make_float2(d, d);
@@ -71,7 +111,7 @@ template <int FMT, bool SR, bool FOS>
 __device__ __forceinline__ HalfResult encode_half(const f2 (&x)[4], uint32_t amax_bits,
                                                   const SliceScale& ss, const float* s_d,
                                                   const float* s_inv, const uint4& rb,
-                                                  bool want_dq) {
+                                                  bool want_dq, int rule) {
   HalfResult r;
   const float amax = __uint_as_float(amax_bits << 16);
   const uint32_t c6 = scale_encode<FMT>(__fmul_rn(amax, ss.rden6));
@@ -91,10 +131,13 @@ __device__ __forceinline__ HalfResult encode_half(const f2 (&x)[4], uint32_t ama
     const float d4 = s_d[c4], inv4 = s_inv[c4];
     const uint32_t q4 = round8<SR>(x, inv4, rb);
     f2 v6[4], v4[4];
-    const float h6 = half_sse(x, q6, d6, v6);
-    const float h4 = half_sse(x, q4, d4, v4);
-    const float sse6 = __fadd_rn(h6, __shfl_xor_sync(0xFFFFFFFFu, h6, 1));
-    const float sse4 = __fadd_rn(h4, __shfl_xor_sync(0xFFFFFFFFu, h4, 1));
+    e2m1x8_to_f2(q6, v6);
+    e2m1x8_to_f2(q4, v4);
+    const float h6 = half_metric_q(x, v6, d6, rule);
+    const float h4 = half_metric_q(x, v4, d4, rule);
+    // the lower half (lane with the block's values 0..7) first
+    const float sse6 = combine_halves(h6, __shfl_xor_sync(0xFFFFFFFFu, h6, 1), rule);
+    const float sse4 = combine_halves(h4, __shfl_xor_sync(0xFFFFFFFFu, h4, 1), rule);
     r.pick4 = sse4 < sse6;
     r.codes = r.pick4 ? q4 : q6;
     r.scale = r.pick4 ? c4 : c6;
@@ -141,7 +184,8 @@ template <int FMT, bool SR, bool FOS, class Scales>
 __device__ __forceinline__ BlockResult encode_block(const f2 (&lo)[4], const f2 (&hi)[4],
                                                     uint32_t amax_bits, const SliceScale& ss,
                                                     const Scales& scales, const uint4& rb0,
-                                                    const uint4& rb1, bool want_dq) {
+                                                    const uint4& rb1, bool want_dq,
+                                                    int rule = 0) {
   BlockResult r;
   const float amax = __uint_as_float(amax_bits << 16);
   const uint32_t c6 = scale_encode<FMT>(__fmul_rn(amax, ss.rden6));
@@ -159,9 +203,10 @@ __device__ __forceinline__ BlockResult encode_block(const f2 (&lo)[4], const f2 
     float d4, inv4;
     scales(c4, d4, inv4);
     const uint32_t a4 = round8<SR>(lo, inv4, rb0), b4 = round8<SR>(hi, inv4, rb1);
-    f2 q[4];
-    const float sse6 = __fadd_rn(half_sse(lo, a6, d6, q), half_sse(hi, b6, d6, q));
-    const float sse4 = __fadd_rn(half_sse(lo, a4, d4, q), half_sse(hi, b4, d4, q));
+    const float sse6 =
+        combine_halves(half_metric(lo, a6, d6, rule), half_metric(hi, b6, d6, rule), rule);
+    const float sse4 =
+        combine_halves(half_metric(lo, a4, d4, rule), half_metric(hi, b4, d4, rule), rule);
     r.pick4 = sse4 < sse6;
     r.codes[0] = r.pick4 ? a4 : a6;
     r.codes[1] = r.pick4 ? b4 : b6;

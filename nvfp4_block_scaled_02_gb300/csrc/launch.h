@@ -41,8 +41,10 @@ struct RowParams {
   uint4* dq;            // bf16 dequant, may be null
   int32_t* status;      // may be null
   int64_t slice0;       // first slice of this launch (grids cover <= 65535)
+  int rule;             // 4/6 selection metric: 0 MSE, 1 MAE, 2 max error
 };
-cudaError_t launch_quant_row(const RowParams& p, int64_t S, int fmt, bool sr, bool fos,
+// fos: 0 = 4/6 off, 1 = on with the MSE rule, 2 = on with the rule in the params
+cudaError_t launch_quant_row(const RowParams& p, int64_t S, int fmt, bool sr, int fos,
                              cudaStream_t st);
 
 // Column (16x1) and dual (row + column from one read) quantiser.
@@ -63,9 +65,10 @@ struct DualParams {
   uint32_t* c_choice;
   uint16_t* c_dq;
   int32_t* status;
+  int rule;             // 4/6 selection metric
 };
 cudaError_t launch_quant_dual(const DualParams& p, int64_t S, bool rows_too, int fmt, bool sr,
-                              bool fos, cudaStream_t st);
+                              int fos, cudaStream_t st);
 
 // Per-token (per-row outer scale) quantiser, amax and encoding in one pass.
 struct TokenParams {
@@ -79,8 +82,9 @@ struct TokenParams {
   uint32_t* choice;     // [R][ceil(C/512)] words (may be null when 4/6 is off)
   uint4* dq;            // may be null
   int32_t* status;
+  int rule;             // 4/6 selection metric
 };
-cudaError_t launch_quant_token(const TokenParams& p, int fmt, bool sr, bool fos, cudaStream_t st);
+cudaError_t launch_quant_token(const TokenParams& p, int fmt, bool sr, int fos, cudaStream_t st);
 
 // Per-slice global amax.
 cudaError_t launch_amax(const uint16_t* x, int64_t S, int64_t n, float* amax, int32_t* status,

@@ -43,7 +43,7 @@ __device__ __forceinline__ uint32_t even_bits8(uint32_t b) {  // lanes 0,2,..,14
   return b;
 }
 
-template <int FMT, bool SR, bool FOS, bool ROWS>
+template <int FMT, bool SR, int FOS, bool ROWS>
 __global__ void __launch_bounds__(kThreads) quant_dual_kernel(const DualParams p, int64_t tiles_r,
                                                               int64_t tiles_c) {
   __shared__ __align__(16) uint16_t tile[TR * TC];
@@ -110,7 +110,8 @@ __global__ void __launch_bounds__(kThreads) quant_dual_kernel(const DualParams p
       const int64_t e = s * slice_elems + r * C + c;  // flat row-layout index
       uint4 rb = make_uint4(0, 0, 0, 0);
       if constexpr (SR) rb = sr_group_bits(p.seed, p.step, 0u, (uint64_t)e);
-      const HalfResult hr = encode_half<FMT, SR, FOS>(x, m, ss, s_d, s_inv, rb, want_dq);
+      const HalfResult hr = encode_half<FMT, SR, FOS != 0>(x, m, ss, s_d, s_inv, rb, want_dq,
+                                                              FOS == 2 ? p.rule : 0);
       if (ok[k]) {
         reinterpret_cast<uint32_t*>(p.r_codes)[e / 8] = hr.codes;
         if (want_dq) __stcs(reinterpret_cast<uint4*>(p.r_dq + e), hr.dq);
@@ -161,7 +162,8 @@ __global__ void __launch_bounds__(kThreads) quant_dual_kernel(const DualParams p
         rb1 = sr_group_bits(p.seed, p.step, 1u, (uint64_t)e + 8);
       }
       const BlockResult br =
-          encode_block<FMT, SR, FOS>(lo, hi, m, ss, TableScales{s_d, s_inv}, rb0, rb1, want_dq);
+          encode_block<FMT, SR, FOS != 0>(lo, hi, m, ss, TableScales{s_d, s_inv}, rb0, rb1,
+                                          want_dq, FOS == 2 ? p.rule : 0);
       if (okc) {
         *reinterpret_cast<uint2*>(p.c_codes + e / 2) = make_uint2(br.codes[0], br.codes[1]);
         p.c_scales[e / 16] = (uint8_t)br.scale;
@@ -193,7 +195,7 @@ __global__ void __launch_bounds__(kThreads) quant_dual_kernel(const DualParams p
   }
 }
 
-template <int FMT, bool SR, bool FOS, bool ROWS>
+template <int FMT, bool SR, int FOS, bool ROWS>
 cudaError_t launch_t(const DualParams& p, int64_t S, cudaStream_t st) {
   const int64_t tiles_r = (p.R + TR - 1) / TR, tiles_c = (p.C + TC - 1) / TC;
   const int64_t n = S * tiles_r * tiles_c;
@@ -205,17 +207,15 @@ cudaError_t launch_t(const DualParams& p, int64_t S, cudaStream_t st) {
 }  // namespace
 
 cudaError_t launch_quant_dual(const DualParams& p, int64_t S, bool rows_too, int fmt, bool sr,
-                              bool fos, cudaStream_t st) {
+                              int fos, cudaStream_t st) {
 #define NVFP4_DUAL(F, R, O, B) \
   if (fmt == F && sr == R && fos == O && rows_too == B) return launch_t<F, R, O, B>(p, S, st);
-  NVFP4_DUAL(0, false, false, false) NVFP4_DUAL(0, false, true, false)
-  NVFP4_DUAL(0, true, false, false) NVFP4_DUAL(0, true, true, false)
-  NVFP4_DUAL(1, false, false, false) NVFP4_DUAL(1, false, true, false)
-  NVFP4_DUAL(1, true, false, false) NVFP4_DUAL(1, true, true, false)
-  NVFP4_DUAL(0, false, false, true) NVFP4_DUAL(0, false, true, true)
-  NVFP4_DUAL(0, true, false, true) NVFP4_DUAL(0, true, true, true)
-  NVFP4_DUAL(1, false, false, true) NVFP4_DUAL(1, false, true, true)
-  NVFP4_DUAL(1, true, false, true) NVFP4_DUAL(1, true, true, true)
+#define NVFP4_DUAL_FOS(F, R, B) NVFP4_DUAL(F, R, 0, B) NVFP4_DUAL(F, R, 1, B) NVFP4_DUAL(F, R, 2, B)
+  NVFP4_DUAL_FOS(0, false, false) NVFP4_DUAL_FOS(0, true, false)
+  NVFP4_DUAL_FOS(1, false, false) NVFP4_DUAL_FOS(1, true, false)
+  NVFP4_DUAL_FOS(0, false, true) NVFP4_DUAL_FOS(0, true, true)
+  NVFP4_DUAL_FOS(1, false, true) NVFP4_DUAL_FOS(1, true, true)
+#undef NVFP4_DUAL_FOS
 #undef NVFP4_DUAL
   return cudaErrorInvalidValue;
 }

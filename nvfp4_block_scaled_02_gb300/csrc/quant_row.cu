@@ -20,7 +20,7 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kStages = 4;  // tiles in flight per warp (cp.async groups)
 
-template <int FMT, bool SR, bool FOS>
+template <int FMT, bool SR, int FOS>
 __global__ void __launch_bounds__(kThreads) quant_row_kernel(const RowParams p) {
   // stage[slot][w][c]: chunk c (0..63) of warp w's tile; chunk c holds values
   // 8c .. 8c+7 of the tile, i.e. half c%2 of block c/2.
@@ -77,7 +77,8 @@ __global__ void __launch_bounds__(kThreads) quant_row_kernel(const RowParams p) 
       rb1 = sr_group_bits(p.seed, p.step, 0u, (uint64_t)gblk * 16 + 8);
     }
     const BlockResult r =
-        encode_block<FMT, SR, FOS>(lo, hi, m, ss, TableScales{s_d, s_inv}, rb0, rb1, want_dq);
+        encode_block<FMT, SR, FOS != 0>(lo, hi, m, ss, TableScales{s_d, s_inv}, rb0, rb1, want_dq,
+                                        FOS == 2 ? p.rule : 0);
     if (ok) {
       __stcs(reinterpret_cast<uint2*>(p.codes) + gblk, make_uint2(r.codes[0], r.codes[1]));
       if (want_dq) {
@@ -95,7 +96,7 @@ __global__ void __launch_bounds__(kThreads) quant_row_kernel(const RowParams p) 
   cp_async_wait<0>();
 }
 
-template <int FMT, bool SR, bool FOS>
+template <int FMT, bool SR, int FOS>
 cudaError_t launch_t(const RowParams& p, int64_t S, cudaStream_t st) {
   const int64_t ntiles = (p.Bs + 31) / 32;
   const int64_t want = (ntiles + kWarps - 1) / kWarps;
@@ -115,13 +116,13 @@ cudaError_t launch_t(const RowParams& p, int64_t S, cudaStream_t st) {
 
 }  // namespace
 
-cudaError_t launch_quant_row(const RowParams& p, int64_t S, int fmt, bool sr, bool fos,
+cudaError_t launch_quant_row(const RowParams& p, int64_t S, int fmt, bool sr, int fos,
                              cudaStream_t st) {
 #define NVFP4_ROW(F, R, O) \
   if (fmt == F && sr == R && fos == O) return launch_t<F, R, O>(p, S, st);
-  NVFP4_ROW(0, false, false) NVFP4_ROW(0, false, true) NVFP4_ROW(0, true, false)
-  NVFP4_ROW(0, true, true) NVFP4_ROW(1, false, false) NVFP4_ROW(1, false, true)
-  NVFP4_ROW(1, true, false) NVFP4_ROW(1, true, true)
+  NVFP4_ROW(0, false, 0) NVFP4_ROW(0, false, 1) NVFP4_ROW(0, false, 2) NVFP4_ROW(0, true, 0)
+  NVFP4_ROW(0, true, 1) NVFP4_ROW(0, true, 2) NVFP4_ROW(1, false, 0) NVFP4_ROW(1, false, 1)
+  NVFP4_ROW(1, false, 2) NVFP4_ROW(1, true, 0) NVFP4_ROW(1, true, 1) NVFP4_ROW(1, true, 2)
 #undef NVFP4_ROW
   return cudaErrorInvalidValue;
 }

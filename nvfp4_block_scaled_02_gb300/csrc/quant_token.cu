@@ -22,7 +22,7 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kRowLoads = 16;  // 16-byte loads per lane in flight in the amax pass
 
-template <int FMT, bool SR, bool FOS>
+template <int FMT, bool SR, int FOS>
 __global__ void __launch_bounds__(kThreads) quant_token_kernel(const TokenParams p) {
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = (int64_t)gridDim.x * kWarps;
@@ -70,7 +70,8 @@ __global__ void __launch_bounds__(kThreads) quant_token_kernel(const TokenParams
         rb1 = sr_group_bits(p.seed, p.step, 0u, (uint64_t)gblk * 16 + 8);
       }
       const BlockResult r =
-          encode_block<FMT, SR, FOS>(lo, hi, mb, ss, scales, rb0, rb1, want_dq);
+          encode_block<FMT, SR, FOS != 0>(lo, hi, mb, ss, scales, rb0, rb1, want_dq,
+                                          FOS == 2 ? p.rule : 0);
       if (ok) {
         __stcs(reinterpret_cast<uint2*>(p.codes) + gblk, make_uint2(r.codes[0], r.codes[1]));
         if (want_dq) {
@@ -92,7 +93,7 @@ __global__ void __launch_bounds__(kThreads) quant_token_kernel(const TokenParams
 // amax and builds one entry of the row's scale table (d and 1/d of one scale
 // code), warp 0 the two per-row reciprocals 1/(k g) -> barrier -> encode with
 // table lookups, as the per-slice kernel does.
-template <int FMT, bool SR, bool FOS, int K>
+template <int FMT, bool SR, int FOS, int K>
 __global__ void __launch_bounds__(kThreads) quant_token_cta_kernel(const TokenParams p) {
   __shared__ uint32_t s_max[kWarps];
   __shared__ float s_d[256], s_inv[256];
@@ -161,8 +162,9 @@ __global__ void __launch_bounds__(kThreads) quant_token_cta_kernel(const TokenPa
         rb0 = sr_group_bits(p.seed, p.step, 0u, (uint64_t)gblk * 16);
         rb1 = sr_group_bits(p.seed, p.step, 0u, (uint64_t)gblk * 16 + 8);
       }
-      const BlockResult r = encode_block<FMT, SR, FOS>(lo, hi, mb, ss, TableScales{s_d, s_inv},
-                                                       rb0, rb1, want_dq);
+      const BlockResult r =
+          encode_block<FMT, SR, FOS != 0>(lo, hi, mb, ss, TableScales{s_d, s_inv}, rb0, rb1,
+                                          want_dq, FOS == 2 ? p.rule : 0);
       if (ok) {
         __stcs(reinterpret_cast<uint2*>(p.codes) + gblk, make_uint2(r.codes[0], r.codes[1]));
         if (want_dq) {
@@ -186,7 +188,7 @@ __global__ void __launch_bounds__(kThreads) quant_token_cta_kernel(const TokenPa
   }
 }
 
-template <int FMT, bool SR, bool FOS>
+template <int FMT, bool SR, int FOS>
 cudaError_t launch_t(const TokenParams& p, cudaStream_t st) {
   const int64_t Bs = p.C / 16;
   auto run_cta = [&](auto kernel) {
@@ -210,12 +212,12 @@ cudaError_t launch_t(const TokenParams& p, cudaStream_t st) {
 
 }  // namespace
 
-cudaError_t launch_quant_token(const TokenParams& p, int fmt, bool sr, bool fos, cudaStream_t st) {
+cudaError_t launch_quant_token(const TokenParams& p, int fmt, bool sr, int fos, cudaStream_t st) {
 #define NVFP4_TOK(F, R, O) \
   if (fmt == F && sr == R && fos == O) return launch_t<F, R, O>(p, st);
-  NVFP4_TOK(0, false, false) NVFP4_TOK(0, false, true) NVFP4_TOK(0, true, false)
-  NVFP4_TOK(0, true, true) NVFP4_TOK(1, false, false) NVFP4_TOK(1, false, true)
-  NVFP4_TOK(1, true, false) NVFP4_TOK(1, true, true)
+  NVFP4_TOK(0, false, 0) NVFP4_TOK(0, false, 1) NVFP4_TOK(0, false, 2) NVFP4_TOK(0, true, 0)
+  NVFP4_TOK(0, true, 1) NVFP4_TOK(0, true, 2) NVFP4_TOK(1, false, 0) NVFP4_TOK(1, false, 1)
+  NVFP4_TOK(1, false, 2) NVFP4_TOK(1, true, 0) NVFP4_TOK(1, true, 1) NVFP4_TOK(1, true, 2)
 #undef NVFP4_TOK
   return cudaErrorInvalidValue;
 }

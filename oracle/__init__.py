@@ -81,13 +81,13 @@ def _declare(L):
     L.orc_scale_encode_array.argtypes = [C.c_int, _f32p, _i64, _u8p]
     L.orc_e2m1_sr_array.argtypes = [_f32p, _u32p, _i64, _u8p]
     L.orc_sr_bits_array.argtypes = [C.c_uint32, C.c_uint32, C.c_uint32, C.c_uint64, _i64, _u32p]
-    L.orc_encode_block.argtypes = [_f32p, C.c_float, C.c_int, C.c_int, C.c_int,
+    L.orc_encode_block.argtypes = [_f32p, C.c_float, C.c_int, C.c_int, C.c_int, C.c_int,
                                    C.c_uint32, C.c_uint32, C.c_uint32, C.c_uint64,
                                    _u8p, _u8p, _u8p, _u16p, _f32p, _f32p]
     L.orc_global_amax.restype = C.c_int
     L.orc_global_amax.argtypes = [_u16p, _i64, _i64, _f32p]
     L.orc_quantize.restype = C.c_int
-    L.orc_quantize.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int, C.c_float,
+    L.orc_quantize.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_float,
                                C.c_uint32, C.c_uint32, _u16p, _i64, _i64, _i64, _f32p,
                                _u8p, _u8p, _u32p, _u16p, _u8p, _u8p, _u32p, _u16p]
     L.orc_fakequant_fwd.restype = C.c_int
@@ -175,7 +175,8 @@ def sr_bits(seed: int, step: int, direction: int, idx0: int, n: int) -> np.ndarr
 # ---------------------------------------------------------- block level --
 
 def encode_block(x16, g: float, fmt: int = 0, rounding: int = 0, fos: int = 0,
-                 seed: int = 0, step: int = 0, direction: int = 0, idx0: int = 0) -> dict:
+                 seed: int = 0, step: int = 0, direction: int = 0, idx0: int = 0,
+                 rule: int = 0) -> dict:
     x = np.ascontiguousarray(x16, dtype=np.float32)
     assert x.shape == (16,)
     codes = np.empty(16, np.uint8)
@@ -184,7 +185,7 @@ def encode_block(x16, g: float, fmt: int = 0, rounding: int = 0, fos: int = 0,
     dq = np.empty(16, np.uint16)
     dqf = np.empty(16, np.float32)
     sse = np.empty(2, np.float32)
-    lib().orc_encode_block(_p(x, _f32p), g, fmt, rounding, fos, seed, step, direction, idx0,
+    lib().orc_encode_block(_p(x, _f32p), g, fmt, rounding, fos, rule, seed, step, direction, idx0,
                            _p(codes, _u8p), _p(scale, _u8p), _p(choice, _u8p),
                            _p(dq, _u16p), _p(dqf, _f32p), _p(sse, _f32p))
     return dict(codes=codes, scale=int(scale[0]), choice=int(choice[0]), dq=dq, dqf=dqf,
@@ -203,7 +204,7 @@ def global_amax(x_bf16: np.ndarray, slices: int = 1):
 
 def quantize(x_bf16: np.ndarray, gamax: np.ndarray, *, blocks: int = 1, scale_fmt: int = 0,
              rounding: int = 0, four_over_six: int = 0, scale_max: float = 0.0,
-             seed: int = 0, step: int = 0, dequant: bool = True) -> dict:
+             seed: int = 0, step: int = 0, dequant: bool = True, rule: int = 0) -> dict:
     """x_bf16: uint16 array shaped [S, R, C] (or [R, C]); gamax: float32 [S]."""
     x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
     if x.ndim == 2:
@@ -226,7 +227,7 @@ def quantize(x_bf16: np.ndarray, gamax: np.ndarray, *, blocks: int = 1, scale_fm
     if blocks & 2:
         alloc("col_", Cc, R)
     g = out.get
-    st = lib().orc_quantize(blocks, scale_fmt, rounding, four_over_six, scale_max, seed, step,
+    st = lib().orc_quantize(blocks, scale_fmt, rounding, four_over_six, rule, scale_max, seed, step,
                             _p(x, _u16p), S, R, Cc, _p(gam, _f32p),
                             _p(g("row_codes"), _u8p), _p(g("row_scales"), _u8p),
                             _p(g("row_choice"), _u32p), _p(g("row_dq"), _u16p),

@@ -54,6 +54,8 @@
  *  R6 4/6 compares the block sums of squared errors (the MSE denominator is
  *     the same for both): e_i = fma(-q_i, d, x_i); the sum uses the fixed
  *     order of block_sum() below; pick 4 iff sse4 < sse6 (ties keep 6).
+ *     The other two rules the 4/6 pages evaluate: MAE (sum of |e_i| with
+ *     plain adds in the same order) and max error (max |e_i|); same tie rule.
  *  R7 Dequantised value = bf16_rne(q_i * d) with the product rounded to fp32.
  *  R8 Column (16x1) blocks: the encoding of slice X is the row (1x16)
  *     encoding of X^T, with direction 1 in the random counter.
@@ -226,6 +228,24 @@ static float block_sum(const float* a, const float* b) {
   return half[0] + half[1];
 }
 
+/* The MAE form of block_sum(): |e_i| added (no fma) in the same order. */
+static float block_abs_sum(const float* e) {
+  float half[2];
+  for (int h = 0; h < 2; ++h) {
+    float acc[2] = {0.0f, 0.0f};
+    for (int p = 0; p < 2; ++p)
+      for (int j = 0; j < 4; ++j) acc[p] = acc[p] + fabsf(e[8 * h + p + 2 * j]);
+    half[h] = acc[0] + acc[1];
+  }
+  return half[0] + half[1];
+}
+static float block_abs_max(const float* e) {
+  float m = 0.0f;
+  for (int i = 0; i < 16; ++i)
+    if (fabsf(e[i]) > m) m = fabsf(e[i]);
+  return m;
+}
+
 /* ----------------------------------------------------- scale policy ----- */
 /* R3: the global decode scale of a slice. Returns the status bit for a bad
  * amax (and uses g = 1 then, so the result stays defined). */
@@ -244,6 +264,8 @@ typedef struct {
   uint8_t q[16];     /* E2M1 codes                          */
   float qv[16];      /* their values                        */
   float sse;         /* block sum of squared errors (R6)    */
+  float sae;         /* block sum of |errors|               */
+  float emax;        /* largest |error|                     */
 } cand_t;
 
 static void encode_candidate(const float* x, float amax, float g, float k, int fmt,
@@ -267,14 +289,23 @@ static void encode_candidate(const float* x, float amax, float g, float k, int f
   float e[16];
   for (int i = 0; i < 16; ++i) e[i] = fmaf(-c->qv[i], c->d, x[i]);
   c->sse = block_sum(e, e);
+  c->sae = block_abs_sum(e);
+  c->emax = block_abs_max(e);
+}
+
+/* The 4/6 selection metric: 0 = sum of squares (MSE), 1 = sum of |e| (MAE),
+ * 2 = max |e|. */
+static float fos_metric(const cand_t* c, int rule) {
+  return rule == 1 ? c->sae : (rule == 2 ? c->emax : c->sse);
 }
 
 /* Encode one block of 16 fp32 values (the steps of one block, in the pages'
  * order: block amax -> scale -> element rounding -> 4/6 choice -> dequant).
  * idx0 is the flat encoded-layout index of element 0 (for the random bits).
  * Outputs: codes[16] (one code per byte), *scale, *choice (1 = target 4),
- * dq[16] (bf16 bits), dqf[16] (fp32 q*d), sse[2] = {sse6, sse4}. */
-void orc_encode_block(const float* x, float g, int fmt, int rounding, int fos,
+ * dq[16] (bf16 bits), dqf[16] (fp32 q*d), sse[2] = the 4/6 metric of the two
+ * candidates {k=6, k=4} under `rule`. */
+void orc_encode_block(const float* x, float g, int fmt, int rounding, int fos, int rule,
                       uint32_t seed, uint32_t step, uint32_t dir, uint64_t idx0,
                       uint8_t* codes, uint8_t* scale, uint8_t* choice,
                       uint16_t* dq, float* dqf, float* sse) {
@@ -289,13 +320,13 @@ void orc_encode_block(const float* x, float g, int fmt, int rounding, int fos,
   cand_t c6, c4;
   encode_candidate(x, amax, g, 6.0f, fmt, rounding, v16, &c6);
   const cand_t* pick = &c6;
-  sse[0] = c6.sse;
+  sse[0] = fos_metric(&c6, rule);
   sse[1] = 0.0f;
   *choice = 0;
   if (fos) {
     encode_candidate(x, amax, g, 4.0f, fmt, rounding, v16, &c4);
-    sse[1] = c4.sse;
-    if (c4.sse < c6.sse) { pick = &c4; *choice = 1; }
+    sse[1] = fos_metric(&c4, rule);
+    if (sse[1] < sse[0]) { pick = &c4; *choice = 1; }
   }
   *scale = pick->scale;
   for (int i = 0; i < 16; ++i) {
@@ -311,7 +342,7 @@ void orc_encode_block(const float* x, float g, int fmt, int rounding, int fos,
  * 32-bit words (bit b % 32 of word b / 32 for block b of the slice, B =
  * Rm*Cm/16), dequant bf16 [S][Rm][Cm]. */
 static int encode_rows(const float* xs, int64_t S, int64_t Rm, int64_t Cm,
-                       const float* g, int fmt, int rounding, int fos,
+                       const float* g, int fmt, int rounding, int fos, int rule,
                        uint32_t seed, uint32_t step, uint32_t dir,
                        uint8_t* codes, uint8_t* scales, uint32_t* choice, uint16_t* dq) {
   int64_t B = Rm * Cm / 16, W = (B + 31) / 32;
@@ -322,7 +353,7 @@ static int encode_rows(const float* xs, int64_t S, int64_t Rm, int64_t Cm,
       uint8_t q[16], sc, ch;
       uint16_t d16[16];
       float df[16], sse[2];
-      orc_encode_block(xs + e0, g[s], fmt, rounding, fos, seed, step, dir,
+      orc_encode_block(xs + e0, g[s], fmt, rounding, fos, rule, seed, step, dir,
                        (uint64_t)e0, q, &sc, &ch, d16, df, sse);
       if (codes)
         for (int i = 0; i < 16; i += 2)
@@ -354,7 +385,7 @@ int orc_global_amax(const uint16_t* x, int64_t S, int64_t n, float* amax) {
 
 /* Full quantisation (a2..a7). blocks: 1 = rows, 2 = columns, 3 = both.
  * scale_max 0 selects 256 with 4/6 and 448 without (R3). */
-int orc_quantize(int blocks, int fmt, int rounding, int fos, float scale_max,
+int orc_quantize(int blocks, int fmt, int rounding, int fos, int rule, float scale_max,
                  uint32_t seed, uint32_t step,
                  const uint16_t* x, int64_t S, int64_t R, int64_t C, const float* gamax,
                  uint8_t* r_codes, uint8_t* r_scales, uint32_t* r_choice, uint16_t* r_dq,
@@ -370,7 +401,7 @@ int orc_quantize(int blocks, int fmt, int rounding, int fos, float scale_max,
     xf[i] = orc_bf16_to_f32(x[i]);
   }
   if (blocks & 1)
-    encode_rows(xf, S, R, C, g, fmt, rounding, fos, seed, step, 0,
+    encode_rows(xf, S, R, C, g, fmt, rounding, fos, rule, seed, step, 0,
                 r_codes, r_scales, r_choice, r_dq);
   if (blocks & 2) {
     float* xt = (float*)malloc((size_t)(N > 0 ? N : 1) * sizeof(float));
@@ -378,7 +409,7 @@ int orc_quantize(int blocks, int fmt, int rounding, int fos, float scale_max,
       for (int64_t r = 0; r < R; ++r)
         for (int64_t c = 0; c < C; ++c)
           xt[s * R * C + c * R + r] = xf[s * R * C + r * C + c];
-    encode_rows(xt, S, C, R, g, fmt, rounding, fos, seed, step, 1,
+    encode_rows(xt, S, C, R, g, fmt, rounding, fos, rule, seed, step, 1,
                 c_codes, c_scales, c_choice, c_dq);
     free(xt);
   }

@@ -74,7 +74,8 @@ def q(L, cfg, x=FAKE, S=1, R=16, Cc=32, amax=FAKE, row=None, col=None, status=No
 def test_quantize_argument_errors(L):
     assert q(L, None) == 1
     for bad in (dict(blocks=0), dict(blocks=4), dict(scale_fmt=2), dict(rounding=3),
-                dict(four_over_six=2), dict(scale_max=-1.0), dict(scale_max=float("nan"))):
+                dict(four_over_six=2), dict(scale_max=-1.0), dict(scale_max=float("nan")),
+                dict(four_over_six_rule=3), dict(four_over_six_rule=-1)):
         assert q(L, _cfg(**bad), row=_out(), col=_out()) == 4, bad
     assert q(L, _cfg(blocks=1), Cc=24, row=_out()) == 2      # cols % 16 for row blocks
     assert q(L, _cfg(blocks=2), R=24, col=_out()) == 2       # rows % 16 for column blocks

@@ -204,3 +204,27 @@ def test_periodic_helper_refreshes_on_schedule():
         seen.append(pa(dev_bits(xb), t).item())
     want = [oracle.global_amax(xs[t - t % 2])[0][0] for t in range(5)]
     assert seen == [float(w) for w in want] and pa.refreshes == 3
+
+
+@pytest.mark.parametrize("rule", [1, 2])
+@pytest.mark.parametrize("blocks", [1, 3])
+@pytest.mark.parametrize("rounding", [0, 1])
+def test_alternative_four_over_six_rules(rule, blocks, rounding):
+    xb = synth.student_t(160, 272, seed=13 + rule)[None]
+    gamax, _ = oracle.global_amax(xb)
+    x = dev_bits(xb)
+    cfg = nv.Config(blocks=blocks, four_over_six=1, rounding=rounding, seed=7,
+                    four_over_six_rule=rule)
+    out = nv.nvfp4_quantize(x, torch.from_numpy(gamax).cuda(), cfg)
+    torch.cuda.synchronize()
+    ref = oracle.quantize(xb, gamax, blocks=blocks, four_over_six=1, rounding=rounding, seed=7,
+                          rule=rule)
+    compare_encoding(out["row"], ref, "row_", f"rule {rule} row", True)
+    if blocks & 2:
+        compare_encoding(out["col"], ref, "col_", f"rule {rule} col", True)
+    tok = nv.nvfp4_quantize_per_token(x[0], cfg if blocks == 1 else nv.Config(
+        four_over_six=1, rounding=rounding, seed=7, four_over_six_rule=rule))
+    s = xb[0].reshape(-1, 1, 272)
+    a, _ = oracle.global_amax(s, s.shape[0])
+    rt = oracle.quantize(s, a, four_over_six=1, rounding=rounding, seed=7, rule=rule)
+    compare_encoding(tok, rt, "row_", f"rule {rule} per-token", True)

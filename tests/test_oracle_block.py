@@ -104,6 +104,7 @@ def _candidate64(x: np.ndarray, g: float, k: float):
     y = (x.astype(np.float32) * inv).astype(np.float32)
     v = textbook_minifloat(np.abs(y), mbits=1, emin=0, vmax=6.0) * np.where(np.signbit(y), -1, 1)
     err = x.astype(np.float64) - v * np.float64(d)
+    _candidate64.err = err
     return float(np.sum(err * err)), v, float(d)
 
 
@@ -135,6 +136,41 @@ def test_four_over_six_picks_lower_error_candidate(orc, dist):
         assert np.array_equal(orc.e2m1_value(r["codes"]).astype(np.float64), v)
         assert np.array_equal(r["dqf"], (v * d).astype(np.float32))
     assert picked[0] > 0 and picked[1] > 0
+
+
+@pytest.mark.parametrize("rule", [1, 2])
+def test_alternative_rules_pick_lower_error_candidate(orc, rule):
+    """Four Over Six summaries: the selection rules evaluated are smallest max
+    error, smallest L1 norm (MAE) and smallest MSE. Float64 brute force."""
+    rng = np.random.default_rng(31 + rule)
+    picked = [0, 0]
+    for _ in range(600):
+        x = (rng.standard_t(3, 16) * rng.uniform(0.1, 10)).astype(np.float32)
+        g = float(np.float32(np.exp(rng.uniform(-2, 2))) / np.float32(2688.0))
+        r = orc.encode_block(x, g, fos=1, rule=rule)
+        _candidate64(x, g, 6.0)
+        e6 = _candidate64.err.copy()
+        _candidate64(x, g, 4.0)
+        e4 = _candidate64.err.copy()
+        m6, m4 = (np.sum(np.abs(e6)), np.sum(np.abs(e4))) if rule == 1 else \
+                 (np.max(np.abs(e6)), np.max(np.abs(e4)))
+        if rule == 1 and abs(m4 - m6) <= 1e-5 * max(m4, m6, 1e-30):
+            continue
+        want = 1 if m4 < m6 else 0
+        if rule == 2 and m4 == m6:
+            want = 0
+        assert r["choice"] == want
+        picked[want] += 1
+    assert picked[0] > 0 and picked[1] > 0
+
+
+@pytest.mark.parametrize("rule", [0, 1, 2])
+def test_vignettes_under_every_rule(orc, rule):
+    e1, e2 = W["four_over_six_1"], W["four_over_six_2"]
+    assert orc.encode_block(_block(e1["block"]), 1.0, fos=1, rule=rule)["choice"] == 1
+    assert orc.encode_block(_block(e2["block"]), 1.0, fos=1, rule=rule)["choice"] == 0
+    r = orc.encode_block(_block(e1["block"]), 1.0, fos=1, rule=rule)
+    assert r["sse6"] == {0: 17.3125, 1: 5.75, 2: 4.0}[rule] and r["sse4"] == 0.0
 
 
 def test_four_over_six_never_increases_tensor_error(orc):
