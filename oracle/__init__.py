@@ -90,6 +90,23 @@ def _declare(L):
     L.orc_quantize.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_float,
                                C.c_uint32, C.c_uint32, _u16p, _i64, _i64, _i64, _f32p,
                                _u8p, _u8p, _u32p, _u16p, _u8p, _u8p, _u32p, _u16p]
+    L.orc_e4m3_sr.restype = C.c_uint8
+    L.orc_e4m3_sr.argtypes = [C.c_float, C.c_uint32]
+    L.orc_e4m3_rne.restype = C.c_uint8
+    L.orc_e4m3_rne.argtypes = [C.c_float]
+    L.orc_e4m3_signed_value.restype = C.c_float
+    L.orc_e4m3_signed_value.argtypes = [C.c_uint8]
+    L.orc_mx_shared_exp.restype = C.c_int
+    L.orc_mx_shared_exp.argtypes = [C.c_float]
+    L.orc_mx_encode.argtypes = [_f32p, _i64, C.c_int, C.c_uint32, C.c_uint32, C.c_uint32,
+                                C.c_uint64, _u8p, _u8p]
+    L.orc_dequant.restype = C.c_int
+    L.orc_dequant.argtypes = [C.c_int, C.c_float, C.c_int, _u8p, _u8p, _i64, _i64, _i64, _f32p,
+                              _f32p]
+    L.orc_requant.restype = C.c_int
+    L.orc_requant.argtypes = [C.c_int, C.c_float, C.c_int, _u8p, _u8p, _i64, _i64, _i64, _f32p,
+                              C.c_int, C.c_int, C.c_uint32, C.c_uint32, C.c_int, C.c_int,
+                              C.c_float, _u8p, _u8p, _u32p]
     L.orc_fakequant_fwd.restype = C.c_int
     L.orc_fakequant_fwd.argtypes = [_u16p, _i64, _i64, _f32p, _f32p, _u16p]
     L.orc_scale_grad_bwd.restype = C.c_int
@@ -261,3 +278,74 @@ def scale_grad_bwd(x_bf16, gq_bf16, s_pre, s_post=None, want_gx: bool = True):
                                   _p(so, _f32p), _p(gx, _u16p), _p(gs_pre, _f32p),
                                   _p(gs_post, _f32p))
     return dict(gx=gx, gs_pre=gs_pre, gs_post=gs_post, status=st)
+
+
+# ------------------------------------------------------- re-quantisation --
+
+def e4m3_sr(y, v16) -> np.ndarray:
+    L = lib()
+    y = np.asarray(y, np.float32).ravel()
+    v = np.broadcast_to(np.asarray(v16, np.uint32), y.shape).ravel()
+    return np.array([L.orc_e4m3_sr(float(a), int(b)) for a, b in zip(y, v)], np.uint8)
+
+
+def e4m3_rne(y) -> np.ndarray:
+    L = lib()
+    return np.array([L.orc_e4m3_rne(float(a)) for a in np.asarray(y, np.float32).ravel()],
+                    np.uint8)
+
+
+def e4m3_signed_value(codes) -> np.ndarray:
+    L = lib()
+    c = np.asarray(codes, np.uint8)
+    return np.array([L.orc_e4m3_signed_value(int(v)) for v in c.ravel()],
+                    np.float32).reshape(c.shape)
+
+
+def mx_shared_exp(amax: float) -> int:
+    return lib().orc_mx_shared_exp(float(amax))
+
+
+def mx_encode(v, rounding=1, seed=0, step=0, direction=2, idx0=0):
+    v = np.ascontiguousarray(v, np.float32).ravel()
+    codes = np.empty(v.size, np.uint8)
+    scales = np.empty(v.size // 32, np.uint8)
+    lib().orc_mx_encode(_p(v, _f32p), v.size, rounding, seed, step, direction, idx0,
+                        _p(codes, _u8p), _p(scales, _u8p))
+    return codes, scales
+
+
+def dequant(codes, scales, gamax, *, scale_fmt=0, scale_max=0.0, four_over_six=0):
+    """fp32 values of a row encoding: codes [S][R][C/2], scales [S][R][C/16]."""
+    codes = np.ascontiguousarray(codes, np.uint8)
+    scales = np.ascontiguousarray(scales, np.uint8)
+    S, R, half = codes.shape
+    out = np.empty((S, R, 2 * half), np.float32)
+    gam = np.ascontiguousarray(gamax, np.float32)
+    st = lib().orc_dequant(scale_fmt, scale_max, four_over_six, _p(codes, _u8p),
+                           _p(scales, _u8p), S, R, 2 * half, _p(gam, _f32p), _p(out, _f32p))
+    return out, st
+
+
+def requant(codes, scales, gamax, *, target=0, rounding=1, seed=0, step=0, src_fmt=0,
+            src_scale_max=0.0, src_fos=0, dst_fmt=0, dst_fos=0, dst_scale_max=0.0) -> dict:
+    """De-quantise a row encoding [S][R][C], transpose, re-quantise: target 0 =
+    MXFP8 (codes [S][C][R], E8M0 scales [S][C][R/32]), 1 = NVFP4 (codes
+    [S][C][R/2], scales [S][C][R/16], bitmap when dst_fos)."""
+    codes = np.ascontiguousarray(codes, np.uint8)
+    scales = np.ascontiguousarray(scales, np.uint8)
+    S, R, half = codes.shape
+    Cc = 2 * half
+    gam = np.ascontiguousarray(gamax, np.float32)
+    if target == 0:
+        oc = np.zeros((S, Cc, R), np.uint8)
+        os_ = np.zeros((S, Cc, R // 32), np.uint8)
+        ch = None
+    else:
+        oc = np.zeros((S, Cc, R // 2), np.uint8)
+        os_ = np.zeros((S, Cc, R // 16), np.uint8)
+        ch = np.zeros((S, (R * Cc // 16 + 31) // 32), np.uint32) if dst_fos else None
+    st = lib().orc_requant(src_fmt, src_scale_max, src_fos, _p(codes, _u8p), _p(scales, _u8p),
+                           S, R, Cc, _p(gam, _f32p), target, rounding, seed, step, dst_fmt,
+                           dst_fos, dst_scale_max, _p(oc, _u8p), _p(os_, _u8p), _p(ch, _u32p))
+    return dict(codes=oc, scales=os_, choice=ch, status=st)

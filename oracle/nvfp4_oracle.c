@@ -489,3 +489,136 @@ int orc_scale_grad_bwd(const uint16_t* x, const uint16_t* gq, int64_t R, int64_t
   }
   return st;
 }
+
+/* ------------------------------------------------- re-quantisation -------- */
+/* End-to-End 4-Bit Training, "Re-quantization with stochastic rounding" and
+ * its quantised-linear-layer figure: the backward pass de-quantises the
+ * forward NVFP4 tensor, transposes it in higher precision and re-quantises it
+ * with stochastic rounding, to MXFP8 (the pages' choice) or to NVFP4.
+ *
+ * Readings:
+ *  R9  De-quantised value (fp32, no bf16 rounding): q * d with
+ *      d = dec(scale) * g exactly as in the forward encoding.
+ *  R10 MXFP8 (the pages name MXFP8: E4M3 values with one E8M0 power-of-two
+ *      scale per 32): per block of 32 values along the transposed rows, the
+ *      shared exponent e is the smallest integer with amax <= 448 * 2^e
+ *      (448 = E4M3's largest normal), i.e. floor(log2(amax)) - 8, plus 1 when
+ *      amax's significand exceeds 1.75; clamped to [-127, 127] (amax = 0 gives
+ *      -127); scale byte = e + 127. The pages require the re-quantised tensor
+ *      to equal the forward one in expectation; the plain floor(log2) - 8
+ *      exponent would clip block maxima between 448 and 512 times the scale,
+ *      a bias, so the scale is rounded up instead. Element = E4M3 code of
+ *      y = v * 2^-e (one fp32 rounding), by RNE or by stochastic rounding onto
+ *      the E4M3 grid (R5's rule and bits, direction 2); |y| <= 448 always.
+ *  R11 NVFP4 target: the row encoding (R1..R8) of the transposed fp32 values,
+ *      with the forward's per-slice global amax and direction 2. */
+
+/* Stochastic rounding of y onto the signed E4M3 grid (sign in bit 7),
+ * saturating at 448, with the 16 random bits v16 (R5's rule). */
+uint8_t orc_e4m3_sr(float y, uint32_t v16) {
+  uint8_t s = signbit(y) ? 0x80 : 0;
+  double a = fabs((double)y);
+  if (!(a < 448.0)) return (uint8_t)(s | 0x7E);
+  int lo = 0;
+  while (lo < 126 && e4m3_mag(lo + 1) <= a) ++lo;
+  double p = (a - e4m3_mag(lo)) / (e4m3_mag(lo + 1) - e4m3_mag(lo));
+  double u = (double)(v16 & 0xFFFFu) / 65536.0;
+  return (uint8_t)(s | (u < p ? lo + 1 : lo));
+}
+/* Round-to-nearest-even of y onto the signed E4M3 grid, saturating. */
+uint8_t orc_e4m3_rne(float y) {
+  uint8_t s = signbit(y) ? 0x80 : 0;
+  return (uint8_t)(s | nearest_index(fabs((double)y), e4m3_mag, 127));
+}
+float orc_e4m3_signed_value(uint8_t code) {
+  float v = orc_e4m3_value(code & 0x7F);
+  return (code & 0x80) ? -v : v;
+}
+
+/* R10: the MX shared exponent of a block whose largest |value| is amax: the
+ * smallest e with amax <= 448 * 2^e, within [-127, 127]. */
+int orc_mx_shared_exp(float amax) {
+  if (!(amax > 0.0f)) return -127;
+  int e2;
+  float m = frexpf(amax, &e2); /* amax = m * 2^e2, m in [0.5, 1) */
+  int e = (e2 - 1) - 8 + (2.0f * m > 1.75f ? 1 : 0);
+  if (e < -127) e = -127;
+  if (e > 127) e = 127;
+  return e;
+}
+
+/* MXFP8 encoding of n values (n % 32 == 0), blocks of 32 consecutive values;
+ * idx0 = flat index of v[0] in the output layout (for the random bits). */
+void orc_mx_encode(const float* v, int64_t n, int rounding, uint32_t seed, uint32_t step,
+                   uint32_t dir, uint64_t idx0, uint8_t* codes, uint8_t* scales) {
+  for (int64_t b = 0; b < n / 32; ++b) {
+    const float* vb = v + 32 * b;
+    float amax = 0.0f;
+    for (int i = 0; i < 32; ++i)
+      if (fabsf(vb[i]) > amax) amax = fabsf(vb[i]);
+    int e = orc_mx_shared_exp(amax);
+    scales[b] = (uint8_t)(e + 127);
+    for (int i = 0; i < 32; ++i) {
+      float y = ldexpf(vb[i], -e);
+      uint64_t idx = idx0 + (uint64_t)(32 * b + i);
+      codes[32 * b + i] = rounding ? orc_e4m3_sr(y, orc_sr_bits(seed, step, dir, idx))
+                                   : orc_e4m3_rne(y);
+    }
+  }
+}
+
+/* R9: de-quantise a row encoding [S][R][C] (codes two per byte, scale bytes
+ * per 16) to fp32. fmt / scale_max / fos describe the forward encoding. */
+int orc_dequant(int fmt, float scale_max, int fos, const uint8_t* codes,
+                const uint8_t* scales, int64_t S, int64_t R, int64_t C, const float* gamax,
+                float* out) {
+  int st = 0;
+  float M = scale_max > 0.0f ? scale_max : (fos ? 256.0f : 448.0f);
+  for (int64_t s = 0; s < S; ++s) {
+    float g;
+    st |= global_decode_scale(gamax[s], M, &g);
+    for (int64_t i = 0; i < R * C; ++i) {
+      int64_t e = s * R * C + i;
+      float d = orc_scale_value(fmt, scales[e / 16]) * g;
+      uint8_t c = (e & 1) ? (codes[e / 2] >> 4) : (codes[e / 2] & 15);
+      out[e] = orc_e2m1_value(c) * d;
+    }
+  }
+  return st;
+}
+
+/* De-quantise -> transpose -> re-quantise. target 0 = MXFP8 (out_codes
+ * [S][C][R] E4M3 bytes, out_scales [S][C][R/32] E8M0 bytes; R % 32 == 0),
+ * target 1 = NVFP4 (out_codes [S][C][R/2], out_scales [S][C][R/16], 4/6
+ * bitmap when dst_fos). */
+int orc_requant(int src_fmt, float src_scale_max, int src_fos, const uint8_t* codes,
+                const uint8_t* scales, int64_t S, int64_t R, int64_t C, const float* gamax,
+                int target, int rounding, uint32_t seed, uint32_t step, int dst_fmt,
+                int dst_fos, float dst_scale_max, uint8_t* out_codes, uint8_t* out_scales,
+                uint32_t* out_choice) {
+  int64_t N = S * R * C;
+  float* xh = (float*)malloc((size_t)(N > 0 ? N : 1) * sizeof(float));
+  float* xt = (float*)malloc((size_t)(N > 0 ? N : 1) * sizeof(float));
+  int st = orc_dequant(src_fmt, src_scale_max, src_fos, codes, scales, S, R, C, gamax, xh);
+  for (int64_t s = 0; s < S; ++s)
+    for (int64_t r = 0; r < R; ++r)
+      for (int64_t c = 0; c < C; ++c) xt[s * R * C + c * R + r] = xh[s * R * C + r * C + c];
+  if (target == 0) {
+    for (int64_t s = 0; s < S; ++s)
+      for (int64_t c = 0; c < C; ++c) {
+        int64_t e0 = s * C * R + c * R;
+        orc_mx_encode(xt + e0, R, rounding, seed, step, 2, (uint64_t)e0, out_codes + e0,
+                      out_scales + e0 / 32);
+      }
+  } else {
+    float M = dst_scale_max > 0.0f ? dst_scale_max : (dst_fos ? 256.0f : 448.0f);
+    float* g = (float*)malloc((size_t)(S > 0 ? S : 1) * sizeof(float));
+    for (int64_t s = 0; s < S; ++s) st |= global_decode_scale(gamax[s], M, &g[s]);
+    encode_rows(xt, S, C, R, g, dst_fmt, rounding, dst_fos, 0, seed, step, 2, out_codes,
+                out_scales, out_choice, NULL);
+    free(g);
+  }
+  free(xh);
+  free(xt);
+  return st;
+}
