@@ -1,6 +1,6 @@
 """Throughput of the NVFP4 hot path on one or more GB300s.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..8] [--impl ours|reference]
 
 A step is one pass of the hot path over one batch of synthetic input already
 resident in HBM. The default workload is the activation tensor 8192 x 4096 bf16
@@ -410,8 +410,92 @@ class PerTokenActivation(Activation):
         "outputs codes, scales, 4/6 bitmap, dequant, row amax"))
 
 
+class RequantActivation(Workload):
+    """The activation tensor's forward NVFP4 encoding (4/6 on, written once,
+    untimed) re-quantised for the backward pass: de-quantise, transpose,
+    stochastic rounding to MXFP8 (E4M3 values, E8M0 scale per 32)."""
+
+    def __init__(self, device, rows=8192, cols=4096, seed=1, target=0):
+        self.rows, self.cols, self.target = rows, cols, target
+        self.elements = rows * cols
+        xb = synth.student_t(rows, cols, seed=seed)
+        self.host_x = xb
+        x = torch.from_numpy(xb.view(np.int16)).to(device)
+        self.gamax = nv.nvfp4_amax(x)
+        self.src_cfg = nv.Config(four_over_six=1)
+        enc = nv.nvfp4_quantize(x, self.gamax, self.src_cfg, dequant=False)["row"]
+        del x
+        torch.cuda.synchronize()
+        self.dst_cfg = nv.Config(rounding=1, seed=7, step=0, four_over_six=int(target == 1))
+        in_bytes = self.elements * (0.5 + 1 / 16)
+        out_bytes = self.elements * ((1 + 1 / 32) if target == 0 else (0.5 + 1 / 16 + 1 / 128))
+        per_set = in_bytes + out_bytes
+        self.nsets = max(2, int(np.ceil(2.5 * L2_BYTES / per_set)))
+        self.codes = [enc["codes"]] + [enc["codes"].clone() for _ in range(self.nsets - 1)]
+        self.scales = [enc["scales"]] + [enc["scales"].clone() for _ in range(self.nsets - 1)]
+        self.out = [nv.alloc_requant(1, rows, cols, device, target, target == 1)
+                    for _ in range(self.nsets)]
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.r_bytes = in_bytes + out_bytes
+        self.working_set = per_set * self.nsets
+        L = nv.lib()
+        st = torch.cuda.current_stream(device).cuda_stream
+        self._s, self._d = self.src_cfg.c(), self.dst_cfg.c()
+        self._outs = [nv._Out(o["codes"].data_ptr(), o["scales"].data_ptr(),
+                              o["choice"].data_ptr() if o.get("choice") is not None else None,
+                              None) for o in self.out]
+
+        def rq(i):
+            return L.nvfp4_requant_transpose(C.byref(self._s), C.byref(self._d), target,
+                                             self.codes[i].data_ptr(), self.scales[i].data_ptr(),
+                                             1, rows, cols, self.gamax.data_ptr(),
+                                             C.byref(self._outs[i]), self.status.data_ptr(), st)
+        self._rq = rq
+        self.dominant = "requant_mxfp8_sr" if target == 0 else "requant_nvfp4_sr"
+
+    def kernels(self, k, i):
+        return [Kernel(self.dominant, self.r_bytes, lambda: self._rq(i))]
+
+    def e2e_io(self, k):
+        o = self.out[0]
+        outs = [o["codes"], o["scales"]] + ([o["choice"]] if self.target == 1 else [])
+        return [self.codes[0], self.scales[0], self.gamax], outs
+
+    def cpu_sample(self, budget_s):
+        import oracle
+        rows = 32
+        xb = self.host_x
+        a, _ = oracle.global_amax(xb)
+        q = oracle.quantize(xb[:1024], a, four_over_six=1, dequant=False)
+
+        def once(n):
+            t0 = time.perf_counter()
+            oracle.requant(q["row_codes"][:, :n], q["row_scales"][:, :n], a, target=self.target,
+                           rounding=1, seed=7, src_fos=1, dst_fos=int(self.target == 1))
+            return time.perf_counter() - t0
+        per_row = once(rows) / rows
+        rows = int(min(1024, max(32, budget_s / max(per_row, 1e-9))))
+        rows -= rows % 32
+        return rows * self.cols, once(rows), \
+            f"first {rows} of {self.rows} source rows (de-quantise, transpose, re-quantise)"
+
+    bytes_per_elem = property(lambda self: self.r_bytes / self.elements)
+    workload = property(lambda self: (
+        f"activation {self.rows}x{self.cols} bf16, 0.5*Student-t(nu=3), forward NVFP4 row "
+        "encoding (E4M3 scales, Four-Over-Six) re-quantised for the backward GEMM: de-quantise, "
+        "transpose, stochastic rounding to "
+        + ("MXFP8 (E4M3, E8M0 scale per 32)" if self.target == 0 else
+           "NVFP4 (E4M3 scales, Four-Over-Six)") + "; outputs codes, scales"))
+
+
+class RequantActivationNvfp4(RequantActivation):
+    def __init__(self, device):
+        super().__init__(device, target=1)
+
+
 WORKLOADS = {1: SmallNormal, 2: Activation, 3: ScaleLearning, 4: DriftingGradient,
-             5: MoeExperts, 6: PerTokenActivation}
+             5: MoeExperts, 6: PerTokenActivation, 7: RequantActivation,
+             8: RequantActivationNvfp4}
 
 
 # --------------------------------------------------------------- clocks --
@@ -658,6 +742,35 @@ def _reference_sample(args):
             return sub.size, time.perf_counter() - t0
         return "gradient 16384x4096 UE5M3 SR periodic", 2.5625 + 2 / 16, \
             f"first {sub.shape[0]} of 16384 rows per step", step
+    if args.config == 6:
+        xb = synth.student_t(8192, 4096, seed=1)
+        sub = xb[:args.ref_rows].reshape(-1, 1, 4096)
+
+        def step():
+            t0 = time.perf_counter()
+            a, _ = oracle.global_amax(sub, sub.shape[0])
+            oracle.quantize(sub, a, four_over_six=1)
+            return sub.size, time.perf_counter() - t0
+        return "activation 8192x4096 per-token outer scales, row 4/6", \
+            2 + 0.5 + 1 / 16 + 1 / 128 + 2 + 4 / 4096, \
+            f"first {sub.shape[0]} of 8192 rows per step", step
+    if args.config in (7, 8):
+        target = args.config - 7
+        xb = synth.student_t(8192, 4096, seed=1)
+        a, _ = oracle.global_amax(xb)
+        n = max(32, args.ref_rows - args.ref_rows % 32) // 4
+        n -= n % 32
+        q = oracle.quantize(xb[:n], a, four_over_six=1, dequant=False)
+
+        def step():
+            t0 = time.perf_counter()
+            oracle.requant(q["row_codes"], q["row_scales"], a, target=target, rounding=1,
+                           seed=7, src_fos=1, dst_fos=target)
+            return n * 4096, time.perf_counter() - t0
+        bpe = 0.5 + 1 / 16 + ((1 + 1 / 32) if target == 0 else (0.5 + 1 / 16 + 1 / 128))
+        return ("activation 8192x4096 NVFP4 (4/6) re-quantised, transposed, SR to "
+                + ("MXFP8" if target == 0 else "NVFP4")), bpe, \
+            f"first {n} of 8192 source rows per step", step
     xb = synth.moe_experts(1, 2048, 7168, seed=4)[0]
     sub = xb[:max(16, args.ref_rows - args.ref_rows % 16)]
 
@@ -702,7 +815,8 @@ def main():
     wl = WORKLOADS[args.config](device, **extra)
     if args.steps is None:
         # about two seconds of device time, so the clock samples cover the run
-        args.steps = {1: 20000, 2: 40000, 3: 10000, 4: 16000, 5: 150, 6: 50000}[args.config]
+        args.steps = {1: 20000, 2: 40000, 3: 10000, 4: 16000, 5: 150, 6: 50000, 7: 40000,
+                      8: 40000}[args.config]
     total_ms, per_kernel, clk, wall = time_ours(wl, args, world, local)
     total_ms = max_over_ranks(total_ms, world)
     units = wl.elements * args.steps * world

@@ -180,20 +180,65 @@ NVFP4_API nvfp4_status nvfp4_scale_grad_bwd(const void* x, const void* gq, int64
                                   float* gs_pre, float* gs_post, int32_t* status,
                                   void* stream);
 
+/* nvfp4_requant_transpose target */
+#define NVFP4_TARGET_MXFP8 0 /* E4M3 values, one E8M0 power-of-two scale per 32 */
+#define NVFP4_TARGET_NVFP4 1 /* the NVFP4 row encoding of the transposed tensor  */
+
+/* Backward-operand re-quantisation (End-to-End 4-Bit Training,
+ * "Re-quantization with stochastic rounding" and its quantised-linear-layer
+ * figure): de-quantise the forward row encoding of X [slices][rows][cols],
+ * transpose it, and quantise it again along the other axis, so that the
+ * backward GEMM sees X^T blocked along its own contraction dimension.
+ * Input: codes [S][R][C/2] and scales [S][R][C/16] exactly as nvfp4_quantize's
+ * row encoding wrote them, with src its config (scale_fmt, four_over_six and
+ * scale_max fix the decoding; other fields are ignored) and global_amax
+ * (fp32 [S]) the amax it was given. De-quantised value: the fp32 product
+ * e2m1(code) * (dec(scale) * g), never rounded to bf16.
+ * target NVFP4_TARGET_MXFP8 (rows % 32 == 0): per 32 consecutive values of a
+ * column, shared exponent e = the smallest integer with amax <= 448 * 2^e
+ * (clamped to [-127, 127]); out->scales [S][C][R/32] receives e + 127 (E8M0);
+ * out->codes [S][C][R] one signed E4M3 byte per value, the code of v * 2^-e
+ * (RNE, or stochastic rounding onto the E4M3 grid), never saturating.
+ * target NVFP4_TARGET_NVFP4 (rows % 16 == 0): out is the row encoding of the
+ * fp32 matrix X^T with the outer scale g = global_amax / (6 M_dst) and the
+ * block-scale format, 4/6 mode and rule of dst: codes [S][C][R/2], scales
+ * [S][C][R/16], choice [S][ceil(R*C/512)] words (required iff
+ * dst->four_over_six).
+ * dst supplies rounding, seed and step (both targets) and scale_fmt,
+ * four_over_six, four_over_six_rule and scale_max (NVFP4 target); dst->blocks
+ * is ignored. Stochastic rounding draws its bits as nvfp4_quantize does, with
+ * direction 2 in the counter and idx the flat index of the output layout.
+ * out->dequant must be NULL. A de-quantised value that is not finite (a
+ * scale times g overflowing fp32) sets NVFP4_DEV_NONFINITE_INPUT; a bad
+ * global amax sets NVFP4_DEV_BAD_AMAX.
+ * Errors: NULL required pointers, non-NULL out->dequant (NVFP4_ERR_ENUM),
+ * cols % 16, rows % 32 (MXFP8) or % 16 (NVFP4), enum fields out of range,
+ * misaligned buffers (codes, scales and outputs 16-byte aligned). */
+NVFP4_API nvfp4_status nvfp4_requant_transpose(const nvfp4_config* src, const nvfp4_config* dst,
+                                               int32_t target, const uint8_t* codes,
+                                               const uint8_t* scales, int64_t slices,
+                                               int64_t rows, int64_t cols,
+                                               const float* global_amax, const nvfp4_out* out,
+                                               int32_t* status, void* stream);
+
 /* ---- diagnostics: the device codecs element by element -------------------
  * For exhaustive checks of the conversions the kernels use. op:
  *   0: out[i] = E2M1 RNE code of in[i]
  *   1: out[i] = E4M3 code of in[i] >= 0        (block-scale encoder)
  *   2: out[i] = UE5M3 code of in[i] >= 0       (block-scale encoder)
  *   3: out[i] = E2M1 stochastic code of in[i] with random bits aux[i] & 0xFFFF
+ *   4: out[i] = signed E4M3 RNE code of in[i]   (MXFP8 element encoder)
+ *   5: out[i] = signed E4M3 stochastic code of in[i] with bits aux[i] & 0xFFFF
+ *   6: out[i] = E8M0 byte (e + 127) of the MX shared exponent for amax in[i]
  * Ops 0 and 3 convert groups of 8 consecutive inputs exactly as the kernels do.
- * in, aux (op 3 only): device arrays of n elements; out: device uint8 [n].
+ * in, aux (ops 3, 5): device arrays of n elements; out: device uint8 [n].
  * This entry point has no counterpart on the pages; it exists for testing. */
 NVFP4_API nvfp4_status nvfp4_codec_probe(int32_t op, const float* in, const uint32_t* aux, int64_t n,
                                uint8_t* out, void* stream);
 
 /* The 16 random bits the stochastic rounder draws for elements idx0 ..
- * idx0 + n - 1 of an encoding (direction 0 = rows, 1 = columns), written to
+ * idx0 + n - 1 of an encoding (direction 0 = rows, 1 = columns, 2 =
+ * re-quantisation), written to
  * out (device uint32 [n]). Diagnostics; no counterpart on the pages. */
 NVFP4_API nvfp4_status nvfp4_sr_bits(uint32_t seed, uint32_t step, uint32_t direction, uint64_t idx0,
                            int64_t n, uint32_t* out, void* stream);

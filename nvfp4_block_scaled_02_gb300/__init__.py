@@ -22,8 +22,8 @@ import torch
 __all__ = [
     "Config", "Nvfp4Error", "build", "lib", "nvfp4_amax", "nvfp4_quantize",
     "nvfp4_fakequant_fwd", "nvfp4_scale_grad_bwd", "nvfp4_codec_probe", "nvfp4_sr_bits",
-    "nvfp4_quantize_per_token",
-    "alloc_encoding", "PeriodicAmax", "BLOCKS_ROW", "BLOCKS_COL", "BLOCKS_BOTH",
+    "nvfp4_quantize_per_token", "nvfp4_requant_transpose", "TARGET_MXFP8", "TARGET_NVFP4",
+    "alloc_encoding", "alloc_requant", "PeriodicAmax", "BLOCKS_ROW", "BLOCKS_COL", "BLOCKS_BOTH",
     "SCALE_E4M3", "SCALE_UE5M3", "ROUND_RNE", "ROUND_SR", "FOS_MSE", "FOS_MAE", "FOS_MAX",
     "DEV_NONFINITE_INPUT", "DEV_BAD_SCALE", "DEV_BAD_AMAX",
 ]
@@ -36,6 +36,7 @@ FOS_MSE, FOS_MAE, FOS_MAX = 0, 1, 2
 SCALE_E4M3, SCALE_UE5M3 = 0, 1
 ROUND_RNE, ROUND_SR = 0, 1
 DEV_NONFINITE_INPUT, DEV_BAD_SCALE, DEV_BAD_AMAX = 1, 2, 4
+TARGET_MXFP8, TARGET_NVFP4 = 0, 1
 
 _STATUS = {0: "ok", 1: "null pointer", 2: "shape", 3: "alignment", 4: "enum", 6: "cuda"}
 
@@ -104,12 +105,15 @@ def lib() -> C.CDLL:
             L.nvfp4_fakequant_fwd.argtypes = [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp]
             L.nvfp4_scale_grad_bwd.argtypes = [_vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp,
                                                _vp, _vp]
+            L.nvfp4_requant_transpose.argtypes = [C.POINTER(_Config), C.POINTER(_Config), _i32,
+                                                  _vp, _vp, _i64, _i64, _i64, _vp,
+                                                  C.POINTER(_Out), _vp, _vp]
             L.nvfp4_codec_probe.argtypes = [_i32, _vp, _vp, _i64, _vp, _vp]
             L.nvfp4_sr_bits.argtypes = [_u32, _u32, _u32, C.c_uint64, _i64, _vp, _vp]
             L.nvfp4_status_string.restype = C.c_char_p
             L.nvfp4_status_string.argtypes = [C.c_int]
             for name in ("nvfp4_amax", "nvfp4_quantize", "nvfp4_quantize_per_token",
-                         "nvfp4_fakequant_fwd",
+                         "nvfp4_requant_transpose", "nvfp4_fakequant_fwd",
                          "nvfp4_scale_grad_bwd", "nvfp4_codec_probe", "nvfp4_sr_bits"):
                 getattr(L, name).restype = C.c_int
             _lib = L
@@ -229,6 +233,52 @@ def nvfp4_quantize_per_token(x: torch.Tensor, cfg: Config | None = None, out: di
         _dev(status, "status"), _stream(x.device)))
     out = dict(out)
     out["row_amax"] = row_amax
+    return out
+
+
+def alloc_requant(slices: int, rows: int, cols: int, device, target: int,
+                  four_over_six: bool = False) -> dict:
+    """Outputs of nvfp4_requant_transpose for a [slices, rows, cols] source:
+    the transposed [slices, cols, rows] tensor in MXFP8 or NVFP4."""
+    if target == TARGET_MXFP8:
+        return {"codes": torch.empty((slices, cols, rows), dtype=torch.uint8, device=device),
+                "scales": torch.empty((slices, cols, rows // 32), dtype=torch.uint8,
+                                      device=device),
+                "choice": None}
+    return alloc_encoding(slices, cols, rows, device, four_over_six, dequant=False)
+
+
+def nvfp4_requant_transpose(codes: torch.Tensor, scales: torch.Tensor,
+                            global_amax: torch.Tensor, src: Config | None = None,
+                            dst: Config | None = None, target: int = TARGET_MXFP8,
+                            out: dict | None = None,
+                            status: torch.Tensor | None = None) -> dict:
+    """Re-quantise a row encoding (codes [S, R, C/2], scales [S, R, C/16], as
+    nvfp4_quantize wrote them under `src`) to the transposed [S, C, R] tensor in
+    MXFP8 (target 0) or NVFP4 (target 1, config `dst`), rounding per `dst`."""
+    src = src or Config()
+    dst = dst or Config(rounding=ROUND_SR)
+    if codes.dim() == 2:
+        S, (R, half) = 1, codes.shape
+    elif codes.dim() == 3:
+        S, R, half = codes.shape
+    else:
+        raise ValueError("codes must be [rows, cols/2] or [slices, rows, cols/2]")
+    if codes.dtype != torch.uint8 or scales.dtype != torch.uint8:
+        raise TypeError("codes and scales must be uint8")
+    Cc = 2 * half
+    if scales.numel() != S * R * (Cc // 16):
+        raise ValueError("scales must hold one byte per 16 values")
+    if out is None:
+        out = alloc_requant(S, R, Cc, codes.device, target,
+                            bool(dst.four_over_six) and target == TARGET_NVFP4)
+    o = _Out(_dev(out["codes"], "codes"), _dev(out["scales"], "scales"),
+             _dev(out.get("choice"), "choice"), None)
+    cs, cd = src.c(), dst.c()
+    _check("nvfp4_requant_transpose", lib().nvfp4_requant_transpose(
+        C.byref(cs), C.byref(cd), target, _dev(codes, "codes"), _dev(scales, "scales"), S, R, Cc,
+        _dev(global_amax, "global_amax"), C.byref(o), _dev(status, "status"),
+        _stream(codes.device)))
     return out
 
 

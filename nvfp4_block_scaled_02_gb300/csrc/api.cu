@@ -181,6 +181,63 @@ nvfp4_status nvfp4_quantize_per_token(const nvfp4_config* cfg, const void* x, in
                                                fos_mode(cfg), static_cast<cudaStream_t>(stream)));
 }
 
+nvfp4_status nvfp4_requant_transpose(const nvfp4_config* src, const nvfp4_config* dst,
+                                     int32_t target, const uint8_t* codes, const uint8_t* scales,
+                                     int64_t slices, int64_t rows, int64_t cols,
+                                     const float* global_amax, const nvfp4_out* out,
+                                     int32_t* status, void* stream) {
+  if (!src || !dst) return NVFP4_ERR_NULL;
+  if (target < 0 || target > 1) return NVFP4_ERR_ENUM;
+  if (src->scale_fmt < 0 || src->scale_fmt > 1 || src->four_over_six < 0 ||
+      src->four_over_six > 1 || !(src->scale_max >= 0.0f) ||
+      !(src->scale_max <= 3.402823466e+38f))
+    return NVFP4_ERR_ENUM;
+  if (dst->rounding < 0 || dst->rounding > 1) return NVFP4_ERR_ENUM;
+  const bool nv = target == NVFP4_TARGET_NVFP4;
+  if (nv && (dst->scale_fmt < 0 || dst->scale_fmt > 1 || dst->four_over_six < 0 ||
+             dst->four_over_six > 1 || dst->four_over_six_rule < 0 ||
+             dst->four_over_six_rule > 2 || !(dst->scale_max >= 0.0f) ||
+             !(dst->scale_max <= 3.402823466e+38f)))
+    return NVFP4_ERR_ENUM;
+  if (slices < 0 || rows < 0 || cols < 0 || cols % 16 != 0 || rows % (nv ? 16 : 32) != 0)
+    return NVFP4_ERR_SHAPE;
+  if (slices == 0 || rows == 0 || cols == 0) return NVFP4_OK;
+  if (!codes || !scales || !global_amax || !out || !out->codes || !out->scales)
+    return NVFP4_ERR_NULL;
+  const bool fos = nv && dst->four_over_six != 0;
+  if (fos && !out->choice) return NVFP4_ERR_NULL;
+  if (out->dequant) return NVFP4_ERR_ENUM;
+  if (!aligned(codes, 16) || !aligned(scales, 16) || !aligned(global_amax, 4) ||
+      !aligned(status, 4) || !aligned(out->codes, 16) || !aligned(out->scales, 16) ||
+      (fos && !aligned(out->choice, 16)))
+    return NVFP4_ERR_ALIGN;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (fos) {
+    const size_t W = (size_t)((rows * cols / 16 + 31) / 32);
+    if (cudaMemsetAsync(out->choice, 0, (size_t)slices * W * sizeof(uint32_t), st) != cudaSuccess)
+      return NVFP4_ERR_CUDA;
+  }
+  nvfp4::RequantParams p{};
+  p.codes = codes;
+  p.scales = scales;
+  p.S = slices;
+  p.R = rows;
+  p.C = cols;
+  p.gamax = global_amax;
+  p.src_fmt = src->scale_fmt;
+  p.M_src = src->scale_max > 0.0f ? src->scale_max : (src->four_over_six ? 256.0f : 448.0f);
+  p.M_dst = dst->scale_max > 0.0f ? dst->scale_max : (fos ? 256.0f : 448.0f);
+  p.seed = dst->seed;
+  p.step = dst->step;
+  p.out_codes = out->codes;
+  p.out_scales = out->scales;
+  p.out_choice = fos ? out->choice : nullptr;
+  p.status = status;
+  p.rule = dst->four_over_six_rule;
+  return cuda_status(nvfp4::launch_requant(p, target, dst->scale_fmt, dst->rounding == NVFP4_ROUND_SR,
+                                           nv ? fos_mode(dst) : 0, st));
+}
+
 static nvfp4_status ste_common(const void* x, int64_t rows, int64_t cols, const float* s_pre) {
   if (rows < 0 || cols < 0 || cols % 16 != 0) return NVFP4_ERR_SHAPE;
   if (rows == 0 || cols == 0) return NVFP4_OK;
@@ -231,10 +288,10 @@ nvfp4_status nvfp4_scale_grad_bwd(const void* x, const void* gq, int64_t rows, i
 
 nvfp4_status nvfp4_codec_probe(int32_t op, const float* in, const uint32_t* aux, int64_t n,
                                uint8_t* out, void* stream) {
-  if (op < 0 || op > 3) return NVFP4_ERR_ENUM;
+  if (op < 0 || op > 6) return NVFP4_ERR_ENUM;
   if (n < 0) return NVFP4_ERR_SHAPE;
   if (n == 0) return NVFP4_OK;
-  if (!in || !out || (op == 3 && !aux)) return NVFP4_ERR_NULL;
+  if (!in || !out || ((op == 3 || op == 5) && !aux)) return NVFP4_ERR_NULL;
   if (!aligned(in, 4) || !aligned(aux, 4)) return NVFP4_ERR_ALIGN;
   return cuda_status(
       nvfp4::launch_codec_probe(op, in, aux, n, out, static_cast<cudaStream_t>(stream)));

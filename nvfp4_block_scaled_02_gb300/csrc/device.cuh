@@ -218,6 +218,48 @@ __device__ __forceinline__ uint32_t sr8(const f2 (&y)[4], const uint4& rb) {
   return w;
 }
 
+// ------------------------------------------------- MXFP8 (E4M3 elements) --
+// Signed E4M3 codes of four fp32 values (y0 in bits 0..7), round to nearest
+// even, saturating to +-448 (cvt ... satfinite; the sign of y is kept).
+__device__ __forceinline__ uint32_t e4m3x4_rn(float y0, float y1, float y2, float y3) {
+  uint32_t w;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(w) : "f"(y0), "f"(y1), "f"(y2), "f"(y3));
+  return w;
+}
+// Stochastic rounding of y onto the signed E4M3 grid with nv = 0xFFFF - v
+// (v the 16 random bits): |y| rounds up iff v / 2^16 < p, p the position of
+// |y| between its two grid neighbours. Same construction as sr_mag: with
+// T = code_lo * 2^16 + ceil(p * 2^16) the magnitude code is (T + nv) >> 16.
+// Normal range (|y| >= 2^-6): the top 3 mantissa bits and the exponent of the
+// fp32 pattern ARE code_lo once the exponent is rebiased (127 -> 7), and the
+// 20 bits below them are p * 2^20, so T = (bits - (120 << 23) + 15) >> 4.
+// Subnormal range (step 2^-9): T = ceil(|y| * 2^25), one fma rounded up
+// against 2^23. |y| >= 448 (and NaN) is capped at 448, code 0x7E.
+__device__ __forceinline__ uint32_t e4m3_sr(float y, uint32_t nv) {
+  const uint32_t sign = (__float_as_uint(y) >> 24) & 0x80u;
+  const float a = fminf(fabsf(y), 448.0f);
+  const uint32_t tn = (__float_as_uint(a) - 0x3C000000u + 15u) >> 4;
+  const uint32_t ts = __float_as_uint(__fmaf_ru(a, 33554432.0f, 8388608.0f)) - 0x4B000000u;
+  return sign | (((a < 0.015625f ? ts : tn) + nv) >> 16);
+}
+// Shared exponent of an MX block whose largest |value| is amax: the smallest
+// e with amax <= 448 * 2^e (448 = E4M3's largest value), i.e. the unbiased
+// exponent of amax minus 8, plus 1 when its significand exceeds 1.75,
+// clamped to [-127, 127] (zero and fp32-subnormal amax give -127).
+__device__ __forceinline__ int mx_shared_exp(float amax) {
+  const uint32_t A = __float_as_uint(amax);
+  int e = (int)(A >> 23) - 135 + ((A & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+  return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+// 2^-e for e in [-127, 127] (2^-127 is an fp32 subnormal).
+__device__ __forceinline__ float exp2_neg(int e) {
+  return e == 127 ? __uint_as_float(0x00200000u) : __uint_as_float((uint32_t)(127 - e) << 23);
+}
+
 // ------------------------------------------------------------- cp.async ---
 // 16-byte global -> shared copy that bypasses L1 (streamed data), grouped and
 // awaited per thread: a thread only ever reads back the slots it filled, so

@@ -180,14 +180,15 @@ struct DirectScales {
   }
 };
 
+// The block's amax is given as an fp32 value (encode_block_f: fp32 inputs, as
+// in re-quantisation) or as bf16 bits (encode_block: bf16 inputs).
 template <int FMT, bool SR, bool FOS, class Scales>
-__device__ __forceinline__ BlockResult encode_block(const f2 (&lo)[4], const f2 (&hi)[4],
-                                                    uint32_t amax_bits, const SliceScale& ss,
-                                                    const Scales& scales, const uint4& rb0,
-                                                    const uint4& rb1, bool want_dq,
-                                                    int rule = 0) {
+__device__ __forceinline__ BlockResult encode_block_f(const f2 (&lo)[4], const f2 (&hi)[4],
+                                                      float amax, const SliceScale& ss,
+                                                      const Scales& scales, const uint4& rb0,
+                                                      const uint4& rb1, bool want_dq,
+                                                      int rule = 0) {
   BlockResult r;
-  const float amax = __uint_as_float(amax_bits << 16);
   const uint32_t c6 = scale_encode<FMT>(__fmul_rn(amax, ss.rden6));
   float d6, inv6;
   scales(c6, d6, inv6);
@@ -221,6 +222,15 @@ __device__ __forceinline__ BlockResult encode_block(const f2 (&lo)[4], const f2 
     r.dq[1] = dequant8(q, d);
   }
   return r;
+}
+template <int FMT, bool SR, bool FOS, class Scales>
+__device__ __forceinline__ BlockResult encode_block(const f2 (&lo)[4], const f2 (&hi)[4],
+                                                    uint32_t amax_bits, const SliceScale& ss,
+                                                    const Scales& scales, const uint4& rb0,
+                                                    const uint4& rb1, bool want_dq,
+                                                    int rule = 0) {
+  return encode_block_f<FMT, SR, FOS>(lo, hi, __uint_as_float(amax_bits << 16), ss, scales, rb0,
+                                      rb1, want_dq, rule);
 }
 
 // Per-slice block-scale table in shared memory: for every code c of the

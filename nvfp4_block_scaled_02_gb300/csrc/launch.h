@@ -86,6 +86,25 @@ struct TokenParams {
 };
 cudaError_t launch_quant_token(const TokenParams& p, int fmt, bool sr, int fos, cudaStream_t st);
 
+// De-quantise -> transpose -> re-quantise of a row encoding of [S][R][C].
+struct RequantParams {
+  const uint8_t* codes;   // source codes [S][R][C/2]
+  const uint8_t* scales;  // source scale bytes [S][R][C/16]
+  int64_t S, R, C;
+  const float* gamax;     // [S], the forward encoding's global amax
+  int src_fmt;            // source block-scale format
+  float M_src, M_dst;     // outer-scale FP8 maxima of the source and target
+  uint32_t seed, step;
+  uint8_t* out_codes;     // MX: [S][C][R] E4M3; NVFP4: [S][C][R/2]
+  uint8_t* out_scales;    // MX: [S][C][R/32] E8M0; NVFP4: [S][C][R/16]
+  uint32_t* out_choice;   // NVFP4 with 4/6: pre-zeroed bitmap
+  int32_t* status;
+  int rule;               // 4/6 selection metric
+};
+// target 0 = MXFP8, 1 = NVFP4 (dst_fmt, fos as launch_quant_row)
+cudaError_t launch_requant(const RequantParams& p, int target, int dst_fmt, bool sr, int fos,
+                           cudaStream_t st);
+
 // Per-slice global amax.
 cudaError_t launch_amax(const uint16_t* x, int64_t S, int64_t n, float* amax, int32_t* status,
                         cudaStream_t st);

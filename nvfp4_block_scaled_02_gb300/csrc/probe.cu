@@ -9,7 +9,8 @@ namespace nvfp4 {
 namespace {
 
 // Ops 0 and 3 run the kernels' own 8-value helpers (e2m1x8_rn, sr8) on
-// groups of 8 consecutive inputs; ops 1 and 2 the block-scale encoders.
+// groups of 8 consecutive inputs; ops 1 and 2 the block-scale encoders; ops
+// 4..6 the MXFP8 element encoders and shared exponent of re-quantisation.
 __global__ void codec_probe_kernel(int op, const float* __restrict__ in,
                                    const uint32_t* __restrict__ aux, int64_t n,
                                    uint8_t* __restrict__ out) {
@@ -18,6 +19,16 @@ __global__ void codec_probe_kernel(int op, const float* __restrict__ in,
   if (op == 1 || op == 2) {
     for (int64_t i = t0; i < n; i += stride)
       out[i] = (uint8_t)(op == 1 ? e4m3_encode(in[i]) : ue5m3_encode(in[i]));
+    return;
+  }
+  if (op >= 4) {  // MXFP8 element encoders and the shared exponent
+    for (int64_t i = t0; i < n; i += stride) {
+      uint32_t c;
+      if (op == 4) c = e4m3x4_rn(in[i], 0.0f, 0.0f, 0.0f);
+      else if (op == 5) c = e4m3_sr(in[i], 0xFFFFu - (aux[i] & 0xFFFFu));
+      else c = (uint32_t)(mx_shared_exp(in[i]) + 127);
+      out[i] = (uint8_t)(c & 0xFFu);
+    }
     return;
   }
   const int64_t ngroups = (n + 7) / 8;

@@ -106,7 +106,10 @@ def _declare(L):
     L.orc_requant.restype = C.c_int
     L.orc_requant.argtypes = [C.c_int, C.c_float, C.c_int, _u8p, _u8p, _i64, _i64, _i64, _f32p,
                               C.c_int, C.c_int, C.c_uint32, C.c_uint32, C.c_int, C.c_int,
-                              C.c_float, _u8p, _u8p, _u32p]
+                              C.c_int, C.c_float, _u8p, _u8p, _u32p]
+    L.orc_e4m3_rne_array.argtypes = [_f32p, _i64, _u8p]
+    L.orc_e4m3_sr_array.argtypes = [_f32p, _u32p, _i64, _u8p]
+    L.orc_mx_shared_exp_array.argtypes = [_f32p, _i64, _u8p]
     L.orc_fakequant_fwd.restype = C.c_int
     L.orc_fakequant_fwd.argtypes = [_u16p, _i64, _i64, _f32p, _f32p, _u16p]
     L.orc_scale_grad_bwd.restype = C.c_int
@@ -283,16 +286,28 @@ def scale_grad_bwd(x_bf16, gq_bf16, s_pre, s_post=None, want_gx: bool = True):
 # ------------------------------------------------------- re-quantisation --
 
 def e4m3_sr(y, v16) -> np.ndarray:
-    L = lib()
-    y = np.asarray(y, np.float32).ravel()
-    v = np.broadcast_to(np.asarray(v16, np.uint32), y.shape).ravel()
-    return np.array([L.orc_e4m3_sr(float(a), int(b)) for a, b in zip(y, v)], np.uint8)
+    """Signed E4M3 codes of y by stochastic rounding with 16-bit draws v16."""
+    y = _c(np.asarray(y, np.float32).ravel(), np.float32)
+    v = _c(np.broadcast_to(np.asarray(v16, np.uint32), y.shape), np.uint32)
+    out = np.empty(y.size, np.uint8)
+    lib().orc_e4m3_sr_array(_p(y, _f32p), _p(v, _u32p), y.size, _p(out, _u8p))
+    return out
 
 
 def e4m3_rne(y) -> np.ndarray:
-    L = lib()
-    return np.array([L.orc_e4m3_rne(float(a)) for a in np.asarray(y, np.float32).ravel()],
-                    np.uint8)
+    """Signed E4M3 codes of y, round to nearest even, saturating at 448."""
+    y = _c(np.asarray(y, np.float32).ravel(), np.float32)
+    out = np.empty(y.size, np.uint8)
+    lib().orc_e4m3_rne_array(_p(y, _f32p), y.size, _p(out, _u8p))
+    return out
+
+
+def mx_shared_exp_bytes(amax) -> np.ndarray:
+    """E8M0 bytes (e + 127) of the MX shared exponents of the given amaxes."""
+    a = _c(np.asarray(amax, np.float32).ravel(), np.float32)
+    out = np.empty(a.size, np.uint8)
+    lib().orc_mx_shared_exp_array(_p(a, _f32p), a.size, _p(out, _u8p))
+    return out
 
 
 def e4m3_signed_value(codes) -> np.ndarray:
@@ -328,7 +343,8 @@ def dequant(codes, scales, gamax, *, scale_fmt=0, scale_max=0.0, four_over_six=0
 
 
 def requant(codes, scales, gamax, *, target=0, rounding=1, seed=0, step=0, src_fmt=0,
-            src_scale_max=0.0, src_fos=0, dst_fmt=0, dst_fos=0, dst_scale_max=0.0) -> dict:
+            src_scale_max=0.0, src_fos=0, dst_fmt=0, dst_fos=0, dst_rule=0,
+            dst_scale_max=0.0) -> dict:
     """De-quantise a row encoding [S][R][C], transpose, re-quantise: target 0 =
     MXFP8 (codes [S][C][R], E8M0 scales [S][C][R/32]), 1 = NVFP4 (codes
     [S][C][R/2], scales [S][C][R/16], bitmap when dst_fos)."""
@@ -347,5 +363,6 @@ def requant(codes, scales, gamax, *, target=0, rounding=1, seed=0, step=0, src_f
         ch = np.zeros((S, (R * Cc // 16 + 31) // 32), np.uint32) if dst_fos else None
     st = lib().orc_requant(src_fmt, src_scale_max, src_fos, _p(codes, _u8p), _p(scales, _u8p),
                            S, R, Cc, _p(gam, _f32p), target, rounding, seed, step, dst_fmt,
-                           dst_fos, dst_scale_max, _p(oc, _u8p), _p(os_, _u8p), _p(ch, _u32p))
+                           dst_fos, dst_rule, dst_scale_max, _p(oc, _u8p), _p(os_, _u8p),
+                           _p(ch, _u32p))
     return dict(codes=oc, scales=os_, choice=ch, status=st)

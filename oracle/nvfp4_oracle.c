@@ -498,7 +498,9 @@ int orc_scale_grad_bwd(const uint16_t* x, const uint16_t* gq, int64_t R, int64_t
  *
  * Readings:
  *  R9  De-quantised value (fp32, no bf16 rounding): q * d with
- *      d = dec(scale) * g exactly as in the forward encoding.
+ *      d = dec(scale) * g exactly as in the forward encoding. A value that
+ *      is not finite (scale times g overflowing fp32, possible only for a
+ *      global amax near FLT_MAX) is reported as non-finite input.
  *  R10 MXFP8 (the pages name MXFP8: E4M3 values with one E8M0 power-of-two
  *      scale per 32): per block of 32 values along the transposed rows, the
  *      shared exponent e is the smallest integer with amax <= 448 * 2^e
@@ -533,6 +535,18 @@ uint8_t orc_e4m3_rne(float y) {
 float orc_e4m3_signed_value(uint8_t code) {
   float v = orc_e4m3_value(code & 0x7F);
   return (code & 0x80) ? -v : v;
+}
+
+/* Array forms, used by the exhaustive codec tests. */
+void orc_e4m3_rne_array(const float* y, int64_t n, uint8_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_e4m3_rne(y[i]);
+}
+void orc_e4m3_sr_array(const float* y, const uint32_t* v16, int64_t n, uint8_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_e4m3_sr(y[i], v16[i]);
+}
+int orc_mx_shared_exp(float amax);
+void orc_mx_shared_exp_array(const float* amax, int64_t n, uint8_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = (uint8_t)(orc_mx_shared_exp(amax[i]) + 127);
 }
 
 /* R10: the MX shared exponent of a block whose largest |value| is amax: the
@@ -582,6 +596,7 @@ int orc_dequant(int fmt, float scale_max, int fos, const uint8_t* codes,
       float d = orc_scale_value(fmt, scales[e / 16]) * g;
       uint8_t c = (e & 1) ? (codes[e / 2] >> 4) : (codes[e / 2] & 15);
       out[e] = orc_e2m1_value(c) * d;
+      if (!isfinite(out[e])) st |= ORC_ST_NONFINITE_INPUT;
     }
   }
   return st;
@@ -590,12 +605,12 @@ int orc_dequant(int fmt, float scale_max, int fos, const uint8_t* codes,
 /* De-quantise -> transpose -> re-quantise. target 0 = MXFP8 (out_codes
  * [S][C][R] E4M3 bytes, out_scales [S][C][R/32] E8M0 bytes; R % 32 == 0),
  * target 1 = NVFP4 (out_codes [S][C][R/2], out_scales [S][C][R/16], 4/6
- * bitmap when dst_fos). */
+ * bitmap when dst_fos, selected under dst_rule). */
 int orc_requant(int src_fmt, float src_scale_max, int src_fos, const uint8_t* codes,
                 const uint8_t* scales, int64_t S, int64_t R, int64_t C, const float* gamax,
                 int target, int rounding, uint32_t seed, uint32_t step, int dst_fmt,
-                int dst_fos, float dst_scale_max, uint8_t* out_codes, uint8_t* out_scales,
-                uint32_t* out_choice) {
+                int dst_fos, int dst_rule, float dst_scale_max, uint8_t* out_codes,
+                uint8_t* out_scales, uint32_t* out_choice) {
   int64_t N = S * R * C;
   float* xh = (float*)malloc((size_t)(N > 0 ? N : 1) * sizeof(float));
   float* xt = (float*)malloc((size_t)(N > 0 ? N : 1) * sizeof(float));
@@ -614,7 +629,7 @@ int orc_requant(int src_fmt, float src_scale_max, int src_fos, const uint8_t* co
     float M = dst_scale_max > 0.0f ? dst_scale_max : (dst_fos ? 256.0f : 448.0f);
     float* g = (float*)malloc((size_t)(S > 0 ? S : 1) * sizeof(float));
     for (int64_t s = 0; s < S; ++s) st |= global_decode_scale(gamax[s], M, &g[s]);
-    encode_rows(xt, S, C, R, g, dst_fmt, rounding, dst_fos, 0, seed, step, 2, out_codes,
+    encode_rows(xt, S, C, R, g, dst_fmt, rounding, dst_fos, dst_rule, seed, step, 2, out_codes,
                 out_scales, out_choice, NULL);
     free(g);
   }

@@ -112,6 +112,44 @@ def test_per_token_argument_errors(L):
     assert pt(C.byref(_cfg()), None, 0, 32, None, None, None, None) == 0
 
 
+def rq(L, src, dst, target=0, codes=FAKE, scales=FAKE, S=1, R=32, Cc=32, amax=FAKE, out=None,
+       status=None):
+    return L.nvfp4_requant_transpose(C.byref(src) if src is not None else None,
+                                     C.byref(dst) if dst is not None else None, target, codes,
+                                     scales, S, R, Cc, amax,
+                                     C.byref(out) if out is not None else None, status, None)
+
+
+def test_requant_argument_errors(L):
+    s, d = _cfg(), _cfg(rounding=1)
+    ok = _out(dq=0)
+    assert rq(L, None, d, out=ok) == 1
+    assert rq(L, s, None, out=ok) == 1
+    assert rq(L, s, d, target=2, out=ok) == 4
+    for bad in (dict(scale_fmt=2), dict(four_over_six=2), dict(scale_max=-1.0)):
+        assert rq(L, _cfg(**bad), d, out=ok) == 4, bad
+    assert rq(L, s, _cfg(rounding=2), out=ok) == 4
+    # target-side format fields matter only for the NVFP4 target
+    assert rq(L, s, _cfg(scale_fmt=5), target=1, out=ok) == 4
+    assert rq(L, s, _cfg(four_over_six_rule=3), target=1, out=ok) == 4
+    assert rq(L, s, d, R=16, out=ok) == 2                # MXFP8 needs rows % 32
+    assert rq(L, s, d, target=1, R=8, out=ok) == 2       # NVFP4 needs rows % 16
+    assert rq(L, s, d, Cc=24, out=ok) == 2               # the source needs cols % 16
+    assert rq(L, s, d, S=-1, out=ok) == 2
+    assert rq(L, s, d, codes=0, out=ok) == 1
+    assert rq(L, s, d, scales=0, out=ok) == 1
+    assert rq(L, s, d, amax=0, out=ok) == 1
+    assert rq(L, s, d, out=None) == 1
+    assert rq(L, s, d, out=_out(codes=0, dq=0)) == 1
+    assert rq(L, s, _cfg(four_over_six=1), target=1, out=_out(choice=0, dq=0)) == 1
+    assert rq(L, s, d, out=_out()) == 4                  # dequant output not offered
+    assert rq(L, s, d, codes=FAKE + 8, out=ok) == 3
+    assert rq(L, s, d, out=_out(scales=FAKE + 1, dq=0)) == 3
+    assert rq(L, s, d, amax=FAKE + 2, out=ok) == 3
+    for S, R, Cc in ((0, 32, 32), (1, 0, 32), (1, 32, 0)):
+        assert rq(L, s, d, codes=0, scales=0, S=S, R=R, Cc=Cc, amax=0, out=None) == 0
+
+
 def test_amax_argument_errors(L):
     assert L.nvfp4_amax(FAKE, -1, 4, 4, FAKE, None, None) == 2
     assert L.nvfp4_amax(FAKE, 1, 4, 4, None, None, None) == 1
