@@ -230,21 +230,39 @@ __device__ __forceinline__ uint32_t e4m3x4_rn(float y0, float y1, float y2, floa
       : "=r"(w) : "f"(y0), "f"(y1), "f"(y2), "f"(y3));
   return w;
 }
-// Stochastic rounding of y onto the signed E4M3 grid with nv = 0xFFFF - v
-// (v the 16 random bits): |y| rounds up iff v / 2^16 < p, p the position of
-// |y| between its two grid neighbours. Same construction as sr_mag: with
-// T = code_lo * 2^16 + ceil(p * 2^16) the magnitude code is (T + nv) >> 16.
-// Normal range (|y| >= 2^-6): the top 3 mantissa bits and the exponent of the
-// fp32 pattern ARE code_lo once the exponent is rebiased (127 -> 7), and the
-// 20 bits below them are p * 2^20, so T = (bits - (120 << 23) + 15) >> 4.
-// Subnormal range (step 2^-9): T = ceil(|y| * 2^25), one fma rounded up
-// against 2^23. |y| >= 448 (and NaN) is capped at 448, code 0x7E.
+// Stochastic rounding onto the signed E4M3 grid, for |y| <= 448: |y| rounds
+// up iff v / 2^16 < p, p the position of |y| between its two grid neighbours
+// and v the 16 random bits. n8 = ((0xFFFF - v) << 8) | 0x400000F0 (the
+// constant fills bytes the random bits do not use). Returns a word whose top
+// byte is the signed code.
+// Construction (as in sr_mag): with T = code_lo * 2^16 + ceil(p * 2^16), the
+// magnitude code is (T + 0xFFFF - v) >> 16. Normal range (|y| >= 2^-6): the
+// exponent and top 3 mantissa bits of the fp32 pattern are code_lo once the
+// exponent is rebiased (127 -> 7) and the 20 bits below are p * 2^20, so with
+// everything scaled by 16, (bits << 4) - (120 << 27) + 15 * 16 + ((0xFFFF - v)
+// << 8) holds the code in its top byte (the sign bit is shifted out; 15 * 16
+// rounds the 4 dropped bits up). Below 2^-6 (the subnormals; the grid
+// spacing is 2^-9 up to 2^-5): T = ceil(|y| * 2^25), one fma rounded up
+// against 2^23, and the same expression is reached from the stand-in pattern
+// (120 << 23) + 16 T. The sign is OR-ed in from y.
+__device__ __forceinline__ uint32_t e4m3_sr_hi(float y, uint32_t n8) {
+  const uint32_t Y = __float_as_uint(y);
+  const float a = fabsf(y);
+  const uint32_t F = __float_as_uint(__fmaf_ru(a, 33554432.0f, 8388608.0f));
+  const uint32_t Ys = F * 16u + 0x8C000000u;  // (120 << 23) + 16 (F - (150 << 23))
+  const uint32_t Ye = a < 0.015625f ? Ys : Y;
+  return ((Ye << 4) + n8) | (Y & 0x80000000u);
+}
+// (0xFFFF - v) << 8 | 0x400000F0 for the 16-bit half h of the complemented
+// draw word nw = ~w (v = half h of w): one byte permute.
+__device__ __forceinline__ uint32_t e4m3_sr_n8(uint32_t nw, int h) {
+  return __byte_perm(nw, 0x400000F0u, h ? 0x7324u : 0x7104u);
+}
+// One value, saturating: |y| >= 448 (and NaN) gives +-448 (code 0x7E).
 __device__ __forceinline__ uint32_t e4m3_sr(float y, uint32_t nv) {
-  const uint32_t sign = (__float_as_uint(y) >> 24) & 0x80u;
-  const float a = fminf(fabsf(y), 448.0f);
-  const uint32_t tn = (__float_as_uint(a) - 0x3C000000u + 15u) >> 4;
-  const uint32_t ts = __float_as_uint(__fmaf_ru(a, 33554432.0f, 8388608.0f)) - 0x4B000000u;
-  return sign | (((a < 0.015625f ? ts : tn) + nv) >> 16);
+  const float c = __uint_as_float(__float_as_uint(fminf(fabsf(y), 448.0f)) |
+                                  (__float_as_uint(y) & 0x80000000u));
+  return e4m3_sr_hi(c, ((nv & 0xFFFFu) << 8) | 0x400000F0u) >> 24;
 }
 // Shared exponent of an MX block whose largest |value| is amax: the smallest
 // e with amax <= 448 * 2^e (448 = E4M3's largest value), i.e. the unbiased
