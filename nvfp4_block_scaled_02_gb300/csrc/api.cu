@@ -288,10 +288,10 @@ nvfp4_status nvfp4_scale_grad_bwd(const void* x, const void* gq, int64_t rows, i
 
 nvfp4_status nvfp4_codec_probe(int32_t op, const float* in, const uint32_t* aux, int64_t n,
                                uint8_t* out, void* stream) {
-  if (op < 0 || op > 6) return NVFP4_ERR_ENUM;
+  if (op < 0 || op > 7) return NVFP4_ERR_ENUM;
   if (n < 0) return NVFP4_ERR_SHAPE;
   if (n == 0) return NVFP4_OK;
-  if (!in || !out || ((op == 3 || op == 5) && !aux)) return NVFP4_ERR_NULL;
+  if (!in || !out || ((op == 3 || op == 5 || op == 7) && !aux)) return NVFP4_ERR_NULL;
   if (!aligned(in, 4) || !aligned(aux, 4)) return NVFP4_ERR_ALIGN;
   return cuda_status(
       nvfp4::launch_codec_probe(op, in, aux, n, out, static_cast<cudaStream_t>(stream)));

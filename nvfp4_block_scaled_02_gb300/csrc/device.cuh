@@ -188,6 +188,14 @@ __device__ __forceinline__ float fmin3(float a, float b, float c) {
   return r;
 }
 
+// Three-input fp32 maximum (one instruction on sm_100 and later); like fmaxf
+// it returns the other operands when one is NaN.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // Stochastic E2M1 rounding of 8 values (4 pairs) with the group's 128 random
 // bits rb (value k uses the 16-bit half k%2 of word k/2): |y| rounds up to the
 // next grid value iff v / 2^16 < p, p = (|y| - lo) / (hi - lo).
@@ -252,6 +260,14 @@ __device__ __forceinline__ uint32_t e4m3_sr_hi(float y, uint32_t n8) {
   const uint32_t Ys = F * 16u + 0x8C000000u;  // (120 << 23) + 16 (F - (150 << 23))
   const uint32_t Ye = a < 0.015625f ? Ys : Y;
   return ((Ye << 4) + n8) | (Y & 0x80000000u);
+}
+// The same for a y known to be 0 or at least 2^-6 in magnitude: clamping |y|
+// up to 2^-7 sends zeros to code 0 through the normal-range expression (their
+// pattern then contributes (120 << 23) << 4, which the constant cancels).
+__device__ __forceinline__ uint32_t e4m3_sr_hi_normal(float y, uint32_t n8) {
+  const uint32_t Y = __float_as_uint(y);
+  const uint32_t A = __float_as_uint(fmaxf(fabsf(y), 0.0078125f));
+  return ((A << 4) + n8) | (Y & 0x80000000u);
 }
 // (0xFFFF - v) << 8 | 0x400000F0 for the 16-bit half h of the complemented
 // draw word nw = ~w (v = half h of w): one byte permute.

@@ -10,7 +10,7 @@ namespace {
 
 // Ops 0 and 3 run the kernels' own 8-value helpers (e2m1x8_rn, sr8) on
 // groups of 8 consecutive inputs; ops 1 and 2 the block-scale encoders; ops
-// 4..6 the MXFP8 element encoders and shared exponent of re-quantisation.
+// 4..7 the MXFP8 element encoders and shared exponent of re-quantisation.
 __global__ void codec_probe_kernel(int op, const float* __restrict__ in,
                                    const uint32_t* __restrict__ aux, int64_t n,
                                    uint8_t* __restrict__ out) {
@@ -26,6 +26,8 @@ __global__ void codec_probe_kernel(int op, const float* __restrict__ in,
       uint32_t c;
       if (op == 4) c = e4m3x4_rn(in[i], 0.0f, 0.0f, 0.0f);
       else if (op == 5) c = e4m3_sr(in[i], 0xFFFFu - (aux[i] & 0xFFFFu));
+      else if (op == 7)
+        c = e4m3_sr_hi_normal(in[i], (((0xFFFFu - aux[i]) & 0xFFFFu) << 8) | 0x400000F0u) >> 24;
       else c = (uint32_t)(mx_shared_exp(in[i]) + 127);
       out[i] = (uint8_t)(c & 0xFFu);
     }

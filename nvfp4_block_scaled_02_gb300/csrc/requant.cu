@@ -135,26 +135,24 @@ __device__ __forceinline__ uint4 sr_bits_or_zero(const RequantParams& p, uint64_
   else return make_uint4(0, 0, 0, 0);
 }
 
-// 8 values scaled by sc -> 8 E4M3 codes (two words, element 0 in the low
-// byte of the first), RNE or stochastic with the group's random bits rb.
-template <bool SR>
-__device__ __forceinline__ uint2 e4m3x8(const float* v, float sc, const uint4& rb) {
-  float y[8];
+// 8 scaled values -> 8 E4M3 codes by stochastic rounding with the group's
+// random bits rb (two words, element 0 in the low byte of the first).
+// normal: every value is 0 or at least 2^-6 in magnitude.
+__device__ __forceinline__ uint2 e4m3x8_sr(const float* y, const uint4& rb, bool normal) {
+  const uint32_t nw[4] = {~rb.x, ~rb.y, ~rb.z, ~rb.w};
+  uint32_t x[8];
+  if (normal) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) y[i] = __fmul_rn(v[i], sc);
-  if constexpr (!SR) {
-    return make_uint2(e4m3x4_rn(y[0], y[1], y[2], y[3]), e4m3x4_rn(y[4], y[5], y[6], y[7]));
+    for (int i = 0; i < 8; ++i) x[i] = e4m3_sr_hi_normal(y[i], e4m3_sr_n8(nw[i >> 1], i & 1));
   } else {
-    const uint32_t nw[4] = {~rb.x, ~rb.y, ~rb.z, ~rb.w};
-    uint32_t x[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) x[i] = e4m3_sr_hi(y[i], e4m3_sr_n8(nw[i >> 1], i & 1));
-    // the codes are the top bytes
-    return make_uint2(__byte_perm(__byte_perm(x[0], x[1], 0x0073u),
-                                  __byte_perm(x[2], x[3], 0x0073u), 0x5410u),
-                      __byte_perm(__byte_perm(x[4], x[5], 0x0073u),
-                                  __byte_perm(x[6], x[7], 0x0073u), 0x5410u));
   }
+  // the codes are the top bytes
+  return make_uint2(__byte_perm(__byte_perm(x[0], x[1], 0x0073u),
+                                __byte_perm(x[2], x[3], 0x0073u), 0x5410u),
+                    __byte_perm(__byte_perm(x[4], x[5], 0x0073u),
+                                __byte_perm(x[6], x[7], 0x0073u), 0x5410u));
 }
 
 // Resident CTAs per SM the register allocation is held to (the kernel is
@@ -172,6 +170,11 @@ __global__ void __launch_bounds__(kThreads, min_blocks(TARGET, SR, FOS)) requant
   __shared__ __align__(16) float4 s_x[TR * kSlots];
   __shared__ float s_src[256];
   __shared__ float s_d[NV ? 256 : 1], s_inv[NV ? 256 : 1];
+  // MXFP8 with stochastic rounding: per 16-row band and 16-column block of the
+  // tile, the smallest non-zero source block scale d (fp32 bits; two buffers
+  // by tile parity so the next tile's can be cleared while this one is read)
+  constexpr bool MXSR = !NV && SR;
+  __shared__ uint32_t s_dmin[MXSR ? 2 : 1][4][8];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int q = lane & 3, cp = lane >> 2;  // phase 2: 16-row quarter, column pair
@@ -196,6 +199,9 @@ __global__ void __launch_bounds__(kThreads, min_blocks(TARGET, SR, FOS)) requant
   const int cpair = 16 * warp + 2 * cp;
   const int64_t out_off0 = (int64_t)cpair * R + 16 * q;
 
+  if constexpr (MXSR) {
+    if (tid < 32) (&s_dmin[0][0][0])[tid] = 0x7F800000u;  // ordered by the first table barrier
+  }
   SrcRegs v;
   load_src(p, ntiles > 0, ti, L, v);
   int64_t cur_slice = -1;
@@ -214,6 +220,9 @@ __global__ void __launch_bounds__(kThreads, min_blocks(TARGET, SR, FOS)) requant
       const int bi = k * kThreads + tid;
       const int row = bi >> 3, cb = bi & 7;
       const float d = s_src[v.scale[k]];
+      if constexpr (MXSR) {
+        if (d > 0.0f) atomicMin(&s_dmin[it & 1][row >> 4][cb], __float_as_uint(d));
+      }
       f2 qv[4];
       float4* dst = s_x + row * kSlots;
       const f2 dd = make_float2(d, d);
@@ -246,29 +255,65 @@ __global__ void __launch_bounds__(kThreads, min_blocks(TARGET, SR, FOS)) requant
     float2 xv[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) xv[i] = xc[i * (TC / 2)];
+    if constexpr (!NV) {
+      // both columns at once: amax, shared exponent, scaling (packed)
+      float m0 = 0.0f, m1 = 0.0f;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int c = cpair + h;
-      const bool ok = row_ok && c0 + c < C;
-      float x[16];
+      for (int i = 0; i < 16; i += 2) {
+        m0 = fmax3(m0, fabsf(xv[i].x), fabsf(xv[i + 1].x));
+        m1 = fmax3(m1, fabsf(xv[i].y), fabsf(xv[i + 1].y));
+      }
+      // MX block of 32 = quarters q and q ^ 1
+      m0 = fmaxf(m0, __shfl_xor_sync(0xFFFFFFFFu, m0, 1));
+      m1 = fmaxf(m1, __shfl_xor_sync(0xFFFFFFFFu, m1, 1));
+      const int ex0 = mx_shared_exp(m0), ex1 = mx_shared_exp(m1);
+      const f2 scv = make_float2(exp2_neg(ex0), exp2_neg(ex1));
+      f2 y[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) x[i] = h ? xv[i].y : xv[i].x;
-      const int64_t e0 = out_base + out_off0 + h * R;  // flat output index of x[0]
-      float amax = 0.0f;
+      for (int i = 0; i < 16; ++i) y[i] = f2_mul(xv[i], scv);
+      if constexpr (MXSR) {
+        if (tid < 32) (&s_dmin[(it + 1) & 1][0][0])[tid] = 0x7F800000u;  // for the next tile
+      }
 #pragma unroll
-      for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
-      if constexpr (!NV) {
-        // MX block of 32 = quarters q and q ^ 1
-        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-        const int e = mx_shared_exp(amax);
-        const float sc = exp2_neg(e);
-        const uint2 lo = e4m3x8<SR>(x, sc, sr_bits_or_zero<SR>(p, (uint64_t)e0));
-        const uint2 hi = e4m3x8<SR>(x + 8, sc, sr_bits_or_zero<SR>(p, (uint64_t)e0 + 8));
-        if (ok) {
-          __stcs(reinterpret_cast<uint4*>(p.out_codes + e0), make_uint4(lo.x, lo.y, hi.x, hi.y));
-          if ((q & 1) == 0) p.out_scales[e0 / 32] = (uint8_t)(e + 127);
+      for (int h = 0; h < 2; ++h) {
+        const int c = cpair + h;
+        const bool ok = row_ok && c0 + c < C;
+        const int64_t e0 = out_base + out_off0 + h * R;  // flat output index of y[0].h
+        float yc[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) yc[i] = h ? y[i].y : y[i].x;
+        uint4 w;
+        if constexpr (!SR) {
+          w = make_uint4(e4m3x4_rn(yc[0], yc[1], yc[2], yc[3]), e4m3x4_rn(yc[4], yc[5], yc[6], yc[7]),
+                         e4m3x4_rn(yc[8], yc[9], yc[10], yc[11]),
+                         e4m3x4_rn(yc[12], yc[13], yc[14], yc[15]));
+        } else {
+          // every non-zero value of these 16 is at least 0.5 * dmin * 2^-e:
+          // when that is >= 2^-6 no value needs the 2^-9-spaced range
+          const float dmin = __uint_as_float(s_dmin[it & 1][q][warp]);
+          const bool normal = __fmul_rn(__fmul_rn(0.5f, dmin), h ? scv.y : scv.x) >= 0.015625f;
+          const uint2 a = e4m3x8_sr(yc, sr_group_bits(p.seed, p.step, 2u, (uint64_t)e0), normal);
+          const uint2 b =
+              e4m3x8_sr(yc + 8, sr_group_bits(p.seed, p.step, 2u, (uint64_t)e0 + 8), normal);
+          w = make_uint4(a.x, a.y, b.x, b.y);
         }
-      } else {
+        if (ok) {
+          __stcs(reinterpret_cast<uint4*>(p.out_codes + e0), w);
+          if ((q & 1) == 0) p.out_scales[e0 / 32] = (uint8_t)((h ? ex1 : ex0) + 127);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int c = cpair + h;
+        const bool ok = row_ok && c0 + c < C;
+        float x[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[i] = h ? xv[i].y : xv[i].x;
+        const int64_t e0 = out_base + out_off0 + h * R;  // flat output index of x[0]
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) amax = fmax3(amax, fabsf(x[i]), fabsf(x[i + 1]));
         f2 lo[4], hi[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {

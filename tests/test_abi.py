@@ -172,7 +172,8 @@ def test_ste_argument_errors(L):
 
 
 def test_diagnostics_argument_errors(L):
-    assert L.nvfp4_codec_probe(7, FAKE, None, 4, FAKE, None) == 4
+    assert L.nvfp4_codec_probe(8, FAKE, None, 4, FAKE, None) == 4
+    assert L.nvfp4_codec_probe(7, FAKE, None, 4, FAKE, None) == 1
     assert L.nvfp4_codec_probe(3, FAKE, None, 4, FAKE, None) == 1
     assert L.nvfp4_codec_probe(0, FAKE, None, -1, FAKE, None) == 2
     assert L.nvfp4_sr_bits(0, 0, 0, 0, 4, None, None) == 1

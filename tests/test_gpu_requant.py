@@ -96,6 +96,42 @@ def test_e4m3_stochastic_rounder_exhaustive_over_draws():
     assert_exact(got, oracle.e4m3_sr(y, v), "stochastic E4M3, all draws")
 
 
+def test_e4m3_stochastic_rounder_fast_form_exhaustive_over_draws():
+    """The form used when a group holds only zeros and values >= 2^-6: every
+    16-bit draw for values across its domain (zeros of both signs included)."""
+    cells = np.array([0.0, -0.0, 2.0 ** -6, 2.0 ** -6 * 1.01, -0.0173, 0.07, 1.3, 2.9, 17.0,
+                      100.1, 300.0, 447.9, 448.0, -5.5, -447.0], np.float32)
+    y = np.repeat(cells, 65536)
+    v = np.tile(np.arange(65536, dtype=np.uint32), cells.size)
+    got = nv.nvfp4_codec_probe(7, torch.from_numpy(y).cuda(),
+                               torch.from_numpy(v.view(np.int32)).cuda()).cpu().numpy()
+    assert_exact(got, oracle.e4m3_sr(y, v), "stochastic E4M3 (fast form), all draws")
+
+
+def test_e4m3_stochastic_rounder_fast_form_random():
+    rng = np.random.default_rng(33)
+    n = 1 << 22
+    mag = (rng.integers(0x3C800000, 0x43E00001, n, dtype=np.uint32)).view(np.float32)
+    y = np.where(rng.integers(0, 2, n) == 1, -mag, mag).astype(np.float32)
+    y[::97] = 0.0
+    v = rng.integers(0, 1 << 16, y.size, dtype=np.uint32)
+    got = nv.nvfp4_codec_probe(7, torch.from_numpy(y).cuda(),
+                               torch.from_numpy(v.view(np.int32)).cuda()).cpu().numpy()
+    assert_exact(got, oracle.e4m3_sr(y, v), "stochastic E4M3 (fast form)")
+
+
+def test_tiny_values_take_the_exact_rounder():
+    """Source blocks whose scale is 2^-16 of the others put values in the E4M3
+    2^-9-spaced range of their MX blocks (the kernel's exact form)."""
+    codes, scales, gam = _source((1, 64, 128), seed=30)
+    scales = scales.copy()
+    scales[0, ::5, ::3] = 0x01  # the smallest E4M3 scale: these values land below 2^-6
+    r = oracle.requant(codes, scales, gam, target=0, rounding=1, seed=3)
+    vals = np.abs(oracle.e4m3_signed_value(r["codes"]))
+    assert ((vals > 0) & (vals < 2.0 ** -6)).any()
+    run_both(codes, scales, gam, target=0, rounding=1, seed=3)
+
+
 # ------------------------------------------------------------ whole path --
 
 def _source(shape, *, fmt=0, fos=0, seed=0, dist="t3", stale=1.0):
