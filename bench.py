@@ -873,32 +873,51 @@ def main():
         dist.destroy_process_group()
 
 
-def kernel_source_hash() -> str:
-    """sha256 over the CUDA sources, so committed ncu counters can be matched
-    to the kernels they were taken from."""
+# the CUDA sources each timed kernel is built from
+_COMMON = ["device.cuh", "encode.cuh", "launch.h"]
+KERNEL_SOURCES = {
+    "amax": ["amax.cu", "device.cuh", "launch.h"],
+    "quantize_row": ["quant_row.cu"] + _COMMON,
+    "quantize_row_sr": ["quant_row.cu"] + _COMMON,
+    "quantize_dual": ["quant_dual.cu"] + _COMMON,
+    "quantize_per_token": ["quant_token.cu"] + _COMMON,
+    "fakequant_fwd": ["ste.cu", "device.cuh", "launch.h"],
+    "scale_grad_bwd": ["ste.cu", "device.cuh", "launch.h"],
+    "requant_mxfp8_sr": ["requant.cu"] + _COMMON,
+    "requant_nvfp4_sr": ["requant.cu"] + _COMMON,
+}
+
+
+def kernel_source_hash(kernel: str | None = None) -> str:
+    """sha256 over the CUDA sources of `kernel` (all of csrc/ when None), so
+    committed ncu counters can be matched to the code they were taken from."""
     import glob
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "nvfp4_block_scaled_02_gb300", "csrc")
-    for f in sorted(glob.glob(os.path.join(csrc, "*"))):
-        if f.endswith((".cu", ".cuh", ".h")):
-            with open(f, "rb") as fh:
-                h.update(os.path.basename(f).encode() + b"\0" + fh.read())
+    if kernel is None:
+        files = sorted(os.path.basename(f) for f in glob.glob(os.path.join(csrc, "*"))
+                       if f.endswith((".cu", ".cuh", ".h")))
+    else:
+        files = sorted(KERNEL_SOURCES.get(kernel, []))
+    for name in files:
+        with open(os.path.join(csrc, name), "rb") as fh:
+            h.update(name.encode() + b"\0" + fh.read())
     return h.hexdigest()[:16]
 
 
 def _committed_traffic(config: int, kernel: str):
     """DRAM bytes (read + write) per launch of `kernel` from the committed ncu
     summary (profiles/traffic.json), or None when absent or taken from other
-    kernel sources than the ones built now."""
+    sources of that kernel than the ones built now."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
             d = json.load(f)
-        if d.get("source_sha") != kernel_source_hash():
+        e = d.get("workloads", {}).get(str(config), {}).get(kernel)
+        if not e or e.get("source_sha") != kernel_source_hash(kernel):
             return None
-        v = d.get("workloads", {}).get(str(config), {}).get(kernel)
-        return None if v is None else float(v)
+        return float(e["bytes"])
     except Exception:
         return None
 
