@@ -110,6 +110,15 @@ def _declare(L):
     L.orc_e4m3_rne_array.argtypes = [_f32p, _i64, _u8p]
     L.orc_e4m3_sr_array.argtypes = [_f32p, _u32p, _i64, _u8p]
     L.orc_mx_shared_exp_array.argtypes = [_f32p, _i64, _u8p]
+    L.orc_fakequant_fwd_fp8.restype = C.c_int
+    L.orc_fakequant_fwd_fp8.argtypes = [_u16p, _i64, _i64, _f32p, _f32p, C.c_float, _u16p]
+    L.orc_scale_grad_bwd_fp8.restype = C.c_int
+    L.orc_scale_grad_bwd_fp8.argtypes = [_u16p, _u16p, _i64, _i64, _f32p, _f32p, C.c_float,
+                                         _u16p, _f32p, _f32p]
+    L.orc_scale_init_mse.restype = C.c_int
+    L.orc_scale_init_mse.argtypes = [_u16p, _i64, _i64, C.c_float, _u8p, _f32p, _f32p]
+    L.orc_export_scales.restype = C.c_int
+    L.orc_export_scales.argtypes = [_u16p, _i64, _i64, _f32p, _f32p, C.c_float, _u8p, _u8p]
     L.orc_fakequant_fwd.restype = C.c_int
     L.orc_fakequant_fwd.argtypes = [_u16p, _i64, _i64, _f32p, _f32p, _u16p]
     L.orc_scale_grad_bwd.restype = C.c_int
@@ -281,6 +290,63 @@ def scale_grad_bwd(x_bf16, gq_bf16, s_pre, s_post=None, want_gx: bool = True):
                                   _p(so, _f32p), _p(gx, _u16p), _p(gs_pre, _f32p),
                                   _p(gs_post, _f32p))
     return dict(gx=gx, gs_pre=gs_pre, gs_post=gs_post, status=st)
+
+
+# ------------------------------------------- scale learning, FP8 scales --
+
+def fakequant_fwd_fp8(x_bf16, s_pre, s_post, gamax):
+    """Fake quantisation at the FP8-rounded scales (s_post None = tied)."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    R, Cc = x.shape
+    sp = np.ascontiguousarray(s_pre, dtype=np.float32)
+    so = None if s_post is None else np.ascontiguousarray(s_post, dtype=np.float32)
+    xq = np.empty_like(x)
+    st = lib().orc_fakequant_fwd_fp8(_p(x, _u16p), R, Cc, _p(sp, _f32p), _p(so, _f32p),
+                                     float(gamax), _p(xq, _u16p))
+    return xq, st
+
+
+def scale_grad_bwd_fp8(x_bf16, gq_bf16, s_pre, s_post, gamax, want_gx: bool = True):
+    """STE backward at the FP8-rounded scales, gradients passed straight through."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    gq = np.ascontiguousarray(gq_bf16, dtype=np.uint16)
+    R, Cc = x.shape
+    sp = np.ascontiguousarray(s_pre, dtype=np.float32)
+    so = None if s_post is None else np.ascontiguousarray(s_post, dtype=np.float32)
+    gx = np.empty_like(x) if want_gx else None
+    gs_pre = np.empty(sp.shape, np.float32)
+    gs_post = None if so is None else np.empty(sp.shape, np.float32)
+    st = lib().orc_scale_grad_bwd_fp8(_p(x, _u16p), _p(gq, _u16p), R, Cc, _p(sp, _f32p),
+                                      _p(so, _f32p), float(gamax), _p(gx, _u16p),
+                                      _p(gs_pre, _f32p), _p(gs_post, _f32p))
+    return dict(gx=gx, gs_pre=gs_pre, gs_post=gs_post, status=st)
+
+
+def scale_init_mse(x_bf16, gamax):
+    """MSE scale setting with the FP8 sweep: per block the E4M3 code, its scale
+    dec(code) * g and the winning block sum of squared errors."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    R, Cc = x.shape
+    codes = np.empty((R, Cc // 16), np.uint8)
+    s = np.empty((R, Cc // 16), np.float32)
+    sse = np.empty((R, Cc // 16), np.float32)
+    st = lib().orc_scale_init_mse(_p(x, _u16p), R, Cc, float(gamax), _p(codes, _u8p),
+                                  _p(s, _f32p), _p(sse, _f32p))
+    return dict(codes=codes, s=s, sse=sse, status=st)
+
+
+def export_scales(x_bf16, s_pre, s_post, gamax):
+    """NVFP4 row encoding carrying the learned post-scales: codes [R][C/2] and
+    E4M3 scale bytes [R][C/16] (s_post None = tied)."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    R, Cc = x.shape
+    sp = np.ascontiguousarray(s_pre, dtype=np.float32)
+    so = None if s_post is None else np.ascontiguousarray(s_post, dtype=np.float32)
+    codes = np.empty((R, Cc // 2), np.uint8)
+    scales = np.empty((R, Cc // 16), np.uint8)
+    st = lib().orc_export_scales(_p(x, _u16p), R, Cc, _p(sp, _f32p), _p(so, _f32p),
+                                 float(gamax), _p(codes, _u8p), _p(scales, _u8p))
+    return dict(codes=codes, scales=scales, status=st)
 
 
 # ------------------------------------------------------- re-quantisation --

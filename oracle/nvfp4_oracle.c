@@ -637,3 +637,162 @@ int orc_requant(int src_fmt, float src_scale_max, int src_fos, const uint8_t* co
   free(xt);
   return st;
 }
+
+/* --------------------------------------------- scale learning, FP8 scales - */
+/* Scale Learning blog, "How Scale Learning Works" (the block scale is itself
+ * quantised to FP8, with a straight-through estimator there as well) and
+ * "Using Scale Learning" (MSE scale setting with an FP8 scale sweep; the
+ * learned post-scale is what the exported checkpoint carries).
+ *
+ * Readings:
+ *  R12 FP8 scale unit per tensor: g = gamax / (6 * 448) (g = 1 for a zero
+ *      amax, as R3 with M = 448), rg = 1/g clamped to FLT_MAX;
+ *      Q8(s) = dec(E4M3(s * rg)) * g for s >= 0 (E4M3 by R2).
+ *  R13 STE through the FP8 scale: the fake-quant forward and the STE backward
+ *      are evaluated at Q8(s_pre), Q8(s_post) (one Q8(s) when tied); their
+ *      scale gradients are returned as the gradients of the unquantised
+ *      scales (the derivative of Q8 taken as 1). Bad scale: s_pre not a
+ *      normal positive number, s_post negative or not finite, or
+ *      Q8(s_pre) < FLT_MIN.
+ *  R14 MSE scale setting with an FP8 sweep: per 1x16 block, every positive
+ *      finite E4M3 code c = 1..126 is a candidate scale s_c = dec(c) * g; its
+ *      error is the fake quantisation of the block at s_c: q_i =
+ *      clamp(round(x_i * inv_c)), inv_c = 1/s_c (clamped to FLT_MAX, 0 when
+ *      s_c = 0), e_i = fma(-q_i, s_c, x_i), summed as block_sum(e, e). The
+ *      smallest sum wins; ties keep the smaller code.
+ *  R15 Export: the codes are the FP8-scale fake-quant forward's q (rounding
+ *      at Q8(s_pre)), the scale byte is E4M3(s_post * rg); de-quantised with
+ *      the same g (R9) it reproduces that forward. */
+
+typedef struct {
+  float g, rg;
+} fp8_unit;
+
+static int fp8_scale_unit(float gamax, fp8_unit* u) {
+  int st = global_decode_scale(gamax, 448.0f, &u->g);
+  float rg = 1.0f / u->g;
+  u->rg = rg > FLT_MAX ? FLT_MAX : rg;
+  return st;
+}
+static uint8_t q8_code(float s, const fp8_unit* u) { return orc_scale_encode(0, s * u->rg); }
+static float q8_value(float s, const fp8_unit* u) {
+  return orc_scale_value(0, q8_code(s, u)) * u->g;
+}
+
+/* R13: bad-scale status of the raw scales and their FP8 roundings. */
+static int fp8_scale_status(const float* s_pre, const float* s_post, int64_t nb,
+                            const float* sp_q) {
+  int st = 0;
+  for (int64_t b = 0; b < nb; ++b) {
+    float sp = s_pre[b], so = s_post ? s_post[b] : sp;
+    if (!(sp >= FLT_MIN && sp <= FLT_MAX) || !(so >= 0.0f && so <= FLT_MAX) ||
+        !(sp_q[b] >= FLT_MIN))
+      st |= ORC_ST_BAD_SCALE;
+  }
+  return st;
+}
+
+/* R12/R13: Q8 of every scale of an array (NULL in, NULL out). */
+static float* q8_array(const float* s, int64_t nb, const fp8_unit* u) {
+  if (!s) return NULL;
+  float* out = (float*)malloc((size_t)(nb > 0 ? nb : 1) * sizeof(float));
+  for (int64_t b = 0; b < nb; ++b) out[b] = s[b] >= 0.0f ? q8_value(s[b], u) : 0.0f;
+  return out;
+}
+
+int orc_fakequant_fwd_fp8(const uint16_t* x, int64_t R, int64_t C, const float* s_pre,
+                          const float* s_post, float gamax, uint16_t* xq) {
+  fp8_unit u;
+  int64_t nb = R * C / 16;
+  int st = fp8_scale_unit(gamax, &u);
+  float* sp = q8_array(s_pre, nb, &u);
+  float* so = q8_array(s_post, nb, &u);
+  st |= fp8_scale_status(s_pre, s_post, nb, sp);
+  st |= orc_fakequant_fwd(x, R, C, sp, so, xq);
+  free(sp);
+  free(so);
+  return st;
+}
+
+int orc_scale_grad_bwd_fp8(const uint16_t* x, const uint16_t* gq, int64_t R, int64_t C,
+                           const float* s_pre, const float* s_post, float gamax, uint16_t* gx,
+                           float* gs_pre, float* gs_post) {
+  fp8_unit u;
+  int64_t nb = R * C / 16;
+  int st = fp8_scale_unit(gamax, &u);
+  float* sp = q8_array(s_pre, nb, &u);
+  float* so = q8_array(s_post, nb, &u);
+  st |= fp8_scale_status(s_pre, s_post, nb, sp);
+  st |= orc_scale_grad_bwd(x, gq, R, C, sp, so, gx, gs_pre, gs_post);
+  free(sp);
+  free(so);
+  return st;
+}
+
+/* R14: the block SSE of fake quantisation at scale s (inv as R14 says). */
+static float fakequant_sse(const float* x, float s) {
+  float inv = 0.0f;
+  if (s > 0.0f) {
+    inv = 1.0f / s;
+    if (inv > FLT_MAX) inv = FLT_MAX;
+  }
+  float e[16];
+  for (int i = 0; i < 16; ++i) {
+    float q = orc_e2m1_value(orc_e2m1_rne(x[i] * inv));
+    e[i] = fmaf(-q, s, x[i]);
+  }
+  return block_sum(e, e);
+}
+
+int orc_scale_init_mse(const uint16_t* x, int64_t R, int64_t C, float gamax, uint8_t* codes,
+                       float* s_out, float* sse_out) {
+  fp8_unit u;
+  int st = fp8_scale_unit(gamax, &u);
+  int64_t nb = R * C / 16;
+  for (int64_t b = 0; b < nb; ++b) {
+    float xb[16];
+    for (int i = 0; i < 16; ++i) {
+      uint16_t h = x[b * 16 + i];
+      if ((h & 0x7FFFu) >= 0x7F80u) st |= ORC_ST_NONFINITE_INPUT;
+      xb[i] = orc_bf16_to_f32(h);
+    }
+    int best = 1;
+    float best_sse = 0.0f;
+    for (int c = 1; c <= 126; ++c) {
+      float sse = fakequant_sse(xb, orc_scale_value(0, (uint8_t)c) * u.g);
+      if (c == 1 || sse < best_sse) {
+        best = c;
+        best_sse = sse;
+      }
+    }
+    if (codes) codes[b] = (uint8_t)best;
+    if (s_out) s_out[b] = orc_scale_value(0, (uint8_t)best) * u.g;
+    if (sse_out) sse_out[b] = best_sse;
+  }
+  return st;
+}
+
+/* R15: export of learned scales to an NVFP4 row encoding [R][C]. */
+int orc_export_scales(const uint16_t* x, int64_t R, int64_t C, const float* s_pre,
+                      const float* s_post, float gamax, uint8_t* codes, uint8_t* scales) {
+  fp8_unit u;
+  int64_t nb = R * C / 16;
+  int st = fp8_scale_unit(gamax, &u);
+  float* sp = q8_array(s_pre, nb, &u);
+  st |= fp8_scale_status(s_pre, s_post, nb, sp);
+  for (int64_t b = 0; b < nb; ++b) {
+    float inv = 1.0f / sp[b];
+    float so = s_post ? s_post[b] : s_pre[b];
+    scales[b] = so >= 0.0f ? q8_code(so, &u) : 0;
+    for (int i = 0; i < 16; i += 2) {
+      int64_t e = b * 16 + i;
+      if ((x[e] & 0x7FFFu) >= 0x7F80u || (x[e + 1] & 0x7FFFu) >= 0x7F80u)
+        st |= ORC_ST_NONFINITE_INPUT;
+      uint8_t q0 = orc_e2m1_rne(orc_bf16_to_f32(x[e]) * inv);
+      uint8_t q1 = orc_e2m1_rne(orc_bf16_to_f32(x[e + 1]) * inv);
+      codes[e / 2] = (uint8_t)((q0 & 15) | ((q1 & 15) << 4));
+    }
+  }
+  free(sp);
+  return st;
+}
