@@ -1,6 +1,6 @@
 """Throughput of the NVFP4 hot path on one or more GB300s.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..8] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..10] [--impl ours|reference]
 
 A step is one pass of the hot path over one batch of synthetic input already
 resident in HBM. The default workload is the activation tensor 8192 x 4096 bf16
@@ -488,6 +488,122 @@ class RequantActivation(Workload):
            "NVFP4 (E4M3 scales, Four-Over-Six)") + "; outputs codes, scales"))
 
 
+class ScaleLearningFp8(ScaleLearning):
+    """Workload 3's scale-learning step with FP8 block scales: fake-quant
+    forward and STE backward at the E4M3-rounded dual scales, the gradients
+    passed straight through."""
+
+    def __init__(self, device, rows=14336, cols=4096, seed=2):
+        super().__init__(device, rows, cols, seed)
+        wb = self.host[0]
+        gam = float(np.abs(synth.bf16_bits_to_f32(wb)).max())
+        self.gamax = torch.tensor([gam * 1.5], dtype=torch.float32, device=device)
+        L = nv.lib()
+        st = torch.cuda.current_stream(device).cuda_stream
+        R, Cc = rows, cols
+
+        def fwd(i):
+            d = self.sets[i]
+            return L.nvfp4_fakequant_fwd_fp8scale(d["w"].data_ptr(), R, Cc, d["sp"].data_ptr(),
+                                                  d["so"].data_ptr(), self.gamax.data_ptr(),
+                                                  d["xq"].data_ptr(), self.status.data_ptr(), st)
+
+        def bwd(i):
+            d = self.sets[i]
+            return L.nvfp4_scale_grad_bwd_fp8scale(
+                d["w"].data_ptr(), d["g"].data_ptr(), R, Cc, d["sp"].data_ptr(),
+                d["so"].data_ptr(), self.gamax.data_ptr(), d["gx"].data_ptr(),
+                d["gsp"].data_ptr(), d["gso"].data_ptr(), self.status.data_ptr(), st)
+        self._fwd, self._bwd = fwd, bwd
+
+    def kernels(self, k, i):
+        return [Kernel("fakequant_fwd_fp8", self.f_bytes, lambda: self._fwd(i)),
+                Kernel("scale_grad_bwd_fp8", self.b_bytes, lambda: self._bwd(i))]
+
+    def cpu_sample(self, budget_s):
+        import oracle
+        wb, gb, s = self.host
+        gam = float(self.gamax.item())
+        rows = 256
+        t0 = time.perf_counter()
+        oracle.fakequant_fwd_fp8(wb[:rows], s[:rows], s[:rows], gam)
+        oracle.scale_grad_bwd_fp8(wb[:rows], gb[:rows], s[:rows], s[:rows], gam)
+        per_row = (time.perf_counter() - t0) / rows
+        rows = int(min(self.rows, max(256, budget_s / max(per_row, 1e-9))))
+        t0 = time.perf_counter()
+        oracle.fakequant_fwd_fp8(wb[:rows], s[:rows], s[:rows], gam)
+        oracle.scale_grad_bwd_fp8(wb[:rows], gb[:rows], s[:rows], s[:rows], gam)
+        return rows * self.cols, time.perf_counter() - t0, \
+            f"first {rows} of {self.rows} rows (forward + backward, FP8 scales)"
+
+    dominant = "scale_grad_bwd_fp8"
+    workload = property(lambda self: (
+        f"scale-learning step on weight {self.rows}x{self.cols} bf16 N(0,0.02) with FP8 "
+        "(E4M3) dual block scales in units of 1.5*amax/2688 (init amax/6, jittered): fake-quant "
+        "forward + STE backward at the rounded scales, gradients passed straight through"))
+
+
+class ScaleInitExport(ScaleLearningFp8):
+    """MSE scale setting over every E4M3 scale of each block, then the export
+    of the (post-)scales to an NVFP4 encoding, on workload 3's weight."""
+
+    def __init__(self, device, rows=14336, cols=4096, seed=2):
+        super().__init__(device, rows, cols, seed)
+        L = nv.lib()
+        st = torch.cuda.current_stream(device).cuda_stream
+        R, Cc = rows, cols
+        for d in self.sets:
+            d["codes"] = torch.empty((R, Cc // 16), dtype=torch.uint8, device=device)
+            d["enc"] = nv.alloc_encoding(1, R, Cc, device, False, dequant=False)
+            d["eo"] = nv._Out(d["enc"]["codes"].data_ptr(), d["enc"]["scales"].data_ptr(), None,
+                              None)
+        self.i_bytes = self.elements * (2 + 1 / 16 + 4 / 16)
+        self.e_bytes = self.elements * (2 + 0.5 + 0.5 + 1 / 16)
+
+        def init(i):
+            d = self.sets[i]
+            return L.nvfp4_scale_init_mse(d["w"].data_ptr(), R, Cc, self.gamax.data_ptr(),
+                                          d["codes"].data_ptr(), d["sp"].data_ptr(),
+                                          self.status.data_ptr(), st)
+
+        def export(i):
+            d = self.sets[i]
+            return L.nvfp4_export_scales(d["w"].data_ptr(), R, Cc, d["sp"].data_ptr(),
+                                         d["so"].data_ptr(), self.gamax.data_ptr(),
+                                         C.byref(d["eo"]), self.status.data_ptr(), st)
+        self._init, self._export = init, export
+
+    def kernels(self, k, i):
+        return [Kernel("scale_init_mse", self.i_bytes, lambda: self._init(i)),
+                Kernel("export_scales", self.e_bytes, lambda: self._export(i))]
+
+    def e2e_io(self, k):
+        d = self.sets[0]
+        return [d["w"], d["so"]], [d["codes"], d["sp"], d["enc"]["codes"], d["enc"]["scales"]]
+
+    def cpu_sample(self, budget_s):
+        import oracle
+        wb, _, s = self.host
+        gam = float(self.gamax.item())
+        rows = 4
+        t0 = time.perf_counter()
+        oracle.scale_init_mse(wb[:rows], gam)
+        per_row = (time.perf_counter() - t0) / rows
+        rows = int(min(self.rows, max(4, budget_s / max(per_row, 1e-9))))
+        t0 = time.perf_counter()
+        oracle.scale_init_mse(wb[:rows], gam)
+        oracle.export_scales(wb[:rows], s[:rows], s[:rows], gam)
+        return rows * self.cols, time.perf_counter() - t0, \
+            f"first {rows} of {self.rows} rows (MSE sweep over 126 E4M3 scales + export)"
+
+    bytes_per_elem = property(lambda self: (self.i_bytes + self.e_bytes) / self.elements)
+    dominant = "scale_init_mse"
+    workload = property(lambda self: (
+        f"weight {self.rows}x{self.cols} bf16 N(0,0.02): MSE scale setting over all 126 E4M3 "
+        "scales per 1x16 block (codes + fp32 scales), then export of the post-scales to an "
+        "NVFP4 row encoding (codes + E4M3 scale bytes)"))
+
+
 class RequantActivationNvfp4(RequantActivation):
     def __init__(self, device):
         super().__init__(device, target=1)
@@ -495,7 +611,7 @@ class RequantActivationNvfp4(RequantActivation):
 
 WORKLOADS = {1: SmallNormal, 2: Activation, 3: ScaleLearning, 4: DriftingGradient,
              5: MoeExperts, 6: PerTokenActivation, 7: RequantActivation,
-             8: RequantActivationNvfp4}
+             8: RequantActivationNvfp4, 9: ScaleLearningFp8, 10: ScaleInitExport}
 
 
 # --------------------------------------------------------------- clocks --
@@ -771,6 +887,28 @@ def _reference_sample(args):
         return ("activation 8192x4096 NVFP4 (4/6) re-quantised, transposed, SR to "
                 + ("MXFP8" if target == 0 else "NVFP4")), bpe, \
             f"first {n} of 8192 source rows per step", step
+    if args.config in (9, 10):
+        wb, gb, s = synth.scale_learning(seed=2)
+        gam = float(np.abs(synth.bf16_bits_to_f32(wb)).max()) * 1.5
+        if args.config == 9:
+            n = args.ref_rows
+
+            def step():
+                t0 = time.perf_counter()
+                oracle.fakequant_fwd_fp8(wb[:n], s[:n], s[:n], gam)
+                oracle.scale_grad_bwd_fp8(wb[:n], gb[:n], s[:n], s[:n], gam)
+                return n * wb.shape[1], time.perf_counter() - t0
+            return "scale-learning step 14336x4096, FP8 scales", 11.5, \
+                f"first {n} of 14336 rows per step", step
+        n = max(1, args.ref_rows // 64)
+
+        def step():
+            t0 = time.perf_counter()
+            oracle.scale_init_mse(wb[:n], gam)
+            oracle.export_scales(wb[:n], s[:n], s[:n], gam)
+            return n * wb.shape[1], time.perf_counter() - t0
+        return "MSE scale sweep + export 14336x4096", 2 + 1 / 16 + 4 / 16 + 2 + 0.5 + 0.5 + 1 / 16, \
+            f"first {n} of 14336 rows per step", step
     xb = synth.moe_experts(1, 2048, 7168, seed=4)[0]
     sub = xb[:max(16, args.ref_rows - args.ref_rows % 16)]
 
@@ -816,7 +954,7 @@ def main():
     if args.steps is None:
         # about two seconds of device time, so the clock samples cover the run
         args.steps = {1: 20000, 2: 40000, 3: 10000, 4: 16000, 5: 150, 6: 50000, 7: 40000,
-                      8: 40000}[args.config]
+                      8: 40000, 9: 10000, 10: 300}[args.config]
     total_ms, per_kernel, clk, wall = time_ours(wl, args, world, local)
     total_ms = max_over_ranks(total_ms, world)
     units = wl.elements * args.steps * world
@@ -881,10 +1019,14 @@ KERNEL_SOURCES = {
     "quantize_row_sr": ["quant_row.cu"] + _COMMON,
     "quantize_dual": ["quant_dual.cu"] + _COMMON,
     "quantize_per_token": ["quant_token.cu"] + _COMMON,
-    "fakequant_fwd": ["ste.cu", "device.cuh", "launch.h"],
-    "scale_grad_bwd": ["ste.cu", "device.cuh", "launch.h"],
+    "fakequant_fwd": ["ste.cu"] + _COMMON,
+    "scale_grad_bwd": ["ste.cu"] + _COMMON,
     "requant_mxfp8_sr": ["requant.cu"] + _COMMON,
     "requant_nvfp4_sr": ["requant.cu"] + _COMMON,
+    "fakequant_fwd_fp8": ["ste.cu"] + _COMMON,
+    "scale_grad_bwd_fp8": ["ste.cu"] + _COMMON,
+    "scale_init_mse": ["scale_init.cu"] + _COMMON,
+    "export_scales": ["ste.cu"] + _COMMON,
 }
 
 

@@ -180,6 +180,61 @@ NVFP4_API nvfp4_status nvfp4_scale_grad_bwd(const void* x, const void* gq, int64
                                   float* gs_pre, float* gs_post, int32_t* status,
                                   void* stream);
 
+/* ---- scale learning with FP8 block scales --------------------------------
+ * Scale Learning blog, "How Scale Learning Works" (the per-block scale is
+ * itself quantised to FP8 and passed through with a straight-through
+ * estimator; the learned post-scale is baked into the exported checkpoint)
+ * and "Using Scale Learning" (MSE scale setting with an FP8 scale sweep).
+ * Shared definitions: global_amax is a device fp32 [1] holding the tensor's
+ * global amax; g = global_amax / (6 * 448) (1 when it is 0), rg = 1/g clamped
+ * to FLT_MAX; Q8(s) = dec(E4M3_RNE(s * rg)) * g for s >= 0. x: bf16
+ * [rows][cols], cols % 16 == 0; per-block arrays [rows][cols/16]. */
+
+/* As nvfp4_fakequant_fwd, evaluated at Q8(s_pre) and Q8(s_post) (Q8(s_pre)
+ * alone when s_post is NULL). NVFP4_DEV_BAD_SCALE also when s_post is
+ * negative or Q8(s_pre) is below FLT_MIN; NVFP4_DEV_BAD_AMAX for a NaN, Inf or
+ * negative global amax. */
+NVFP4_API nvfp4_status nvfp4_fakequant_fwd_fp8scale(const void* x, int64_t rows, int64_t cols,
+                                                    const float* s_pre, const float* s_post,
+                                                    const float* global_amax, void* xq,
+                                                    int32_t* status, void* stream);
+
+/* As nvfp4_scale_grad_bwd, evaluated at the FP8-rounded scales; the scale
+ * gradients are returned as the gradients of the unrounded scales (the
+ * derivative of Q8 taken as 1). Same errors as the fp32 form plus those of
+ * nvfp4_fakequant_fwd_fp8scale. */
+NVFP4_API nvfp4_status nvfp4_scale_grad_bwd_fp8scale(const void* x, const void* gq, int64_t rows,
+                                                     int64_t cols, const float* s_pre,
+                                                     const float* s_post,
+                                                     const float* global_amax, void* gx,
+                                                     float* gs_pre, float* gs_post,
+                                                     int32_t* status, void* stream);
+
+/* MSE scale setting: per 1x16 block, every E4M3 scale s_c = dec(c) * g for
+ * c = 1..126 is tried; the block is fake-quantised at s_c (q =
+ * clamp(round(x * (1/s_c))), 1/s_c clamped to FLT_MAX) and the error
+ * e = fma(-q, s_c, x) summed in the fixed block order of
+ * nvfp4_scale_grad_bwd; the smallest sum wins, ties keep the smaller code.
+ * Outputs (either may be NULL, not both): scale_codes u8 [rows][cols/16], the
+ * winning code; s fp32 [rows][cols/16], its scale dec(code) * g (an initial
+ * s_pre = s_post for scale learning). Errors: NULL x / global_amax / both
+ * outputs, cols % 16, misalignment. */
+NVFP4_API nvfp4_status nvfp4_scale_init_mse(const void* x, int64_t rows, int64_t cols,
+                                            const float* global_amax, uint8_t* scale_codes,
+                                            float* s, int32_t* status, void* stream);
+
+/* Export of learned scales to an NVFP4 row encoding: out->codes [rows][cols/2]
+ * are the codes of nvfp4_fakequant_fwd_fp8scale (rounding x * (1/Q8(s_pre))),
+ * out->scales [rows][cols/16] the E4M3 bytes of s_post (of s_pre when s_post
+ * is NULL) in units of g, so that de-quantising with the same global amax
+ * (M = 448, E4M3 scales) gives that forward's output. out->choice is ignored;
+ * out->dequant must be NULL (NVFP4_ERR_ENUM). Errors and status bits as
+ * nvfp4_fakequant_fwd_fp8scale. */
+NVFP4_API nvfp4_status nvfp4_export_scales(const void* x, int64_t rows, int64_t cols,
+                                           const float* s_pre, const float* s_post,
+                                           const float* global_amax, const nvfp4_out* out,
+                                           int32_t* status, void* stream);
+
 /* nvfp4_requant_transpose target */
 #define NVFP4_TARGET_MXFP8 0 /* E4M3 values, one E8M0 power-of-two scale per 32 */
 #define NVFP4_TARGET_NVFP4 1 /* the NVFP4 row encoding of the transposed tensor  */

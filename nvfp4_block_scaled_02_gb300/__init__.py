@@ -23,6 +23,8 @@ __all__ = [
     "Config", "Nvfp4Error", "build", "lib", "nvfp4_amax", "nvfp4_quantize",
     "nvfp4_fakequant_fwd", "nvfp4_scale_grad_bwd", "nvfp4_codec_probe", "nvfp4_sr_bits",
     "nvfp4_quantize_per_token", "nvfp4_requant_transpose", "TARGET_MXFP8", "TARGET_NVFP4",
+    "nvfp4_fakequant_fwd_fp8scale", "nvfp4_scale_grad_bwd_fp8scale", "nvfp4_scale_init_mse",
+    "nvfp4_export_scales",
     "alloc_encoding", "alloc_requant", "PeriodicAmax", "BLOCKS_ROW", "BLOCKS_COL", "BLOCKS_BOTH",
     "SCALE_E4M3", "SCALE_UE5M3", "ROUND_RNE", "ROUND_SR", "FOS_MSE", "FOS_MAE", "FOS_MAX",
     "DEV_NONFINITE_INPUT", "DEV_BAD_SCALE", "DEV_BAD_AMAX",
@@ -108,12 +110,21 @@ def lib() -> C.CDLL:
             L.nvfp4_requant_transpose.argtypes = [C.POINTER(_Config), C.POINTER(_Config), _i32,
                                                   _vp, _vp, _i64, _i64, _i64, _vp,
                                                   C.POINTER(_Out), _vp, _vp]
+            L.nvfp4_fakequant_fwd_fp8scale.argtypes = [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp,
+                                                       _vp]
+            L.nvfp4_scale_grad_bwd_fp8scale.argtypes = [_vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp,
+                                                        _vp, _vp, _vp, _vp]
+            L.nvfp4_scale_init_mse.argtypes = [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp]
+            L.nvfp4_export_scales.argtypes = [_vp, _i64, _i64, _vp, _vp, _vp, C.POINTER(_Out),
+                                              _vp, _vp]
             L.nvfp4_codec_probe.argtypes = [_i32, _vp, _vp, _i64, _vp, _vp]
             L.nvfp4_sr_bits.argtypes = [_u32, _u32, _u32, C.c_uint64, _i64, _vp, _vp]
             L.nvfp4_status_string.restype = C.c_char_p
             L.nvfp4_status_string.argtypes = [C.c_int]
             for name in ("nvfp4_amax", "nvfp4_quantize", "nvfp4_quantize_per_token",
                          "nvfp4_requant_transpose", "nvfp4_fakequant_fwd",
+                         "nvfp4_fakequant_fwd_fp8scale", "nvfp4_scale_grad_bwd_fp8scale",
+                         "nvfp4_scale_init_mse", "nvfp4_export_scales",
                          "nvfp4_scale_grad_bwd", "nvfp4_codec_probe", "nvfp4_sr_bits"):
                 getattr(L, name).restype = C.c_int
             _lib = L
@@ -311,6 +322,63 @@ def nvfp4_scale_grad_bwd(x: torch.Tensor, gq: torch.Tensor, s_pre: torch.Tensor,
         _stream(x.device)))
     return {"gx": gx if want_gx else None, "gs_pre": gs_pre,
             "gs_post": gs_post if s_post is not None else None}
+
+
+def nvfp4_fakequant_fwd_fp8scale(x: torch.Tensor, s_pre: torch.Tensor,
+                                 s_post: torch.Tensor | None, global_amax: torch.Tensor,
+                                 out: torch.Tensor | None = None,
+                                 status: torch.Tensor | None = None) -> torch.Tensor:
+    """Fake quantisation at FP8-rounded block scales (global_amax: fp32 [1])."""
+    R, Cc = x.shape
+    out = torch.empty_like(x) if out is None else out
+    _check("nvfp4_fakequant_fwd_fp8scale", lib().nvfp4_fakequant_fwd_fp8scale(
+        _bf16(x, "x"), R, Cc, _dev(s_pre, "s_pre"), _dev(s_post, "s_post"),
+        _dev(global_amax, "global_amax"), _bf16(out, "out"), _dev(status, "status"),
+        _stream(x.device)))
+    return out
+
+
+def nvfp4_scale_grad_bwd_fp8scale(x: torch.Tensor, gq: torch.Tensor, s_pre: torch.Tensor,
+                                  s_post: torch.Tensor | None, global_amax: torch.Tensor,
+                                  want_gx: bool = True,
+                                  status: torch.Tensor | None = None) -> dict:
+    """STE backward at FP8-rounded block scales, gradients passed straight through."""
+    R, Cc = x.shape
+    gx = torch.empty_like(x) if want_gx else None
+    gs_pre = torch.empty_like(s_pre)
+    gs_post = torch.empty_like(s_post) if s_post is not None else None
+    _check("nvfp4_scale_grad_bwd_fp8scale", lib().nvfp4_scale_grad_bwd_fp8scale(
+        _bf16(x, "x"), _bf16(gq, "gq"), R, Cc, _dev(s_pre, "s_pre"), _dev(s_post, "s_post"),
+        _dev(global_amax, "global_amax"), _dev(gx, "gx"), _dev(gs_pre, "gs_pre"),
+        _dev(gs_post, "gs_post"), _dev(status, "status"), _stream(x.device)))
+    return {"gx": gx, "gs_pre": gs_pre, "gs_post": gs_post}
+
+
+def nvfp4_scale_init_mse(x: torch.Tensor, global_amax: torch.Tensor,
+                         status: torch.Tensor | None = None) -> dict:
+    """MSE scale setting over every E4M3 scale per 1x16 block: {"codes", "s"}."""
+    R, Cc = x.shape
+    codes = torch.empty((R, Cc // 16), dtype=torch.uint8, device=x.device)
+    s = torch.empty((R, Cc // 16), dtype=torch.float32, device=x.device)
+    _check("nvfp4_scale_init_mse", lib().nvfp4_scale_init_mse(
+        _bf16(x, "x"), R, Cc, _dev(global_amax, "global_amax"), _dev(codes, "codes"),
+        _dev(s, "s"), _dev(status, "status"), _stream(x.device)))
+    return {"codes": codes, "s": s}
+
+
+def nvfp4_export_scales(x: torch.Tensor, s_pre: torch.Tensor, s_post: torch.Tensor | None,
+                        global_amax: torch.Tensor, out: dict | None = None,
+                        status: torch.Tensor | None = None) -> dict:
+    """NVFP4 row encoding carrying learned post-scales: {"codes", "scales"}."""
+    R, Cc = x.shape
+    if out is None:
+        out = alloc_encoding(1, R, Cc, x.device, False, dequant=False)
+    o = _Out(_dev(out["codes"], "codes"), _dev(out["scales"], "scales"), None, None)
+    _check("nvfp4_export_scales", lib().nvfp4_export_scales(
+        _bf16(x, "x"), R, Cc, _dev(s_pre, "s_pre"), _dev(s_post, "s_post"),
+        _dev(global_amax, "global_amax"), C.byref(o), _dev(status, "status"),
+        _stream(x.device)))
+    return out
 
 
 def nvfp4_codec_probe(op: int, inp: torch.Tensor, aux: torch.Tensor | None = None,

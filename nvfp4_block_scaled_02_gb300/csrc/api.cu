@@ -286,6 +286,100 @@ nvfp4_status nvfp4_scale_grad_bwd(const void* x, const void* gq, int64_t rows, i
   return cuda_status(nvfp4::launch_scale_grad_bwd(p, static_cast<cudaStream_t>(stream)));
 }
 
+static nvfp4_status fp8_common(const float* global_amax, int32_t* status) {
+  if (!global_amax) return NVFP4_ERR_NULL;
+  if (!aligned(global_amax, 4) || !aligned(status, 4)) return NVFP4_ERR_ALIGN;
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_fakequant_fwd_fp8scale(const void* x, int64_t rows, int64_t cols,
+                                          const float* s_pre, const float* s_post,
+                                          const float* global_amax, void* xq, int32_t* status,
+                                          void* stream) {
+  nvfp4_status e = ste_common(x, rows, cols, s_pre);
+  if (e != NVFP4_OK || rows == 0 || cols == 0) return e;
+  if ((e = fp8_common(global_amax, status)) != NVFP4_OK) return e;
+  if (!xq) return NVFP4_ERR_NULL;
+  if (!aligned(xq, 16) || !aligned(s_post, 4)) return NVFP4_ERR_ALIGN;
+  nvfp4::SteParams p{};
+  p.x = static_cast<const uint4*>(x);
+  p.nblocks = rows * cols / 16;
+  p.s_pre = s_pre;
+  p.s_post = s_post;
+  p.out = static_cast<uint4*>(xq);
+  p.status = status;
+  p.gamax = global_amax;
+  return cuda_status(nvfp4::launch_fakequant_fwd(p, static_cast<cudaStream_t>(stream)));
+}
+
+nvfp4_status nvfp4_scale_grad_bwd_fp8scale(const void* x, const void* gq, int64_t rows,
+                                           int64_t cols, const float* s_pre, const float* s_post,
+                                           const float* global_amax, void* gx, float* gs_pre,
+                                           float* gs_post, int32_t* status, void* stream) {
+  nvfp4_status e = ste_common(x, rows, cols, s_pre);
+  if (e != NVFP4_OK || rows == 0 || cols == 0) return e;
+  if ((e = fp8_common(global_amax, status)) != NVFP4_OK) return e;
+  if (!gq || !gs_pre) return NVFP4_ERR_NULL;
+  if (s_post && !gs_post) return NVFP4_ERR_NULL;
+  if (!s_post && gs_post) return NVFP4_ERR_NULL;
+  if (!aligned(gq, 16) || !aligned(gx, 16) || !aligned(gs_pre, 4) || !aligned(gs_post, 4) ||
+      !aligned(s_post, 4))
+    return NVFP4_ERR_ALIGN;
+  nvfp4::SteParams p{};
+  p.x = static_cast<const uint4*>(x);
+  p.gq = static_cast<const uint4*>(gq);
+  p.nblocks = rows * cols / 16;
+  p.s_pre = s_pre;
+  p.s_post = s_post;
+  p.out = static_cast<uint4*>(gx);
+  p.gs_pre = gs_pre;
+  p.gs_post = gs_post;
+  p.status = status;
+  p.gamax = global_amax;
+  return cuda_status(nvfp4::launch_scale_grad_bwd(p, static_cast<cudaStream_t>(stream)));
+}
+
+nvfp4_status nvfp4_scale_init_mse(const void* x, int64_t rows, int64_t cols,
+                                  const float* global_amax, uint8_t* scale_codes, float* s,
+                                  int32_t* status, void* stream) {
+  if (rows < 0 || cols < 0 || cols % 16 != 0) return NVFP4_ERR_SHAPE;
+  if (rows == 0 || cols == 0) return NVFP4_OK;
+  if (!x || (!scale_codes && !s)) return NVFP4_ERR_NULL;
+  nvfp4_status e = fp8_common(global_amax, status);
+  if (e != NVFP4_OK) return e;
+  if (!aligned(x, 16) || !aligned(s, 4)) return NVFP4_ERR_ALIGN;
+  nvfp4::ScaleInitParams p{};
+  p.x = static_cast<const uint4*>(x);
+  p.nblocks = rows * cols / 16;
+  p.gamax = global_amax;
+  p.codes = scale_codes;
+  p.s = s;
+  p.status = status;
+  return cuda_status(nvfp4::launch_scale_init_mse(p, static_cast<cudaStream_t>(stream)));
+}
+
+nvfp4_status nvfp4_export_scales(const void* x, int64_t rows, int64_t cols, const float* s_pre,
+                                 const float* s_post, const float* global_amax,
+                                 const nvfp4_out* out, int32_t* status, void* stream) {
+  nvfp4_status e = ste_common(x, rows, cols, s_pre);
+  if (e != NVFP4_OK || rows == 0 || cols == 0) return e;
+  if ((e = fp8_common(global_amax, status)) != NVFP4_OK) return e;
+  if (!out || !out->codes || !out->scales) return NVFP4_ERR_NULL;
+  if (out->dequant) return NVFP4_ERR_ENUM;
+  if (!aligned(out->codes, 16) || !aligned(out->scales, 16) || !aligned(s_post, 4))
+    return NVFP4_ERR_ALIGN;
+  nvfp4::SteParams p{};
+  p.x = static_cast<const uint4*>(x);
+  p.nblocks = rows * cols / 16;
+  p.s_pre = s_pre;
+  p.s_post = s_post;
+  p.status = status;
+  p.gamax = global_amax;
+  p.codes = out->codes;
+  p.scales = out->scales;
+  return cuda_status(nvfp4::launch_export_scales(p, static_cast<cudaStream_t>(stream)));
+}
+
 nvfp4_status nvfp4_codec_probe(int32_t op, const float* in, const uint32_t* aux, int64_t n,
                                uint8_t* out, void* stream) {
   if (op < 0 || op > 7) return NVFP4_ERR_ENUM;

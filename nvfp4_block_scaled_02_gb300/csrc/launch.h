@@ -120,9 +120,24 @@ struct SteParams {
   float* gs_pre;
   float* gs_post;
   int32_t* status;
+  const float* gamax;   // [1]: FP8-rounded scales in units of gamax / (6 * 448); null = fp32 scales
+  uint8_t* codes;       // export: NVFP4 codes [R][C/2]
+  uint8_t* scales;      // export: E4M3 scale bytes [R][C/16]
 };
 cudaError_t launch_fakequant_fwd(const SteParams& p, cudaStream_t st);
 cudaError_t launch_scale_grad_bwd(const SteParams& p, cudaStream_t st);
+cudaError_t launch_export_scales(const SteParams& p, cudaStream_t st);
+
+// MSE scale setting over every E4M3 scale of each 1x16 block.
+struct ScaleInitParams {
+  const uint4* x;       // bf16 [R][C], C % 16 == 0
+  int64_t nblocks;
+  const float* gamax;   // [1]
+  uint8_t* codes;       // [nblocks] or null
+  float* s;             // [nblocks] or null
+  int32_t* status;
+};
+cudaError_t launch_scale_init_mse(const ScaleInitParams& p, cudaStream_t st);
 
 // Diagnostics.
 cudaError_t launch_codec_probe(int op, const float* in, const uint32_t* aux, int64_t n,

@@ -1,6 +1,7 @@
 // ste.cu -- scale learning: fake quantisation forward and the straight-
 // through-estimator backward for single (tied) and dual (pre/post) per-block
-// scales (Scale Learning blog, "How Scale Learning Works").
+// scales, with fp32 or FP8-rounded scales, and the export of learned scales
+// to an NVFP4 encoding (Scale Learning blog, "How Scale Learning Works").
 //
 // Both kernels stream 1x16 row blocks with two lanes per block (8 values and
 // one 128-bit load per lane per tensor). Per-block sums are fp32 in the fixed
@@ -26,14 +27,49 @@ __device__ __forceinline__ bool finite8(const uint4& v) {
   return absmax_bits4(v) < 0x7F80u;
 }
 
+// FP8 block scales (Scale Learning blog, "How Scale Learning Works": the scale
+// is itself quantised to FP8): per tensor g = gamax / (6 * 448) (1 for a zero
+// or bad amax), rg = 1/g clamped to FLT_MAX; Q8(s) = dec(E4M3(s * rg)) * g
+// for s >= 0. The raw scales must be usable too: s_pre a normal positive
+// number, s_post finite and not negative, and Q8(s_pre) not below FLT_MIN.
+struct Fp8Unit {
+  float g, rg;
+  bool bad;
+};
+__device__ __forceinline__ Fp8Unit fp8_unit(const float* gamax) {
+  const SliceScale ss = slice_scale(*gamax, 448.0f);
+  return Fp8Unit{ss.g, fminf(__frcp_rn(ss.g), kFltMax), ss.bad};
+}
+__device__ __forceinline__ uint32_t q8_code(float s, const Fp8Unit& u) {
+  return e4m3_encode(__fmul_rn(s, u.rg));
+}
+__device__ __forceinline__ float q8(float s, const Fp8Unit& u) {
+  return s >= 0.0f ? __fmul_rn(e4m3_value(q8_code(s, u)), u.g) : 0.0f;
+}
+__device__ __forceinline__ bool raw_fp8_scales_ok(float sp, float so, float spq) {
+  return sp >= kFltMin && sp <= kFltMax && so >= 0.0f && so <= kFltMax && spq >= kFltMin;
+}
+
+template <bool Q8>
 __global__ void __launch_bounds__(kThreads) fakequant_fwd_kernel(const SteParams p) {
   const int64_t nchunks = p.nblocks * 2;
   const int64_t stride = (int64_t)gridDim.x * kThreads;
+  Fp8Unit u{1.0f, 1.0f, false};
+  if constexpr (Q8) {
+    u = fp8_unit(p.gamax);
+    if (u.bad && blockIdx.x == 0 && threadIdx.x == 0) flag(p.status, NVFP4_DEV_BAD_AMAX_BIT);
+  }
   for (int64_t ch = (int64_t)blockIdx.x * kThreads + threadIdx.x; ch < nchunks; ch += stride) {
     const int64_t b = ch >> 1;
     const uint4 v = __ldcs(p.x + ch);
-    const float sp = p.s_pre[b];
-    const float so = p.s_post ? p.s_post[b] : sp;
+    float sp = p.s_pre[b];
+    float so = p.s_post ? p.s_post[b] : sp;
+    if constexpr (Q8) {
+      const float spr = sp, sor = so;
+      sp = q8(spr, u);
+      so = q8(sor, u);
+      if ((ch & 1) == 0 && !raw_fp8_scales_ok(spr, sor, sp)) flag(p.status, NVFP4_DEV_BAD_SCALE_BIT);
+    }
     if ((ch & 1) == 0 && !scale_ok(sp, so)) flag(p.status, NVFP4_DEV_BAD_SCALE_BIT);
     if (!finite8(v)) flag(p.status, NVFP4_DEV_NONFINITE_INPUT_BIT);
     const float inv = __frcp_rn(sp);
@@ -47,10 +83,15 @@ __global__ void __launch_bounds__(kThreads) fakequant_fwd_kernel(const SteParams
   }
 }
 
-template <bool TIED, bool WANT_GX>
+template <bool TIED, bool WANT_GX, bool Q8>
 __global__ void __launch_bounds__(kThreads) scale_grad_bwd_kernel(const SteParams p) {
   const int64_t nchunks = p.nblocks * 2;
   const int64_t stride = (int64_t)gridDim.x * kThreads;
+  Fp8Unit u{1.0f, 1.0f, false};
+  if constexpr (Q8) {
+    u = fp8_unit(p.gamax);
+    if (u.bad && blockIdx.x == 0 && threadIdx.x == 0) flag(p.status, NVFP4_DEV_BAD_AMAX_BIT);
+  }
   // all lanes of a warp iterate together (stride and start are warp-aligned),
   // so the pair shuffle below always has its partner
   const int64_t start = (int64_t)blockIdx.x * kThreads + threadIdx.x;
@@ -66,6 +107,14 @@ __global__ void __launch_bounds__(kThreads) scale_grad_bwd_kernel(const SteParam
       gv = __ldcs(p.gq + ch);
       sp = p.s_pre[b];
       so = TIED ? sp : p.s_post[b];
+      if constexpr (Q8) {
+        // the gradients below are those of the rounded scales, passed through
+        const float spr = sp, sor = so;
+        sp = q8(spr, u);
+        so = TIED ? sp : q8(sor, u);
+        if ((ch & 1) == 0 && !raw_fp8_scales_ok(spr, sor, sp))
+          flag(p.status, NVFP4_DEV_BAD_SCALE_BIT);
+      }
       if ((ch & 1) == 0 && !scale_ok(sp, so)) flag(p.status, NVFP4_DEV_BAD_SCALE_BIT);
       if (!finite8(xv) || !finite8(gv)) flag(p.status, NVFP4_DEV_NONFINITE_INPUT_BIT);
     }
@@ -117,6 +166,37 @@ __global__ void __launch_bounds__(kThreads) scale_grad_bwd_kernel(const SteParam
   }
 }
 
+// Export (Scale Learning blog, "How Scale Learning Works": the post-scale is
+// baked into the checkpoint, the pre-scale discarded): the fake-quant
+// forward's codes (rounding at Q8(s_pre)) and the E4M3 byte of s_post, an
+// NVFP4 row encoding whose de-quantisation is that forward. Two lanes per
+// block, 8 codes (one 32-bit word) each; the even lane writes the scale byte.
+__global__ void __launch_bounds__(kThreads) export_scales_kernel(const SteParams p) {
+  const int64_t nchunks = p.nblocks * 2;
+  const int64_t stride = (int64_t)gridDim.x * kThreads;
+  const Fp8Unit u = fp8_unit(p.gamax);
+  if (u.bad && blockIdx.x == 0 && threadIdx.x == 0) flag(p.status, NVFP4_DEV_BAD_AMAX_BIT);
+  for (int64_t ch = (int64_t)blockIdx.x * kThreads + threadIdx.x; ch < nchunks; ch += stride) {
+    const int64_t b = ch >> 1;
+    const uint4 v = __ldcs(p.x + ch);
+    const float spr = p.s_pre[b];
+    const float sor = p.s_post ? p.s_post[b] : spr;
+    const float sp = q8(spr, u);
+    if ((ch & 1) == 0) {
+      if (!raw_fp8_scales_ok(spr, sor, sp)) flag(p.status, NVFP4_DEV_BAD_SCALE_BIT);
+      p.scales[b] = (uint8_t)(sor >= 0.0f ? q8_code(sor, u) : 0u);
+    }
+    if (!finite8(v)) flag(p.status, NVFP4_DEV_NONFINITE_INPUT_BIT);
+    const float inv = __frcp_rn(sp);
+    f2 x[4], y[4];
+    unpack8(v, x);
+    const f2 iv = make_float2(inv, inv);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) y[k] = f2_mul(x[k], iv);
+    __stcs(reinterpret_cast<uint32_t*>(p.codes) + ch, e2m1x8_rn(y));
+  }
+}
+
 unsigned grid_for(int64_t nchunks) {
   const int64_t want = (nchunks + kThreads - 1) / kThreads;
   const int64_t cap = (int64_t)sm_count() * 8;
@@ -126,17 +206,30 @@ unsigned grid_for(int64_t nchunks) {
 }  // namespace
 
 cudaError_t launch_fakequant_fwd(const SteParams& p, cudaStream_t st) {
-  fakequant_fwd_kernel<<<grid_for(p.nblocks * 2), kThreads, 0, st>>>(p);
+  const unsigned grid = grid_for(p.nblocks * 2);
+  if (p.gamax) fakequant_fwd_kernel<true><<<grid, kThreads, 0, st>>>(p);
+  else fakequant_fwd_kernel<false><<<grid, kThreads, 0, st>>>(p);
   return cudaGetLastError();
+}
+
+template <bool Q8>
+void launch_bwd_t(const SteParams& p, unsigned grid, cudaStream_t st) {
+  const bool tied = p.s_post == nullptr, want_gx = p.out != nullptr;
+  if (tied && want_gx) scale_grad_bwd_kernel<true, true, Q8><<<grid, kThreads, 0, st>>>(p);
+  else if (tied) scale_grad_bwd_kernel<true, false, Q8><<<grid, kThreads, 0, st>>>(p);
+  else if (want_gx) scale_grad_bwd_kernel<false, true, Q8><<<grid, kThreads, 0, st>>>(p);
+  else scale_grad_bwd_kernel<false, false, Q8><<<grid, kThreads, 0, st>>>(p);
 }
 
 cudaError_t launch_scale_grad_bwd(const SteParams& p, cudaStream_t st) {
   const unsigned grid = grid_for(p.nblocks * 2);
-  const bool tied = p.s_post == nullptr, want_gx = p.out != nullptr;
-  if (tied && want_gx) scale_grad_bwd_kernel<true, true><<<grid, kThreads, 0, st>>>(p);
-  else if (tied) scale_grad_bwd_kernel<true, false><<<grid, kThreads, 0, st>>>(p);
-  else if (want_gx) scale_grad_bwd_kernel<false, true><<<grid, kThreads, 0, st>>>(p);
-  else scale_grad_bwd_kernel<false, false><<<grid, kThreads, 0, st>>>(p);
+  if (p.gamax) launch_bwd_t<true>(p, grid, st);
+  else launch_bwd_t<false>(p, grid, st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_export_scales(const SteParams& p, cudaStream_t st) {
+  export_scales_kernel<<<grid_for(p.nblocks * 2), kThreads, 0, st>>>(p);
   return cudaGetLastError();
 }
 

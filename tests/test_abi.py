@@ -150,6 +150,33 @@ def test_requant_argument_errors(L):
         assert rq(L, s, d, codes=0, scales=0, S=S, R=R, Cc=Cc, amax=0, out=None) == 0
 
 
+def test_fp8_scale_learning_argument_errors(L):
+    fq = L.nvfp4_fakequant_fwd_fp8scale
+    assert fq(FAKE, 4, 32, FAKE, None, None, FAKE, None, None) == 1       # no global amax
+    assert fq(FAKE, 4, 24, FAKE, None, FAKE, FAKE, None, None) == 2
+    assert fq(FAKE, 4, 32, FAKE, None, FAKE + 2, FAKE, None, None) == 3
+    assert fq(FAKE, 4, 32, FAKE, None, FAKE, None, None, None) == 1
+    assert fq(None, 0, 32, None, None, None, None, None, None) == 0
+    bwd = L.nvfp4_scale_grad_bwd_fp8scale
+    assert bwd(FAKE, FAKE, 4, 32, FAKE, FAKE, None, FAKE, FAKE, FAKE, None, None) == 1
+    assert bwd(FAKE, FAKE, 4, 32, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None) == 1
+    assert bwd(FAKE, FAKE, 4, 32, FAKE, None, FAKE, FAKE, FAKE, FAKE, None, None) == 1
+    init = L.nvfp4_scale_init_mse
+    assert init(FAKE, 4, 32, FAKE, None, None, None, None) == 1           # no output
+    assert init(FAKE, 4, 24, FAKE, FAKE, None, None, None) == 2
+    assert init(FAKE, 4, 32, None, FAKE, None, None, None) == 1
+    assert init(FAKE + 8, 4, 32, FAKE, FAKE, None, None, None) == 3
+    assert init(FAKE, 4, 32, FAKE, None, FAKE + 2, None, None) == 3
+    assert init(None, 4, 0, None, None, None, None, None) == 0
+    ex = L.nvfp4_export_scales
+    assert ex(FAKE, 4, 32, FAKE, None, FAKE, None, None, None) == 1
+    assert ex(FAKE, 4, 32, FAKE, None, FAKE, C.byref(_out(scales=0, dq=0)), None, None) == 1
+    assert ex(FAKE, 4, 32, FAKE, None, FAKE, C.byref(_out()), None, None) == 4   # dequant
+    assert ex(FAKE, 4, 32, FAKE, None, FAKE, C.byref(_out(codes=FAKE + 4, dq=0)), None,
+              None) == 3
+    assert ex(FAKE, 4, 32, FAKE, None, None, C.byref(_out(dq=0)), None, None) == 1
+
+
 def test_amax_argument_errors(L):
     assert L.nvfp4_amax(FAKE, -1, 4, 4, FAKE, None, None) == 2
     assert L.nvfp4_amax(FAKE, 1, 4, 4, None, None, None) == 1
