@@ -110,6 +110,10 @@ def _declare(L):
     L.orc_e4m3_rne_array.argtypes = [_f32p, _i64, _u8p]
     L.orc_e4m3_sr_array.argtypes = [_f32p, _u32p, _i64, _u8p]
     L.orc_mx_shared_exp_array.argtypes = [_f32p, _i64, _u8p]
+    L.orc_quantize_tile16.restype = C.c_int
+    L.orc_quantize_tile16.argtypes = [C.c_int, C.c_int, C.c_float, C.c_uint32, C.c_uint32, _u16p,
+                                      _i64, _i64, _i64, _f32p, _u8p, _u8p, _u16p, _u8p, _u8p,
+                                      _u16p]
     L.orc_fakequant_fwd_fp8.restype = C.c_int
     L.orc_fakequant_fwd_fp8.argtypes = [_u16p, _i64, _i64, _f32p, _f32p, C.c_float, _u16p]
     L.orc_scale_grad_bwd_fp8.restype = C.c_int
@@ -263,6 +267,32 @@ def quantize(x_bf16: np.ndarray, gamax: np.ndarray, *, blocks: int = 1, scale_fm
                             _p(g("col_codes"), _u8p), _p(g("col_scales"), _u8p),
                             _p(g("col_choice"), _u32p), _p(g("col_dq"), _u16p))
     out["status"] = st
+    return out
+
+
+def quantize_tile16(x_bf16: np.ndarray, gamax: np.ndarray, *, scale_fmt: int = 0,
+                    rounding: int = 0, scale_max: float = 0.0, seed: int = 0, step: int = 0,
+                    dequant: bool = True) -> dict:
+    """One scale per 16x16 tile: the row encoding of x [S, R, C] and its exact
+    transpose as the column encoding (keys as quantize())."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    if x.ndim == 2:
+        x = x[None]
+    S, R, Cc = x.shape
+    gam = np.ascontiguousarray(gamax, dtype=np.float32).reshape(-1)
+    out = {"row_codes": np.zeros((S, R, Cc // 2), np.uint8),
+           "row_scales": np.zeros((S, R, Cc // 16), np.uint8),
+           "row_dq": np.zeros((S, R, Cc), np.uint16),
+           "col_codes": np.zeros((S, Cc, R // 2), np.uint8),
+           "col_scales": np.zeros((S, Cc, R // 16), np.uint8),
+           "col_dq": np.zeros((S, Cc, R), np.uint16)}
+    g = out.get
+    out["status"] = lib().orc_quantize_tile16(
+        scale_fmt, rounding, scale_max, seed, step, _p(x, _u16p), S, R, Cc, _p(gam, _f32p),
+        _p(g("row_codes"), _u8p), _p(g("row_scales"), _u8p), _p(g("row_dq"), _u16p),
+        _p(g("col_codes"), _u8p), _p(g("col_scales"), _u8p), _p(g("col_dq"), _u16p))
+    if not dequant:
+        out["row_dq"] = out["col_dq"] = None
     return out
 
 

@@ -796,3 +796,71 @@ int orc_export_scales(const uint16_t* x, int64_t R, int64_t C, const float* s_pr
   free(sp);
   return st;
 }
+
+/* --------------------------------------------------- 16x16 tile scale ---- */
+/* End-to-End 4-Bit Training, "Block-scaled backward passes": for weights one
+ * scale per 16x16 square tile, from the tile's largest value, keeps the
+ * scales identical when the tensor is transposed.
+ *
+ * Reading:
+ *  R16 A tile's scale is the 1x16 block scale of R4 with k = 6 computed from
+ *      the tile's amax (no 4/6: the pages pair the tile scale with plain
+ *      NVFP4); every 1x16 row block inside the tile is encoded with it
+ *      (element rounding R1 or R5 with the row layout's indices, direction 0).
+ *      The row encoding has the layout of encode_rows, each row block storing
+ *      its tile's scale byte; the column encoding is that encoding transposed
+ *      (codes, scales, dequant), so the backward operand is bit for bit the
+ *      forward one transposed. R % 16 == 0 and C % 16 == 0. */
+int orc_quantize_tile16(int fmt, int rounding, float scale_max, uint32_t seed, uint32_t step,
+                        const uint16_t* x, int64_t S, int64_t R, int64_t C, const float* gamax,
+                        uint8_t* r_codes, uint8_t* r_scales, uint16_t* r_dq,
+                        uint8_t* c_codes, uint8_t* c_scales, uint16_t* c_dq) {
+  int st = 0;
+  float M = scale_max > 0.0f ? scale_max : 448.0f;
+  for (int64_t s = 0; s < S; ++s) {
+    float g;
+    st |= global_decode_scale(gamax[s], M, &g);
+    for (int64_t tr = 0; tr < R / 16; ++tr)
+      for (int64_t tc = 0; tc < C / 16; ++tc) {
+        float amax = 0.0f;
+        for (int rr = 0; rr < 16; ++rr)
+          for (int cc = 0; cc < 16; ++cc) {
+            uint16_t h = x[s * R * C + (16 * tr + rr) * C + 16 * tc + cc];
+            if ((h & 0x7FFFu) >= 0x7F80u) st |= ORC_ST_NONFINITE_INPUT;
+            float a = fabsf(orc_bf16_to_f32(h));
+            if (a > amax) amax = a;
+          }
+        for (int rr = 0; rr < 16; ++rr) {
+          int64_t e0 = s * R * C + (16 * tr + rr) * C + 16 * tc;
+          float xb[16];
+          uint32_t v16[16] = {0};
+          for (int i = 0; i < 16; ++i) {
+            xb[i] = orc_bf16_to_f32(x[e0 + i]);
+            if (rounding) v16[i] = orc_sr_bits(seed, step, 0, (uint64_t)(e0 + i));
+          }
+          cand_t cd;
+          encode_candidate(xb, amax, g, 6.0f, fmt, rounding, v16, &cd);
+          if (r_codes)
+            for (int i = 0; i < 16; i += 2)
+              r_codes[(e0 + i) / 2] = (uint8_t)((cd.q[i] & 15) | ((cd.q[i + 1] & 15) << 4));
+          if (r_scales) r_scales[e0 / 16] = cd.scale;
+          if (r_dq)
+            for (int i = 0; i < 16; ++i) r_dq[e0 + i] = orc_f32_to_bf16(cd.qv[i] * cd.d);
+        }
+      }
+  }
+  /* the column encoding: the row encoding transposed */
+  for (int64_t s = 0; s < S; ++s)
+    for (int64_t r = 0; r < R; ++r)
+      for (int64_t c = 0; c < C; ++c) {
+        int64_t e = s * R * C + r * C + c, t = s * R * C + c * R + r;
+        if (c_codes) {
+          uint8_t q = (e & 1) ? (r_codes[e / 2] >> 4) : (r_codes[e / 2] & 15);
+          if (t & 1) c_codes[t / 2] = (uint8_t)((c_codes[t / 2] & 0x0F) | (q << 4));
+          else c_codes[t / 2] = (uint8_t)((c_codes[t / 2] & 0xF0) | q);
+        }
+        if (c_scales && r % 16 == 0) c_scales[t / 16] = r_scales[e / 16];
+        if (c_dq) c_dq[t] = r_dq[e];
+      }
+  return st;
+}
