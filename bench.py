@@ -1,6 +1,6 @@
 """Throughput of the NVFP4 hot path on one or more GB300s.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..10] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..11] [--impl ours|reference]
 
 A step is one pass of the hot path over one batch of synthetic input already
 resident in HBM. The default workload is the activation tensor 8192 x 4096 bf16
@@ -604,6 +604,72 @@ class ScaleInitExport(ScaleLearningFp8):
         "NVFP4 row encoding (codes + E4M3 scale bytes)"))
 
 
+class TileWeight(Workload):
+    """Weight 14336 x 4096: amax + one scale per 16x16 tile, the row encoding
+    and its transpose (codes, scales, both dequants) from one read."""
+
+    def __init__(self, device, rows=14336, cols=4096, seed=2):
+        wb, _, _ = synth.scale_learning(rows, cols, seed=seed)
+        self.rows, self.cols = rows, cols
+        self.elements = rows * cols
+        self.host_x = wb
+        x0 = torch.from_numpy(wb.view(np.int16)).to(device)
+        per_set = self.elements * (2 + 2 * (0.5 + 1 / 16 + 2))
+        self.nsets = max(2, int(np.ceil(2.5 * L2_BYTES / per_set)))
+        self.x = [x0] + [x0.clone() for _ in range(self.nsets - 1)]
+        self.amax = [torch.empty(1, dtype=torch.float32, device=device) for _ in range(self.nsets)]
+        self.row = [nv.alloc_encoding(1, rows, cols, device, False) for _ in range(self.nsets)]
+        self.col = [nv.alloc_encoding(1, cols, rows, device, False) for _ in range(self.nsets)]
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.t_bytes = self.elements * (2 + 2 * (0.5 + 1 / 16 + 2))
+        self.a_bytes = self.elements * 2
+        self.working_set = per_set * self.nsets
+        L = nv.lib()
+        st = torch.cuda.current_stream(device).cuda_stream
+        self._c = nv.Config(blocks=nv.BLOCKS_TILE16).c()
+        self._ro = [nv._out(o) for o in self.row]
+        self._co = [nv._out(o) for o in self.col]
+
+        def amax(i):
+            return L.nvfp4_amax(self.x[i].data_ptr(), 1, rows, cols, self.amax[i].data_ptr(),
+                                self.status.data_ptr(), st)
+
+        def tile(i):
+            return L.nvfp4_quantize(C.byref(self._c), self.x[i].data_ptr(), 1, rows, cols,
+                                    self.amax[i].data_ptr(), C.byref(self._ro[i]),
+                                    C.byref(self._co[i]), self.status.data_ptr(), st)
+        self._amax, self._tile = amax, tile
+
+    def kernels(self, k, i):
+        return [Kernel("amax", self.a_bytes, lambda: self._amax(i)),
+                Kernel("quantize_tile16", self.t_bytes, lambda: self._tile(i))]
+
+    def e2e_io(self, k):
+        names = ("codes", "scales", "dequant")
+        return [self.x[0]], [self.row[0][n] for n in names] + [self.col[0][n] for n in names]
+
+    def cpu_sample(self, budget_s):
+        import oracle
+        rows = 16
+        t0 = time.perf_counter()
+        a, _ = oracle.global_amax(self.host_x[:rows])
+        oracle.quantize_tile16(self.host_x[:rows], a)
+        per_row = (time.perf_counter() - t0) / rows
+        rows = int(min(self.rows, max(16, budget_s / max(per_row, 1e-9))))
+        rows -= rows % 16
+        t0 = time.perf_counter()
+        a, _ = oracle.global_amax(self.host_x[:rows])
+        oracle.quantize_tile16(self.host_x[:rows], a)
+        return rows * self.cols, time.perf_counter() - t0, \
+            f"first {rows} of {self.rows} rows (amax + 16x16 tile encoding and transpose)"
+
+    bytes_per_elem = property(lambda self: (self.t_bytes + self.a_bytes) / self.elements)
+    dominant = "quantize_tile16"
+    workload = property(lambda self: (
+        f"weight {self.rows}x{self.cols} bf16 N(0,0.02): amax + one E4M3 scale per 16x16 tile "
+        "(RNE), row encoding and its transpose with both dequants from one read"))
+
+
 class RequantActivationNvfp4(RequantActivation):
     def __init__(self, device):
         super().__init__(device, target=1)
@@ -611,7 +677,8 @@ class RequantActivationNvfp4(RequantActivation):
 
 WORKLOADS = {1: SmallNormal, 2: Activation, 3: ScaleLearning, 4: DriftingGradient,
              5: MoeExperts, 6: PerTokenActivation, 7: RequantActivation,
-             8: RequantActivationNvfp4, 9: ScaleLearningFp8, 10: ScaleInitExport}
+             8: RequantActivationNvfp4, 9: ScaleLearningFp8, 10: ScaleInitExport,
+             11: TileWeight}
 
 
 # --------------------------------------------------------------- clocks --
@@ -887,6 +954,17 @@ def _reference_sample(args):
         return ("activation 8192x4096 NVFP4 (4/6) re-quantised, transposed, SR to "
                 + ("MXFP8" if target == 0 else "NVFP4")), bpe, \
             f"first {n} of 8192 source rows per step", step
+    if args.config == 11:
+        wb, _, _ = synth.scale_learning(seed=2)
+        n = max(16, args.ref_rows - args.ref_rows % 16)
+
+        def step():
+            t0 = time.perf_counter()
+            a, _ = oracle.global_amax(wb[:n])
+            oracle.quantize_tile16(wb[:n], a)
+            return n * wb.shape[1], time.perf_counter() - t0
+        return "weight 14336x4096 16x16 tile scale + transpose", 2 + 2 + 2 * (0.5 + 1 / 16 + 2), \
+            f"first {n} of 14336 rows per step", step
     if args.config in (9, 10):
         wb, gb, s = synth.scale_learning(seed=2)
         gam = float(np.abs(synth.bf16_bits_to_f32(wb)).max()) * 1.5
@@ -954,7 +1032,7 @@ def main():
     if args.steps is None:
         # about two seconds of device time, so the clock samples cover the run
         args.steps = {1: 20000, 2: 40000, 3: 10000, 4: 16000, 5: 150, 6: 50000, 7: 40000,
-                      8: 40000, 9: 10000, 10: 300}[args.config]
+                      8: 40000, 9: 10000, 10: 300, 11: 8000}[args.config]
     total_ms, per_kernel, clk, wall = time_ours(wl, args, world, local)
     total_ms = max_over_ranks(total_ms, world)
     units = wl.elements * args.steps * world
@@ -1027,6 +1105,7 @@ KERNEL_SOURCES = {
     "scale_grad_bwd_fp8": ["ste.cu"] + _COMMON,
     "scale_init_mse": ["scale_init.cu"] + _COMMON,
     "export_scales": ["ste.cu"] + _COMMON,
+    "quantize_tile16": ["quant_tile16.cu"] + _COMMON,
 }
 
 

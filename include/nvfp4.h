@@ -66,6 +66,7 @@ typedef enum {
 #define NVFP4_BLOCKS_ROW 1  /* 1x16 blocks along the last dimension            */
 #define NVFP4_BLOCKS_COL 2  /* 16x1 blocks along rows: the row encoding of X^T */
 #define NVFP4_BLOCKS_BOTH 3 /* both encodings from one read of X               */
+#define NVFP4_BLOCKS_TILE16 4 /* one scale per 16x16 tile (see nvfp4_quantize)   */
 /* nvfp4_config.scale_fmt */
 #define NVFP4_SCALE_E4M3 0
 #define NVFP4_SCALE_UE5M3 1
@@ -131,6 +132,16 @@ NVFP4_API nvfp4_status nvfp4_amax(const void* x, int64_t slices, int64_t rows, i
  * counter (idx/8 low word, idx/8 high word, 0 for rows / 1 for columns, 0),
  * 16-bit half idx%2 of word (idx%8)/2; the value rounds up iff
  * bits/65536 < (|y| - lo) / (hi - lo).
+ * blocks = NVFP4_BLOCKS_TILE16 (End-to-End 4-Bit Training, "Block-scaled
+ * backward passes": one scale per 16x16 tile from its largest value, the same
+ * when the tensor is transposed): rows % 16 == 0 and cols % 16 == 0; each
+ * tile's scale is the block scale (target 6) of the tile's amax and every
+ * 1x16 row block of the tile is encoded with it; `row` (required) receives
+ * the row-encoding layout, every row block of a tile carrying the tile's
+ * scale byte; `col` (optional) receives exactly its transpose (codes, scales,
+ * dequant: the stochastic draws are the row layout's, so the two are bit for
+ * bit transposes); both or neither write dequant; four_over_six must be 0
+ * (NVFP4_ERR_ENUM); M defaults to 448; choice is ignored.
  * Errors: NULL required pointers, ROW with cols % 16, COL with rows % 16,
  * enum fields out of range, scale_max < 0, misaligned buffers. */
 NVFP4_API nvfp4_status nvfp4_quantize(const nvfp4_config* cfg, const void* x, int64_t slices,

@@ -26,6 +26,7 @@ __all__ = [
     "nvfp4_fakequant_fwd_fp8scale", "nvfp4_scale_grad_bwd_fp8scale", "nvfp4_scale_init_mse",
     "nvfp4_export_scales",
     "alloc_encoding", "alloc_requant", "PeriodicAmax", "BLOCKS_ROW", "BLOCKS_COL", "BLOCKS_BOTH",
+    "BLOCKS_TILE16",
     "SCALE_E4M3", "SCALE_UE5M3", "ROUND_RNE", "ROUND_SR", "FOS_MSE", "FOS_MAE", "FOS_MAX",
     "DEV_NONFINITE_INPUT", "DEV_BAD_SCALE", "DEV_BAD_AMAX",
 ]
@@ -33,7 +34,7 @@ __all__ = [
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libnvfp4.so")
 
-BLOCKS_ROW, BLOCKS_COL, BLOCKS_BOTH = 1, 2, 3
+BLOCKS_ROW, BLOCKS_COL, BLOCKS_BOTH, BLOCKS_TILE16 = 1, 2, 3, 4
 FOS_MSE, FOS_MAE, FOS_MAX = 0, 1, 2
 SCALE_E4M3, SCALE_UE5M3 = 0, 1
 ROUND_RNE, ROUND_SR = 0, 1
@@ -210,6 +211,15 @@ def nvfp4_quantize(x: torch.Tensor, global_amax: torch.Tensor, cfg: Config | Non
     cfg = cfg or Config()
     S, R, Cc = _shape3(x)
     fos = bool(cfg.four_over_six)
+    if cfg.blocks == BLOCKS_TILE16:
+        # one scale per 16x16 tile: the row encoding and its transpose
+        row = row if row is not None else alloc_encoding(S, R, Cc, x.device, False, dequant)
+        col = col if col is not None else alloc_encoding(S, Cc, R, x.device, False, dequant)
+        ro, co, c = _out(row), _out(col), cfg.c()
+        _check("nvfp4_quantize", lib().nvfp4_quantize(
+            C.byref(c), _bf16(x, "x"), S, R, Cc, _dev(global_amax, "global_amax"), C.byref(ro),
+            C.byref(co), _dev(status, "status"), _stream(x.device)))
+        return {"row": row, "col": col}
     if cfg.blocks & 1 and row is None:
         row = alloc_encoding(S, R, Cc, x.device, fos, dequant)
     if cfg.blocks & 2 and col is None:

@@ -44,6 +44,41 @@ nvfp4_status check_out(const nvfp4_out* o, bool fos) {
   return NVFP4_OK;
 }
 
+// blocks == NVFP4_BLOCKS_TILE16: validation and dispatch.
+nvfp4_status quantize_tile16(const nvfp4_config* cfg, const void* x, int64_t slices, int64_t rows,
+                             int64_t cols, const float* global_amax, const nvfp4_out* row,
+                             const nvfp4_out* col, int32_t* status, void* stream) {
+  if (cfg->four_over_six) return NVFP4_ERR_ENUM;
+  if (rows % 16 != 0 || cols % 16 != 0) return NVFP4_ERR_SHAPE;
+  if (slices == 0 || rows == 0 || cols == 0) return NVFP4_OK;
+  if (!x || !global_amax) return NVFP4_ERR_NULL;
+  if (!aligned(x, 16) || !aligned(global_amax, 4) || !aligned(status, 4)) return NVFP4_ERR_ALIGN;
+  nvfp4_status e = check_out(row, false);
+  if (e != NVFP4_OK) return e;
+  if (col && (e = check_out(col, false)) != NVFP4_OK) return e;
+  if (col && (row->dequant == nullptr) != (col->dequant == nullptr)) return NVFP4_ERR_NULL;
+  nvfp4::Tile16Params p{};
+  p.x = static_cast<const uint4*>(x);
+  p.S = slices;
+  p.R = rows;
+  p.C = cols;
+  p.gamax = global_amax;
+  p.M = cfg->scale_max > 0.0f ? cfg->scale_max : 448.0f;
+  p.seed = cfg->seed;
+  p.step = cfg->step;
+  p.r_codes = reinterpret_cast<uint32_t*>(row->codes);
+  p.r_scales = row->scales;
+  p.r_dq = static_cast<uint4*>(row->dequant);
+  if (col) {
+    p.c_codes = reinterpret_cast<uint32_t*>(col->codes);
+    p.c_scales = col->scales;
+    p.c_dq = static_cast<uint4*>(col->dequant);
+  }
+  p.status = status;
+  return cuda_status(nvfp4::launch_quant_tile16(p, cfg->scale_fmt, cfg->rounding == NVFP4_ROUND_SR,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
 }  // namespace
 
 extern "C" {
@@ -76,11 +111,14 @@ nvfp4_status nvfp4_quantize(const nvfp4_config* cfg, const void* x, int64_t slic
                             const nvfp4_out* col, int32_t* status, void* stream) {
   if (!cfg) return NVFP4_ERR_NULL;
   if (cfg->four_over_six_rule < 0 || cfg->four_over_six_rule > 2) return NVFP4_ERR_ENUM;
-  if (cfg->blocks < 1 || cfg->blocks > 3 || cfg->scale_fmt < 0 || cfg->scale_fmt > 1 ||
+  if (cfg->blocks < 1 || cfg->blocks > 4 || cfg->scale_fmt < 0 || cfg->scale_fmt > 1 ||
       cfg->rounding < 0 || cfg->rounding > 1 || cfg->four_over_six < 0 || cfg->four_over_six > 1 ||
       !(cfg->scale_max >= 0.0f) || !(cfg->scale_max <= 3.402823466e+38f))
     return NVFP4_ERR_ENUM;
   if (slices < 0 || rows < 0 || cols < 0) return NVFP4_ERR_SHAPE;
+  if (cfg->blocks == NVFP4_BLOCKS_TILE16) return quantize_tile16(cfg, x, slices, rows, cols,
+                                                                 global_amax, row, col, status,
+                                                                 stream);
   const bool do_row = cfg->blocks & 1, do_col = cfg->blocks & 2;
   if (do_row && cols % 16 != 0) return NVFP4_ERR_SHAPE;
   if (do_col && rows % 16 != 0) return NVFP4_ERR_SHAPE;

@@ -70,6 +70,23 @@ struct DualParams {
 cudaError_t launch_quant_dual(const DualParams& p, int64_t S, bool rows_too, int fmt, bool sr,
                               int fos, cudaStream_t st);
 
+// One block scale per 16x16 tile; row encoding and (optionally) its transpose.
+struct Tile16Params {
+  const uint4* x;       // bf16 [S][R][C], R % 16 == 0, C % 16 == 0
+  int64_t S, R, C;
+  const float* gamax;   // [S]
+  float M;
+  uint32_t seed, step;
+  uint32_t* r_codes;    // 8 codes per word, row layout
+  uint8_t* r_scales;
+  uint4* r_dq;          // may be null
+  uint32_t* c_codes;    // column encoding (the transpose), null = not written
+  uint8_t* c_scales;
+  uint4* c_dq;          // may be null
+  int32_t* status;
+};
+cudaError_t launch_quant_tile16(const Tile16Params& p, int fmt, bool sr, cudaStream_t st);
+
 // Per-token (per-row outer scale) quantiser, amax and encoding in one pass.
 struct TokenParams {
   const uint4* x;       // bf16 [R][C], C % 16 == 0

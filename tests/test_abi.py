@@ -73,7 +73,7 @@ def q(L, cfg, x=FAKE, S=1, R=16, Cc=32, amax=FAKE, row=None, col=None, status=No
 
 def test_quantize_argument_errors(L):
     assert q(L, None) == 1
-    for bad in (dict(blocks=0), dict(blocks=4), dict(scale_fmt=2), dict(rounding=3),
+    for bad in (dict(blocks=0), dict(blocks=5), dict(scale_fmt=2), dict(rounding=3),
                 dict(four_over_six=2), dict(scale_max=-1.0), dict(scale_max=float("nan")),
                 dict(four_over_six_rule=3), dict(four_over_six_rule=-1)):
         assert q(L, _cfg(**bad), row=_out(), col=_out()) == 4, bad
@@ -90,6 +90,19 @@ def test_quantize_argument_errors(L):
     assert q(L, _cfg(blocks=1), row=_out(codes=FAKE + 4)) == 3
     assert q(L, _cfg(blocks=1), row=_out(dq=FAKE + 8)) == 3
     assert q(L, _cfg(blocks=1), amax=FAKE + 1, row=_out()) == 3
+
+
+def test_tile16_argument_errors(L):
+    t = _cfg(blocks=4)
+    assert q(L, _cfg(blocks=5), row=_out(), col=_out()) == 4
+    assert q(L, _cfg(blocks=4, four_over_six=1), row=_out(), col=_out()) == 4
+    assert q(L, t, R=24, row=_out(), col=_out()) == 2       # rows % 16
+    assert q(L, t, Cc=24, row=_out(), col=_out()) == 2      # cols % 16
+    assert q(L, t, row=None, col=_out()) == 1               # row encoding required
+    assert q(L, t, x=0, row=_out(), col=_out()) == 1
+    assert q(L, t, row=_out(), col=_out(dq=0)) == 1          # dequant for both or neither
+    assert q(L, t, row=_out(codes=FAKE + 4), col=_out()) == 3
+    assert q(L, t, x=0, S=0, amax=0, row=None, col=None) == 0
 
 
 def test_empty_inputs_enqueue_nothing(L):

@@ -1,0 +1,97 @@
+"""CUDA 16x16 tile-scale quantiser against the oracle: row encoding and its
+transposed column encoding bit-exact (codes, scales, dequant), both scale
+formats, RNE and stochastic rounding, several slices, bad amax, and the
+activation-size tensor on sampled row bands."""
+import numpy as np
+import pytest
+import torch
+
+import nvfp4_block_scaled_02_gb300 as nv
+import oracle
+from helpers import assert_exact, dev_bits, host_u16, host_u8
+from nvfp4_block_scaled_02_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def run_both(xb, gamax, *, fmt=0, rounding=0, seed=0, step=0, scale_max=0.0, dequant=True):
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cfg = nv.Config(blocks=nv.BLOCKS_TILE16, scale_fmt=fmt, rounding=rounding, seed=seed,
+                    step=step, scale_max=scale_max)
+    out = nv.nvfp4_quantize(dev_bits(xb), torch.from_numpy(np.asarray(gamax, np.float32)).cuda(),
+                            cfg, status=st, dequant=dequant)
+    torch.cuda.synchronize()
+    ref = oracle.quantize_tile16(xb, gamax, scale_fmt=fmt, rounding=rounding, seed=seed, step=step,
+                                 scale_max=scale_max, dequant=dequant)
+    return out, ref, int(st.item())
+
+
+def _check(out, ref, st, dequant=True):
+    assert st == ref["status"]
+    for side in ("row", "col"):
+        o = out[side]
+        assert_exact(host_u8(o["codes"]), ref[side + "_codes"], side + " codes")
+        assert_exact(host_u8(o["scales"]), ref[side + "_scales"], side + " scales")
+        if dequant:
+            assert_exact(host_u16(o["dequant"]), ref[side + "_dq"], side + " dequant")
+
+
+SHAPES = [(1, 16, 16), (2, 48, 80), (3, 64, 272), (1, 512, 1024)]
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+@pytest.mark.parametrize("rounding", [0, 1])
+@pytest.mark.parametrize("shape", SHAPES)
+def test_tile16_matches_oracle(shape, fmt, rounding):
+    S, R, Cc = shape
+    xb = synth.outlier_normal(S * R, Cc, seed=R + Cc).reshape(shape)
+    gamax, _ = oracle.global_amax(xb, S)
+    out, ref, st = run_both(xb, gamax, fmt=fmt, rounding=rounding, seed=5, step=7)
+    _check(out, ref, st)
+
+
+def test_tile16_without_dequant_and_stale_amax():
+    xb = synth.student_t(96, 160, seed=3).reshape(1, 96, 160)
+    gamax, _ = oracle.global_amax(xb)
+    out, ref, st = run_both(xb, gamax * np.float32(0.1), dequant=False)  # saturating scales
+    _check(out, ref, st, dequant=False)
+
+
+def test_tile16_bad_amax_is_flagged():
+    xb = synth.outlier_normal(32, 32, seed=1).reshape(1, 32, 32)
+    _, _, st = run_both(xb, np.array([np.nan], np.float32))
+    assert st & nv.DEV_BAD_AMAX
+
+
+def test_tile16_column_is_transposed_row_on_device():
+    xb = synth.student_t(128, 256, seed=4).reshape(1, 128, 256)
+    gamax, _ = oracle.global_amax(xb)
+    out, _, _ = run_both(xb, gamax, rounding=1, seed=3)
+    rd = host_u16(out["row"]["dequant"]).reshape(128, 256)
+    cd = host_u16(out["col"]["dequant"]).reshape(256, 128)
+    assert np.array_equal(cd, rd.T)
+
+
+def test_tile16_activation_size_sampled_bands():
+    """8192 x 4096 in one launch (RNE); 6 row bands of 16 re-encoded by the
+    oracle on their own (tiles are independent given the slice's global
+    amax). Stochastic rounding is compared at the smaller sizes, where the
+    oracle sees the same flat indices."""
+    xb = synth.student_t(8192, 4096, seed=1)
+    gamax, _ = oracle.global_amax(xb)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = nv.nvfp4_quantize(dev_bits(xb), torch.from_numpy(gamax).cuda(),
+                            nv.Config(blocks=nv.BLOCKS_TILE16), status=st)
+    rc = host_u8(out["row"]["codes"]).reshape(8192, 2048)
+    rs = host_u8(out["row"]["scales"]).reshape(8192, 256)
+    cc = host_u8(out["col"]["codes"]).reshape(4096, 4096)
+    cs = host_u8(out["col"]["scales"]).reshape(4096, 512)
+    bands = np.random.default_rng(2).choice(512, 6, replace=False)
+    bands[:2] = (0, 511)
+    for b in bands:
+        ref = oracle.quantize_tile16(xb[16 * b:16 * b + 16], gamax, dequant=False)
+        assert_exact(rc[16 * b:16 * b + 16], ref["row_codes"][0], f"band {b} codes")
+        assert_exact(rs[16 * b:16 * b + 16], ref["row_scales"][0], f"band {b} scales")
+        assert_exact(cc[:, 8 * b:8 * b + 8], ref["col_codes"][0], f"band {b} column codes")
+        assert_exact(cs[:, b], ref["col_scales"][0][:, 0], f"band {b} column scales")
+    assert int(st.item()) == 0
