@@ -19,6 +19,7 @@ constexpr int kUnroll = 4;
 
 __global__ void __launch_bounds__(kThreads) amax_kernel(const uint16_t* __restrict__ x, int64_t n,
                                                         uint32_t* amax_bits, int32_t* status) {
+  pdl_begin();
   const int64_t s = blockIdx.y;
   const uint16_t* base = x + s * n;
   const int64_t head0 = ((16 - ((uintptr_t)base & 15)) & 15) / 2;
@@ -67,9 +68,8 @@ cudaError_t launch_amax(const uint16_t* x, int64_t S, int64_t n, float* amax, in
   const int64_t cap = std::max<int64_t>(1, (int64_t)sm_count() * 8 / std::max<int64_t>(1, S));
   for (int64_t s0 = 0; s0 < S; s0 += 65535) {
     dim3 grid((unsigned)std::min(want, cap), (unsigned)std::min<int64_t>(S - s0, 65535));
-    amax_kernel<<<grid, kThreads, 0, st>>>(x + s0 * n, n, reinterpret_cast<uint32_t*>(amax + s0),
-                                           status);
-    e = cudaGetLastError();
+    e = launch_pdl(amax_kernel, grid, dim3(kThreads), st, x + s0 * n, n,
+                   reinterpret_cast<uint32_t*>(amax + s0), status);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -310,6 +310,18 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// ------------------------------------------ programmatic dependent launch --
+// Kernels are launched with programmatic stream serialisation (launch_pdl),
+// so a kernel may be scheduled while the preceding kernel on the stream is
+// still draining. Every kernel therefore waits for its predecessor to
+// complete (and its writes to be visible) before it touches global memory,
+// then lets its own dependent launch early; both are hardware operations
+// (griddepcontrol), no-ops when the launch had no programmatic dependency.
+__device__ __forceinline__ void pdl_begin() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------- status word ---
 __device__ __forceinline__ void flag(int32_t* status, int32_t bit) {
   if (status) atomicOr(status, bit);

@@ -27,6 +27,25 @@ int resident_ctas(Kernel kernel, int threads, size_t smem = 0) {
   return n;
 }
 
+// Launch with programmatic stream serialisation: the kernel may start while
+// the previous kernel on the stream drains (it calls pdl_begin() before any
+// memory access, which waits for that kernel to complete).
+template <class... KArgs, class... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = grid;
+  lc.blockDim = block;
+  lc.dynamicSmemBytes = 0;
+  lc.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = at;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, kernel, static_cast<Args&&>(args)...);
+}
+
 // Row (1x16) quantiser over a stack of S slices of Bs blocks each.
 struct RowParams {
   const uint4* x;       // bf16 input, 8 values per uint4

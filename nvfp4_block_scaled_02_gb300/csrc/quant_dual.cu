@@ -46,6 +46,7 @@ __device__ __forceinline__ uint32_t even_bits8(uint32_t b) {  // lanes 0,2,..,14
 template <int FMT, bool SR, int FOS, bool ROWS>
 __global__ void __launch_bounds__(kThreads) quant_dual_kernel(const DualParams p, int64_t tiles_r,
                                                               int64_t tiles_c) {
+  pdl_begin();
   __shared__ __align__(16) uint16_t tile[TR * TC];
   __shared__ float s_d[256], s_inv[256];
   __shared__ uint8_t s_cpick[TR / 16][TC];
@@ -200,8 +201,8 @@ cudaError_t launch_t(const DualParams& p, int64_t S, cudaStream_t st) {
   const int64_t tiles_r = (p.R + TR - 1) / TR, tiles_c = (p.C + TC - 1) / TC;
   const int64_t n = S * tiles_r * tiles_c;
   if (n > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
-  quant_dual_kernel<FMT, SR, FOS, ROWS><<<(unsigned)n, kThreads, 0, st>>>(p, tiles_r, tiles_c);
-  return cudaGetLastError();
+  return launch_pdl(quant_dual_kernel<FMT, SR, FOS, ROWS>, dim3((unsigned)n), dim3(kThreads), st,
+                    p, tiles_r, tiles_c);
 }
 
 }  // namespace

@@ -22,6 +22,7 @@ constexpr int kStages = 4;  // tiles in flight per warp (cp.async groups)
 
 template <int FMT, bool SR, int FOS>
 __global__ void __launch_bounds__(kThreads) quant_row_kernel(const RowParams p) {
+  pdl_begin();
   // stage[slot][w][c]: chunk c (0..63) of warp w's tile; chunk c holds values
   // 8c .. 8c+7 of the tile, i.e. half c%2 of block c/2.
   __shared__ __align__(16) uint4 stage[kStages][kWarps][64];
@@ -107,8 +108,7 @@ cudaError_t launch_t(const RowParams& p, int64_t S, cudaStream_t st) {
   for (int64_t s0 = 0; s0 < S; s0 += 65535) {
     q.slice0 = s0;
     dim3 grid((unsigned)std::min(want, cap), (unsigned)std::min<int64_t>(S - s0, 65535));
-    quant_row_kernel<FMT, SR, FOS><<<grid, kThreads, 0, st>>>(q);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(quant_row_kernel<FMT, SR, FOS>, grid, dim3(kThreads), st, q);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -52,6 +52,7 @@ struct WarpTileCursor {
 template <int FMT, bool SR>
 __global__ void __launch_bounds__(kThreads) quant_tile16_kernel(const Tile16Params p,
                                                                 int64_t tiles_r, int64_t tiles_c) {
+  pdl_begin();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int r = lane >> 1, h = lane & 1;
   const int64_t R = p.R, C = p.C;
@@ -117,8 +118,7 @@ cudaError_t launch_t(const Tile16Params& p, cudaStream_t st) {
   const int64_t want = (total + kWarps - 1) / kWarps;
   const int64_t cap = (int64_t)sm_count() * resident_ctas(k, kThreads);
   const unsigned grid = (unsigned)(want < cap ? want : cap);
-  k<<<grid, kThreads, 0, st>>>(p, tiles_r, tiles_c);
-  return cudaGetLastError();
+  return launch_pdl(k, dim3(grid), dim3(kThreads), st, p, tiles_r, tiles_c);
 }
 
 }  // namespace

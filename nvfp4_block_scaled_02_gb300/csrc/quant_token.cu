@@ -24,6 +24,7 @@ constexpr int kRowLoads = 16;  // 16-byte loads per lane in flight in the amax p
 
 template <int FMT, bool SR, int FOS>
 __global__ void __launch_bounds__(kThreads) quant_token_kernel(const TokenParams p) {
+  pdl_begin();
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = (int64_t)gridDim.x * kWarps;
   const int64_t Bs = p.C / 16, W = (Bs + 31) / 32, nch = p.C / 8;
@@ -95,6 +96,7 @@ __global__ void __launch_bounds__(kThreads) quant_token_kernel(const TokenParams
 // table lookups, as the per-slice kernel does.
 template <int FMT, bool SR, int FOS, int K>
 __global__ void __launch_bounds__(kThreads) quant_token_cta_kernel(const TokenParams p) {
+  pdl_begin();
   __shared__ uint32_t s_max[kWarps];
   __shared__ float s_d[256], s_inv[256];
   __shared__ SliceScale s_ss;
@@ -194,20 +196,14 @@ cudaError_t launch_t(const TokenParams& p, cudaStream_t st) {
   auto run_cta = [&](auto kernel) {
     static const int per_sm = resident_ctas(kernel, kThreads);
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(p.R, (int64_t)sm_count() * per_sm));
-    kernel<<<(unsigned)grid, kThreads, 0, st>>>(p);
+    return launch_pdl(kernel, dim3((unsigned)grid), dim3(kThreads), st, p);
   };
-  if (Bs <= kThreads) {
-    run_cta(quant_token_cta_kernel<FMT, SR, FOS, 1>);
-  } else if (Bs <= 2 * kThreads) {
-    run_cta(quant_token_cta_kernel<FMT, SR, FOS, 2>);
-  } else if (Bs <= 4 * kThreads) {
-    run_cta(quant_token_cta_kernel<FMT, SR, FOS, 4>);
-  } else {
-    const int64_t want = (p.R + kWarps - 1) / kWarps;
-    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sm_count() * 8));
-    quant_token_kernel<FMT, SR, FOS><<<(unsigned)grid, kThreads, 0, st>>>(p);
-  }
-  return cudaGetLastError();
+  if (Bs <= kThreads) return run_cta(quant_token_cta_kernel<FMT, SR, FOS, 1>);
+  if (Bs <= 2 * kThreads) return run_cta(quant_token_cta_kernel<FMT, SR, FOS, 2>);
+  if (Bs <= 4 * kThreads) return run_cta(quant_token_cta_kernel<FMT, SR, FOS, 4>);
+  const int64_t want = (p.R + kWarps - 1) / kWarps;
+  const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sm_count() * 8));
+  return launch_pdl(quant_token_kernel<FMT, SR, FOS>, dim3((unsigned)grid), dim3(kThreads), st, p);
 }
 
 }  // namespace

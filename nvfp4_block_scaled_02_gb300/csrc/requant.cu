@@ -166,6 +166,7 @@ constexpr int min_blocks(int target, bool sr, int fos) {
 template <int TARGET, int DFMT, bool SR, int FOS>
 __global__ void __launch_bounds__(kThreads, min_blocks(TARGET, SR, FOS)) requant_kernel(const RequantParams p, int64_t tiles_r,
                                                            int64_t tiles_c) {
+  pdl_begin();
   constexpr bool NV = TARGET == 1;
   __shared__ __align__(16) float4 s_x[TR * kSlots];
   __shared__ float s_src[256];
@@ -353,8 +354,7 @@ cudaError_t launch_t(const RequantParams& p, cudaStream_t st) {
   auto k = requant_kernel<TARGET, DFMT, SR, FOS>;
   const int64_t cap = (int64_t)sm_count() * resident_ctas(k, kThreads);
   const unsigned grid = (unsigned)(total < cap ? total : cap);
-  k<<<grid, kThreads, 0, st>>>(p, tiles_r, tiles_c);
-  return cudaGetLastError();
+  return launch_pdl(k, dim3(grid), dim3(kThreads), st, p, tiles_r, tiles_c);
 }
 
 template <int DFMT, bool SR>

@@ -20,6 +20,7 @@ namespace {
 constexpr int kThreads = 256;
 
 __global__ void __launch_bounds__(kThreads) scale_init_mse_kernel(const ScaleInitParams p) {
+  pdl_begin();
   __shared__ float s_d[128], s_inv[128];
   const SliceScale ss = slice_scale(*p.gamax, 448.0f);
   if (threadIdx.x < 128) scale_entry<0>((uint32_t)threadIdx.x, ss.g, s_d[threadIdx.x],
@@ -59,8 +60,7 @@ cudaError_t launch_scale_init_mse(const ScaleInitParams& p, cudaStream_t st) {
   const int64_t want = (p.nblocks + kThreads - 1) / kThreads;
   const int64_t cap = (int64_t)sm_count() * resident_ctas(scale_init_mse_kernel, kThreads);
   const unsigned grid = (unsigned)(want < cap ? (want > 0 ? want : 1) : cap);
-  scale_init_mse_kernel<<<grid, kThreads, 0, st>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(scale_init_mse_kernel, dim3(grid), dim3(kThreads), st, p);
 }
 
 }  // namespace nvfp4

@@ -52,6 +52,7 @@ __device__ __forceinline__ bool raw_fp8_scales_ok(float sp, float so, float spq)
 
 template <bool Q8>
 __global__ void __launch_bounds__(kThreads) fakequant_fwd_kernel(const SteParams p) {
+  pdl_begin();
   const int64_t nchunks = p.nblocks * 2;
   const int64_t stride = (int64_t)gridDim.x * kThreads;
   Fp8Unit u{1.0f, 1.0f, false};
@@ -85,6 +86,7 @@ __global__ void __launch_bounds__(kThreads) fakequant_fwd_kernel(const SteParams
 
 template <bool TIED, bool WANT_GX, bool Q8>
 __global__ void __launch_bounds__(kThreads) scale_grad_bwd_kernel(const SteParams p) {
+  pdl_begin();
   const int64_t nchunks = p.nblocks * 2;
   const int64_t stride = (int64_t)gridDim.x * kThreads;
   Fp8Unit u{1.0f, 1.0f, false};
@@ -172,6 +174,7 @@ __global__ void __launch_bounds__(kThreads) scale_grad_bwd_kernel(const SteParam
 // NVFP4 row encoding whose de-quantisation is that forward. Two lanes per
 // block, 8 codes (one 32-bit word) each; the even lane writes the scale byte.
 __global__ void __launch_bounds__(kThreads) export_scales_kernel(const SteParams p) {
+  pdl_begin();
   const int64_t nchunks = p.nblocks * 2;
   const int64_t stride = (int64_t)gridDim.x * kThreads;
   const Fp8Unit u = fp8_unit(p.gamax);
@@ -207,30 +210,27 @@ unsigned grid_for(int64_t nchunks) {
 
 cudaError_t launch_fakequant_fwd(const SteParams& p, cudaStream_t st) {
   const unsigned grid = grid_for(p.nblocks * 2);
-  if (p.gamax) fakequant_fwd_kernel<true><<<grid, kThreads, 0, st>>>(p);
-  else fakequant_fwd_kernel<false><<<grid, kThreads, 0, st>>>(p);
-  return cudaGetLastError();
+  if (p.gamax) return launch_pdl(fakequant_fwd_kernel<true>, dim3(grid), dim3(kThreads), st, p);
+  return launch_pdl(fakequant_fwd_kernel<false>, dim3(grid), dim3(kThreads), st, p);
 }
 
 template <bool Q8>
-void launch_bwd_t(const SteParams& p, unsigned grid, cudaStream_t st) {
+cudaError_t launch_bwd_t(const SteParams& p, unsigned grid, cudaStream_t st) {
   const bool tied = p.s_post == nullptr, want_gx = p.out != nullptr;
-  if (tied && want_gx) scale_grad_bwd_kernel<true, true, Q8><<<grid, kThreads, 0, st>>>(p);
-  else if (tied) scale_grad_bwd_kernel<true, false, Q8><<<grid, kThreads, 0, st>>>(p);
-  else if (want_gx) scale_grad_bwd_kernel<false, true, Q8><<<grid, kThreads, 0, st>>>(p);
-  else scale_grad_bwd_kernel<false, false, Q8><<<grid, kThreads, 0, st>>>(p);
+  const dim3 g(grid), b(kThreads);
+  if (tied && want_gx) return launch_pdl(scale_grad_bwd_kernel<true, true, Q8>, g, b, st, p);
+  if (tied) return launch_pdl(scale_grad_bwd_kernel<true, false, Q8>, g, b, st, p);
+  if (want_gx) return launch_pdl(scale_grad_bwd_kernel<false, true, Q8>, g, b, st, p);
+  return launch_pdl(scale_grad_bwd_kernel<false, false, Q8>, g, b, st, p);
 }
 
 cudaError_t launch_scale_grad_bwd(const SteParams& p, cudaStream_t st) {
   const unsigned grid = grid_for(p.nblocks * 2);
-  if (p.gamax) launch_bwd_t<true>(p, grid, st);
-  else launch_bwd_t<false>(p, grid, st);
-  return cudaGetLastError();
+  return p.gamax ? launch_bwd_t<true>(p, grid, st) : launch_bwd_t<false>(p, grid, st);
 }
 
 cudaError_t launch_export_scales(const SteParams& p, cudaStream_t st) {
-  export_scales_kernel<<<grid_for(p.nblocks * 2), kThreads, 0, st>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(export_scales_kernel, dim3(grid_for(p.nblocks * 2)), dim3(kThreads), st, p);
 }
 
 }  // namespace nvfp4
