@@ -53,7 +53,7 @@ typedef enum {
   NVFP4_ERR_SHAPE = 2, /* negative size, or a blocked dim not a multiple of 16 */
   NVFP4_ERR_ALIGN = 3, /* a pointer is not aligned as required                 */
   NVFP4_ERR_ENUM = 4,  /* a configuration field is out of range                */
-  NVFP4_ERR_CUDA = 6   /* a CUDA launch or memset failed                       */
+  NVFP4_ERR_CUDA = 6   /* a CUDA launch failed                                 */
 } nvfp4_status;
 
 /* Bits of the device status word. */

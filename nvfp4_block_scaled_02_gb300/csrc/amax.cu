@@ -56,11 +56,27 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const uint16_t* __restri
   }
 }
 
+// Zeroes n 32-bit words (the amax output before its atomic max, 4/6 bitmaps
+// before their atomic ORs): a kernel of our own, launched like every other so
+// that it overlaps the previous kernel's tail, where a memset would not.
+__global__ void zero_words_kernel(uint32_t* p, int64_t n) {
+  pdl_begin();
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) p[i] = 0u;
+}
+
 }  // namespace
+
+cudaError_t launch_zero_words(uint32_t* p, int64_t n, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  const int64_t want = (n + 255) / 256, cap = (int64_t)sm_count() * 4;
+  return launch_pdl(zero_words_kernel, dim3((unsigned)(want < cap ? want : cap)), dim3(256), st, p,
+                    n);
+}
 
 cudaError_t launch_amax(const uint16_t* x, int64_t S, int64_t n, float* amax, int32_t* status,
                         cudaStream_t st) {
-  cudaError_t e = cudaMemsetAsync(amax, 0, (size_t)S * sizeof(float), st);
+  cudaError_t e = launch_zero_words(reinterpret_cast<uint32_t*>(amax), S, st);  // for the atomic max
   if (e != cudaSuccess) return e;
   if (n == 0) return cudaSuccess;
   const int64_t nvec = n / 8 + 1;

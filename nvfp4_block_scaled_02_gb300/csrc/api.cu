@@ -158,8 +158,10 @@ nvfp4_status nvfp4_quantize(const nvfp4_config* cfg, const void* x, int64_t slic
   // column blocks (alone or with row blocks): the bitmaps are OR-ed into
   if (fos) {
     const size_t bytes = (size_t)(slices * W) * sizeof(uint32_t);
-    if (do_row && cudaMemsetAsync(row->choice, 0, bytes, st) != cudaSuccess) return NVFP4_ERR_CUDA;
-    if (cudaMemsetAsync(col->choice, 0, bytes, st) != cudaSuccess) return NVFP4_ERR_CUDA;
+    const int64_t words = (int64_t)(bytes / sizeof(uint32_t));
+    if (do_row && nvfp4::launch_zero_words(row->choice, words, st) != cudaSuccess)
+      return NVFP4_ERR_CUDA;
+    if (nvfp4::launch_zero_words(col->choice, words, st) != cudaSuccess) return NVFP4_ERR_CUDA;
   }
   nvfp4::DualParams p{};
   p.x = static_cast<const uint16_t*>(x);
@@ -252,7 +254,7 @@ nvfp4_status nvfp4_requant_transpose(const nvfp4_config* src, const nvfp4_config
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (fos) {
     const size_t W = (size_t)((rows * cols / 16 + 31) / 32);
-    if (cudaMemsetAsync(out->choice, 0, (size_t)slices * W * sizeof(uint32_t), st) != cudaSuccess)
+    if (nvfp4::launch_zero_words(out->choice, (int64_t)(slices * W), st) != cudaSuccess)
       return NVFP4_ERR_CUDA;
   }
   nvfp4::RequantParams p{};

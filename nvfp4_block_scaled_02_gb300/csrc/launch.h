@@ -141,6 +141,9 @@ struct RequantParams {
 cudaError_t launch_requant(const RequantParams& p, int target, int dst_fmt, bool sr, int fos,
                            cudaStream_t st);
 
+// Zero n 32-bit words on the stream (overlaps the previous kernel's tail).
+cudaError_t launch_zero_words(uint32_t* p, int64_t n, cudaStream_t st);
+
 // Per-slice global amax.
 cudaError_t launch_amax(const uint16_t* x, int64_t S, int64_t n, float* amax, int32_t* status,
                         cudaStream_t st);
