@@ -165,6 +165,7 @@ nvfp4_status nvfp4_quantize(const nvfp4_config* cfg, const void* x, int64_t slic
   }
   nvfp4::DualParams p{};
   p.x = static_cast<const uint16_t*>(x);
+  p.S = slices;
   p.R = rows;
   p.C = cols;
   p.gamax = global_amax;
