@@ -56,10 +56,12 @@ def measured_peak():
 # ------------------------------------------------------------ workloads --
 
 class Kernel:
-    """A launch of one of our kernels and its algorithmic HBM bytes."""
+    """One call of the C ABI, its algorithmic HBM bytes and the number of our
+    kernels it launches (a zeroing kernel precedes the atomic amax and the
+    OR-ed 4/6 bitmaps of the column, dual and re-quantisation kernels)."""
 
-    def __init__(self, name, nbytes, fn):
-        self.name, self.nbytes, self.fn = name, nbytes, fn
+    def __init__(self, name, nbytes, fn, launches=1):
+        self.name, self.nbytes, self.fn, self.launches = name, nbytes, fn, launches
 
 
 class Workload:
@@ -115,7 +117,7 @@ class Activation(Workload):
         self._amax, self._quant = amax, quant
 
     def kernels(self, k, i):
-        return [Kernel("amax", self.a_bytes, lambda: self._amax(i)),
+        return [Kernel("amax", self.a_bytes, lambda: self._amax(i), 2),
                 Kernel("quantize_row", self.q_bytes, lambda: self._quant(i))]
 
     def e2e_io(self, k):
@@ -269,7 +271,7 @@ class DriftingGradient(Workload):
         t = k % self.nsets
         ks = []
         if t % self.period == 0:
-            ks.append(Kernel("amax", self.a_bytes, lambda: self._amax(t)))
+            ks.append(Kernel("amax", self.a_bytes, lambda: self._amax(t), 2))
         ks.append(Kernel("quantize_row_sr", self.q_bytes, lambda: self._quant(t)))
         return ks
 
@@ -337,8 +339,8 @@ class MoeExperts(Workload):
         self._amax, self._dual = amax, dual
 
     def kernels(self, k, i):
-        return [Kernel("amax", self.a_bytes, self._amax),
-                Kernel("quantize_dual", self.d_bytes, self._dual)]
+        return [Kernel("amax", self.a_bytes, self._amax, 2),
+                Kernel("quantize_dual", self.d_bytes, self._dual, 3)]
 
     def e2e_io(self, k):
         names = ("codes", "scales", "choice", "dequant")
@@ -454,7 +456,7 @@ class RequantActivation(Workload):
         self.dominant = "requant_mxfp8_sr" if target == 0 else "requant_nvfp4_sr"
 
     def kernels(self, k, i):
-        return [Kernel(self.dominant, self.r_bytes, lambda: self._rq(i))]
+        return [Kernel(self.dominant, self.r_bytes, lambda: self._rq(i), 2 if self.target == 1 else 1)]
 
     def e2e_io(self, k):
         o = self.out[0]
@@ -641,7 +643,7 @@ class TileWeight(Workload):
         self._amax, self._tile = amax, tile
 
     def kernels(self, k, i):
-        return [Kernel("amax", self.a_bytes, lambda: self._amax(i)),
+        return [Kernel("amax", self.a_bytes, lambda: self._amax(i), 2),
                 Kernel("quantize_tile16", self.t_bytes, lambda: self._tile(i))]
 
     def e2e_io(self, k):
@@ -820,7 +822,8 @@ def time_ours(wl, args, world, local):
     total_ms = a.elapsed_time(b)
     per_kernel = {}
     for kern, e0, e1 in evs:
-        d = per_kernel.setdefault(kern.name, {"ms": 0.0, "n": 0, "bytes": kern.nbytes})
+        d = per_kernel.setdefault(kern.name, {"ms": 0.0, "n": 0, "bytes": kern.nbytes,
+                                              "launches": kern.launches})
         d["ms"] += e0.elapsed_time(e1)
         d["n"] += 1
     return total_ms, per_kernel, clk, wall
@@ -1059,7 +1062,8 @@ def main():
     dom_ms = dom["ms"] / dom["n"]
     achieved = dom["bytes"] / (dom_ms * 1e-3) / 1e9
     traffic = _committed_traffic(args.config, wl.dominant)
-    kernels = {name: {"launches": d["n"], "avg_us": round(1e3 * d["ms"] / d["n"], 3),
+    kernels = {name: {"calls": d["n"], "kernels_per_call": d["launches"],
+                      "avg_us": round(1e3 * d["ms"] / d["n"], 3),
                       "alg_bytes": int(d["bytes"]),
                       "gbs": round(d["bytes"] / (d["ms"] / d["n"] * 1e-3) / 1e9, 1),
                       "frac_of_peak": round(d["bytes"] / (d["ms"] / d["n"] * 1e-3) / 1e9 / peak, 4)}
@@ -1079,7 +1083,7 @@ def main():
                      "traffic": traffic, "kernel": wl.dominant,
                      "peak_source": f"{peak_kind} HBM copy bandwidth"},
         "kernels": kernels,
-        "gpu_launches": sum(d["n"] for d in per_kernel.values()),
+        "gpu_launches": sum(d["n"] * d["launches"] for d in per_kernel.values()),
         "clocks": clk,
         "host_wall_s": round(wall, 3),
     }
