@@ -110,6 +110,9 @@ def _declare(L):
     L.orc_e4m3_rne_array.argtypes = [_f32p, _i64, _u8p]
     L.orc_e4m3_sr_array.argtypes = [_f32p, _u32p, _i64, _u8p]
     L.orc_mx_shared_exp_array.argtypes = [_f32p, _i64, _u8p]
+    L.orc_mx_quantize.restype = C.c_int
+    L.orc_mx_quantize.argtypes = [C.c_int, C.c_int, C.c_uint32, C.c_uint32, _u16p, _i64, _i64,
+                                  _i64, _u8p, _u8p, _u8p, _u8p]
     L.orc_quantize_tile16.restype = C.c_int
     L.orc_quantize_tile16.argtypes = [C.c_int, C.c_int, C.c_float, C.c_uint32, C.c_uint32, _u16p,
                                       _i64, _i64, _i64, _f32p, _u8p, _u8p, _u16p, _u8p, _u8p,
@@ -267,6 +270,26 @@ def quantize(x_bf16: np.ndarray, gamax: np.ndarray, *, blocks: int = 1, scale_fm
                             _p(g("col_codes"), _u8p), _p(g("col_scales"), _u8p),
                             _p(g("col_choice"), _u32p), _p(g("col_dq"), _u16p))
     out["status"] = st
+    return out
+
+
+def mx_quantize(x_bf16: np.ndarray, *, blocks: int = 3, rounding: int = 1, seed: int = 0,
+                step: int = 0) -> dict:
+    """MXFP8 encodings of a bf16 [S, R, C] tensor: rows (blocks of 32 along C,
+    codes [S, R, C], E8M0 scales [S, R, C/32]) and/or columns (the row encoding
+    of the transpose, codes [S, C, R], scales [S, C, R/32])."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    if x.ndim == 2:
+        x = x[None]
+    S, R, Cc = x.shape
+    out = {"row_codes": np.zeros((S, R, Cc), np.uint8) if blocks & 1 else None,
+           "row_scales": np.zeros((S, R, Cc // 32), np.uint8) if blocks & 1 else None,
+           "col_codes": np.zeros((S, Cc, R), np.uint8) if blocks & 2 else None,
+           "col_scales": np.zeros((S, Cc, R // 32), np.uint8) if blocks & 2 else None}
+    g = out.get
+    out["status"] = lib().orc_mx_quantize(
+        blocks, rounding, seed, step, _p(x, _u16p), S, R, Cc, _p(g("row_codes"), _u8p),
+        _p(g("row_scales"), _u8p), _p(g("col_codes"), _u8p), _p(g("col_scales"), _u8p))
     return out
 
 

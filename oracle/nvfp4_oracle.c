@@ -864,3 +864,49 @@ int orc_quantize_tile16(int fmt, int rounding, float scale_max, uint32_t seed, u
       }
   return st;
 }
+
+/* ------------------------------------------ MXFP8 quantisation of bf16 ---- */
+/* End-to-End 4-Bit Training, the quantised-linear-layer figure: the bf16
+ * output gradient is quantised to MXFP8 with stochastic rounding for the
+ * DGRAD GEMM and, transposed, again for the WGRAD GEMM.
+ *
+ * Reading:
+ *  R17 Row encoding: per 32 consecutive values along C, the MX encoding of
+ *      R10 (E8M0 shared exponent rounded up, E4M3 elements by RNE or by the
+ *      stochastic rule with direction 0 and the row layout's flat indices);
+ *      codes [S][R][C], scales [S][R][C/32]. Column encoding: the row
+ *      encoding of X^T with direction 1 (codes [S][C][R], scales
+ *      [S][C][R/32]). C % 32 == 0 for rows, R % 32 == 0 for columns. */
+int orc_mx_quantize(int blocks, int rounding, uint32_t seed, uint32_t step, const uint16_t* x,
+                    int64_t S, int64_t R, int64_t C, uint8_t* r_codes, uint8_t* r_scales,
+                    uint8_t* c_codes, uint8_t* c_scales) {
+  int st = 0;
+  int64_t N = S * R * C;
+  float* xf = (float*)malloc((size_t)(N > 0 ? N : 1) * sizeof(float));
+  for (int64_t i = 0; i < N; ++i) {
+    if ((x[i] & 0x7FFFu) >= 0x7F80u) st |= ORC_ST_NONFINITE_INPUT;
+    xf[i] = orc_bf16_to_f32(x[i]);
+  }
+  if (blocks & 1)
+    for (int64_t s = 0; s < S; ++s)
+      for (int64_t r = 0; r < R; ++r) {
+        int64_t e0 = s * R * C + r * C;
+        orc_mx_encode(xf + e0, C, rounding, seed, step, 0, (uint64_t)e0, r_codes + e0,
+                      r_scales + e0 / 32);
+      }
+  if (blocks & 2) {
+    float* xt = (float*)malloc((size_t)(N > 0 ? N : 1) * sizeof(float));
+    for (int64_t s = 0; s < S; ++s)
+      for (int64_t r = 0; r < R; ++r)
+        for (int64_t c = 0; c < C; ++c) xt[s * R * C + c * R + r] = xf[s * R * C + r * C + c];
+    for (int64_t s = 0; s < S; ++s)
+      for (int64_t c = 0; c < C; ++c) {
+        int64_t e0 = s * C * R + c * R;
+        orc_mx_encode(xt + e0, R, rounding, seed, step, 1, (uint64_t)e0, c_codes + e0,
+                      c_scales + e0 / 32);
+      }
+    free(xt);
+  }
+  free(xf);
+  return st;
+}
