@@ -672,6 +672,69 @@ class TileWeight(Workload):
         "(RNE), row encoding and its transpose with both dequants from one read"))
 
 
+class GradientMx(Workload):
+    """The 16384 x 4096 gradient quantised to MXFP8 for the backward GEMMs: rows
+    (for DGRAD) and the transpose (for WGRAD) from one read, E8M0 scale per 32,
+    E4M3 elements by stochastic rounding."""
+
+    def __init__(self, device, rows=16384, cols=4096, seed=3):
+        gen = synth.DriftingGradient(rows, cols, seed=seed)
+        self.rows, self.cols = rows, cols
+        self.elements = rows * cols
+        self.m_bytes = self.elements * (2 + 2 * (1 + 1 / 32))
+        self.nsets = max(2, int(np.ceil(2.5 * L2_BYTES / self.m_bytes)))
+        self.host0 = gen.step(0)
+        self.x = [torch.from_numpy(gen.step(t).view(np.int16)).to(device)
+                  for t in range(self.nsets)]
+        self.row = [nv.alloc_mx(1, rows, cols, device) for _ in range(self.nsets)]
+        self.col = [nv.alloc_mx(1, cols, rows, device) for _ in range(self.nsets)]
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.working_set = self.m_bytes * self.nsets
+        L = nv.lib()
+        st = torch.cuda.current_stream(device).cuda_stream
+        self._cfgs = [nv.Config(blocks=nv.BLOCKS_BOTH, rounding=1, seed=12, step=t).c()
+                      for t in range(64)]
+        self._ro = [nv._Out(o["codes"].data_ptr(), o["scales"].data_ptr(), None, None)
+                    for o in self.row]
+        self._co = [nv._Out(o["codes"].data_ptr(), o["scales"].data_ptr(), None, None)
+                    for o in self.col]
+
+        def mx(k, i):
+            return L.nvfp4_mx_quantize(C.byref(self._cfgs[k % 64]), self.x[i].data_ptr(), 1, rows,
+                                       cols, C.byref(self._ro[i]), C.byref(self._co[i]),
+                                       self.status.data_ptr(), st)
+        self._mx = mx
+
+    def kernels(self, k, i):
+        return [Kernel("mx_quantize_sr", self.m_bytes, lambda: self._mx(k, i))]
+
+    def e2e_io(self, k):
+        return [self.x[0]], [self.row[0]["codes"], self.row[0]["scales"], self.col[0]["codes"],
+                             self.col[0]["scales"]]
+
+    def cpu_sample(self, budget_s):
+        import oracle
+        rows = 32
+
+        def once(n):
+            t0 = time.perf_counter()
+            oracle.mx_quantize(self.host0[:n], blocks=3, rounding=1, seed=12, step=0)
+            return time.perf_counter() - t0
+        per_row = once(rows) / rows
+        rows = int(min(self.rows, max(32, budget_s / max(per_row, 1e-9))))
+        rows -= rows % 32
+        return rows * self.cols, once(rows), \
+            f"first {rows} of {self.rows} rows (MXFP8 rows and transpose, stochastic rounding)"
+
+    bytes_per_elem = property(lambda self: self.m_bytes / self.elements)
+    dominant = "mx_quantize_sr"
+    workload = property(lambda self: (
+        f"gradient {self.rows}x{self.cols} bf16 N(0,1) x per-row lognormal(0,2) quantised to "
+        "MXFP8 for the backward GEMMs: rows and the transpose from one read, E8M0 scale per 32, "
+        "E4M3 elements by stochastic rounding (Philox4x32-10, key seed/step); outputs codes, "
+        "scales"))
+
+
 class RequantActivationNvfp4(RequantActivation):
     def __init__(self, device):
         super().__init__(device, target=1)
@@ -680,7 +743,7 @@ class RequantActivationNvfp4(RequantActivation):
 WORKLOADS = {1: SmallNormal, 2: Activation, 3: ScaleLearning, 4: DriftingGradient,
              5: MoeExperts, 6: PerTokenActivation, 7: RequantActivation,
              8: RequantActivationNvfp4, 9: ScaleLearningFp8, 10: ScaleInitExport,
-             11: TileWeight}
+             11: TileWeight, 12: GradientMx}
 
 
 # --------------------------------------------------------------- clocks --
@@ -980,6 +1043,16 @@ def _reference_sample(args):
             return n * wb.shape[1], time.perf_counter() - t0
         return "weight 14336x4096 16x16 tile scale + transpose", 2 + 2 + 2 * (0.5 + 1 / 16 + 2), \
             f"first {n} of 14336 rows per step", step
+    if args.config == 12:
+        xb = synth.DriftingGradient(seed=3).step(0)
+        n = max(32, args.ref_rows - args.ref_rows % 32)
+
+        def step():
+            t0 = time.perf_counter()
+            oracle.mx_quantize(xb[:n], blocks=3, rounding=1, seed=12, step=0)
+            return n * xb.shape[1], time.perf_counter() - t0
+        return "gradient 16384x4096 MXFP8 rows + transpose, SR", 2 + 2 * (1 + 1 / 32), \
+            f"first {n} of 16384 rows per step", step
     if args.config in (9, 10):
         wb, gb, s = synth.scale_learning(seed=2)
         gam = float(np.abs(synth.bf16_bits_to_f32(wb)).max()) * 1.5
@@ -1047,7 +1120,7 @@ def main():
     if args.steps is None:
         # about two seconds of device time, so the clock samples cover the run
         args.steps = {1: 20000, 2: 40000, 3: 10000, 4: 16000, 5: 150, 6: 50000, 7: 40000,
-                      8: 40000, 9: 10000, 10: 300, 11: 8000}[args.config]
+                      8: 40000, 9: 10000, 10: 300, 11: 8000, 12: 30000}[args.config]
     total_ms, per_kernel, clk, wall = time_ours(wl, args, world, local)
     total_ms = max_over_ranks(total_ms, world)
     units = wl.elements * args.steps * world
@@ -1122,6 +1195,7 @@ KERNEL_SOURCES = {
     "scale_init_mse": ["scale_init.cu"] + _COMMON,
     "export_scales": ["ste.cu"] + _COMMON,
     "quantize_tile16": ["quant_tile16.cu"] + _COMMON,
+    "mx_quantize_sr": ["mx_quant.cu", "mx_quant.h"] + _COMMON,
 }
 
 

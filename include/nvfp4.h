@@ -287,6 +287,33 @@ NVFP4_API nvfp4_status nvfp4_requant_transpose(const nvfp4_config* src, const nv
                                                const float* global_amax, const nvfp4_out* out,
                                                int32_t* status, void* stream);
 
+/* MXFP8 quantisation of a bf16 tensor x [slices][rows][cols] (End-to-End
+ * 4-Bit Training, the quantised-linear-layer figure: the bf16 output gradient
+ * is quantised to MXFP8 with stochastic rounding for the DGRAD GEMM and,
+ * transposed, for the WGRAD GEMM). Per 32 consecutive values: shared
+ * exponent e = the smallest integer with amax <= 448 * 2^e (clamped to
+ * [-127, 127]; 448 = E4M3's largest value), scale byte e + 127 (E8M0);
+ * element byte = the signed E4M3 code of v * 2^-e (one fp32 rounding), by
+ * RNE or by stochastic rounding onto the E4M3 grid; never saturating, as
+ * |v * 2^-e| <= 448.
+ * cfg: blocks NVFP4_BLOCKS_ROW / COL / BOTH (both from one read of x),
+ * rounding, seed, step; the other fields are ignored.
+ *   row encoding (blocks along cols, cols % 32 == 0): row->codes
+ *     [S][R][C] bytes, row->scales [S][R][C/32];
+ *   col encoding (the row encoding of X^T, rows % 32 == 0): col->codes
+ *     [S][C][R], col->scales [S][C][R/32].
+ * choice is ignored; dequant must be NULL (NVFP4_ERR_ENUM). Stochastic
+ * rounding: the 16 random bits of the element at flat index idx of its
+ * output layout are those nvfp4_quantize uses, with direction 0 (rows) or 1
+ * (columns) in the counter. A block holding NaN or Inf sets
+ * NVFP4_DEV_NONFINITE_INPUT; its bytes are then unspecified.
+ * Errors: NULL cfg / x / a required output, blocks or rounding out of range,
+ * negative sizes, cols % 32 (rows wanted) or rows % 32 (columns wanted), x
+ * or a codes buffer not 16-byte aligned, status not 4-byte aligned. */
+NVFP4_API nvfp4_status nvfp4_mx_quantize(const nvfp4_config* cfg, const void* x, int64_t slices,
+                                         int64_t rows, int64_t cols, const nvfp4_out* row,
+                                         const nvfp4_out* col, int32_t* status, void* stream);
+
 /* ---- diagnostics: the device codecs element by element -------------------
  * For exhaustive checks of the conversions the kernels use. op:
  *   0: out[i] = E2M1 RNE code of in[i]

@@ -24,7 +24,7 @@ __all__ = [
     "nvfp4_fakequant_fwd", "nvfp4_scale_grad_bwd", "nvfp4_codec_probe", "nvfp4_sr_bits",
     "nvfp4_quantize_per_token", "nvfp4_requant_transpose", "TARGET_MXFP8", "TARGET_NVFP4",
     "nvfp4_fakequant_fwd_fp8scale", "nvfp4_scale_grad_bwd_fp8scale", "nvfp4_scale_init_mse",
-    "nvfp4_export_scales",
+    "nvfp4_export_scales", "nvfp4_mx_quantize", "alloc_mx",
     "alloc_encoding", "alloc_requant", "PeriodicAmax", "BLOCKS_ROW", "BLOCKS_COL", "BLOCKS_BOTH",
     "BLOCKS_TILE16",
     "SCALE_E4M3", "SCALE_UE5M3", "ROUND_RNE", "ROUND_SR", "FOS_MSE", "FOS_MAE", "FOS_MAX",
@@ -118,6 +118,8 @@ def lib() -> C.CDLL:
             L.nvfp4_scale_init_mse.argtypes = [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp]
             L.nvfp4_export_scales.argtypes = [_vp, _i64, _i64, _vp, _vp, _vp, C.POINTER(_Out),
                                               _vp, _vp]
+            L.nvfp4_mx_quantize.argtypes = [C.POINTER(_Config), _vp, _i64, _i64, _i64,
+                                            C.POINTER(_Out), C.POINTER(_Out), _vp, _vp]
             L.nvfp4_codec_probe.argtypes = [_i32, _vp, _vp, _i64, _vp, _vp]
             L.nvfp4_sr_bits.argtypes = [_u32, _u32, _u32, C.c_uint64, _i64, _vp, _vp]
             L.nvfp4_status_string.restype = C.c_char_p
@@ -125,7 +127,7 @@ def lib() -> C.CDLL:
             for name in ("nvfp4_amax", "nvfp4_quantize", "nvfp4_quantize_per_token",
                          "nvfp4_requant_transpose", "nvfp4_fakequant_fwd",
                          "nvfp4_fakequant_fwd_fp8scale", "nvfp4_scale_grad_bwd_fp8scale",
-                         "nvfp4_scale_init_mse", "nvfp4_export_scales",
+                         "nvfp4_scale_init_mse", "nvfp4_export_scales", "nvfp4_mx_quantize",
                          "nvfp4_scale_grad_bwd", "nvfp4_codec_probe", "nvfp4_sr_bits"):
                 getattr(L, name).restype = C.c_int
             _lib = L
@@ -301,6 +303,36 @@ def nvfp4_requant_transpose(codes: torch.Tensor, scales: torch.Tensor,
         _dev(global_amax, "global_amax"), C.byref(o), _dev(status, "status"),
         _stream(codes.device)))
     return out
+
+
+def alloc_mx(slices: int, rows: int, cols: int, device) -> dict:
+    """Output tensors of one MXFP8 encoding of a [slices, rows, cols] input, for
+    blocks of 32 along `cols` (pass the transposed dims for the columns)."""
+    return {"codes": torch.empty((slices, rows, cols), dtype=torch.uint8, device=device),
+            "scales": torch.empty((slices, rows, cols // 32), dtype=torch.uint8, device=device)}
+
+
+def nvfp4_mx_quantize(x: torch.Tensor, cfg: Config | None = None, row: dict | None = None,
+                      col: dict | None = None, status: torch.Tensor | None = None) -> dict:
+    """MXFP8-encode a bf16 tensor (E8M0 scale per 32 values, E4M3 elements):
+    rows and/or the transpose per cfg.blocks, RNE or stochastic per
+    cfg.rounding. Returns {"row": {...}, "col": {...}} (allocated here unless
+    passed in)."""
+    cfg = cfg or Config(blocks=BLOCKS_BOTH, rounding=ROUND_SR)
+    S, R, Cc = _shape3(x)
+    if cfg.blocks & 1 and row is None:
+        row = alloc_mx(S, R, Cc, x.device)
+    if cfg.blocks & 2 and col is None:
+        col = alloc_mx(S, Cc, R, x.device)
+    ro = _Out(_dev(row["codes"], "codes"), _dev(row["scales"], "scales"), None, None) \
+        if cfg.blocks & 1 else None
+    co = _Out(_dev(col["codes"], "codes"), _dev(col["scales"], "scales"), None, None) \
+        if cfg.blocks & 2 else None
+    c = cfg.c()
+    _check("nvfp4_mx_quantize", lib().nvfp4_mx_quantize(
+        C.byref(c), _bf16(x, "x"), S, R, Cc, C.byref(ro) if ro is not None else None,
+        C.byref(co) if co is not None else None, _dev(status, "status"), _stream(x.device)))
+    return {"row": row if cfg.blocks & 1 else None, "col": col if cfg.blocks & 2 else None}
 
 
 def nvfp4_fakequant_fwd(x: torch.Tensor, s_pre: torch.Tensor, s_post: torch.Tensor | None = None,

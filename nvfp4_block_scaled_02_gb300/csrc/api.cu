@@ -5,6 +5,7 @@
 #include <mutex>
 
 #include "launch.h"
+#include "mx_quant.h"
 
 namespace nvfp4 {
 
@@ -277,6 +278,44 @@ nvfp4_status nvfp4_requant_transpose(const nvfp4_config* src, const nvfp4_config
   p.rule = dst->four_over_six_rule;
   return cuda_status(nvfp4::launch_requant(p, target, dst->scale_fmt, dst->rounding == NVFP4_ROUND_SR,
                                            nv ? fos_mode(dst) : 0, st));
+}
+
+nvfp4_status nvfp4_mx_quantize(const nvfp4_config* cfg, const void* x, int64_t slices,
+                               int64_t rows, int64_t cols, const nvfp4_out* row,
+                               const nvfp4_out* col, int32_t* status, void* stream) {
+  if (!cfg) return NVFP4_ERR_NULL;
+  if (cfg->blocks < 1 || cfg->blocks > 3 || cfg->rounding < 0 || cfg->rounding > 1)
+    return NVFP4_ERR_ENUM;
+  const bool do_row = cfg->blocks & 1, do_col = cfg->blocks & 2;
+  if (slices < 0 || rows < 0 || cols < 0 || (do_row && cols % 32 != 0) ||
+      (do_col && rows % 32 != 0))
+    return NVFP4_ERR_SHAPE;
+  if (slices == 0 || rows == 0 || cols == 0) return NVFP4_OK;
+  if (!x || (do_row && (!row || !row->codes || !row->scales)) ||
+      (do_col && (!col || !col->codes || !col->scales)))
+    return NVFP4_ERR_NULL;
+  if ((do_row && row->dequant) || (do_col && col->dequant)) return NVFP4_ERR_ENUM;
+  if (!aligned(x, 16) || !aligned(status, 4) || (do_row && !aligned(row->codes, 16)) ||
+      (do_col && !aligned(col->codes, 16)))
+    return NVFP4_ERR_ALIGN;
+  nvfp4::MxParams p{};
+  p.x = static_cast<const uint16_t*>(x);
+  p.S = slices;
+  p.R = rows;
+  p.C = cols;
+  p.seed = cfg->seed;
+  p.step = cfg->step;
+  if (do_row) {
+    p.r_codes = row->codes;
+    p.r_scales = row->scales;
+  }
+  if (do_col) {
+    p.c_codes = col->codes;
+    p.c_scales = col->scales;
+  }
+  p.status = status;
+  return cuda_status(nvfp4::launch_mx_quant(p, do_row, do_col, cfg->rounding == NVFP4_ROUND_SR,
+                                            static_cast<cudaStream_t>(stream)));
 }
 
 static nvfp4_status ste_common(const void* x, int64_t rows, int64_t cols, const float* s_pre) {

@@ -163,6 +163,36 @@ def test_requant_argument_errors(L):
         assert rq(L, s, d, codes=0, scales=0, S=S, R=R, Cc=Cc, amax=0, out=None) == 0
 
 
+def mx(L, cfg, x=FAKE, S=1, R=32, Cc=64, row=None, col=None, status=None):
+    return L.nvfp4_mx_quantize(C.byref(cfg) if cfg is not None else None, x, S, R, Cc,
+                               C.byref(row) if row is not None else None,
+                               C.byref(col) if col is not None else None, status, None)
+
+
+def test_mx_quantize_argument_errors(L):
+    ok = _out(choice=0, dq=0)
+    assert mx(L, None, row=ok, col=ok) == 1
+    for bad in (dict(blocks=0), dict(blocks=4), dict(rounding=2), dict(rounding=-1)):
+        assert mx(L, _cfg(**bad), row=ok, col=ok) == 4, bad
+    assert mx(L, _cfg(blocks=1), Cc=48, row=ok) == 2       # rows need cols % 32
+    assert mx(L, _cfg(blocks=2), R=16, col=ok) == 2        # columns need rows % 32
+    assert mx(L, _cfg(blocks=3), R=48, row=ok, col=ok) == 2
+    assert mx(L, _cfg(blocks=3), S=-1, row=ok, col=ok) == 2
+    assert mx(L, _cfg(blocks=1), x=0, row=ok) == 1
+    assert mx(L, _cfg(blocks=1), row=None) == 1
+    assert mx(L, _cfg(blocks=2), col=None) == 1
+    assert mx(L, _cfg(blocks=3), row=ok, col=_out(scales=0, choice=0, dq=0)) == 1
+    assert mx(L, _cfg(blocks=1), row=_out(choice=0)) == 4  # dequant output not offered
+    assert mx(L, _cfg(blocks=1), x=FAKE + 2, row=ok) == 3
+    assert mx(L, _cfg(blocks=1), row=_out(codes=FAKE + 8, choice=0, dq=0)) == 3
+    assert mx(L, _cfg(blocks=2), col=_out(codes=FAKE + 4, choice=0, dq=0)) == 3
+    assert mx(L, _cfg(blocks=1), row=ok, status=FAKE + 2) == 3
+    # a column-only call does not need cols % 32 (nor a row output)
+    assert mx(L, _cfg(blocks=2), Cc=40, col=ok, x=FAKE + 2) == 3
+    for S, R, Cc in ((0, 32, 32), (1, 0, 32), (1, 32, 0)):
+        assert mx(L, _cfg(blocks=3), x=0, S=S, R=R, Cc=Cc) == 0
+
+
 def test_fp8_scale_learning_argument_errors(L):
     fq = L.nvfp4_fakequant_fwd_fp8scale
     assert fq(FAKE, 4, 32, FAKE, None, None, FAKE, None, None) == 1       # no global amax
