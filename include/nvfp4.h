@@ -323,8 +323,8 @@ NVFP4_API nvfp4_status nvfp4_mx_quantize(const nvfp4_config* cfg, const void* x,
  *   4: out[i] = signed E4M3 RNE code of in[i]   (MXFP8 element encoder)
  *   5: out[i] = signed E4M3 stochastic code of in[i] with bits aux[i] & 0xFFFF
  *   6: out[i] = E8M0 byte (e + 127) of the MX shared exponent for amax in[i]
- *   7: as 5, by the form the kernel uses when every value of a group is 0 or
- *      at least 2^-6 in magnitude (defined for those inputs, |in[i]| <= 448)
+ *   7: as 5, by the unsaturated form the kernels use (defined for
+ *      |in[i]| <= 448)
  * Ops 0 and 3 convert groups of 8 consecutive inputs exactly as the kernels do.
  * in, aux (ops 3, 5): device arrays of n elements; out: device uint8 [n].
  * This entry point has no counterpart on the pages; it exists for testing. */

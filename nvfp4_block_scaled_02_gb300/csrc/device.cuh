@@ -242,32 +242,27 @@ __device__ __forceinline__ uint32_t e4m3x4_rn(float y0, float y1, float y2, floa
 // up iff v / 2^16 < p, p the position of |y| between its two grid neighbours
 // and v the 16 random bits. n8 = ((0xFFFF - v) << 8) | 0x400000F0 (the
 // constant fills bytes the random bits do not use). Returns a word whose top
-// byte is the signed code.
-// Construction (as in sr_mag): with T = code_lo * 2^16 + ceil(p * 2^16), the
-// magnitude code is (T + 0xFFFF - v) >> 16. Normal range (|y| >= 2^-6): the
-// exponent and top 3 mantissa bits of the fp32 pattern are code_lo once the
-// exponent is rebiased (127 -> 7) and the 20 bits below are p * 2^20, so with
-// everything scaled by 16, (bits << 4) - (120 << 27) + 15 * 16 + ((0xFFFF - v)
-// << 8) holds the code in its top byte (the sign bit is shifted out; 15 * 16
-// rounds the 4 dropped bits up). Below 2^-6 (the subnormals; the grid
-// spacing is 2^-9 up to 2^-5): T = ceil(|y| * 2^25), one fma rounded up
-// against 2^23, and the same expression is reached from the stand-in pattern
-// (120 << 23) + 16 T. The sign is OR-ed in from y.
-__device__ __forceinline__ uint32_t e4m3_sr_hi(float y, uint32_t n8) {
-  const uint32_t Y = __float_as_uint(y);
+// byte is the magnitude code (e4m3_sr_mag_hi) or the signed code (e4m3_sr_hi).
+// Construction: let P be an fp32 pattern whose exponent and top 3 mantissa
+// bits spell the lower neighbour's code once the exponent is rebiased
+// (127 -> 7) and whose 20 mantissa bits below hold f = ceil(p * 2^20). Then
+// in 16 P + n8 the 0x40 byte does the rebias (mod 2^32; the sign bit and the
+// top exponent bits fall off), 0xF0 rounds f up to 16 bits, and the carry
+// out of the fraction, which happens iff ceil(f / 16) = ceil(p * 2^16) > v,
+// lifts the code to the upper neighbour. For |y| >= 2^-6 (E4M3 normals) P is
+// the pattern of |y| itself. Below 2^-6 the grid is uniform with spacing
+// 2^-9 (the subnormals), and P is the pattern of 2^-7 + |y| / 2 rounded up:
+// that value lies in [2^-7, 2^-6), where fp32 values are 2^-30 apart, so its
+// mantissa is ceil(|y| * 2^29) = code * 2^20 + f over the exponent of 2^-7,
+// which the rebias turns into code 0. One maximum picks the right pattern:
+// 2^-7 + |y| / 2 exceeds |y| exactly when |y| < 2^-6 (and rounding it up
+// never lifts it above |y| otherwise).
+__device__ __forceinline__ uint32_t e4m3_sr_mag_hi(float y, uint32_t n8) {
   const float a = fabsf(y);
-  const uint32_t F = __float_as_uint(__fmaf_ru(a, 33554432.0f, 8388608.0f));
-  const uint32_t Ys = F * 16u + 0x8C000000u;  // (120 << 23) + 16 (F - (150 << 23))
-  const uint32_t Ye = a < 0.015625f ? Ys : Y;
-  return ((Ye << 4) + n8) | (Y & 0x80000000u);
+  return (__float_as_uint(fmaxf(a, __fmaf_ru(a, 0.5f, 0.0078125f))) << 4) + n8;
 }
-// The same for a y known to be 0 or at least 2^-6 in magnitude: clamping |y|
-// up to 2^-7 sends zeros to code 0 through the normal-range expression (their
-// pattern then contributes (120 << 23) << 4, which the constant cancels).
-__device__ __forceinline__ uint32_t e4m3_sr_hi_normal(float y, uint32_t n8) {
-  const uint32_t Y = __float_as_uint(y);
-  const uint32_t A = __float_as_uint(fmaxf(fabsf(y), 0.0078125f));
-  return ((A << 4) + n8) | (Y & 0x80000000u);
+__device__ __forceinline__ uint32_t e4m3_sr_hi(float y, uint32_t n8) {
+  return e4m3_sr_mag_hi(y, n8) | (__float_as_uint(y) & 0x80000000u);
 }
 // (0xFFFF - v) << 8 | 0x400000F0 for the 16-bit half h of the complemented
 // draw word nw = ~w (v = half h of w): one byte permute.

@@ -10,8 +10,11 @@
 // One CTA (256 threads) per 64 (R) x 128 (C) tile of one slice:
 //  1. thread t loads chunks k * 256 + t (k = 0..3) of 8 bf16 (a warp reads two
 //     whole 256-byte tile rows per load); a 32-value row block is 4
-//     consecutive lanes, which combine their amax with two xor shuffles, and
-//     each lane encodes its 8 values from registers (one Philox group);
+//     consecutive lanes, which combine their amax with two xor shuffles;
+//     once all four chunks are in, each lane encodes its 8 values per chunk
+//     from registers (one Philox group; the stochastic rounder yields
+//     magnitudes and the signs are OR-ed in four at a time from the source
+//     words with one byte permute);
 //  2. the chunks go to a 16 KiB shared tile of 32-bit words (two columns
 //     each), word w of row r stored at w ^ (((r >> 4) & 3) << 3);
 //  3. lane (cp, q) = (lane >> 2, lane & 3) of warp w reads rows 16q .. 16q+15
@@ -37,29 +40,101 @@ __device__ __forceinline__ int word_of(int r, int w) {
   return r * kWords + (w ^ (((r >> 4) & 3) << 3));
 }
 
-// E4M3 codes of 8 scaled values (|y| <= 448), RNE or stochastic with the
-// group's random bits rb (value i uses the 16-bit half i % 2 of word i / 2).
-template <bool SR>
-__device__ __forceinline__ uint2 e4m3x8(const float* y, const uint4& rb) {
-  if constexpr (!SR) {
-    return make_uint2(e4m3x4_rn(y[0], y[1], y[2], y[3]), e4m3x4_rn(y[4], y[5], y[6], y[7]));
-  } else {
-    const uint32_t nw[4] = {~rb.x, ~rb.y, ~rb.z, ~rb.w};
-    uint32_t x[8];
+// Stochastic E4M3 rounding of 8 scaled values (|y| <= 448) with the group's
+// random bits rb (value i uses the 16-bit half i % 2 of word i / 2): the
+// magnitude codes in order (value 0 in the low byte of the first word); the
+// caller ORs in the signs, four at a time, from the source bf16 words.
+__device__ __forceinline__ uint2 e4m3x8_sr_mag(const float* y, const uint4& rb) {
+  const uint32_t nw[4] = {~rb.x, ~rb.y, ~rb.z, ~rb.w};
+  uint32_t x[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) x[i] = e4m3_sr_hi(y[i], e4m3_sr_n8(nw[i >> 1], i & 1));
-    // the codes are the top bytes
-    return make_uint2(__byte_perm(__byte_perm(x[0], x[1], 0x0073u),
-                                  __byte_perm(x[2], x[3], 0x0073u), 0x5410u),
-                      __byte_perm(__byte_perm(x[4], x[5], 0x0073u),
-                                  __byte_perm(x[6], x[7], 0x0073u), 0x5410u));
+  for (int i = 0; i < 8; ++i) x[i] = e4m3_sr_mag_hi(y[i], e4m3_sr_n8(nw[i >> 1], i & 1));
+  // the codes are the top bytes
+  return make_uint2(__byte_perm(__byte_perm(x[0], x[1], 0x0073u),
+                                __byte_perm(x[2], x[3], 0x0073u), 0x5410u),
+                    __byte_perm(__byte_perm(x[4], x[5], 0x0073u),
+                                __byte_perm(x[6], x[7], 0x0073u), 0x5410u));
+}
+
+// Row blocks: this thread's chunks k (8 values each, v[k]) under shared
+// exponents ex[k]; writes codes and (one lane of four) the scale byte.
+template <bool SR>
+__device__ __forceinline__ void encode_rows(const MxParams& p, const uint4 (&v)[4],
+                                            const int (&ex)[4], const int64_t (&e)[4],
+                                            const bool (&ok)[4], int lane) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const f2 sc = make_float2(exp2_neg(ex[k]), exp2_neg(ex[k]));
+    f2 x[4];
+    unpack8(v[k], x);
+    float y[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const f2 t = f2_mul(x[i], sc);
+      y[2 * i] = t.x;
+      y[2 * i + 1] = t.y;
+    }
+    uint2 codes;
+    if constexpr (SR) {
+      codes = e4m3x8_sr_mag(y, sr_group_bits(p.seed, p.step, 0u, (uint64_t)e[k]));
+      codes.x |= __byte_perm(v[k].x, v[k].y, 0x7531u) & 0x80808080u;  // signs of values 0..3
+      codes.y |= __byte_perm(v[k].z, v[k].w, 0x7531u) & 0x80808080u;
+    } else {
+      codes = make_uint2(e4m3x4_rn(y[0], y[1], y[2], y[3]), e4m3x4_rn(y[4], y[5], y[6], y[7]));
+    }
+    if (ok[k]) {
+      __stcs(reinterpret_cast<uint2*>(p.r_codes + e[k]), codes);
+      if ((lane & 3) == 0) p.r_scales[e[k] / 32] = (uint8_t)(ex[k] + 127);
+    }
   }
 }
 
+// Column blocks: this lane's 16 rows (w[i] = columns cg, cg + 1 of row i)
+// under shared exponents ex[0], ex[1]; ce = flat column-layout index of the
+// first value of column cg.
 template <bool SR>
-__device__ __forceinline__ uint4 group_bits(const MxParams& p, uint32_t dir, int64_t idx0) {
-  if constexpr (SR) return sr_group_bits(p.seed, p.step, dir, (uint64_t)idx0);
-  else return make_uint4(0, 0, 0, 0);
+__device__ __forceinline__ void encode_cols(const MxParams& p, const uint32_t (&w)[16],
+                                            const int (&ex)[2], int64_t ce, bool ok0, bool ok1,
+                                            bool write_scale) {
+  uint32_t sg[2][4];  // signs of values 4k..4k+3 of each column
+  if constexpr (SR) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t a = __byte_perm(w[4 * k], w[4 * k + 1], 0x7351u);
+      const uint32_t b = __byte_perm(w[4 * k + 2], w[4 * k + 3], 0x7351u);
+      sg[0][k] = __byte_perm(a, b, 0x5410u) & 0x80808080u;
+      sg[1][k] = __byte_perm(a, b, 0x7632u) & 0x80808080u;
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {  // column cg + h
+    const f2 sc = make_float2(exp2_neg(ex[h]), exp2_neg(ex[h]));
+    float y[16];
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+      const f2 t = f2_mul(h ? make_float2(bf16_hi(w[i]), bf16_hi(w[i + 1]))
+                            : make_float2(bf16_lo(w[i]), bf16_lo(w[i + 1])), sc);
+      y[i] = t.x;
+      y[i + 1] = t.y;
+    }
+    const int64_t e = ce + h * p.R;
+    uint2 a, b;
+    if constexpr (SR) {
+      a = e4m3x8_sr_mag(y, sr_group_bits(p.seed, p.step, 1u, (uint64_t)e));
+      b = e4m3x8_sr_mag(y + 8, sr_group_bits(p.seed, p.step, 1u, (uint64_t)e + 8));
+      a.x |= sg[h][0];
+      a.y |= sg[h][1];
+      b.x |= sg[h][2];
+      b.y |= sg[h][3];
+    } else {
+      a = make_uint2(e4m3x4_rn(y[0], y[1], y[2], y[3]), e4m3x4_rn(y[4], y[5], y[6], y[7]));
+      b = make_uint2(e4m3x4_rn(y[8], y[9], y[10], y[11]), e4m3x4_rn(y[12], y[13], y[14], y[15]));
+    }
+    if (h ? ok1 : ok0) {
+      __stcs(reinterpret_cast<uint4*>(p.c_codes + e), make_uint4(a.x, a.y, b.x, b.y));
+      if (write_scale) p.c_scales[e / 32] = (uint8_t)(ex[h] + 127);
+    }
+  }
 }
 
 template <bool SR, bool ROWS, bool COLS>
@@ -77,14 +152,17 @@ __global__ void __launch_bounds__(kThreads) mx_quant_kernel(const MxParams p, in
 
   // ---- 1: load, flag non-finite values, encode the row blocks ------------
   uint4 v[4];
+  bool ok[4];
+  int64_t e[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const int chunk = k * kThreads + threadIdx.x;
     const int lr = chunk / kChunksPerRow, lc = (chunk % kChunksPerRow) * 8;
     const int64_t r = r0 + lr, c = c0 + lc;
-    const bool ok = r < R && c < C;
+    ok[k] = r < R && c < C;
+    e[k] = (s * R + r) * C + c;  // flat row-layout index
     v[k] = make_uint4(0, 0, 0, 0);
-    if (ok) {
+    if (ok[k]) {
       if (vec) {
         v[k] = __ldcs(reinterpret_cast<const uint4*>(xs + r * C + c));
       } else {  // column-only encoding of a tensor whose rows are not 16 B multiples
@@ -95,28 +173,22 @@ __global__ void __launch_bounds__(kThreads) mx_quant_kernel(const MxParams p, in
                           h[6] | (h[7] << 16));
       }
     }
-    uint32_t m = absmax_bits4(v[k]);
-    if (m >= 0x7F80u) flag(p.status, NVFP4_DEV_NONFINITE_INPUT_BIT);
-    if constexpr (ROWS) {  // C % 32 == 0: a block's four chunks are all in range or all out
+  }
+  if constexpr (ROWS) {  // C % 32 == 0: a block's four chunks are all in range or all out
+    int ex[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint32_t m = absmax_bits4(v[k]);
+      if (m >= 0x7F80u) flag(p.status, NVFP4_DEV_NONFINITE_INPUT_BIT);
       m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
       m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-      const int ex = mx_shared_exp(__uint_as_float(m << 16));
-      const float sc = exp2_neg(ex);
-      f2 x[4];
-      unpack8(v[k], x);
-      float y[8];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        y[2 * i] = __fmul_rn(x[i].x, sc);
-        y[2 * i + 1] = __fmul_rn(x[i].y, sc);
-      }
-      const int64_t e = (s * R + r) * C + c;  // flat row-layout index
-      const uint2 codes = e4m3x8<SR>(y, group_bits<SR>(p, 0u, e));
-      if (ok) {
-        __stcs(reinterpret_cast<uint2*>(p.r_codes + e), codes);
-        if ((lane & 3) == 0) p.r_scales[e / 32] = (uint8_t)(ex + 127);
-      }
+      ex[k] = mx_shared_exp(__uint_as_float(m << 16));
     }
+    encode_rows<SR>(p, v, ex, e, ok, lane);
+  } else {
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      if (absmax_bits4(v[k]) >= 0x7F80u) flag(p.status, NVFP4_DEV_NONFINITE_INPUT_BIT);
   }
 
   if constexpr (COLS) {
@@ -139,21 +211,12 @@ __global__ void __launch_bounds__(kThreads) mx_quant_kernel(const MxParams p, in
 #pragma unroll
     for (int i = 0; i < 16; ++i) mm = __vmaxu2(mm, w[i] & 0x7FFF7FFFu);
     mm = __vmaxu2(mm, __shfl_xor_sync(0xFFFFFFFFu, mm, 1));
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {  // column cg + h
-      const int ex = mx_shared_exp(__uint_as_float(h ? (mm & 0xFFFF0000u) : (mm << 16)));
-      const float sc = exp2_neg(ex);
-      float y[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) y[i] = __fmul_rn(h ? bf16_hi(w[i]) : bf16_lo(w[i]), sc);
-      const int64_t ce = (s * C + cg + h) * R + r0 + 16 * q;  // flat column-layout index
-      const uint2 a = e4m3x8<SR>(y, group_bits<SR>(p, 1u, ce));
-      const uint2 b = e4m3x8<SR>(y + 8, group_bits<SR>(p, 1u, ce + 8));
-      if (row_ok && cg + h < C) {
-        __stcs(reinterpret_cast<uint4*>(p.c_codes + ce), make_uint4(a.x, a.y, b.x, b.y));
-        if ((q & 1) == 0) p.c_scales[ce / 32] = (uint8_t)(ex + 127);
-      }
-    }
+    int ex[2];
+    ex[0] = mx_shared_exp(__uint_as_float(mm << 16));
+    ex[1] = mx_shared_exp(__uint_as_float(mm & 0xFFFF0000u));
+    const int64_t ce = (s * C + cg) * R + r0 + 16 * q;  // flat column-layout index
+    const bool ok0 = row_ok && cg < C, ok1 = row_ok && cg + 1 < C;
+    encode_cols<SR>(p, w, ex, ce, ok0, ok1, (q & 1) == 0);
   }
 }
 

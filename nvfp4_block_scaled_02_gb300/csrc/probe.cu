@@ -27,7 +27,7 @@ __global__ void codec_probe_kernel(int op, const float* __restrict__ in,
       if (op == 4) c = e4m3x4_rn(in[i], 0.0f, 0.0f, 0.0f);
       else if (op == 5) c = e4m3_sr(in[i], 0xFFFFu - (aux[i] & 0xFFFFu));
       else if (op == 7)
-        c = e4m3_sr_hi_normal(in[i], (((0xFFFFu - aux[i]) & 0xFFFFu) << 8) | 0x400000F0u) >> 24;
+        c = e4m3_sr_hi(in[i], (((0xFFFFu - aux[i]) & 0xFFFFu) << 8) | 0x400000F0u) >> 24;
       else c = (uint32_t)(mx_shared_exp(in[i]) + 127);
       out[i] = (uint8_t)(c & 0xFFu);
     }

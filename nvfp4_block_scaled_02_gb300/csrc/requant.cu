@@ -137,17 +137,11 @@ __device__ __forceinline__ uint4 sr_bits_or_zero(const RequantParams& p, uint64_
 
 // 8 scaled values -> 8 E4M3 codes by stochastic rounding with the group's
 // random bits rb (two words, element 0 in the low byte of the first).
-// normal: every value is 0 or at least 2^-6 in magnitude.
-__device__ __forceinline__ uint2 e4m3x8_sr(const float* y, const uint4& rb, bool normal) {
+__device__ __forceinline__ uint2 e4m3x8_sr(const float* y, const uint4& rb) {
   const uint32_t nw[4] = {~rb.x, ~rb.y, ~rb.z, ~rb.w};
   uint32_t x[8];
-  if (normal) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) x[i] = e4m3_sr_hi_normal(y[i], e4m3_sr_n8(nw[i >> 1], i & 1));
-  } else {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) x[i] = e4m3_sr_hi(y[i], e4m3_sr_n8(nw[i >> 1], i & 1));
-  }
+  for (int i = 0; i < 8; ++i) x[i] = e4m3_sr_hi(y[i], e4m3_sr_n8(nw[i >> 1], i & 1));
   // the codes are the top bytes
   return make_uint2(__byte_perm(__byte_perm(x[0], x[1], 0x0073u),
                                 __byte_perm(x[2], x[3], 0x0073u), 0x5410u),
@@ -171,11 +165,6 @@ __global__ void __launch_bounds__(kThreads, min_blocks(TARGET, SR, FOS)) requant
   __shared__ __align__(16) float4 s_x[TR * kSlots];
   __shared__ float s_src[256];
   __shared__ float s_d[NV ? 256 : 1], s_inv[NV ? 256 : 1];
-  // MXFP8 with stochastic rounding: per 16-row band and 16-column block of the
-  // tile, the smallest non-zero source block scale d (fp32 bits; two buffers
-  // by tile parity so the next tile's can be cleared while this one is read)
-  constexpr bool MXSR = !NV && SR;
-  __shared__ uint32_t s_dmin[MXSR ? 2 : 1][4][8];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int q = lane & 3, cp = lane >> 2;  // phase 2: 16-row quarter, column pair
@@ -200,9 +189,6 @@ __global__ void __launch_bounds__(kThreads, min_blocks(TARGET, SR, FOS)) requant
   const int cpair = 16 * warp + 2 * cp;
   const int64_t out_off0 = (int64_t)cpair * R + 16 * q;
 
-  if constexpr (MXSR) {
-    if (tid < 32) (&s_dmin[0][0][0])[tid] = 0x7F800000u;  // ordered by the first table barrier
-  }
   SrcRegs v;
   load_src(p, ntiles > 0, ti, L, v);
   int64_t cur_slice = -1;
@@ -221,9 +207,6 @@ __global__ void __launch_bounds__(kThreads, min_blocks(TARGET, SR, FOS)) requant
       const int bi = k * kThreads + tid;
       const int row = bi >> 3, cb = bi & 7;
       const float d = s_src[v.scale[k]];
-      if constexpr (MXSR) {
-        if (d > 0.0f) atomicMin(&s_dmin[it & 1][row >> 4][cb], __float_as_uint(d));
-      }
       f2 qv[4];
       float4* dst = s_x + row * kSlots;
       const f2 dd = make_float2(d, d);
@@ -272,9 +255,6 @@ __global__ void __launch_bounds__(kThreads, min_blocks(TARGET, SR, FOS)) requant
       f2 y[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) y[i] = f2_mul(xv[i], scv);
-      if constexpr (MXSR) {
-        if (tid < 32) (&s_dmin[(it + 1) & 1][0][0])[tid] = 0x7F800000u;  // for the next tile
-      }
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int c = cpair + h;
@@ -289,13 +269,8 @@ __global__ void __launch_bounds__(kThreads, min_blocks(TARGET, SR, FOS)) requant
                          e4m3x4_rn(yc[8], yc[9], yc[10], yc[11]),
                          e4m3x4_rn(yc[12], yc[13], yc[14], yc[15]));
         } else {
-          // every non-zero value of these 16 is at least 0.5 * dmin * 2^-e:
-          // when that is >= 2^-6 no value needs the 2^-9-spaced range
-          const float dmin = __uint_as_float(s_dmin[it & 1][q][warp]);
-          const bool normal = __fmul_rn(__fmul_rn(0.5f, dmin), h ? scv.y : scv.x) >= 0.015625f;
-          const uint2 a = e4m3x8_sr(yc, sr_group_bits(p.seed, p.step, 2u, (uint64_t)e0), normal);
-          const uint2 b =
-              e4m3x8_sr(yc + 8, sr_group_bits(p.seed, p.step, 2u, (uint64_t)e0 + 8), normal);
+          const uint2 a = e4m3x8_sr(yc, sr_group_bits(p.seed, p.step, 2u, (uint64_t)e0));
+          const uint2 b = e4m3x8_sr(yc + 8, sr_group_bits(p.seed, p.step, 2u, (uint64_t)e0 + 8));
           w = make_uint4(a.x, a.y, b.x, b.y);
         }
         if (ok) {

@@ -88,6 +88,16 @@ def test_special_values():
     x[6, 32:64] = 448.0
     x[7, 64:96] = -2.0 ** -20
     x[:, 100] = 0.0                                     # a zero column
+    # smallest value exactly at / just below E4M3's normal range after scaling
+    # (block max 448 gives e = 0): the two sides of the rounder's fast form
+    x[8, :32] = rng.standard_normal(32) * 100
+    x[8, 0], x[8, 5] = 448.0, 2.0 ** -6
+    x[9, :32] = rng.standard_normal(32) * 100
+    x[9, 0], x[9, 5] = 448.0, 2.0 ** -6 - 2.0 ** -14
+    x[32:64, 102] = rng.standard_normal(32) * 100
+    x[32, 102], x[40, 102] = -448.0, -(2.0 ** -6)
+    x[32:64, 103] = rng.standard_normal(32) * 100
+    x[32, 103], x[41, 103] = 448.0, 2.0 ** -6 - 2.0 ** -14
     x[:, 101] = 1.75 * 2.0 ** -30                       # a constant column on the boundary
     xb = synth.to_bf16_bits(x).reshape(1, 64, 256)
     for rounding in (0, 1):

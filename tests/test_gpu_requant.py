@@ -96,33 +96,37 @@ def test_e4m3_stochastic_rounder_exhaustive_over_draws():
     assert_exact(got, oracle.e4m3_sr(y, v), "stochastic E4M3, all draws")
 
 
-def test_e4m3_stochastic_rounder_fast_form_exhaustive_over_draws():
-    """The form used when a group holds only zeros and values >= 2^-6: every
-    16-bit draw for values across its domain (zeros of both signs included)."""
-    cells = np.array([0.0, -0.0, 2.0 ** -6, 2.0 ** -6 * 1.01, -0.0173, 0.07, 1.3, 2.9, 17.0,
-                      100.1, 300.0, 447.9, 448.0, -5.5, -447.0], np.float32)
+def test_e4m3_stochastic_rounder_kernel_form_exhaustive_over_draws():
+    """The unsaturated form the kernels run: every 16-bit draw for values in
+    subnormal cells (fp32 subnormals included), at the subnormal/normal
+    boundary (where the stand-in pattern hands over to the value's own) and
+    across the normal binades, zeros of both signs included."""
+    cells = np.array([0.0, -0.0, 1e-45, -3e-41, 2.0 ** -40, 2.0 ** -11, 3.3 * 2.0 ** -9, 0.0154,
+                      2.0 ** -6 * (1 - 2.0 ** -24), 2.0 ** -6, 2.0 ** -6 * 1.01, -0.0173,
+                      2.0 ** -5 * (1 - 2.0 ** -20), 2.0 ** -5, 0.07, 1.3, 2.9, 17.0, 100.1, 300.0,
+                      447.9, 448.0, -5.5, -447.0], np.float32)
     y = np.repeat(cells, 65536)
     v = np.tile(np.arange(65536, dtype=np.uint32), cells.size)
     got = nv.nvfp4_codec_probe(7, torch.from_numpy(y).cuda(),
                                torch.from_numpy(v.view(np.int32)).cuda()).cpu().numpy()
-    assert_exact(got, oracle.e4m3_sr(y, v), "stochastic E4M3 (fast form), all draws")
+    assert_exact(got, oracle.e4m3_sr(y, v), "stochastic E4M3 (kernel form), all draws")
 
 
-def test_e4m3_stochastic_rounder_fast_form_random():
+def test_e4m3_stochastic_rounder_kernel_form_random():
     rng = np.random.default_rng(33)
     n = 1 << 22
-    mag = (rng.integers(0x3C800000, 0x43E00001, n, dtype=np.uint32)).view(np.float32)
+    mag = (rng.integers(0, 0x43E00001, n, dtype=np.uint32)).view(np.float32)  # [0, 448]
     y = np.where(rng.integers(0, 2, n) == 1, -mag, mag).astype(np.float32)
     y[::97] = 0.0
     v = rng.integers(0, 1 << 16, y.size, dtype=np.uint32)
     got = nv.nvfp4_codec_probe(7, torch.from_numpy(y).cuda(),
                                torch.from_numpy(v.view(np.int32)).cuda()).cpu().numpy()
-    assert_exact(got, oracle.e4m3_sr(y, v), "stochastic E4M3 (fast form)")
+    assert_exact(got, oracle.e4m3_sr(y, v), "stochastic E4M3 (kernel form)")
 
 
-def test_tiny_values_take_the_exact_rounder():
+def test_tiny_values_land_in_the_e4m3_subnormal_range():
     """Source blocks whose scale is 2^-16 of the others put values in the E4M3
-    2^-9-spaced range of their MX blocks (the kernel's exact form)."""
+    2^-9-spaced range of their MX blocks (the rounder's stand-in pattern)."""
     codes, scales, gam = _source((1, 64, 128), seed=30)
     scales = scales.copy()
     scales[0, ::5, ::3] = 0x01  # the smallest E4M3 scale: these values land below 2^-6
