@@ -7,14 +7,20 @@
 //  1. every thread loads 4 chunks of 8 bf16 (128-bit loads, a warp covers two
 //     full 256 B tile rows) and, in BOTH mode, encodes the row blocks straight
 //     from registers (lane pairs hold the two halves of a block);
-//  2. the chunks go to a 16 KiB shared tile;
-//  3. each warp takes a 16-row band of 64 columns: lane l reads the 32-bit
-//     word (2 columns) of each of the 16 rows -- 128 contiguous bytes per row,
-//     no bank conflicts -- and encodes the two column blocks it now holds.
-// Column outputs are the row encoding of X^T: per column c, 8 code bytes, one
-// scale byte and 32 B of dequant per band, each a full aligned segment.
-// 4/6 bits are gathered per tile row / per column and OR-ed into the
-// (pre-zeroed) bitmaps, since a tile's bits share words with other tiles.
+//  2. the chunks go to a 16 KiB shared tile of 32-bit words (two columns
+//     each), word w of row r stored at w ^ (((r >> 4) & 3) << 3);
+//  3. lane (cp, q) = (lane >> 2, lane & 3) of warp w takes column pair
+//     8w + cp in the 16-row band q: it reads one word per row (with the
+//     swizzle the 32 lanes hit 32 distinct banks) and encodes the two column
+//     blocks it now holds.
+// Column outputs are the row encoding of X^T. The four bands of a column sit
+// in four adjacent lanes, so each column's 64 rows go out contiguously from
+// one store instruction: 32 code bytes, 4 scale bytes, 128 B of dequant (two
+// instructions). Scattering a column's bands over four warps instead costs
+// several partial-sector writes per sector.
+// 4/6 bits are gathered per tile row (a ballot) and per column (a ballot over
+// the four band lanes) and OR-ed into the (pre-zeroed) bitmaps, since a
+// tile's bits share words with other tiles.
 #include "encode.cuh"
 #include "launch.h"
 
@@ -26,6 +32,11 @@ constexpr int kThreads = 256;
 constexpr int TR = 64;    // tile rows
 constexpr int TC = 128;   // tile columns
 constexpr int kChunksPerRow = TC / 8;
+constexpr int kWords = TC / 2;  // 32-bit words (column pairs) per tile row
+
+__device__ __forceinline__ int word_of(int r, int w) {
+  return r * kWords + (w ^ (((r >> 4) & 3) << 3));
+}
 
 __device__ __forceinline__ void or_bits(uint32_t* words, int64_t bit0, uint32_t bits, int nbits) {
   if (bits == 0) return;
@@ -47,9 +58,8 @@ template <int FMT, bool SR, int FOS, bool ROWS>
 __global__ void __launch_bounds__(kThreads) quant_dual_kernel(const DualParams p, int64_t tiles_r,
                                                               int64_t tiles_c) {
   pdl_begin();
-  __shared__ __align__(16) uint16_t tile[TR * TC];
+  __shared__ __align__(16) uint32_t tile[TR * kWords];
   __shared__ float s_d[256], s_inv[256];
-  __shared__ uint8_t s_cpick[TR / 16][TC];
 
   const int64_t R = p.R, C = p.C;
   const int64_t bid = blockIdx.x;
@@ -91,7 +101,8 @@ __global__ void __launch_bounds__(kThreads) quant_dual_kernel(const DualParams p
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const int chunk = k * kThreads + threadIdx.x;
-    reinterpret_cast<uint4*>(tile)[chunk] = v[k];
+    const int lr = chunk / kChunksPerRow, lw = (chunk % kChunksPerRow) * 4;
+    *reinterpret_cast<uint4*>(&tile[word_of(lr, lw)]) = v[k];
   }
   __syncthreads();  // tables and tile ready
 
@@ -133,13 +144,11 @@ __global__ void __launch_bounds__(kThreads) quant_dual_kernel(const DualParams p
   // ---- 3: column blocks ---------------------------------------------------
   {
     const bool want_dq = p.c_dq != nullptr;
-    const int cg = warp & 1, band = warp >> 1;
-    const int cl = cg * 64 + 2 * lane;  // local column of this lane's first block
-    const int64_t c = c0 + cl, r = r0 + band * 16;
+    const int q = lane & 3, cpl = warp * 8 + (lane >> 2);  // band, column pair
+    const int64_t c = c0 + 2 * cpl, r = r0 + 16 * q;
     uint32_t w[16];
-    const uint32_t* t32 = reinterpret_cast<const uint32_t*>(tile);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) w[i] = t32[(band * 16 + i) * (TC / 2) + cl / 2];
+    for (int i = 0; i < 16; ++i) w[i] = tile[word_of(16 * q + i, cpl)];
     uint32_t mm = 0;
 #pragma unroll
     for (int i = 0; i < 16; ++i) mm = __vmaxu2(mm, w[i] & 0x7FFF7FFFu);
@@ -173,23 +182,14 @@ __global__ void __launch_bounds__(kThreads) quant_dual_kernel(const DualParams p
           __stcs(reinterpret_cast<uint4*>(p.c_dq + e) + 1, br.dq[1]);
         }
       }
-      if constexpr (FOS) s_cpick[band][cl + j] = (okc && br.pick4) ? 1 : 0;  // one writer each
-    }
-    if constexpr (FOS) {
-      __syncthreads();
-      if (threadIdx.x < TC) {
-        const int64_t cc = c0 + threadIdx.x;
-        if (cc < C) {
-          uint32_t bits = 0;
-          int nb = 0;
-#pragma unroll
-          for (int b = 0; b < TR / 16; ++b)
-            if (r0 + 16 * b < R) {
-              bits |= (uint32_t)s_cpick[b][threadIdx.x] << b;
-              ++nb;
-            }
+      if constexpr (FOS) {
+        // bands 0..3 of this column are lanes 4cp .. 4cp+3: its 4 bits
+        const uint32_t b = __ballot_sync(0xFFFFFFFFu, okc && br.pick4);
+        if (q == 0 && c + j < C) {
           const int64_t Bs = slice_elems / 16, W = (Bs + 31) / 32;
-          or_bits(p.c_choice + s * W, cc * (R / 16) + r0 / 16, bits, nb);
+          const int64_t nb = (R - r0) / 16 < 4 ? (R - r0) / 16 : 4;
+          or_bits(p.c_choice + s * W, (c + j) * (R / 16) + r0 / 16, (b >> (lane & ~3)) & 15u,
+                  (int)nb);
         }
       }
     }
