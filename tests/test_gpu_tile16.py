@@ -95,3 +95,27 @@ def test_tile16_activation_size_sampled_bands():
         assert_exact(cc[:, 8 * b:8 * b + 8], ref["col_codes"][0], f"band {b} column codes")
         assert_exact(cs[:, b], ref["col_scales"][0][:, 0], f"band {b} column scales")
     assert int(st.item()) == 0
+
+
+@pytest.mark.parametrize("shape", [(1, 80, 144), (2, 64, 128)])
+def test_tile16_row_encoding_alone(shape):
+    """The column encoding is optional at the ABI: a call with no column
+    outputs writes the same row encoding."""
+    import ctypes as C
+    S, R, Cc = shape
+    xb = synth.student_t(S * R, Cc, seed=R).reshape(shape)
+    gamax, _ = oracle.global_amax(xb, S)
+    row = nv.alloc_encoding(S, R, Cc, "cuda", False, True)
+    x = dev_bits(xb)
+    gam = torch.from_numpy(np.asarray(gamax, np.float32)).cuda()
+    cfg = nv.Config(blocks=nv.BLOCKS_TILE16, rounding=1, seed=2, step=1).c()
+    ro = nv._out(row)
+    rc = nv.lib().nvfp4_quantize(C.byref(cfg), x.data_ptr(), S, R, Cc, gam.data_ptr(),
+                                 C.byref(ro), None, None,
+                                 torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    ref = oracle.quantize_tile16(xb, gamax, rounding=1, seed=2, step=1)
+    assert_exact(host_u8(row["codes"]), ref["row_codes"], "row codes")
+    assert_exact(host_u8(row["scales"]), ref["row_scales"], "row scales")
+    assert_exact(host_u16(row["dequant"]), ref["row_dq"], "row dequant")
