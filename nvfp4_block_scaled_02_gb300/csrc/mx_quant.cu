@@ -138,9 +138,8 @@ __device__ __forceinline__ void encode_cols(const MxParams& p, const uint32_t (&
 }
 
 template <bool SR, bool ROWS, bool COLS>
-__global__ void __launch_bounds__(kThreads) mx_quant_kernel(const MxParams p, int64_t tiles_r,
-                                                            int64_t tiles_c) {
-  pdl_begin();
+__device__ __forceinline__ void mx_quant_tile(const MxParams& p, int64_t tiles_r,
+                                              int64_t tiles_c) {
   __shared__ __align__(16) uint32_t tile[COLS ? TR * kWords : 4];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t R = p.R, C = p.C;
@@ -220,13 +219,35 @@ __global__ void __launch_bounds__(kThreads) mx_quant_kernel(const MxParams p, in
   }
 }
 
+// Two entry points for the register budget: the RNE kernels wait mostly on
+// memory and run faster with 6 resident CTAs per SM (registers held to 40);
+// the stochastic ones are bound by ALU issue and do best at the 57 registers
+// the compiler picks with no bound (4 CTAs; held to 64 it takes 63 and runs
+// 4 % slower).
+template <bool ROWS, bool COLS>
+__global__ void __launch_bounds__(kThreads, 6) mx_quant_rne_kernel(const MxParams p,
+                                                                   int64_t tiles_r,
+                                                                   int64_t tiles_c) {
+  pdl_begin();
+  mx_quant_tile<false, ROWS, COLS>(p, tiles_r, tiles_c);
+}
+template <bool ROWS, bool COLS>
+__global__ void mx_quant_sr_kernel(const MxParams p, int64_t tiles_r, int64_t tiles_c) {
+  pdl_begin();
+  mx_quant_tile<true, ROWS, COLS>(p, tiles_r, tiles_c);
+}
+
 template <bool SR, bool ROWS, bool COLS>
 cudaError_t launch_t(const MxParams& p, cudaStream_t st) {
   const int64_t tiles_r = (p.R + TR - 1) / TR, tiles_c = (p.C + TC - 1) / TC;
   const int64_t n = p.S * tiles_r * tiles_c;
   if (n > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
-  return launch_pdl(mx_quant_kernel<SR, ROWS, COLS>, dim3((unsigned)n), dim3(kThreads), st, p,
-                    tiles_r, tiles_c);
+  if constexpr (SR)
+    return launch_pdl(mx_quant_sr_kernel<ROWS, COLS>, dim3((unsigned)n), dim3(kThreads), st, p,
+                      tiles_r, tiles_c);
+  else
+    return launch_pdl(mx_quant_rne_kernel<ROWS, COLS>, dim3((unsigned)n), dim3(kThreads), st, p,
+                      tiles_r, tiles_c);
 }
 
 }  // namespace
