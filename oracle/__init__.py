@@ -86,6 +86,8 @@ def _declare(L):
                                    _u8p, _u8p, _u8p, _u16p, _f32p, _f32p]
     L.orc_global_amax.restype = C.c_int
     L.orc_global_amax.argtypes = [_u16p, _i64, _i64, _f32p]
+    L.orc_decode_scale.restype = C.c_float
+    L.orc_decode_scale.argtypes = [C.c_float, C.c_float]
     L.orc_quantize.restype = C.c_int
     L.orc_quantize.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_float,
                                C.c_uint32, C.c_uint32, _u16p, _i64, _i64, _i64, _f32p,
@@ -226,6 +228,11 @@ def encode_block(x16, g: float, fmt: int = 0, rounding: int = 0, fos: int = 0,
                            _p(dq, _u16p), _p(dqf, _f32p), _p(sse, _f32p))
     return dict(codes=codes, scale=int(scale[0]), choice=int(choice[0]), dq=dq, dqf=dqf,
                 sse6=float(sse[0]), sse4=float(sse[1]))
+
+
+def decode_scale(gamax: float, M: float) -> float:
+    """The per-slice decode scale g = gamax / (6 M) (1 for a zero or bad amax)."""
+    return float(lib().orc_decode_scale(float(gamax), float(M)))
 
 
 # ----------------------------------------------------------- whole path --

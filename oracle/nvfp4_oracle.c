@@ -257,6 +257,14 @@ static int global_decode_scale(float gamax, float M, float* g) {
   return 0;
 }
 
+/* R3 as a value: the decode scale g of a slice with global amax gamax and
+ * FP8 maximum M (for tests that encode single blocks of a larger tensor). */
+float orc_decode_scale(float gamax, float M) {
+  float g;
+  global_decode_scale(gamax, M, &g);
+  return g;
+}
+
 /* One candidate encoding of a 16-value block for target k (R4, R1/R5). */
 typedef struct {
   uint8_t scale;     /* block-scale code                    */
