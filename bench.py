@@ -120,10 +120,10 @@ class Activation(Workload):
         return [Kernel("amax", self.a_bytes, lambda: self._amax(i), 2),
                 Kernel("quantize_row", self.q_bytes, lambda: self._quant(i))]
 
-    def e2e_io(self, k):
-        o = self.out[0]
+    def e2e_io(self, k, i):
+        o = self.out[i]
         outs = [o["codes"], o["scales"], o["dequant"]] + ([o["choice"]] if self.fos else [])
-        return [self.x[0]], outs
+        return [self.x[i]], outs
 
     def cpu_sample(self, budget_s):
         import oracle
@@ -206,8 +206,8 @@ class ScaleLearning(Workload):
         return [Kernel("fakequant_fwd", self.f_bytes, lambda: self._fwd(i)),
                 Kernel("scale_grad_bwd", self.b_bytes, lambda: self._bwd(i))]
 
-    def e2e_io(self, k):
-        d = self.sets[0]
+    def e2e_io(self, k, i):
+        d = self.sets[i]
         return [d["w"], d["g"], d["sp"], d["so"]], [d["xq"], d["gx"], d["gsp"], d["gso"]]
 
     def cpu_sample(self, budget_s):
@@ -275,7 +275,7 @@ class DriftingGradient(Workload):
         ks.append(Kernel("quantize_row_sr", self.q_bytes, lambda: self._quant(t)))
         return ks
 
-    def e2e_io(self, k):
+    def e2e_io(self, k, i):  # the step picks its own buffers: input t, output t % 2
         t = k % self.nsets
         o = self.out[t % 2]
         return [self.x[t]], [o["codes"], o["scales"]]
@@ -342,7 +342,7 @@ class MoeExperts(Workload):
         return [Kernel("amax", self.a_bytes, self._amax, 2),
                 Kernel("quantize_dual", self.d_bytes, self._dual, 3)]
 
-    def e2e_io(self, k):
+    def e2e_io(self, k, i):
         names = ("codes", "scales", "choice", "dequant")
         outs = [self.row[n] for n in names] + [self.col[n] for n in names]
         return [self.x], outs
@@ -395,9 +395,9 @@ class PerTokenActivation(Activation):
     def kernels(self, k, i):
         return [Kernel("quantize_per_token", self.t_bytes, lambda: self._tok(i))]
 
-    def e2e_io(self, k):
-        o = self.out[0]
-        return [self.x[0]], [o["codes"], o["scales"], o["dequant"], o["choice"], self.row_amax[0]]
+    def e2e_io(self, k, i):
+        o = self.out[i]
+        return [self.x[i]], [o["codes"], o["scales"], o["dequant"], o["choice"], self.row_amax[i]]
 
     def _cpu_once(self, oracle, rows):
         xb = self.host_x[:rows].reshape(rows, 1, self.cols)
@@ -458,10 +458,10 @@ class RequantActivation(Workload):
     def kernels(self, k, i):
         return [Kernel(self.dominant, self.r_bytes, lambda: self._rq(i), 2 if self.target == 1 else 1)]
 
-    def e2e_io(self, k):
-        o = self.out[0]
+    def e2e_io(self, k, i):
+        o = self.out[i]
         outs = [o["codes"], o["scales"]] + ([o["choice"]] if self.target == 1 else [])
-        return [self.codes[0], self.scales[0], self.gamax], outs
+        return [self.codes[i], self.scales[i], self.gamax], outs
 
     def cpu_sample(self, budget_s):
         import oracle
@@ -579,8 +579,8 @@ class ScaleInitExport(ScaleLearningFp8):
         return [Kernel("scale_init_mse", self.i_bytes, lambda: self._init(i)),
                 Kernel("export_scales", self.e_bytes, lambda: self._export(i))]
 
-    def e2e_io(self, k):
-        d = self.sets[0]
+    def e2e_io(self, k, i):
+        d = self.sets[i]
         return [d["w"], d["so"]], [d["codes"], d["sp"], d["enc"]["codes"], d["enc"]["scales"]]
 
     def cpu_sample(self, budget_s):
@@ -646,9 +646,9 @@ class TileWeight(Workload):
         return [Kernel("amax", self.a_bytes, lambda: self._amax(i), 2),
                 Kernel("quantize_tile16", self.t_bytes, lambda: self._tile(i))]
 
-    def e2e_io(self, k):
+    def e2e_io(self, k, i):
         names = ("codes", "scales", "dequant")
-        return [self.x[0]], [self.row[0][n] for n in names] + [self.col[0][n] for n in names]
+        return [self.x[i]], [self.row[i][n] for n in names] + [self.col[i][n] for n in names]
 
     def cpu_sample(self, budget_s):
         import oracle
@@ -708,9 +708,9 @@ class GradientMx(Workload):
     def kernels(self, k, i):
         return [Kernel("mx_quantize_sr", self.m_bytes, lambda: self._mx(k, i))]
 
-    def e2e_io(self, k):
-        return [self.x[0]], [self.row[0]["codes"], self.row[0]["scales"], self.col[0]["codes"],
-                             self.col[0]["scales"]]
+    def e2e_io(self, k, i):
+        return [self.x[i]], [self.row[i]["codes"], self.row[i]["scales"], self.col[i]["codes"],
+                             self.col[i]["scales"]]
 
     def cpu_sample(self, budget_s):
         import oracle
@@ -893,37 +893,72 @@ def time_ours(wl, args, world, local):
 
 
 def time_e2e(wl, steps, device):
-    """The same metric through the C ABI with host buffers: every step copies
-    its inputs from pinned host memory to the device, runs the kernels and
-    copies every output back to pinned host memory."""
-    ins0, outs0 = wl.e2e_io(0)
+    """The same metric through the C ABI with host buffers, as a user streaming
+    tensors through it would run it: every step copies its inputs from pinned
+    host memory to the device (copy-in stream), runs the kernels (the
+    workload's stream) and copies every output back to pinned host memory
+    (copy-out stream). Step k uses device buffer set k % B (B = 2, or 1 when
+    the workload holds a single set); events order each buffer's reuse, so
+    one step's copies overlap its neighbours' compute and copies. Events
+    bracket the whole run on all three streams."""
+    B = 1 if wl.nsets == 1 else 2
+    ins0, outs0 = wl.e2e_io(0, 0)
     h_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in ins0]
     for h, t in zip(h_in, ins0):
         h.copy_(t.cpu())
-    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs0]
+    h_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs0]
+             for _ in range(B)]
     bi = sum(t.numel() * t.element_size() for t in ins0)
     bo = sum(t.numel() * t.element_size() for t in outs0)
+    comp = torch.cuda.current_stream(device)
+    cin, cout = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    in_free = [None] * B   # compute of the last step that read set b is done
+    out_free = [None] * B  # copy-out of the last step that wrote set b is done
 
     def step(k):
-        ins, outs = wl.e2e_io(k)
-        for h, t in zip(h_in, ins):
-            t.copy_(h, non_blocking=True)
-        for kern in wl.kernels(k, 0):
+        b = k % B
+        ins, outs = wl.e2e_io(k, b)
+        with torch.cuda.stream(cin):
+            if in_free[b] is not None:
+                cin.wait_event(in_free[b])
+            for h, t in zip(h_in, ins):
+                t.copy_(h, non_blocking=True)
+            e_in = torch.cuda.Event()
+            e_in.record(cin)
+        comp.wait_event(e_in)
+        if out_free[b] is not None:
+            comp.wait_event(out_free[b])
+        for kern in wl.kernels(k, b):
             rc = kern.fn()
             if rc != 0:
                 raise nv.Nvfp4Error(kern.name, rc)
-        for h, t in zip(h_out, outs):
-            h.copy_(t, non_blocking=True)
+        e_c = torch.cuda.Event()
+        e_c.record(comp)
+        in_free[b] = e_c
+        with torch.cuda.stream(cout):
+            cout.wait_event(e_c)
+            for h, t in zip(h_out[b], outs):
+                h.copy_(t, non_blocking=True)
+            e_o = torch.cuda.Event()
+            e_o.record(cout)
+        out_free[b] = e_o
+        return e_o
 
     for k in range(2):
         step(k)
     torch.cuda.synchronize()
+    in_free[:] = [None] * B
+    out_free[:] = [None] * B
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
-    a.record()
+    a.record(comp)
+    cin.wait_event(a)
+    cout.wait_event(a)
+    last = None
     for k in range(steps):
-        step(k)
-    b.record()
+        last = step(k)
+    comp.wait_event(last)
+    b.record(comp)
     torch.cuda.synchronize()
     return a.elapsed_time(b), bi, bo
 
