@@ -9,7 +9,7 @@ import torch
 
 import nvfp4_block_scaled_02_gb300 as nv
 import oracle
-from helpers import (assert_exact, compare_encoding, dev_bits, host_u8)
+from helpers import (assert_exact, compare_encoding, dev_bits, host_u16, host_u8)
 from nvfp4_block_scaled_02_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -228,3 +228,22 @@ def test_alternative_four_over_six_rules(rule, blocks, rounding):
     a, _ = oracle.global_amax(s, s.shape[0])
     rt = oracle.quantize(s, a, four_over_six=1, rounding=rounding, seed=7, rule=rule)
     compare_encoding(tok, rt, "row_", f"rule {rule} per-token", True)
+
+
+def test_more_slices_than_one_grid_dimension_holds():
+    """70000 slices of one 16-value row each: the per-slice launches split the
+    slices over several grids (at most 65535 per grid dimension)."""
+    S = 70000
+    xb = synth.outlier_normal(S, 16, seed=12).reshape(S, 1, 16)
+    x = dev_bits(xb)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    amax = nv.nvfp4_amax(x, status=st)
+    out = nv.nvfp4_quantize(x, amax, nv.Config(four_over_six=1), status=st)["row"]
+    ref_amax, _ = oracle.global_amax(xb, S)
+    ref = oracle.quantize(xb, ref_amax, four_over_six=1)
+    assert int(st.item()) == ref["status"] == 0
+    assert_exact(amax.cpu().numpy().view(np.uint32), ref_amax.view(np.uint32), "amaxes")
+    assert_exact(host_u8(out["codes"]), ref["row_codes"], "codes")
+    assert_exact(host_u8(out["scales"]), ref["row_scales"], "scales")
+    assert_exact(out["choice"].cpu().numpy().view(np.uint32), ref["row_choice"], "4/6 choices")
+    assert_exact(host_u16(out["dequant"]), ref["row_dq"], "dequant")
