@@ -53,6 +53,12 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# ALU roofline for a kernel bound by arithmetic by definition: simple fp32
+# operations per second of the whole GPU, 152 SMs x 128 fp32 lanes x the
+# 2070 MHz maximum SM clock (an fma counted as one operation).
+ALU_PEAK_TOPS = 152 * 128 * 2.070e9 / 1e12
+
+
 # ------------------------------------------------------------ workloads --
 
 class Kernel:
@@ -599,6 +605,10 @@ class ScaleInitExport(ScaleLearningFp8):
             f"first {rows} of {self.rows} rows (MSE sweep over 126 E4M3 scales + export)"
 
     bytes_per_elem = property(lambda self: (self.i_bytes + self.e_bytes) / self.elements)
+    # the sweep's algorithmic work: per element and candidate scale (126 E4M3
+    # codes) one scaling multiply, one E2M1 rounding, one decode, the error
+    # fma and the square-accumulate fma
+    alu_ops_per_elem = {"scale_init_mse": 5 * 126}
     dominant = "scale_init_mse"
     workload = property(lambda self: (
         f"weight {self.rows}x{self.cols} bf16 N(0,0.02): MSE scale setting over all 126 E4M3 "
@@ -1174,6 +1184,7 @@ def main():
         dom_ms, dur_src = dom["ms"] / dom["n"], "an event after every call"
     achieved = dom["bytes"] / (dom_ms * 1e-3) / 1e9
     traffic = _committed_traffic(args.config, wl.dominant)
+    alu_ops = getattr(wl, "alu_ops_per_elem", {}).get(wl.dominant)
     kernels = {name: {"calls": d["n"], "kernels_per_call": d["launches"],
                       "avg_us": round(1e3 * d["ms"] / d["n"], 3),
                       "alg_bytes": int(d["bytes"]),
@@ -1190,11 +1201,19 @@ def main():
                    "l2": (f"inputs larger than L2: {wl.nsets} rotating input/output sets, "
                           f"{wl.working_set / 2 ** 20:.0f} MiB > {L2_BYTES / 2 ** 20:.0f} MiB L2")},
         "gelem_per_s": round(units / (total_ms * 1e-3) / 1e9, 3),
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": traffic, "kernel": wl.dominant,
-                     "peak_source": f"{peak_kind} HBM copy bandwidth",
-                     "duration_from": dur_src},
+        "roofline": ({"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                      "unit": "GB/s", "frac": round(achieved / peak, 4),
+                      "traffic": traffic, "kernel": wl.dominant,
+                      "peak_source": f"{peak_kind} HBM copy bandwidth",
+                      "duration_from": dur_src} if alu_ops is None else
+                     {"bound": "alu",
+                      "achieved": round(alu_ops * wl.elements / (dom_ms * 1e-3) / 1e12, 2),
+                      "peak": round(ALU_PEAK_TOPS, 2), "unit": "Top/s",
+                      "frac": round(alu_ops * wl.elements / (dom_ms * 1e-3) / 1e12
+                                    / ALU_PEAK_TOPS, 4),
+                      "traffic": traffic, "kernel": wl.dominant,
+                      "peak_source": "152 SMs x 128 fp32 lanes x 2070 MHz (derived)",
+                      "ops_per_element": alu_ops, "duration_from": dur_src}),
         "kernels": kernels,
         "gpu_launches": sum(d["n"] * d["launches"] for d in per_kernel.values()),
         "clocks": clk,
