@@ -89,7 +89,7 @@ def test_special_values():
     x[7, 64:96] = -2.0 ** -20
     x[:, 100] = 0.0                                     # a zero column
     # smallest value exactly at / just below E4M3's normal range after scaling
-    # (block max 448 gives e = 0): the two sides of the rounder's fast form
+    # (block max 448 gives e = 0): the two sides of the stand-in pattern
     x[8, :32] = rng.standard_normal(32) * 100
     x[8, 0], x[8, 5] = 448.0, 2.0 ** -6
     x[9, :32] = rng.standard_normal(32) * 100
