@@ -181,13 +181,6 @@ __device__ __forceinline__ uint32_t sr_bits_of(const uint4& w, int k) {
   return (k & 1) ? (word >> 16) : (word & 0xFFFFu);
 }
 
-// Three-input fp32 minimum (one instruction on sm_100 and later).
-__device__ __forceinline__ float fmin3(float a, float b, float c) {
-  float r;
-  asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-  return r;
-}
-
 // Three-input fp32 maximum (one instruction on sm_100 and later); like fmaxf
 // it returns the other operands when one is NaN.
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
@@ -199,31 +192,43 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 // Stochastic E2M1 rounding of 8 values (4 pairs) with the group's 128 random
 // bits rb (value k uses the 16-bit half k%2 of word k/2): |y| rounds up to the
 // next grid value iff v / 2^16 < p, p = (|y| - lo) / (hi - lo).
-// On [0, 6] the map u(a) = min(a, 1 + a/2, 2 + a/4) sends the E2M1 grid to the
-// multiples of 1/2 (0..3.5) and is linear inside every grid cell, so with
-// T = ceil(u(|y|) * 2^17) = code_lo * 2^16 + ceil(p * 2^16) the magnitude code
-// is (T + 0xFFFF - v) >> 16. Each line is one fma rounded up against 2^23
-// (exact product, one rounding), and ceil commutes with min; |y| >= 6 (and
-// Inf/NaN) is capped at u = 3.5, code 7. The sign bits are those of the
-// round-to-nearest codes of the same values (both copy the sign of y).
-__device__ __forceinline__ uint32_t sr_mag(float y, uint32_t nv) {
-  const float a = fabsf(y);
-  const float t = fminf(fmin3(__fmaf_ru(a, 131072.0f, 8388608.0f),
-                              __fmaf_ru(a, 65536.0f, 8519680.0f),     // 2^23 + 2^17
-                              __fmaf_ru(a, 32768.0f, 8650752.0f)),    // 2^23 + 2^18
-                        8847360.0f);                                  // 2^23 + 7 * 2^16
-  return (__float_as_uint(t) - 0x4B000000u + nv) >> 16;
+// E2M1 is a small float (2 exponent bits, bias 1, 1 mantissa bit), and the
+// construction is the one of the stochastic E4M3 rounder below: let P be an
+// fp32 pattern whose exponent and top mantissa bit spell the lower
+// neighbour's code once the exponent is rebiased (127 -> 1) and whose 22
+// mantissa bits below hold f = ceil(p * 2^22). In 4 P + n, with
+// n = ((0xFFFF - v) << 8) | 0x040000FC, the 0x04 byte does the rebias (mod 4
+// on the two exponent bits that stay; the bits above the code are not used),
+// 0xFC rounds f up to 16 bits, and the carry out of the fraction, which
+// happens iff ceil(p * 2^16) > v, lifts the code in bits 24..26 to the upper
+// neighbour. For |y| in [1, 6] P is the pattern of |y| (capped at 6, code 7:
+// saturation, and where NaN and Inf land too). Below 1 the grid is uniform
+// with spacing 1/2, and P is the pattern of 1/2 + |y|/2 rounded up, which
+// lies in [1/2, 1), where fp32 values are 2^-24 apart: its mantissa is
+// ceil(|y| * 2^23) = code * 2^22 + f over the exponent of 1/2, which the
+// rebias turns into code 0 or 1. One maximum picks the pattern: 1/2 + |y|/2
+// exceeds |y| exactly when |y| < 1. The codes (top bytes) are gathered with
+// byte permutes, even values in one word and odd values in another, and
+// merged as nibbles; the sign bits are those of the round-to-nearest codes
+// of the same values (both copy the sign of y).
+__device__ __forceinline__ uint32_t e2m1_sr_word(float y, uint32_t n) {
+  const float a = fminf(fabsf(y), 6.0f);
+  return (__float_as_uint(fmaxf(a, __fmaf_ru(a, 0.5f, 0.5f))) << 2) + n;
 }
 __device__ __forceinline__ uint32_t sr8(const f2 (&y)[4], const uint4& rb) {
   const uint32_t sign = e2m1x8_rn(y) & 0x88888888u;
   const uint32_t nw[4] = {~rb.x, ~rb.y, ~rb.z, ~rb.w};  // 0xFFFF - v in each half
-  uint32_t w = sign;
+  uint32_t w[8];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    w += sr_mag(y[k].x, nw[k] & 0xFFFFu) << (8 * k);
-    w += sr_mag(y[k].y, nw[k] >> 16) << (8 * k + 4);
+  for (int k = 0; k < 4; ++k) {  // n for the low / high half of nw[k]
+    w[2 * k] = e2m1_sr_word(y[k].x, __byte_perm(nw[k], 0x040000FCu, 0x7104u));
+    w[2 * k + 1] = e2m1_sr_word(y[k].y, __byte_perm(nw[k], 0x040000FCu, 0x7324u));
   }
-  return w;
+  const uint32_t even = __byte_perm(__byte_perm(w[0], w[2], 0x0073u),
+                                    __byte_perm(w[4], w[6], 0x0073u), 0x5410u);
+  const uint32_t odd = __byte_perm(__byte_perm(w[1], w[3], 0x0073u),
+                                   __byte_perm(w[5], w[7], 0x0073u), 0x5410u);
+  return (even & 0x07070707u) | ((odd & 0x07070707u) << 4) | sign;
 }
 
 // ------------------------------------------------- MXFP8 (E4M3 elements) --
