@@ -215,8 +215,8 @@ __device__ __forceinline__ uint32_t e2m1_sr_word(float y, uint32_t n) {
   const float a = fminf(fabsf(y), 6.0f);
   return (__float_as_uint(fmaxf(a, __fmaf_ru(a, 0.5f, 0.5f))) << 2) + n;
 }
-__device__ __forceinline__ uint32_t sr8(const f2 (&y)[4], const uint4& rb) {
-  const uint32_t sign = e2m1x8_rn(y) & 0x88888888u;
+// sign: the sign bits of the 8 codes (bit 3 of each nibble).
+__device__ __forceinline__ uint32_t sr8_signed(const f2 (&y)[4], const uint4& rb, uint32_t sign) {
   const uint32_t nw[4] = {~rb.x, ~rb.y, ~rb.z, ~rb.w};  // 0xFFFF - v in each half
   uint32_t w[8];
 #pragma unroll
@@ -229,6 +229,13 @@ __device__ __forceinline__ uint32_t sr8(const f2 (&y)[4], const uint4& rb) {
   const uint32_t odd = __byte_perm(__byte_perm(w[1], w[3], 0x0073u),
                                    __byte_perm(w[5], w[7], 0x0073u), 0x5410u);
   return (even & 0x07070707u) | ((odd & 0x07070707u) << 4) | sign;
+}
+// Sign bits of the E2M1 codes of 8 values (bit 3 of each nibble).
+__device__ __forceinline__ uint32_t e2m1_signs(const f2 (&y)[4]) {
+  return e2m1x8_rn(y) & 0x88888888u;
+}
+__device__ __forceinline__ uint32_t sr8(const f2 (&y)[4], const uint4& rb) {
+  return sr8_signed(y, rb, e2m1_signs(y));
 }
 
 // ------------------------------------------------- MXFP8 (E4M3 elements) --

@@ -23,6 +23,19 @@ __device__ __forceinline__ uint32_t round8(const f2 (&x)[4], float inv, const ui
   if constexpr (!SR) return e2m1x8_rn(y);
   else return sr8(y, rb);
 }
+// The same with the codes' sign bits given (sign = e2m1_signs(x)): x * inv
+// has the sign of x for every inv >= 0 (zeros included), so the two 4/6
+// candidates of one block share them.
+template <bool SR>
+__device__ __forceinline__ uint32_t round8s(const f2 (&x)[4], float inv, const uint4& rb,
+                                            uint32_t sign) {
+  f2 y[4];
+  const f2 iv = make_float2(inv, inv);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) y[k] = f2_mul(x[k], iv);
+  if constexpr (!SR) return e2m1x8_rn(y);
+  else return sr8_signed(y, rb, sign);
+}
 
 // Sum over 8 values of (x - q d)^2 in the fixed order: even and odd positions
 // accumulate separately with fma from +0 (one f32x2 accumulator), then
@@ -116,7 +129,8 @@ __device__ __forceinline__ HalfResult encode_half(const f2 (&x)[4], uint32_t ama
   const float amax = __uint_as_float(amax_bits << 16);
   const uint32_t c6 = scale_encode<FMT>(__fmul_rn(amax, ss.rden6));
   const float d6 = s_d[c6], inv6 = s_inv[c6];
-  const uint32_t q6 = round8<SR>(x, inv6, rb);
+  const uint32_t sg = (SR && FOS) ? e2m1_signs(x) : 0u;
+  const uint32_t q6 = FOS ? round8s<SR>(x, inv6, rb, sg) : round8<SR>(x, inv6, rb);
   if constexpr (!FOS) {
     r.codes = q6;
     r.scale = c6;
@@ -129,7 +143,7 @@ __device__ __forceinline__ HalfResult encode_half(const f2 (&x)[4], uint32_t ama
   } else {
     const uint32_t c4 = scale_encode<FMT>(__fmul_rn(amax, ss.rden4));
     const float d4 = s_d[c4], inv4 = s_inv[c4];
-    const uint32_t q4 = round8<SR>(x, inv4, rb);
+    const uint32_t q4 = round8s<SR>(x, inv4, rb, sg);
     f2 v6[4], v4[4];
     e2m1x8_to_f2(q6, v6);
     e2m1x8_to_f2(q4, v4);
@@ -192,7 +206,9 @@ __device__ __forceinline__ BlockResult encode_block_f(const f2 (&lo)[4], const f
   const uint32_t c6 = scale_encode<FMT>(__fmul_rn(amax, ss.rden6));
   float d6, inv6;
   scales(c6, d6, inv6);
-  const uint32_t a6 = round8<SR>(lo, inv6, rb0), b6 = round8<SR>(hi, inv6, rb1);
+  const uint32_t sgl = (SR && FOS) ? e2m1_signs(lo) : 0u, sgh = (SR && FOS) ? e2m1_signs(hi) : 0u;
+  const uint32_t a6 = FOS ? round8s<SR>(lo, inv6, rb0, sgl) : round8<SR>(lo, inv6, rb0);
+  const uint32_t b6 = FOS ? round8s<SR>(hi, inv6, rb1, sgh) : round8<SR>(hi, inv6, rb1);
   float d = d6;
   if constexpr (!FOS) {
     r.codes[0] = a6;
@@ -203,7 +219,7 @@ __device__ __forceinline__ BlockResult encode_block_f(const f2 (&lo)[4], const f
     const uint32_t c4 = scale_encode<FMT>(__fmul_rn(amax, ss.rden4));
     float d4, inv4;
     scales(c4, d4, inv4);
-    const uint32_t a4 = round8<SR>(lo, inv4, rb0), b4 = round8<SR>(hi, inv4, rb1);
+    const uint32_t a4 = round8s<SR>(lo, inv4, rb0, sgl), b4 = round8s<SR>(hi, inv4, rb1, sgh);
     const float sse6 =
         combine_halves(half_metric(lo, a6, d6, rule), half_metric(hi, b6, d6, rule), rule);
     const float sse4 =
