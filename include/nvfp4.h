@@ -309,7 +309,7 @@ NVFP4_API nvfp4_status nvfp4_requant_transpose(const nvfp4_config* src, const nv
  * NVFP4_DEV_NONFINITE_INPUT; its bytes are then unspecified.
  * Errors: NULL cfg / x / a required output, blocks or rounding out of range,
  * negative sizes, cols % 32 (rows wanted) or rows % 32 (columns wanted), x
- * or a codes buffer not 16-byte aligned, status not 4-byte aligned. */
+ * or an output buffer not 16-byte aligned, status not 4-byte aligned. */
 NVFP4_API nvfp4_status nvfp4_mx_quantize(const nvfp4_config* cfg, const void* x, int64_t slices,
                                          int64_t rows, int64_t cols, const nvfp4_out* row,
                                          const nvfp4_out* col, int32_t* status, void* stream);

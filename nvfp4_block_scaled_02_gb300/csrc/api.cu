@@ -295,8 +295,9 @@ nvfp4_status nvfp4_mx_quantize(const nvfp4_config* cfg, const void* x, int64_t s
       (do_col && (!col || !col->codes || !col->scales)))
     return NVFP4_ERR_NULL;
   if ((do_row && row->dequant) || (do_col && col->dequant)) return NVFP4_ERR_ENUM;
-  if (!aligned(x, 16) || !aligned(status, 4) || (do_row && !aligned(row->codes, 16)) ||
-      (do_col && !aligned(col->codes, 16)))
+  if (!aligned(x, 16) || !aligned(status, 4) ||
+      (do_row && (!aligned(row->codes, 16) || !aligned(row->scales, 16))) ||
+      (do_col && (!aligned(col->codes, 16) || !aligned(col->scales, 16))))
     return NVFP4_ERR_ALIGN;
   nvfp4::MxParams p{};
   p.x = static_cast<const uint16_t*>(x);

@@ -186,6 +186,7 @@ def test_mx_quantize_argument_errors(L):
     assert mx(L, _cfg(blocks=1), x=FAKE + 2, row=ok) == 3
     assert mx(L, _cfg(blocks=1), row=_out(codes=FAKE + 8, choice=0, dq=0)) == 3
     assert mx(L, _cfg(blocks=2), col=_out(codes=FAKE + 4, choice=0, dq=0)) == 3
+    assert mx(L, _cfg(blocks=1), row=_out(scales=FAKE + 1, choice=0, dq=0)) == 3
     assert mx(L, _cfg(blocks=1), row=ok, status=FAKE + 2) == 3
     # a column-only call does not need cols % 32 (nor a row output)
     assert mx(L, _cfg(blocks=2), Cc=40, col=ok, x=FAKE + 2) == 3
