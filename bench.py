@@ -21,6 +21,7 @@ from __future__ import annotations
 
 import argparse
 import ctypes as C
+import inspect
 import json
 import os
 import statistics
@@ -756,6 +757,39 @@ WORKLOADS = {1: SmallNormal, 2: Activation, 3: ScaleLearning, 4: DriftingGradien
              11: TileWeight, 12: GradientMx}
 
 
+# constructor arguments fixed by subclasses whose __init__ takes none
+_CTOR_FIXED = {SmallNormal: dict(rows=1024, cols=1024, fos=0),
+               RequantActivationNvfp4: dict(target=1)}
+
+
+def _ctor_args(config, args):
+    """The sizes and options the workload of `config` is built with: its
+    constructors' defaults, subclass-fixed arguments and the command line's."""
+    cls = WORKLOADS[config]
+    kw = {}
+    for k in reversed(cls.__mro__):
+        init = k.__dict__.get("__init__")
+        if init is not None and k is not object:
+            for name, prm in inspect.signature(init).parameters.items():
+                if prm.default is not inspect.Parameter.empty:
+                    kw[name] = prm.default
+    kw.update(_CTOR_FIXED.get(cls, {}))
+    kw.update({5: dict(experts=args.experts), 4: dict(nsteps=args.sr_steps)}.get(config, {}))
+    return kw
+
+
+def describe_workload(config, args):
+    """The `workload` text of `config` without building it on a device (the
+    reference arm reports the same workload as ours)."""
+    cls = WORKLOADS[config]
+    kw = _ctor_args(config, args)
+    stub = cls.__new__(cls)
+    stub.rows, stub.cols = kw.get("rows"), kw.get("cols")
+    stub.fos, stub.target = kw.get("fos", 1), kw.get("target", 0)
+    stub.nsets, stub.period, stub.S = kw.get("nsteps"), kw.get("period"), kw.get("experts")
+    return stub.workload
+
+
 # --------------------------------------------------------------- clocks --
 
 class ClockSampler:
@@ -997,7 +1031,8 @@ def reference_arm(args, world, rank):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * secs / max(1, args.steps), 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": desc, "sample": sample_text},
+        "config": {"workload": describe_workload(args.config, args), "sample": sample_text,
+                   "oracle_workload": desc},
         "gelem_per_s": round(total_e / secs / 1e9, 6),
         "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": cores_used(),
                          "kind": "oracle", "sample": sample_text},

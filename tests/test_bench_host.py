@@ -1,0 +1,52 @@
+"""Host-side pieces of bench.py: the reference arm reports the same workload
+text as the CUDA arm (built from the workloads' own constructor arguments)."""
+import importlib.util
+import os
+import sys
+import types
+
+import pytest
+
+from conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def bench():
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    argv, sys.argv = sys.argv, ["bench.py"]
+    try:
+        spec.loader.exec_module(mod)
+    finally:
+        sys.argv = argv
+    return mod
+
+
+def test_every_workload_has_a_description(bench):
+    args = types.SimpleNamespace(experts=64, sr_steps=32)
+    for c in bench.WORKLOADS:
+        text = bench.describe_workload(c, args)
+        assert isinstance(text, str) and len(text) > 40, c
+
+
+def test_descriptions_follow_constructor_arguments(bench):
+    args = types.SimpleNamespace(experts=64, sr_steps=32)
+    assert bench.describe_workload(1, args).startswith("1024x1024")
+    assert "8192x4096" in bench.describe_workload(2, args)
+    assert "Four-Over-Six on" in bench.describe_workload(2, args)
+    assert "over 32 steps" in bench.describe_workload(4, args)
+    assert "64 x 2048x7168" in bench.describe_workload(5, args)
+    assert "MXFP8" in bench.describe_workload(7, args)
+    assert "to NVFP4" in bench.describe_workload(8, args)
+    small = types.SimpleNamespace(experts=4, sr_steps=8)
+    assert "4 x 2048x7168" in bench.describe_workload(5, small)
+    assert "over 8 steps" in bench.describe_workload(4, small)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("config", [1, 2, 8])
+def test_description_matches_the_built_workload(bench, config):
+    import torch
+    args = types.SimpleNamespace(experts=64, sr_steps=32)
+    wl = bench.WORKLOADS[config](torch.device("cuda"))
+    assert wl.workload == bench.describe_workload(config, args)
