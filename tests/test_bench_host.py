@@ -50,3 +50,35 @@ def test_description_matches_the_built_workload(bench, config):
     args = types.SimpleNamespace(experts=64, sr_steps=32)
     wl = bench.WORKLOADS[config](torch.device("cuda"))
     assert wl.workload == bench.describe_workload(config, args)
+
+
+def _free_port():
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank(rank, world, port, out):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        spec = importlib.util.spec_from_file_location("bench_rank", os.path.join(ROOT, "bench.py"))
+        mod = importlib.util.module_from_spec(spec)
+        sys.argv = ["bench.py"]
+        spec.loader.exec_module(mod)
+        mod.barrier(world)
+        out[rank] = mod.max_over_ranks(1.5 + rank, world)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_step_time_is_the_maximum_over_ranks():
+    """bench.py's timing reduction on two CPU ranks (gloo): every rank gets the
+    slowest rank's time."""
+    import torch.multiprocessing as mp
+    world = 2
+    out = mp.get_context("spawn").Manager().dict()
+    mp.spawn(_rank, args=(world, _free_port(), out), nprocs=world, join=True)
+    assert dict(out) == {0: 2.5, 1: 2.5}
