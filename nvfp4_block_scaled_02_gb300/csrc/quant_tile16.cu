@@ -5,23 +5,24 @@
 //
 // One CTA (256 threads) per 64 x 128 region of one slice (4 x 8 scale tiles):
 //  1. thread t loads chunks k * 256 + t (k = 0..3) of 8 bf16 (a warp reads
-//     two whole 256-byte rows per load) and stages them in a 16 KiB shared
-//     tile of 32-bit words (two columns each), word w of row r stored at
-//     w ^ (((r >> 4) & 3) << 3);
-//  2. lane (cp, q) = (lane >> 2, lane & 3) of warp w reads rows 16q .. 16q+15
-//     of column pair 8w + cp (conflict-free with the swizzle); the eight
-//     lanes of one q cover scale tile (q, w), whose amax three xor shuffles
-//     reduce; its scale is the 1x16 block scale of that amax (target 6),
-//     published in shared memory with d and 1/d;
-//  3. every thread encodes its 8-value chunks from registers with their
-//     tile's scale (RNE, or stochastic with the row layout's random bits),
+//     two whole 256-byte rows per load); chunk k of thread t lies in band k
+//     and tile column (t % 16) / 2, so within a warp the lanes l, l ^ 1,
+//     l ^ 16, l ^ 17 hold that tile column's chunks of the warp's two rows:
+//     two xor shuffles combine them and one shared-memory atomic max per
+//     tile and warp gives the tile amax;
+//  2. after one barrier every thread turns its tiles' amaxes into scales (the
+//     1x16 block scale of the amax, target 6), encodes its chunks from
+//     registers (RNE, or stochastic with the row layout's random bits),
 //     writes the row encoding and stages the code words in a shared code
 //     tile (chunk index XOR-swizzled by the row's band);
-//  4. the column encoding is the same codes transposed: lane (cp, q) gathers
-//     the code byte of its column pair from each of its 16 rows (byte
+//  3. the column encoding is the same codes transposed: lane (cp, q) =
+//     (lane >> 2, lane & 3) of warp w takes column pair 8w + cp in band q,
+//     gathers the code byte of its column pair from each of its 16 rows (byte
 //     permutes), splits the two columns' nibbles, and writes per column 8 code
 //     bytes, the scale byte and 32 B of dequant; the four lanes of a column's
 //     bands are adjacent, so each column's 64 rows leave contiguously.
+// (Staging the bf16 region in shared memory to take the tile amaxes in a
+// column-mapped pass cost a barrier and 16 KiB per CTA: 92.6 vs 77.4 us.)
 #include "encode.cuh"
 #include "launch.h"
 
@@ -33,11 +34,6 @@ constexpr int kThreads = 256;
 constexpr int TR = 64;                 // region rows (4 scale tiles)
 constexpr int TC = 128;                // region columns (8 scale tiles)
 constexpr int kChunksPerRow = TC / 8;  // 16
-constexpr int kWords = TC / 2;         // 32-bit words (column pairs) per row
-
-__device__ __forceinline__ int word_of(int r, int w) {
-  return r * kWords + (w ^ (((r >> 4) & 3) << 3));
-}
 __device__ __forceinline__ int code_of(int r, int ch) {
   return r * kChunksPerRow + (ch ^ (((r >> 4) & 3) << 2));
 }
@@ -50,83 +46,71 @@ __device__ __forceinline__ uint32_t nibbles4(uint32_t B, int j) {
   return (x | (x >> 8)) & 0xFFFFu;
 }
 
-// Six resident CTAs per SM (registers held to 40, no spills): the kernel
-// waits mostly on its loads, and 6 CTAs hide that latency better than the 4
-// that an unbounded register count allows (92 vs 105 us on a 14336 x 4096
-// weight).
+// Six resident CTAs per SM (registers held to 40): the stochastic and UE5M3
+// variants then spill 16 bytes, and still run faster than with 5 CTAs
+// (E4M3 with SR: 101.1 vs 103.6 us on a 14336 x 4096 weight).
 template <int FMT, bool SR>
 __global__ void __launch_bounds__(kThreads, 6) quant_tile16_kernel(const Tile16Params p,
                                                                 int64_t tiles_r, int64_t tiles_c) {
   pdl_begin();
-  __shared__ __align__(16) uint32_t tile[TR * kWords];
   __shared__ uint32_t s_codes[TR * kChunksPerRow];
-  __shared__ float s_d[4][8], s_inv[4][8];
-  __shared__ uint32_t s_code[4][8];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __shared__ uint32_t s_tmax[4][8];  // bf16 bits of each scale tile's amax
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t R = p.R, C = p.C;
   const int64_t bid = blockIdx.x;
   const int64_t tc = bid % tiles_c, tr = (bid / tiles_c) % tiles_r, s = bid / (tiles_c * tiles_r);
   const int64_t r0 = tr * TR, c0 = tc * TC;
-  const SliceScale ss = slice_scale(p.gamax[s], p.M);
-  if (ss.bad && threadIdx.x == 0 && tr == 0 && tc == 0) flag(p.status, NVFP4_DEV_BAD_AMAX_BIT);
 
-  // ---- 1: load and stage (R, C are multiples of 16: a chunk is in or out) --
+  // ---- 1: loads (thread t's chunk k lies in band k, tile column (t % 16) / 2)
   uint4 v[4];
   bool ok[4];
   int64_t e[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const int chunk = k * kThreads + threadIdx.x;
+    const int chunk = k * kThreads + tid;
     const int lr = chunk / kChunksPerRow, lc = (chunk % kChunksPerRow) * 8;
     const int64_t r = r0 + lr, c = c0 + lc;
     ok[k] = r < R && c < C;
     e[k] = (s * R + r) * C + c;  // flat row-layout index
     v[k] = ok[k] ? __ldcs(p.x + e[k] / 8) : make_uint4(0, 0, 0, 0);
-    if (absmax_bits4(v[k]) >= 0x7F80u) flag(p.status, NVFP4_DEV_NONFINITE_INPUT_BIT);
-    *reinterpret_cast<uint4*>(&tile[word_of(lr, (chunk % kChunksPerRow) * 4)]) = v[k];
   }
-  __syncthreads();
-
-  // ---- 2: tile amax and scale -----------------------------------------------
-  const int q = lane & 3, cpl = warp * 8 + (lane >> 2);  // band, column pair
-  {
-    uint32_t mm = 0;
+  if (tid < 32) (&s_tmax[0][0])[tid] = 0u;
+  const SliceScale ss = slice_scale(p.gamax[s], p.M);
+  if (ss.bad && tid == 0 && tr == 0 && tc == 0) flag(p.status, NVFP4_DEV_BAD_AMAX_BIT);
+  __syncthreads();  // s_tmax zeroed
+  const int tcol = (tid % kChunksPerRow) >> 1;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) mm = __vmaxu2(mm, tile[word_of(16 * q + i, cpl)] & 0x7FFF7FFFu);
-    uint32_t m = max(mm & 0xFFFFu, mm >> 16);
-    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
-    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 8));
+  for (int k = 0; k < 4; ++k) {
+    uint32_t m = absmax_bits4(v[k]);
+    if (m >= 0x7F80u) flag(p.status, NVFP4_DEV_NONFINITE_INPUT_BIT);
+    // lanes l, l ^ 1, l ^ 16, l ^ 17 hold this tile column's chunks of the warp's two rows
+    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
     m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
-    if ((lane >> 2) == 0) {
-      const uint32_t code = scale_encode<FMT>(__fmul_rn(__uint_as_float(m << 16), ss.rden6));
-      float d, inv;
-      scale_entry<FMT>(code, ss.g, d, inv);
-      s_code[q][warp] = code;
-      s_d[q][warp] = d;
-      s_inv[q][warp] = inv;
-    }
+    if ((lane & 17) == 0) atomicMax(&s_tmax[k][tcol], m);
   }
-  __syncthreads();
+  __syncthreads();  // tile amaxes complete
 
-  // ---- 3: row encoding --------------------------------------------------------
+  // ---- 2: row encoding with the tile's scale (computed by every thread) ----------
   const bool want_dq = p.r_dq != nullptr, want_cols = p.c_codes != nullptr;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const int chunk = k * kThreads + threadIdx.x;
+    const int chunk = k * kThreads + tid;
     const int lr = chunk / kChunksPerRow, c16 = chunk % kChunksPerRow;
-    const int tb = lr >> 4, tcol = c16 >> 1;
+    const uint32_t code = scale_encode<FMT>(__fmul_rn(__uint_as_float(s_tmax[k][tcol] << 16), ss.rden6));
+    float d, inv;
+    scale_entry<FMT>(code, ss.g, d, inv);
     uint4 rb = make_uint4(0, 0, 0, 0);
     if constexpr (SR) rb = sr_group_bits(p.seed, p.step, 0u, (uint64_t)e[k]);
     f2 x[4];
     unpack8(v[k], x);
-    const uint32_t w = round8<SR>(x, s_inv[tb][tcol], rb);
+    const uint32_t w = round8<SR>(x, inv, rb);
     if (ok[k]) {
       p.r_codes[e[k] / 8] = w;
-      if ((c16 & 1) == 0) p.r_scales[e[k] / 16] = (uint8_t)s_code[tb][tcol];
+      if ((c16 & 1) == 0) p.r_scales[e[k] / 16] = (uint8_t)code;
       if (want_dq) {
         f2 qv[4];
         e2m1x8_to_f2(w, qv);
-        __stcs(p.r_dq + e[k] / 8, dequant8(qv, s_d[tb][tcol]));
+        __stcs(p.r_dq + e[k] / 8, dequant8(qv, d));
       }
     }
     if (want_cols) s_codes[code_of(lr, c16)] = w;
@@ -134,11 +118,12 @@ __global__ void __launch_bounds__(kThreads, 6) quant_tile16_kernel(const Tile16P
   if (!want_cols) return;  // block-uniform
   __syncthreads();
 
-  // ---- 4: column encoding = the codes transposed -------------------------------
+  // ---- 3: column encoding = the codes transposed ---------------------------------
+  const int q = lane & 3, cpl = warp * 8 + (lane >> 2);  // band, column pair
   const int64_t cc = c0 + 2 * cpl, rr = r0 + 16 * q;
   const int ch = cpl >> 2, bsel = cpl & 3;
-  const uint32_t sel = (uint32_t)bsel | ((uint32_t)(bsel + 4) << 4);  // that byte of two words
-  uint32_t B[4];  // code bytes of the column pair for rows 4g .. 4g+3 of the band
+  const uint32_t sel = (uint32_t)bsel | ((uint32_t)(bsel + 4) << 4);
+  uint32_t B[4];
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
     const uint32_t w0 = s_codes[code_of(16 * q + 4 * g, ch)];
@@ -147,14 +132,15 @@ __global__ void __launch_bounds__(kThreads, 6) quant_tile16_kernel(const Tile16P
     const uint32_t w3 = s_codes[code_of(16 * q + 4 * g + 3, ch)];
     B[g] = __byte_perm(__byte_perm(w0, w1, sel), __byte_perm(w2, w3, sel), 0x5410u);
   }
-  const float d = s_d[q][warp];
-  const uint32_t code = s_code[q][warp];
+  const uint32_t code = scale_encode<FMT>(__fmul_rn(__uint_as_float(s_tmax[q][warp] << 16), ss.rden6));
+  float d, inv;
+  scale_entry<FMT>(code, ss.g, d, inv);
   const bool col_dq = p.c_dq != nullptr;
 #pragma unroll
-  for (int j = 0; j < 2; ++j) {  // column cc + j
+  for (int j = 0; j < 2; ++j) {
     const uint32_t cw0 = nibbles4(B[0], j) | (nibbles4(B[1], j) << 16);
     const uint32_t cw1 = nibbles4(B[2], j) | (nibbles4(B[3], j) << 16);
-    const int64_t ce = (s * C + cc + j) * R + rr;  // flat column-layout index
+    const int64_t ce = (s * C + cc + j) * R + rr;
     if (rr < R && cc + j < C) {
       *reinterpret_cast<uint2*>(p.c_codes + ce / 8) = make_uint2(cw0, cw1);
       p.c_scales[ce / 16] = (uint8_t)code;
