@@ -119,3 +119,30 @@ def test_tile16_row_encoding_alone(shape):
     assert_exact(host_u8(row["codes"]), ref["row_codes"], "row codes")
     assert_exact(host_u8(row["scales"]), ref["row_scales"], "row scales")
     assert_exact(host_u16(row["dequant"]), ref["row_dq"], "row dequant")
+
+
+def test_tile16_nonfinite_input_flags_and_other_tiles_exact():
+    """A NaN and an Inf in two tiles set the non-finite status bit; every other
+    tile of both encodings matches the oracle."""
+    xb = synth.student_t(64, 96, seed=8).reshape(1, 64, 96).copy()
+    xb[0, 3, 5] = 0x7FC0    # NaN in tile (0, 0)
+    xb[0, 40, 70] = 0xFF80  # -Inf in tile (2, 4)
+    gamax = np.array([4.0], np.float32)
+    out, ref, st = run_both(xb, gamax)
+    assert st & nv.DEV_NONFINITE_INPUT
+    bad = {(0, 0), (2, 4)}
+    rc = host_u8(out["row"]["codes"]).reshape(64, 48)
+    rs = host_u8(out["row"]["scales"]).reshape(64, 6)
+    cc = host_u8(out["col"]["codes"]).reshape(96, 32)
+    cs = host_u8(out["col"]["scales"]).reshape(96, 4)
+    wrc, wrs = ref["row_codes"].reshape(64, 48), ref["row_scales"].reshape(64, 6)
+    wcc, wcs = ref["col_codes"].reshape(96, 32), ref["col_scales"].reshape(96, 4)
+    for tr in range(4):
+        for tc in range(6):
+            if (tr, tc) in bad:
+                continue
+            rows, cols = slice(16 * tr, 16 * tr + 16), slice(16 * tc, 16 * tc + 16)
+            assert_exact(rc[rows, 8 * tc:8 * tc + 8], wrc[rows, 8 * tc:8 * tc + 8], f"row codes {tr},{tc}")
+            assert_exact(rs[rows, tc], wrs[rows, tc], f"row scales {tr},{tc}")
+            assert_exact(cc[cols, 8 * tr:8 * tr + 8], wcc[cols, 8 * tr:8 * tr + 8], f"col codes {tr},{tc}")
+            assert_exact(cs[cols, tr], wcs[cols, tr], f"col scales {tr},{tc}")
