@@ -40,14 +40,6 @@ __device__ __forceinline__ f2 f2_mul(f2 a, f2 b) { return __fmul2_rn(a, b); }
 __device__ __forceinline__ f2 f2_fma(f2 a, f2 b, f2 c) { return __ffma2_rn(a, b, c); }
 
 // ----------------------------------------------------------------- E2M1 ---
-// Two fp32 -> two E2M1 codes in one byte, round to nearest even, saturating
-// to +-6 (cvt ... satfinite). `even` goes to the low nibble.
-__device__ __forceinline__ uint32_t e2m1x2_rn(float even, float odd) {
-  uint32_t r;
-  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
-      : "=r"(r) : "f"(odd), "f"(even));
-  return r;
-}
 // Eight fp32 values (4 pairs) -> 8 codes in one word, element 0 in bits 0..3:
 // four conversions into byte registers packed by one vector move.
 __device__ __forceinline__ uint32_t e2m1x8_rn(const f2 (&y)[4]) {
@@ -62,14 +54,6 @@ __device__ __forceinline__ uint32_t e2m1x8_rn(const f2 (&y)[4]) {
       : "f"(y[0].x), "f"(y[0].y), "f"(y[1].x), "f"(y[1].y), "f"(y[2].x), "f"(y[2].y),
         "f"(y[3].x), "f"(y[3].y));
   return w;
-}
-// Value of one E2M1 code (low 4 bits of c) as fp32.
-__device__ __forceinline__ float e2m1_value(uint32_t c) {
-  // magnitude codes 2..7 are the fp32 patterns 0x3F000000 + (m << 22);
-  // code 1 is 0.5 and code 0 is 0.
-  uint32_t m = c & 7u;
-  uint32_t bits = m >= 2 ? 0x3F000000u + (m << 22) : (m == 1 ? 0x3F000000u : 0u);
-  return __uint_as_float(bits | ((c & 8u) << 28));
 }
 // Decode the 8 codes of a word into 4 pairs (element 2k in .x of pair k):
 // one vector move splits the bytes, the hardware E2M1x2 -> f16x2 conversion
