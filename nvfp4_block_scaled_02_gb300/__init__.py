@@ -152,6 +152,35 @@ def _bf16(t: torch.Tensor, name: str) -> int:
     return _dev(t, name)
 
 
+_KINDS = {"bf16": (torch.bfloat16, torch.int16, torch.uint16), "f32": (torch.float32,),
+          "u8": (torch.uint8, torch.int8), "i32": (torch.int32, torch.uint32)}
+
+
+def _need(t: torch.Tensor | None, name: str, n: int, kind: str) -> None:
+    """Refuse a buffer the kernels would read or write past: wrong element
+    type, or fewer than n elements (the ABI takes raw pointers and cannot
+    check sizes itself)."""
+    if t is None:
+        return
+    if t.dtype not in _KINDS[kind]:
+        raise TypeError(f"{name} must hold {kind} data, got {t.dtype}")
+    if t.numel() < n:
+        raise ValueError(f"{name} holds {t.numel()} elements; the call needs {n}")
+
+
+def _need_enc(enc: dict | None, name: str, s: int, r: int, c: int, four_over_six: bool) -> None:
+    """An NVFP4 encoding of s x r x c values (blocks of 16 along c)."""
+    if enc is None:
+        return
+    _need(enc["codes"], name + " codes", s * r * c // 2, "u8")
+    _need(enc["scales"], name + " scales", s * r * c // 16, "u8")
+    if four_over_six:
+        if enc.get("choice") is None:
+            raise ValueError(f"{name} needs a choice bitmap under Four-Over-Six")
+        _need(enc["choice"], name + " choice", s * ((r * c // 16 + 31) // 32), "i32")
+    _need(enc.get("dequant"), name + " dequant", s * r * c, "bf16")
+
+
 def _stream(device: torch.device) -> int:
     return torch.cuda.current_stream(device).cuda_stream
 
@@ -175,6 +204,8 @@ def nvfp4_amax(x: torch.Tensor, amax: torch.Tensor | None = None,
                status: torch.Tensor | None = None) -> torch.Tensor:
     """Per-slice max |x| of a bf16 [rows, cols] or [slices, rows, cols] tensor."""
     S, R, Cc = _shape3(x)
+    _need(amax, "amax", S, "f32")
+    _need(status, "status", 1, "i32")
     if amax is None:
         amax = torch.empty(S, dtype=torch.float32, device=x.device)
     _check("nvfp4_amax", lib().nvfp4_amax(_bf16(x, "x"), S, R, Cc, _dev(amax, "amax"),
@@ -213,7 +244,11 @@ def nvfp4_quantize(x: torch.Tensor, global_amax: torch.Tensor, cfg: Config | Non
     cfg = cfg or Config()
     S, R, Cc = _shape3(x)
     fos = bool(cfg.four_over_six)
+    _need(global_amax, "global_amax", S, "f32")
+    _need(status, "status", 1, "i32")
     if cfg.blocks == BLOCKS_TILE16:
+        _need_enc(row, "row", S, R, Cc, False)
+        _need_enc(col, "col", S, Cc, R, False)
         # one scale per 16x16 tile: the row encoding and its transpose
         row = row if row is not None else alloc_encoding(S, R, Cc, x.device, False, dequant)
         col = col if col is not None else alloc_encoding(S, Cc, R, x.device, False, dequant)
@@ -222,6 +257,8 @@ def nvfp4_quantize(x: torch.Tensor, global_amax: torch.Tensor, cfg: Config | Non
             C.byref(c), _bf16(x, "x"), S, R, Cc, _dev(global_amax, "global_amax"), C.byref(ro),
             C.byref(co), _dev(status, "status"), _stream(x.device)))
         return {"row": row, "col": col}
+    _need_enc(row if cfg.blocks & 1 else None, "row", S, R, Cc, fos)
+    _need_enc(col if cfg.blocks & 2 else None, "col", S, Cc, R, fos)
     if cfg.blocks & 1 and row is None:
         row = alloc_encoding(S, R, Cc, x.device, fos, dequant)
     if cfg.blocks & 2 and col is None:
@@ -245,6 +282,9 @@ def nvfp4_quantize_per_token(x: torch.Tensor, cfg: Config | None = None, out: di
     if x.dim() != 2:
         raise ValueError("x must be [rows, cols]")
     R, Cc = x.shape
+    _need_enc(out, "out", R, 1, Cc, bool(cfg.four_over_six))
+    _need(row_amax, "row_amax", R, "f32")
+    _need(status, "status", 1, "i32")
     if out is None:
         out = alloc_encoding(R, 1, Cc, x.device, bool(cfg.four_over_six), dequant)
     if row_amax is None:
@@ -292,6 +332,16 @@ def nvfp4_requant_transpose(codes: torch.Tensor, scales: torch.Tensor,
     Cc = 2 * half
     if scales.numel() != S * R * (Cc // 16):
         raise ValueError("scales must hold one byte per 16 values")
+    _need(global_amax, "global_amax", S, "f32")
+    _need(status, "status", 1, "i32")
+    if out is not None:
+        per = 1 if target == TARGET_MXFP8 else 2  # values per code byte
+        _need(out["codes"], "out codes", S * R * Cc // per, "u8")
+        _need(out["scales"], "out scales", S * R * Cc // (32 if target == TARGET_MXFP8 else 16), "u8")
+        if target == TARGET_NVFP4 and dst.four_over_six:
+            if out.get("choice") is None:
+                raise ValueError("out needs a choice bitmap under Four-Over-Six")
+            _need(out["choice"], "out choice", S * ((R * Cc // 16 + 31) // 32), "i32")
     if out is None:
         out = alloc_requant(S, R, Cc, codes.device, target,
                             bool(dst.four_over_six) and target == TARGET_NVFP4)
@@ -320,6 +370,11 @@ def nvfp4_mx_quantize(x: torch.Tensor, cfg: Config | None = None, row: dict | No
     passed in)."""
     cfg = cfg or Config(blocks=BLOCKS_BOTH, rounding=ROUND_SR)
     S, R, Cc = _shape3(x)
+    for enc, name, on in ((row, "row", cfg.blocks & 1), (col, "col", cfg.blocks & 2)):
+        if on and enc is not None:
+            _need(enc["codes"], name + " codes", S * R * Cc, "u8")
+            _need(enc["scales"], name + " scales", S * R * Cc // 32, "u8")
+    _need(status, "status", 1, "i32")
     if cfg.blocks & 1 and row is None:
         row = alloc_mx(S, R, Cc, x.device)
     if cfg.blocks & 2 and col is None:
@@ -339,6 +394,11 @@ def nvfp4_fakequant_fwd(x: torch.Tensor, s_pre: torch.Tensor, s_post: torch.Tens
                         out: torch.Tensor | None = None,
                         status: torch.Tensor | None = None) -> torch.Tensor:
     R, Cc = x.shape
+    nb = R * Cc // 16
+    _need(s_pre, "s_pre", nb, "f32")
+    _need(s_post, "s_post", nb, "f32")
+    _need(status, "status", 1, "i32")
+    _need(out, "out", R * Cc, "bf16")
     out = torch.empty_like(x) if out is None else out
     _check("nvfp4_fakequant_fwd", lib().nvfp4_fakequant_fwd(
         _bf16(x, "x"), R, Cc, _dev(s_pre, "s_pre"), _dev(s_post, "s_post"), _bf16(out, "out"),
@@ -352,6 +412,14 @@ def nvfp4_scale_grad_bwd(x: torch.Tensor, gq: torch.Tensor, s_pre: torch.Tensor,
                          gs_post: torch.Tensor | None = None,
                          status: torch.Tensor | None = None) -> dict:
     R, Cc = x.shape
+    nb = R * Cc // 16
+    _need(s_pre, "s_pre", nb, "f32")
+    _need(s_post, "s_post", nb, "f32")
+    _need(status, "status", 1, "i32")
+    _need(gq, "gq", R * Cc, "bf16")
+    _need(gx, "gx", R * Cc, "bf16")
+    _need(gs_pre, "gs_pre", nb, "f32")
+    _need(gs_post, "gs_post", nb, "f32")
     if want_gx and gx is None:
         gx = torch.empty_like(x)
     gs_pre = torch.empty_like(s_pre) if gs_pre is None else gs_pre
@@ -372,6 +440,12 @@ def nvfp4_fakequant_fwd_fp8scale(x: torch.Tensor, s_pre: torch.Tensor,
                                  status: torch.Tensor | None = None) -> torch.Tensor:
     """Fake quantisation at FP8-rounded block scales (global_amax: fp32 [1])."""
     R, Cc = x.shape
+    nb = R * Cc // 16
+    _need(s_pre, "s_pre", nb, "f32")
+    _need(s_post, "s_post", nb, "f32")
+    _need(status, "status", 1, "i32")
+    _need(global_amax, "global_amax", 1, "f32")
+    _need(out, "out", R * Cc, "bf16")
     out = torch.empty_like(x) if out is None else out
     _check("nvfp4_fakequant_fwd_fp8scale", lib().nvfp4_fakequant_fwd_fp8scale(
         _bf16(x, "x"), R, Cc, _dev(s_pre, "s_pre"), _dev(s_post, "s_post"),
@@ -386,6 +460,12 @@ def nvfp4_scale_grad_bwd_fp8scale(x: torch.Tensor, gq: torch.Tensor, s_pre: torc
                                   status: torch.Tensor | None = None) -> dict:
     """STE backward at FP8-rounded block scales, gradients passed straight through."""
     R, Cc = x.shape
+    nb = R * Cc // 16
+    _need(s_pre, "s_pre", nb, "f32")
+    _need(s_post, "s_post", nb, "f32")
+    _need(status, "status", 1, "i32")
+    _need(gq, "gq", R * Cc, "bf16")
+    _need(global_amax, "global_amax", 1, "f32")
     gx = torch.empty_like(x) if want_gx else None
     gs_pre = torch.empty_like(s_pre)
     gs_post = torch.empty_like(s_post) if s_post is not None else None
@@ -400,6 +480,8 @@ def nvfp4_scale_init_mse(x: torch.Tensor, global_amax: torch.Tensor,
                          status: torch.Tensor | None = None) -> dict:
     """MSE scale setting over every E4M3 scale per 1x16 block: {"codes", "s"}."""
     R, Cc = x.shape
+    _need(global_amax, "global_amax", 1, "f32")
+    _need(status, "status", 1, "i32")
     codes = torch.empty((R, Cc // 16), dtype=torch.uint8, device=x.device)
     s = torch.empty((R, Cc // 16), dtype=torch.float32, device=x.device)
     _check("nvfp4_scale_init_mse", lib().nvfp4_scale_init_mse(
@@ -413,6 +495,14 @@ def nvfp4_export_scales(x: torch.Tensor, s_pre: torch.Tensor, s_post: torch.Tens
                         status: torch.Tensor | None = None) -> dict:
     """NVFP4 row encoding carrying learned post-scales: {"codes", "scales"}."""
     R, Cc = x.shape
+    nb = R * Cc // 16
+    _need(s_pre, "s_pre", nb, "f32")
+    _need(s_post, "s_post", nb, "f32")
+    _need(status, "status", 1, "i32")
+    _need(global_amax, "global_amax", 1, "f32")
+    if out is not None:
+        _need(out["codes"], "out codes", R * Cc // 2, "u8")
+        _need(out["scales"], "out scales", nb, "u8")
     if out is None:
         out = alloc_encoding(1, R, Cc, x.device, False, dequant=False)
     o = _Out(_dev(out["codes"], "codes"), _dev(out["scales"], "scales"), None, None)
@@ -425,6 +515,9 @@ def nvfp4_export_scales(x: torch.Tensor, s_pre: torch.Tensor, s_post: torch.Tens
 
 def nvfp4_codec_probe(op: int, inp: torch.Tensor, aux: torch.Tensor | None = None,
                       out: torch.Tensor | None = None) -> torch.Tensor:
+    _need(inp, "in", inp.numel(), "f32")
+    _need(aux, "aux", inp.numel(), "i32")
+    _need(out, "out", inp.numel(), "u8")
     out = torch.empty(inp.numel(), dtype=torch.uint8, device=inp.device) if out is None else out
     _check("nvfp4_codec_probe", lib().nvfp4_codec_probe(
         op, _dev(inp, "in"), _dev(aux, "aux"), inp.numel(), _dev(out, "out"),
@@ -434,6 +527,7 @@ def nvfp4_codec_probe(op: int, inp: torch.Tensor, aux: torch.Tensor | None = Non
 
 def nvfp4_sr_bits(seed: int, step: int, direction: int, idx0: int, n: int,
                   device="cuda", out: torch.Tensor | None = None) -> torch.Tensor:
+    _need(out, "out", n, "i32")
     out = torch.empty(n, dtype=torch.int32, device=device) if out is None else out
     _check("nvfp4_sr_bits", lib().nvfp4_sr_bits(seed & 0xFFFFFFFF, step & 0xFFFFFFFF, direction,
                                                 idx0, n, _dev(out, "out"),
