@@ -116,3 +116,66 @@ def test_moe_64x2048x7168_dual_four_over_six_sampled_experts():
                          f"{side} 4/6 choices, expert {e}")
             assert_close_bf16(host_u16(o["dequant"][e]), ref[side + "_dq"],
                               f"{side} dequant, expert {e}")
+
+
+def _bits(words, start, n):
+    """Bits start .. start + n - 1 of a little-endian 4/6 choice bitmap."""
+    b = np.unpackbits(np.ascontiguousarray(words).view(np.uint8), bitorder="little")
+    return b[start:start + n]
+
+
+def test_more_than_two_to_the_31_elements():
+    """524304 x 4096 values (2^31 + 65536): 64-bit index arithmetic in amax and
+    the dual encoding (rows and columns, 4/6), checked on the rows past index
+    2^31 and on sampled columns (each the row encoding of a 524304-value
+    column). The input is generated on the device in seeded chunks."""
+    R, Cc = (1 << 19) + 16, 4096
+    x = torch.empty((R, Cc), dtype=torch.bfloat16, device="cuda")
+    gen = torch.Generator(device="cuda").manual_seed(31)
+    step = 1 << 16
+    for a in range(0, R, step):
+        b = min(R, a + step)
+        x[a:b] = torch.randn((b - a, Cc), generator=gen, device="cuda").to(torch.bfloat16)
+    x[R - 3, 7] = 9.5  # the tensor's amax sits past index 2^31
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    amax = nv.nvfp4_amax(x, status=st)
+    assert float(amax.item()) == float(x.abs().max().item()) == 9.5
+    out = nv.nvfp4_quantize(x, amax, nv.Config(blocks=3, four_over_six=1), status=st,
+                            dequant=False)
+    assert int(st.item()) == 0
+    gam = amax.cpu().numpy()
+    ref = oracle.quantize(host_u16(x[R - 16:]), gam, four_over_six=1, dequant=False)
+    row = out["row"]
+    assert_exact(host_u8(row["codes"][0, R - 16:]), ref["row_codes"], "row codes")
+    assert_exact(host_u8(row["scales"][0, R - 16:]), ref["row_scales"], "row scales")
+    nb = 16 * Cc // 16  # 4/6 bits of the last 16 rows
+    assert_exact(_bits(row["choice"][0].cpu().numpy(), (R - 16) * Cc // 16, nb),
+                 _bits(ref["row_choice"], 0, nb), "row 4/6 choices")
+    col = out["col"]
+    cwords = col["choice"][0].cpu().numpy()
+    for c in (0, 1777, Cc - 1):
+        ref = oracle.quantize(host_u16(x[:, c].contiguous()).reshape(1, 1, R), gam,
+                              four_over_six=1, dequant=False)
+        assert_exact(host_u8(col["codes"][0, c]), ref["row_codes"], f"column {c} codes")
+        assert_exact(host_u8(col["scales"][0, c]), ref["row_scales"], f"column {c} scales")
+        assert_exact(_bits(cwords, c * (R // 16), R // 16), _bits(ref["row_choice"], 0, R // 16),
+                     f"column {c} 4/6 choices")
+    del out, row, col
+    # row-only stochastic rounding: the random bits are keyed on flat indices past 2^31
+    cfg = nv.Config(rounding=1, scale_max=448.0, seed=5, step=2)
+    sr = nv.nvfp4_quantize(x, amax, cfg, status=st, dequant=False)["row"]
+    assert int(st.item()) == 0
+    g = oracle.decode_scale(float(amax.item()), 448.0)
+    nblk = R * Cc // 16
+    blocks = np.concatenate([[0, nblk - 1], (1 << 27) + np.arange(4),
+                             np.random.default_rng(8).choice(nblk, 400, replace=False)])
+    codes = sr["codes"].view(-1, 8)
+    scales = sr["scales"].view(-1)
+    xf = x.view(-1, 16)
+    for b in blocks:
+        b = int(b)
+        r = oracle.encode_block(xf[b].float().cpu().numpy(), g, rounding=1, seed=5, step=2,
+                                direction=0, idx0=b * 16)
+        want = (r["codes"][0::2] | (r["codes"][1::2] << 4)).astype(np.uint8)
+        assert_exact(host_u8(codes[b]), want, f"codes of block {b}")
+        assert int(scales[b].item()) == r["scale"], f"scale of block {b}"
