@@ -313,3 +313,30 @@ def test_nonfinite_input_and_bad_amax_are_flagged(orc):
     y = orc.f32_to_bf16(np.ones((1, 32), np.float32))
     assert orc.quantize(y, np.array([np.nan], np.float32))["status"] & orc.ST_BAD_AMAX
     assert orc.quantize(y, np.array([1.0], np.float32))["status"] == 0
+
+
+def test_bad_amax_values_are_flagged(orc):
+    """A slice amax that is NaN, infinite or negative is reported; zero and
+    tiny positive ones are not (a zero slice takes g = 1)."""
+    y = orc.f32_to_bf16(np.ones((1, 32), np.float32))
+    for bad in (np.nan, np.inf, -np.inf, -1.0, -1e-30):
+        assert orc.quantize(y, np.array([bad], np.float32))["status"] & orc.ST_BAD_AMAX, bad
+    for ok in (0.0, 1e-44, 1e-30, 1.0, 3.0e38):
+        assert orc.quantize(y, np.array([ok], np.float32))["status"] == 0, ok
+    assert orc.decode_scale(0.0, 448.0) == 1.0
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+@pytest.mark.parametrize("fos", [0, 1])
+def test_zero_blocks_encode_to_zero_for_every_slice_amax(orc, fmt, fos):
+    """A block of zeros has amax 0, so its scale target is 0: scale code 0,
+    zero codes and a zero dequant, whatever the slice amax, also where 1/(k g)
+    overflows fp32 (a tiny slice amax)."""
+    x = np.zeros((2, 32), np.float32)
+    x[0, 0] = 3.0
+    xb = orc.f32_to_bf16(x)
+    for gamax in (1e-45, 1e-40, 1e-30, 3.0, 3.0e38):
+        q = orc.quantize(xb, np.array([gamax], np.float32), scale_fmt=fmt, four_over_six=fos)
+        assert np.all(q["row_scales"][0].reshape(-1)[1:] == 0), gamax
+        assert np.all(q["row_codes"][0].reshape(-1)[8:] == 0), gamax
+        assert np.all(q["row_dq"][0].reshape(-1)[16:] == 0), gamax

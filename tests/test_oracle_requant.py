@@ -154,3 +154,20 @@ def test_mx_block_maximum_lands_in_the_top_octave_without_clipping(orc):
     codes, scales = orc.mx_encode(v, rounding=0)
     vals = np.abs(orc.e4m3_signed_value(codes)).reshape(-1, 32).max(axis=1)
     assert np.all((vals >= 224) & (vals <= 448))
+
+
+def test_e4m3_sr_counts_are_exact_at_dyadic_probabilities(orc):
+    """Over all 2^16 random values a value a quarter, a half or three quarters
+    of the way between two E4M3 neighbours rounds up for exactly p * 2^16 of
+    them (u = v / 2^16 < p), in the subnormal range, across binades and at the
+    top of the grid."""
+    table = _e4m3_table()
+    v = np.arange(65536, dtype=np.uint32)
+    for i in (1, 8, 40, 100, 125):
+        lo, hi = table[i], table[i + 1]
+        for k in (1, 2, 3):
+            y = np.float32(lo + (hi - lo) * k / 4)
+            assert float(y) == lo + (hi - lo) * k / 4
+            got = orc.e4m3_signed_value(orc.e4m3_sr(np.full(65536, y, np.float32), v))
+            assert int(np.sum(got == hi)) == k * 16384
+            assert int(np.sum(got == lo)) == 65536 - k * 16384

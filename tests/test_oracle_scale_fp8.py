@@ -172,3 +172,16 @@ def test_export_dequantises_to_the_fake_quant_forward(orc, tied):
     t = ((sp if tied else so) * np.float32(np.float32(1.0) / _g(gam[0]))).astype(np.float32)
     want = torch.from_numpy(t).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
     assert np.array_equal(ex["scales"], want)
+
+
+def test_export_flags_a_pre_scale_that_rounds_to_the_zero_code(orc):
+    """A pre-scale that is a normal fp32 number but rounds to the FP8 zero
+    code gives no usable forward scale: the export reports it like the
+    fake-quant forward does."""
+    wb, _, s = synth.scale_learning(4, 32, seed=18)
+    gam, _ = orc.global_amax(wb)
+    assert orc.export_scales(wb, s, None, gam[0])["status"] == 0
+    sp = s.copy()
+    sp[2, 1] = 1e-30
+    assert orc.export_scales(wb, sp, None, gam[0])["status"] & orc.ST_BAD_SCALE
+    assert orc.fakequant_fwd_fp8(wb, sp, None, gam[0])[1] & orc.ST_BAD_SCALE

@@ -130,3 +130,28 @@ def test_bad_scales_are_flagged(orc):
         assert orc.fakequant_fwd(x, s)[1] & orc.ST_BAD_SCALE
         assert orc.scale_grad_bwd(x, g, s, so)["status"] & orc.ST_BAD_SCALE
     assert orc.scale_grad_bwd(x, g, sp, so)["status"] == 0
+
+
+def test_clamp_bounds_belong_to_the_middle_case(orc):
+    """Scale Learning blog, "How Scale Learning Works": the STE's middle case
+    holds for q_min <= x/s <= q_max, bounds included. At x/s = +-6 the tied
+    term round(x/s) - x/s is 0 and the dual s_pre term is -s_post x / s_pre^2;
+    beyond the bound the term is q_max (tied) or 0 (s_pre), and dL/dx is
+    masked by the same interval. The expected values are the case formulas
+    evaluated by hand."""
+    s = np.float32(0.25)
+    x = np.zeros((1, 16), np.float32)
+    x[0, :3] = [6 * s, -6 * s, 7 * s]  # on both bounds, and beyond the upper one
+    g = np.zeros((1, 16), np.float32)
+    g[0, :3] = [1.0, 2.0, 4.0]
+    xb, gb = orc.f32_to_bf16(x), orc.f32_to_bf16(g)
+    tied = orc.scale_grad_bwd(xb, gb, np.array([[s]], np.float32), None)
+    assert tied["status"] == 0
+    assert tied["gs_pre"][0, 0] == 4.0 * 6.0  # bounds contribute 0, the clamped value q_max
+    assert list(_f(tied["gx"][0, :3])) == [1.0, 2.0, 0.0]
+    so = np.array([[0.5]], np.float32)  # s_post / s_pre = 2
+    dual = orc.scale_grad_bwd(xb, gb, np.array([[s]], np.float32), so)
+    # dL/ds_pre = -(s_post/s_pre) * sum g * x/s_pre over the middle case
+    assert dual["gs_pre"][0, 0] == -2.0 * (1.0 * 6.0 + 2.0 * -6.0)
+    assert dual["gs_post"][0, 0] == 1.0 * 6.0 + 2.0 * -6.0 + 4.0 * 6.0
+    assert list(_f(dual["gx"][0, :3])) == [2.0, 4.0, 0.0]
