@@ -247,3 +247,20 @@ def test_more_slices_than_one_grid_dimension_holds():
     assert_exact(host_u8(out["scales"]), ref["row_scales"], "scales")
     assert_exact(out["choice"].cpu().numpy().view(np.uint32), ref["row_choice"], "4/6 choices")
     assert_exact(host_u16(out["dequant"]), ref["row_dq"], "dequant")
+
+
+@pytest.mark.parametrize("gam", [1e-45, 1e-40, 1e-30])
+def test_zero_blocks_under_a_tiny_slice_amax(gam):
+    """A tiny slice amax makes 1/(k g) overflow fp32 (clamped to FLT_MAX):
+    zero blocks still encode to scale 0, the others as the oracle does, in
+    every encoding."""
+    xb = np.zeros((2, 32, 64), np.uint16)
+    rng = np.random.default_rng(int(-np.log10(gam)))
+    xb[:, ::5, ::7] = synth.to_bf16_bits(rng.standard_normal(xb[:, ::5, ::7].shape) * 1e-38)
+    g = np.full(2, gam, np.float32)
+    for blocks in (1, 3):
+        for fmt in (0, 1):
+            for fos in (0, 1):
+                out, ref, st = run_both(xb, g, blocks=blocks, fmt=fmt, fos=fos, rounding=fos,
+                                        seed=4)
+                assert st == 0

@@ -83,3 +83,29 @@ def test_nonfinite_gradient_flagged():
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     nv.nvfp4_scale_grad_bwd(dev_bits(wb), dev_bits(gb), torch.from_numpy(sp).cuda(), status=st)
     assert int(st.item()) & nv.DEV_NONFINITE_INPUT
+
+
+def test_clamp_bounds_match_the_oracle():
+    """Values exactly on the clamp bounds (x/s = +-6, s a power of two, so the
+    quotient is exact) belong to the middle case of the STE; neighbours just
+    inside and beyond them too."""
+    rng = np.random.default_rng(21)
+    R, Cc = 16, 256
+    s = np.ldexp(1.0, rng.integers(-8, 2, (R, Cc // 16))).astype(np.float32)
+    k = rng.choice(np.array([6.0, -6.0, 5.5, -5.5, 7.0, -7.0, 6.5, 0.25]), (R, Cc))
+    x = (k * np.repeat(s, 16, axis=1)).astype(np.float32)
+    wb = synth.to_bf16_bits(x)
+    assert np.array_equal(synth.bf16_bits_to_f32(wb), x)
+    gb = synth.to_bf16_bits(rng.standard_normal((R, Cc)).astype(np.float32))
+    so = (s * np.float32(1.25)).astype(np.float32)
+    for post in (None, so):
+        got = nv.nvfp4_scale_grad_bwd(dev_bits(wb), dev_bits(gb), torch.from_numpy(s).cuda(),
+                                      None if post is None else torch.from_numpy(post).cuda())
+        want = oracle.scale_grad_bwd(wb, gb, s, post)
+        assert_close_f32(got["gs_pre"].cpu().numpy(), want["gs_pre"], "dL/ds_pre")
+        if post is not None:
+            assert_close_f32(got["gs_post"].cpu().numpy(), want["gs_post"], "dL/ds_post")
+        assert_close_bf16(host_u16(got["gx"]), want["gx"], "dL/dx")
+        fq = nv.nvfp4_fakequant_fwd(dev_bits(wb), torch.from_numpy(s).cuda(),
+                                    None if post is None else torch.from_numpy(post).cuda())
+        assert_close_bf16(host_u16(fq), oracle.fakequant_fwd(wb, s, post)[0], "x~")

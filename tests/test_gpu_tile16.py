@@ -146,3 +146,14 @@ def test_tile16_nonfinite_input_flags_and_other_tiles_exact():
             assert_exact(rs[rows, tc], wrs[rows, tc], f"row scales {tr},{tc}")
             assert_exact(cc[cols, 8 * tr:8 * tr + 8], wcc[cols, 8 * tr:8 * tr + 8], f"col codes {tr},{tc}")
             assert_exact(cs[cols, tr], wcs[cols, tr], f"col scales {tr},{tc}")
+
+
+@pytest.mark.parametrize("gam", [1e-45, 1e-40])
+def test_tile16_zero_tiles_under_a_tiny_slice_amax(gam):
+    xb = np.zeros((1, 64, 128), np.uint16)
+    xb[0, 3, 5] = synth.to_bf16_bits(np.array([2e-39], np.float32))[0]
+    for fmt in (0, 1):
+        out, ref, st = run_both(xb, np.array([gam], np.float32), fmt=fmt)
+        _check(out, ref, st)
+        sc = host_u8(out["row"]["scales"]).reshape(64, 8)  # the 16 row blocks of a tile share its scale
+        assert np.all(sc[:16, 0] == sc[0, 0]) and sc[16:].max() == 0 and sc[:, 1:].max() == 0
