@@ -1,25 +1,27 @@
 // api.cu -- the C ABI declared in include/nvfp4.h: argument validation (all
 // synchronous, before anything is enqueued), output-buffer preparation on the
 // caller's stream, and dispatch to the kernels.
+#include <atomic>
 #include <cstdint>
-#include <mutex>
 
 #include "launch.h"
 #include "mx_quant.h"
 
 namespace nvfp4 {
 
+// SM count of the current device, looked up once per device (calls may come
+// from several host threads: every thread stores the same value).
 int sm_count() {
-  static int cached[64] = {0};
+  static std::atomic<int> cached[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (cached[dev] == 0) {
-    int n = 0;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
       n = 148;
-    cached[dev] = n;
+    cached[dev].store(n, std::memory_order_relaxed);
   }
-  return cached[dev];
+  return n;
 }
 
 }  // namespace nvfp4
