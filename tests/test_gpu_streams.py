@@ -3,8 +3,11 @@ is handed and makes no host-synchronous or allocating CUDA call, so a whole
 step (amax, dual 4/6 encoding, 16x16 tiles, per-token encoding,
 re-quantisation, MXFP8, the scale-learning forward and backward) can be
 captured in a CUDA graph and replayed on new data, and independent steps on
-two streams can overlap. Each case compares its outputs, byte for byte, with
-the same calls run eagerly on the default stream."""
+two streams, or from two host threads, can overlap. Each case compares its
+outputs, byte for byte, with the same calls run eagerly on the default
+stream."""
+import threading
+
 import numpy as np
 import pytest
 import torch
@@ -138,3 +141,35 @@ def test_independent_steps_on_two_streams():
         _same(outs[i], ref)
     assert not np.array_equal(outs[0]["row"]["codes"].cpu().numpy(),
                               outs[1]["row"]["codes"].cpu().numpy())
+
+
+def test_steps_from_two_host_threads():
+    """The binding's foreign calls release the GIL, so two host threads enter
+    the C ABI at the same time, each with its own stream."""
+    dev = torch.device("cuda")
+    ins = [_inputs(51, dev), _inputs(52, dev)]
+    outs = [_alloc(dev), _alloc(dev)]
+    torch.cuda.synchronize()
+    errors = []
+
+    def work(i):
+        try:
+            s = torch.cuda.Stream(device=dev)
+            with torch.cuda.stream(s):
+                for _ in range(4):
+                    _step(*ins[i], outs[i], seed=60 + i)
+            s.synchronize()
+        except Exception as e:  # reported on the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in (0, 1)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for i in (0, 1):
+        ref = _alloc(dev)
+        _step(*ins[i], ref, seed=60 + i)
+        torch.cuda.synchronize()
+        _same(outs[i], ref)
