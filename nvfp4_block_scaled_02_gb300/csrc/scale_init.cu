@@ -3,13 +3,27 @@
 // initialises the learnable scales).
 //
 // Per 1x16 block every positive finite E4M3 scale s_c = dec(c) * g
-// (c = 1..126, g = gamax / (6 * 448)) is tried: the block is fake-quantised at
-// s_c (q = clamp(round(x * (1/s_c))), E2M1 RNE) and its error
-// e = fma(-q, s_c, x) summed in the fixed block order (per half of 8, even
-// and odd positions accumulated separately with fma from +0). The smallest sum
-// wins, ties keep the smaller code. One lane per block holds its 16 values in
-// registers for the whole sweep; d and 1/d of every code come from a per-CTA
-// shared table.
+// (c = 1..126, g = gamax / (6 * 448)) is a candidate: the block is
+// fake-quantised at s_c (q = clamp(round(x * (1/s_c))), E2M1 RNE) and its
+// error e = fma(-q, s_c, x) summed in the fixed block order (per half of 8,
+// even and odd positions accumulated separately with fma from +0). The
+// smallest sum wins, ties keep the smaller code. One lane per block holds its
+// 16 values in registers; d and 1/d of every code come from a per-CTA table.
+//
+// Only the candidates that can win are evaluated, and the result is that of
+// the full sweep. With A the block's largest |x| (finite blocks):
+//  * below: for s_c < A / 6 every q has |q s_c| <= 6 s_c, so the largest
+//    value's error is at least m = A - 6 s_c > 0; its fp32 square is a term
+//    of the computed sum, and the sum of non-negative terms rounded to
+//    nearest never drops below any of them, so the computed sum is at least
+//    RN(m)^2 (1 - 2^-24). A code whose RN(m)^2 (1 - 2^-18) already exceeds the
+//    computed sum B of the amax-derived code (the E4M3 code of A / (6 g))
+//    cannot win; m falls as c grows, so these codes are a prefix 1..c_first-1;
+//  * above: from the first code with s_c >= 4.00002 A on, every x * (1/s_c)
+//    rounds to at most 1/4 and encodes to 0, so every such code has the same
+//    sum (that of the values themselves): only the first of them can win.
+// The codes c_first .. c_last are then swept in increasing order. Blocks with
+// a NaN or Inf are swept whole.
 #include "encode.cuh"
 #include "launch.h"
 
@@ -19,38 +33,71 @@ namespace {
 
 constexpr int kThreads = 256;
 
+// The block's error sum at scale d (1/d = inv), in the fixed order.
+__device__ __forceinline__ float candidate_sse(const f2 (&lo)[4], const f2 (&hi)[4], float2 di) {
+  const uint4 none = make_uint4(0, 0, 0, 0);
+  f2 q[4];
+  return __fadd_rn(half_sse(lo, round8<false>(lo, di.y, none), di.x, q),
+                   half_sse(hi, round8<false>(hi, di.y, none), di.x, q));
+}
+
+// First c in [lo, hi] where pred(c) is false, pred being true on a prefix of
+// [lo, hi]; hi + 1 when it holds everywhere. lo >= 1.
+template <class Pred>
+__device__ __forceinline__ uint32_t first_false(uint32_t lo, uint32_t hi, Pred pred) {
+  while (lo <= hi) {
+    const uint32_t mid = (lo + hi) >> 1;
+    if (pred(mid)) lo = mid + 1;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
 __global__ void __launch_bounds__(kThreads) scale_init_mse_kernel(const ScaleInitParams p) {
   pdl_begin();
-  __shared__ float s_d[128], s_inv[128];
+  __shared__ float2 s_tab[128];  // (d, 1/d) of code c
   const SliceScale ss = slice_scale(*p.gamax, 448.0f);
-  if (threadIdx.x < 128) scale_entry<0>((uint32_t)threadIdx.x, ss.g, s_d[threadIdx.x],
-                                        s_inv[threadIdx.x]);
+  if (threadIdx.x < 128) {
+    float d, inv;
+    scale_entry<0>((uint32_t)threadIdx.x, ss.g, d, inv);
+    s_tab[threadIdx.x] = make_float2(d, inv);
+  }
   if (ss.bad && blockIdx.x == 0 && threadIdx.x == 0) flag(p.status, NVFP4_DEV_BAD_AMAX_BIT);
   __syncthreads();
   const int64_t stride = (int64_t)gridDim.x * kThreads;
   for (int64_t b = (int64_t)blockIdx.x * kThreads + threadIdx.x; b < p.nblocks; b += stride) {
     const uint4 v0 = __ldcs(p.x + 2 * b), v1 = __ldcs(p.x + 2 * b + 1);
-    if (max(absmax_bits4(v0), absmax_bits4(v1)) >= 0x7F80u)
-      flag(p.status, NVFP4_DEV_NONFINITE_INPUT_BIT);
+    const uint32_t abits = max(absmax_bits4(v0), absmax_bits4(v1));
     f2 lo[4], hi[4];
     unpack8(v0, lo);
     unpack8(v1, hi);
-    uint32_t best = 1;
+    uint32_t c_first = 1, c_last = 126;
+    if (abits >= 0x7F80u) {
+      flag(p.status, NVFP4_DEV_NONFINITE_INPUT_BIT);
+    } else {
+      const float A = __uint_as_float(abits << 16);
+      const uint32_t c0 = min(max(e4m3_encode(__fmul_rn(A, ss.rden6)), 1u), 126u);
+      const float B = candidate_sse(lo, hi, s_tab[c0]);
+      const float T = __fmul_rn(A, 4.00002f);
+      c_last = min(first_false(1u, 126u, [&](uint32_t c) { return s_tab[c].x < T; }), 126u);
+      c_first = min(first_false(1u, c0, [&](uint32_t c) {
+        const float m = __fmaf_rn(-6.0f, s_tab[c].x, A);
+        return m > 0.0f && __fmul_rn(__fmul_rn(m, m), 0.999996185302734375f) > B;  // 1 - 2^-18
+      }), c0);
+      c_last = max(c_last, c_first);
+    }
+    uint32_t best = c_first;
     float best_sse = 0.0f;
 #pragma unroll 2
-    for (uint32_t c = 1; c <= 126; ++c) {
-      const float d = s_d[c], inv = s_inv[c];
-      const uint4 none = make_uint4(0, 0, 0, 0);
-      f2 q[4];
-      const float sse = __fadd_rn(half_sse(lo, round8<false>(lo, inv, none), d, q),
-                                  half_sse(hi, round8<false>(hi, inv, none), d, q));
-      if (c == 1 || sse < best_sse) {
+    for (uint32_t c = c_first; c <= c_last; ++c) {
+      const float sse = candidate_sse(lo, hi, s_tab[c]);
+      if (c == c_first || sse < best_sse) {
         best = c;
         best_sse = sse;
       }
     }
     if (p.codes) p.codes[b] = (uint8_t)best;
-    if (p.s) p.s[b] = s_d[best];
+    if (p.s) p.s[b] = s_tab[best].x;
   }
 }
 

@@ -58,6 +58,59 @@ def test_mse_scale_sweep_outliers_zeros_and_tiny_amax():
         assert_exact(got["s"].cpu().numpy().view(np.uint32), want["s"].view(np.uint32), "scales")
 
 
+def _sweep_stress_blocks(rng, n):
+    """n blocks of 16 of many kinds: Gaussian over 12 decades, one large
+    outlier (the best scale may saturate it), a single spike, constant,
+    sparse, two-level, bf16 subnormal, and values near the top of bf16."""
+    kinds = []
+    for k in range(n):
+        t = k % 9
+        if t == 0:
+            b = rng.standard_normal(16) * np.exp(rng.uniform(-14, 14))
+        elif t == 1:
+            b = rng.standard_normal(16) * 0.1
+            b[rng.integers(16)] = rng.uniform(2, 60) * rng.choice([-1, 1])
+        elif t == 2:
+            b = np.zeros(16)
+            b[rng.integers(16)] = np.exp(rng.uniform(-20, 20))
+        elif t == 3:
+            b = np.full(16, np.exp(rng.uniform(-10, 10)))
+        elif t == 4:
+            b = rng.standard_normal(16) * (rng.uniform(size=16) < 0.2)
+        elif t == 5:
+            b = np.where(rng.uniform(size=16) < 0.5, 1.0, rng.uniform(0.001, 0.3, 16))
+            b *= np.exp(rng.uniform(-5, 5)) * rng.choice([-1, 1], 16)
+        elif t == 6:
+            b = rng.standard_normal(16) * 1e-39
+        elif t == 7:
+            b = rng.uniform(-1, 1, 16) * 3.0e38
+        else:
+            b = rng.standard_normal(16) * np.exp(rng.uniform(-3, 3, 16))
+        kinds.append(b)
+    return np.concatenate(kinds).astype(np.float32).reshape(-1, 256)
+
+
+def test_mse_scale_sweep_stress_against_the_full_oracle_sweep():
+    """The kernel evaluates only the candidates that can win; the oracle
+    evaluates all 126. Codes and scales must agree on every kind of block,
+    under slice amaxes from far below to far above the blocks' own."""
+    rng = np.random.default_rng(77)
+    wb = oracle.f32_to_bf16(_sweep_stress_blocks(rng, 9 * 400))
+    # 1e-6 .. 1e12 give 25 to 126 distinct winning codes; the tensor's own
+    # amax (set by the blocks near the top of bf16), 1e-30 and 3e38 make every
+    # candidate of most blocks tie (code 1 wins)
+    own = oracle.global_amax(wb)[0]
+    for g in (1e-6, 1e-3, 1.0, 1e3, 1e6, 1e12, own[0], 1e-30, 3.0e38):
+        gam = np.array([g], np.float32)
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        got = nv.nvfp4_scale_init_mse(dev_bits(wb), _d(gam), status=st)
+        want = oracle.scale_init_mse(wb, gam[0])
+        assert int(st.item()) == want["status"]
+        assert_exact(host_u8(got["codes"]), want["codes"], f"codes (gamax {gam[0]})")
+        assert_exact(got["s"].cpu().numpy().view(np.uint32), want["s"].view(np.uint32),
+                     f"scales (gamax {gam[0]})")
+
+
 @pytest.mark.parametrize("shape", SHAPES)
 @pytest.mark.parametrize("dual", [False, True])
 def test_fp8_scale_fakequant_forward(shape, dual):
