@@ -82,3 +82,22 @@ def test_step_time_is_the_maximum_over_ranks():
     out = mp.get_context("spawn").Manager().dict()
     mp.spawn(_rank, args=(world, _free_port(), out), nprocs=world, join=True)
     assert dict(out) == {0: 2.5, 1: 2.5}
+
+
+def test_sweep_candidate_count_edges(bench):
+    """The MSE sweep's work count: an all-zero block is the probe plus code 1
+    (2 encodings); every count lies between 2 and 127 (the probe plus all 126
+    codes); in a constant block the codes well below amax / 6 are pruned."""
+    import numpy as np
+    z = np.zeros((1, 16), np.uint16)
+    assert bench.sweep_candidates_per_block(z, 1.0) == 2.0
+    rng = np.random.default_rng(5)
+    x = (rng.standard_normal((64, 256)) * np.exp(rng.uniform(-8, 8, (64, 1)))).astype(np.float32)
+    bits = (x.view(np.uint32) >> 16).astype(np.uint16)
+    for gam in (1e-3, 1.0, 1e3):
+        n = bench.sweep_candidates_per_block(bits, gam)
+        assert 2.0 <= n <= 127.0
+    # A = 0.75 with g = 0.75: the codes with 6 s_c well short of A go
+    v = np.full((1, 16), 0.75, np.float32)
+    assert bench.sweep_candidates_per_block((v.view(np.uint32) >> 16).astype(np.uint16),
+                                            2688.0 * 0.75) < 60
