@@ -226,6 +226,8 @@ NVFP4_API nvfp4_status nvfp4_scale_grad_bwd_fp8scale(const void* x, const void* 
  * clamp(round(x * (1/s_c))), 1/s_c clamped to FLT_MAX) and the error
  * e = fma(-q, s_c, x) summed in the fixed block order of
  * nvfp4_scale_grad_bwd; the smallest sum wins, ties keep the smaller code.
+ * (The kernel skips the codes that provably cannot win; the result is that
+ * of trying every code.)
  * Outputs (either may be NULL, not both): scale_codes u8 [rows][cols/16], the
  * winning code; s fp32 [rows][cols/16], its scale dec(code) * g (an initial
  * s_pre = s_post for scale learning). Errors: NULL x / global_amax / both
