@@ -104,6 +104,17 @@ MUTANTS = [
     ("scale_ok_pre", "if (!(s_pre >= FLT_MIN) || !(s_pre <= FLT_MAX)) return 0;", "if (!(s_pre > 0.0f)) return 0;"),
     ("quant_nonfinite", "if ((x[i] & 0x7FFFu) >= 0x7F80u) st |= ORC_ST_NONFINITE_INPUT;\n    xf[i] = orc_bf16_to_f32(x[i]);", "xf[i] = orc_bf16_to_f32(x[i]);", 0),
     ("dq_bf16", "dq[i] = orc_f32_to_bf16(dqf[i]);", "dq[i] = (uint16_t)(f2u(dqf[i]) >> 16);"),
+    ("mae_abs", "acc[p] = acc[p] + fabsf(e[8 * h + p + 2 * j]);", "acc[p] = acc[p] + e[8 * h + p + 2 * j];"),
+    ("maxerr_first", "if (fabsf(e[i]) > m) m = fabsf(e[i]);", "if (fabsf(e[i]) > m) m = e[i];"),
+    ("amax_slice", "uint16_t a = x[s * n + i] & 0x7FFFu;", "uint16_t a = x[i] & 0x7FFFu;"),
+    ("amax_sign", "uint16_t a = x[s * n + i] & 0x7FFFu;", "uint16_t a = x[s * n + i] & 0xFFFFu;"),
+    ("tied_scale", "float sp = s_pre[b], so = s_post ? s_post[b] : s_pre[b];", "float sp = s_pre[b], so = s_post ? s_post[b] : 1.0f;"),
+    ("rq_choice", "out_scales, out_choice, NULL);", "out_scales, NULL, NULL);"),
+    ("export_nibble", "codes[e / 2] = (uint8_t)((q0 & 15) | ((q1 & 15) << 4));", "codes[e / 2] = (uint8_t)((q1 & 15) | ((q0 & 15) << 4));"),
+    ("tile_M", "float M = scale_max > 0.0f ? scale_max : 448.0f;", "float M = scale_max > 0.0f ? scale_max : 256.0f;"),
+    ("tile_dq", "r_dq[e0 + i] = orc_f32_to_bf16(cd.qv[i] * cd.d);", "r_dq[e0 + i] = orc_f32_to_bf16(cd.qv[i]);"),
+    ("mx_scale_idx", "r_scales + e0 / 32);", "r_scales + e0 / 16);"),
+    ("dq_M_fos", "float M = scale_max > 0.0f ? scale_max : (fos ? 256.0f : 448.0f);", "float M = scale_max > 0.0f ? scale_max : 448.0f;", 1),
 ]
 
 EXPECTED_SURVIVORS = {"block_sum_order"}

@@ -340,3 +340,16 @@ def test_zero_blocks_encode_to_zero_for_every_slice_amax(orc, fmt, fos):
         assert np.all(q["row_scales"][0].reshape(-1)[1:] == 0), gamax
         assert np.all(q["row_codes"][0].reshape(-1)[8:] == 0), gamax
         assert np.all(q["row_dq"][0].reshape(-1)[16:] == 0), gamax
+
+
+def test_global_amax_is_the_per_slice_max_abs(orc):
+    """The per-slice global amax equals numpy's max |x| over each slice (the
+    slices scaled apart so a mixed-up slice index shows)."""
+    rng = np.random.default_rng(9)
+    x = (rng.standard_normal((3, 20, 48)) * np.array([1e-3, 1.0, 1e3])[:, None, None])
+    xb = orc.f32_to_bf16(x.astype(np.float32))
+    got, st = orc.global_amax(xb, 3)
+    want = np.abs(orc.bf16_to_f32(xb)).reshape(3, -1).max(axis=1)
+    assert st == 0 and np.array_equal(got, want)
+    one, _ = orc.global_amax(xb)  # one slice over everything
+    assert one[0] == want.max()
