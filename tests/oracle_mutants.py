@@ -115,6 +115,13 @@ MUTANTS = [
     ("tile_dq", "r_dq[e0 + i] = orc_f32_to_bf16(cd.qv[i] * cd.d);", "r_dq[e0 + i] = orc_f32_to_bf16(cd.qv[i]);"),
     ("mx_scale_idx", "r_scales + e0 / 32);", "r_scales + e0 / 16);"),
     ("dq_M_fos", "float M = scale_max > 0.0f ? scale_max : (fos ? 256.0f : 448.0f);", "float M = scale_max > 0.0f ? scale_max : 448.0f;", 1),
+    ("fq_nonfinite", "      if ((x[e] & 0x7FFFu) >= 0x7F80u) st |= ORC_ST_NONFINITE_INPUT;\n      float r = orc_bf16_to_f32(x[e]) * inv;", "      float r = orc_bf16_to_f32(x[e]) * inv;"),
+    ("sg_nonfinite_g", "if ((x[e] & 0x7FFFu) >= 0x7F80u || (gq[e] & 0x7FFFu) >= 0x7F80u)", "if ((x[e] & 0x7FFFu) >= 0x7F80u)"),
+    ("dq_nonfinite", "if (!isfinite(out[e])) st |= ORC_ST_NONFINITE_INPUT;", ""),
+    ("mse_nonfinite", "      if ((h & 0x7FFFu) >= 0x7F80u) st |= ORC_ST_NONFINITE_INPUT;\n      xb[i] = orc_bf16_to_f32(h);", "      xb[i] = orc_bf16_to_f32(h);"),
+    ("export_nonfinite", "if ((x[e] & 0x7FFFu) >= 0x7F80u || (x[e + 1] & 0x7FFFu) >= 0x7F80u)", "if ((x[e] & 0x7FFFu) >= 0x7F80u)"),
+    ("tile_nonfinite", "            if ((h & 0x7FFFu) >= 0x7F80u) st |= ORC_ST_NONFINITE_INPUT;\n            float a = fabsf", "            float a = fabsf"),
+    ("mx_nonfinite", "if ((x[i] & 0x7FFFu) >= 0x7F80u) st |= ORC_ST_NONFINITE_INPUT;\n    xf[i] = orc_bf16_to_f32(x[i]);\n  }\n  if (blocks & 1)\n    for", "xf[i] = orc_bf16_to_f32(x[i]);\n  }\n  if (blocks & 1)\n    for"),
 ]
 
 EXPECTED_SURVIVORS = {"block_sum_order"}
