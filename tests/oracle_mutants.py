@@ -122,6 +122,11 @@ MUTANTS = [
     ("export_nonfinite", "if ((x[e] & 0x7FFFu) >= 0x7F80u || (x[e + 1] & 0x7FFFu) >= 0x7F80u)", "if ((x[e] & 0x7FFFu) >= 0x7F80u)"),
     ("tile_nonfinite", "            if ((h & 0x7FFFu) >= 0x7F80u) st |= ORC_ST_NONFINITE_INPUT;\n            float a = fabsf", "            float a = fabsf"),
     ("mx_nonfinite", "if ((x[i] & 0x7FFFu) >= 0x7F80u) st |= ORC_ST_NONFINITE_INPUT;\n    xf[i] = orc_bf16_to_f32(x[i]);\n  }\n  if (blocks & 1)\n    for", "xf[i] = orc_bf16_to_f32(x[i]);\n  }\n  if (blocks & 1)\n    for"),
+    ("rq_src_fmt", "int st = orc_dequant(src_fmt, src_scale_max, src_fos,", "int st = orc_dequant(0, src_scale_max, src_fos,"),
+    ("rq_src_M", "int st = orc_dequant(src_fmt, src_scale_max, src_fos,", "int st = orc_dequant(src_fmt, 0.0f, src_fos,"),
+    ("quant_scale_max", "float M = scale_max > 0.0f ? scale_max : (fos ? 256.0f : 448.0f);", "float M = fos ? 256.0f : 448.0f;", 0),
+    ("fp8_post_sign", "!(so >= 0.0f && so <= FLT_MAX)", "!(so <= FLT_MAX)"),
+    ("tile_col_nibble", "if (t & 1) c_codes[t / 2] = (uint8_t)((c_codes[t / 2] & 0x0F) | (q << 4));", "if (!(t & 1)) c_codes[t / 2] = (uint8_t)((c_codes[t / 2] & 0x0F) | (q << 4));"),
 ]
 
 EXPECTED_SURVIVORS = {"block_sum_order"}

@@ -353,3 +353,19 @@ def test_global_amax_is_the_per_slice_max_abs(orc):
     assert st == 0 and np.array_equal(got, want)
     one, _ = orc.global_amax(xb)  # one slice over everything
     assert one[0] == want.max()
+
+
+def test_explicit_fp8_maximum_sets_the_outer_scale(orc):
+    """g = gamax / (6 M) with the caller's M: for a block holding the slice
+    amax 1800 and M = 300, g = 1 and the block scale target is 300, which
+    E4M3 rounds to 288 (288 and 320 are neighbours), so 1800 / 288 = 6.25
+    saturates to 6 and de-quantises to 1728; with the default M = 448 the
+    target is 448 and 1800 comes back exactly."""
+    xb = orc.f32_to_bf16(np.array([[1800.0] + [0.0] * 15], np.float32))
+    gam = np.array([1800.0], np.float32)
+    q = orc.quantize(xb, gam, scale_max=300.0)
+    assert orc.scale_value(0, q["row_scales"].reshape(-1)[0]) == 288.0
+    assert orc.bf16_to_f32(q["row_dq"].reshape(-1)[:1])[0] == 1728.0
+    q = orc.quantize(xb, gam)
+    assert orc.scale_value(0, q["row_scales"].reshape(-1)[0]) == 448.0
+    assert orc.bf16_to_f32(q["row_dq"].reshape(-1)[:1])[0] == 1800.0

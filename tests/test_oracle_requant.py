@@ -171,3 +171,23 @@ def test_e4m3_sr_counts_are_exact_at_dyadic_probabilities(orc):
             got = orc.e4m3_signed_value(orc.e4m3_sr(np.full(65536, y, np.float32), v))
             assert int(np.sum(got == hi)) == k * 16384
             assert int(np.sum(got == lo)) == 65536 - k * 16384
+
+
+@pytest.mark.parametrize("fmt,scale_max", [(1, 0.0), (0, 300.0), (1, 1000.0)])
+def test_requant_reads_the_source_encoding_it_is_told(orc, fmt, scale_max):
+    """A UE5M3 or explicit-M forward encoding is de-quantised with that format
+    and M (its bf16 rounding is the forward's own dequant output), and the
+    re-quantisation starts from exactly those values."""
+    rng = np.random.default_rng(11)
+    xb = orc.f32_to_bf16((rng.standard_t(3, (1, 32, 64)) * 0.3).astype(np.float32))
+    gam, _ = orc.global_amax(xb)
+    q = orc.quantize(xb, gam, scale_fmt=fmt, scale_max=scale_max)
+    xh, st = orc.dequant(q["row_codes"], q["row_scales"], gam, scale_fmt=fmt,
+                         scale_max=scale_max)
+    assert st == 0 and np.array_equal(orc.f32_to_bf16(xh), q["row_dq"])
+    r = orc.requant(q["row_codes"], q["row_scales"], gam, target=0, rounding=0,
+                    src_fmt=fmt, src_scale_max=scale_max)
+    xt = np.ascontiguousarray(xh[0].T)
+    for c in range(64):
+        codes, scales = orc.mx_encode(xt[c], rounding=0)
+        assert np.array_equal(r["codes"][0, c], codes) and np.array_equal(r["scales"][0, c], scales)
