@@ -69,11 +69,30 @@ def _e2m1_rne_values(y: np.ndarray) -> np.ndarray:
     return np.copysign(q, y)
 
 
+def _sweep_sse(x: np.ndarray, d: np.ndarray, inv: np.ndarray) -> np.ndarray:
+    """Each block's error sum at its own scale d (1/d = inv), in the fixed
+    block order (float32 steps, the fma products taken exactly in float64)."""
+    f32 = np.float32
+    y = (x * inv[:, None].astype(np.float32)).astype(np.float32)
+    q = _e2m1_rne_values(y)
+    e = (x.astype(np.float64) - q.astype(np.float64) * d[:, None]).astype(np.float32)
+    sq = e.astype(np.float64) ** 2
+    out = np.zeros(len(x), f32)
+    for h in (0, 8):
+        acc = [np.zeros(len(x), f32), np.zeros(len(x), f32)]
+        for i in range(8):
+            acc[i % 2] = (sq[:, h + i] + acc[i % 2]).astype(f32)
+        out = (out + (acc[0] + acc[1]).astype(f32)).astype(f32)
+    return out
+
+
 def sweep_candidates_per_block(w_bits: np.ndarray, gamax: float) -> float:
-    """Mean number of candidate scales the MSE sweep kernel evaluates per 1x16
-    block of this input: the amax-derived code, then c_first .. c_last, with
-    the kernel's bounds replicated in float32 (the fma steps through exact
-    float64 products). A work count for the roofline, not a result."""
+    """Mean number of candidate scales the MSE sweep kernel encodes per 1x16
+    block of this input: the amax-derived code c0, the codes below it down to
+    the first one the bound rules out against the best sum so far, and the
+    codes above it up to the first all-zero code, with the kernel's steps
+    replicated in float32 (the fma steps through exact float64 products). A
+    work count for the roofline, not a result."""
     f32 = np.float32
     x = (np.asarray(w_bits, np.uint16).astype(np.uint32) << 16).view(np.float32).reshape(-1, 16)
     A = np.abs(x).max(axis=1)
@@ -83,32 +102,28 @@ def sweep_candidates_per_block(w_bits: np.ndarray, gamax: float) -> float:
     with np.errstate(divide="ignore", over="ignore"):
         inv = np.where(d > 0, np.minimum(f32(1.0) / np.where(d > 0, d, 1), np.finfo(f32).max), 0)
         rden6 = min(f32(1.0) / f32(f32(6.0) * g), np.finfo(f32).max)
+    inv = inv.astype(np.float32)
     t = np.minimum((A * f32(rden6)).astype(np.float32), f32(448.0))
     c0 = torch.from_numpy(t).to(torch.float8_e4m3fn).view(torch.uint8).numpy().astype(np.int64)
     c0 = np.clip(c0, 1, 126)
-    y = (x * inv[c0][:, None].astype(np.float32)).astype(np.float32)
-    q = _e2m1_rne_values(y)
-    e = (x.astype(np.float64) - q.astype(np.float64) * d[c0][:, None]).astype(np.float32)
-    sq = e.astype(np.float64) ** 2
-    B = np.zeros(len(x), np.float32)
-    for h in (0, 8):
-        acc = [np.zeros(len(x), np.float32), np.zeros(len(x), np.float32)]
-        for i in range(8):
-            acc[i % 2] = (sq[:, h + i] + acc[i % 2]).astype(np.float32)
-        B = (B + (acc[0] + acc[1]).astype(np.float32)).astype(np.float32)
+    best = _sweep_sse(x, d[c0], inv[c0])
     T = (A * f32(4.00002)).astype(np.float32)
-    c_last = np.minimum(np.searchsorted(d[1:127], T, side="left") + 1, 126)
-    lo, hi = np.ones(len(x), np.int64), c0.copy()
-    while np.any(lo <= hi):  # first code in [1, c0] the lower bound does not prune
-        act = lo <= hi
-        mid = (lo + hi) // 2
-        m = (A.astype(np.float64) - 6.0 * d[mid]).astype(np.float32)
+    c_last = np.maximum(np.minimum(np.searchsorted(d[1:127], T, side="left") + 1, 126), c0)
+    down = np.zeros(len(x), np.int64)
+    c = c0 - 1
+    active = c >= 1
+    while np.any(active):  # walk down until the bound rules the code out
+        cc = np.where(active, c, 1)
+        m = (A.astype(np.float64) - 6.0 * d[cc]).astype(np.float32)
         lb = ((m * m).astype(np.float32) * f32(0.999996185302734375)).astype(np.float32)
-        prune = (m > 0) & (lb > B)
-        lo = np.where(act & prune, mid + 1, lo)
-        hi = np.where(act & ~prune, mid - 1, hi)
-    c_first = np.minimum(lo, c0)
-    return float(np.mean(np.maximum(c_last, c_first) - c_first + 2))
+        active &= ~((m > 0) & (lb > best))
+        sse = _sweep_sse(x, d[cc], inv[cc])
+        best = np.where(active & (sse <= best), sse, best)
+        down += active
+        c = c - 1
+        active &= c >= 1
+    return float(np.mean(1 + down + (c_last - c0)))
+
 
 # ------------------------------------------------------------ workloads --
 

@@ -16,14 +16,17 @@
 //    value's error is at least m = A - 6 s_c > 0; its fp32 square is a term
 //    of the computed sum, and the sum of non-negative terms rounded to
 //    nearest never drops below any of them, so the computed sum is at least
-//    RN(m)^2 (1 - 2^-24). A code whose RN(m)^2 (1 - 2^-18) already exceeds the
-//    computed sum B of the amax-derived code (the E4M3 code of A / (6 g))
-//    cannot win; m falls as c grows, so these codes are a prefix 1..c_first-1;
+//    RN(m)^2 (1 - 2^-24). A code whose RN(m)^2 (1 - 2^-18) already exceeds a
+//    computed sum of another code cannot win, and m falls as c grows, so
+//    neither can any code below it;
 //  * above: from the first code with s_c >= 4.00002 A on, every x * (1/s_c)
 //    rounds to at most 1/4 and encodes to 0, so every such code has the same
 //    sum (that of the values themselves): only the first of them can win.
-// The codes c_first .. c_last are then swept in increasing order. Blocks with
-// a NaN or Inf are swept whole.
+// The sweep starts at the amax-derived code c0 (the E4M3 code of A / (6 g)),
+// walks down while the bound lets a code beat the best sum so far (a tie
+// moves to the smaller code), then up to the first all-zero code (a tie stays
+// with the smaller code), so the smallest code with the smallest sum wins as
+// in the full sweep. Blocks with a NaN or Inf are swept whole.
 #include "encode.cuh"
 #include "launch.h"
 
@@ -71,29 +74,43 @@ __global__ void __launch_bounds__(kThreads) scale_init_mse_kernel(const ScaleIni
     f2 lo[4], hi[4];
     unpack8(v0, lo);
     unpack8(v1, hi);
-    uint32_t c_first = 1, c_last = 126;
+    uint32_t best = 1;
+    float best_sse = 0.0f;
     if (abits >= 0x7F80u) {
       flag(p.status, NVFP4_DEV_NONFINITE_INPUT_BIT);
+      for (uint32_t c = 1; c <= 126; ++c) {
+        const float sse = candidate_sse(lo, hi, s_tab[c]);
+        if (c == 1 || sse < best_sse) {
+          best = c;
+          best_sse = sse;
+        }
+      }
     } else {
       const float A = __uint_as_float(abits << 16);
       const uint32_t c0 = min(max(e4m3_encode(__fmul_rn(A, ss.rden6)), 1u), 126u);
-      const float B = candidate_sse(lo, hi, s_tab[c0]);
       const float T = __fmul_rn(A, 4.00002f);
-      c_last = min(first_false(1u, 126u, [&](uint32_t c) { return s_tab[c].x < T; }), 126u);
-      c_first = min(first_false(1u, c0, [&](uint32_t c) {
-        const float m = __fmaf_rn(-6.0f, s_tab[c].x, A);
-        return m > 0.0f && __fmul_rn(__fmul_rn(m, m), 0.999996185302734375f) > B;  // 1 - 2^-18
-      }), c0);
-      c_last = max(c_last, c_first);
-    }
-    uint32_t best = c_first;
-    float best_sse = 0.0f;
+      const uint32_t c_last =
+          max(min(first_false(1u, 126u, [&](uint32_t c) { return s_tab[c].x < T; }), 126u), c0);
+      best = c0;
+      best_sse = candidate_sse(lo, hi, s_tab[c0]);
+#pragma unroll 1
+      for (uint32_t c = c0 - 1; c >= 1; --c) {  // down: stop where the bound rules c out
+        const float2 di = s_tab[c];
+        const float m = __fmaf_rn(-6.0f, di.x, A);
+        if (m > 0.0f && __fmul_rn(__fmul_rn(m, m), 0.999996185302734375f) > best_sse) break;
+        const float sse = candidate_sse(lo, hi, di);
+        if (sse <= best_sse) {
+          best = c;
+          best_sse = sse;
+        }
+      }
 #pragma unroll 2
-    for (uint32_t c = c_first; c <= c_last; ++c) {
-      const float sse = candidate_sse(lo, hi, s_tab[c]);
-      if (c == c_first || sse < best_sse) {
-        best = c;
-        best_sse = sse;
+      for (uint32_t c = c0 + 1; c <= c_last; ++c) {  // up to the first all-zero code
+        const float sse = candidate_sse(lo, hi, s_tab[c]);
+        if (sse < best_sse) {
+          best = c;
+          best_sse = sse;
+        }
       }
     }
     if (p.codes) p.codes[b] = (uint8_t)best;

@@ -85,18 +85,18 @@ def test_step_time_is_the_maximum_over_ranks():
 
 
 def test_sweep_candidate_count_edges(bench):
-    """The MSE sweep's work count: an all-zero block is the probe plus code 1
-    (2 encodings); every count lies between 2 and 127 (the probe plus all 126
-    codes); in a constant block the codes well below amax / 6 are pruned."""
+    """The MSE sweep's work count: an all-zero block encodes code 1 only; every
+    count lies between 1 and 126; in a constant block the codes well below
+    amax / 6 are pruned."""
     import numpy as np
     z = np.zeros((1, 16), np.uint16)
-    assert bench.sweep_candidates_per_block(z, 1.0) == 2.0
+    assert bench.sweep_candidates_per_block(z, 1.0) == 1.0
     rng = np.random.default_rng(5)
     x = (rng.standard_normal((64, 256)) * np.exp(rng.uniform(-8, 8, (64, 1)))).astype(np.float32)
     bits = (x.view(np.uint32) >> 16).astype(np.uint16)
     for gam in (1e-3, 1.0, 1e3):
         n = bench.sweep_candidates_per_block(bits, gam)
-        assert 2.0 <= n <= 127.0
+        assert 1.0 <= n <= 126.0
     # A = 0.75 with g = 0.75: the codes with 6 s_c well short of A go
     v = np.full((1, 16), 0.75, np.float32)
     assert bench.sweep_candidates_per_block((v.view(np.uint32) >> 16).astype(np.uint16),
