@@ -127,6 +127,9 @@ MUTANTS = [
     ("quant_scale_max", "float M = scale_max > 0.0f ? scale_max : (fos ? 256.0f : 448.0f);", "float M = fos ? 256.0f : 448.0f;", 0),
     ("fp8_post_sign", "!(so >= 0.0f && so <= FLT_MAX)", "!(so <= FLT_MAX)"),
     ("tile_col_nibble", "if (t & 1) c_codes[t / 2] = (uint8_t)((c_codes[t / 2] & 0x0F) | (q << 4));", "if (!(t & 1)) c_codes[t / 2] = (uint8_t)((c_codes[t / 2] & 0x0F) | (q << 4));"),
+    ("rq_transpose", "for (int64_t c = 0; c < C; ++c) xt[s * R * C + c * R + r] = xh[s * R * C + r * C + c];", "for (int64_t c = 0; c < C; ++c) xt[s * R * C + c * R + r] = xh[s * R * C + r * C + (C - 1 - c)];"),
+    ("mx_scale_sign", "float y = ldexpf(vb[i], -e);", "float y = ldexpf(vb[i], e);"),
+    ("tile_sr_idx", "if (rounding) v16[i] = orc_sr_bits(seed, step, 0, (uint64_t)(e0 + i));", "if (rounding) v16[i] = orc_sr_bits(seed, step, 0, (uint64_t)(e0 + 15 - i));"),
 ]
 
 EXPECTED_SURVIVORS = {"block_sum_order"}
