@@ -1,21 +1,27 @@
 """Throughput of the NVFP4 hot path on one or more GB300s.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..11] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..13] [--impl ours|reference]
 
 A step is one pass of the hot path over one batch of synthetic input already
-resident in HBM. The default workload is the activation tensor 8192 x 4096 bf16
-(S = 8192 tokens x hidden 4096, 0.5 * Student-t(3) values): current tensor
-scaling (global amax pass), 1x16 row blocks, E4M3 block scales, RNE E2M1,
-Four-Over-Six on, writing codes, scale bytes, the 4/6 bitmap and the dequantised
-tensor. Other --config values time the other workloads (see WORKLOADS).
+resident in HBM. The default workload is the largest one: MoE expert weights,
+64 experts x 2048 x 7168 bf16 (N(0, 0.02) with 0.01 % x50 outliers), per-expert
+global amax, then one pass that writes both the 1x16 row and the 16x1 column
+(transposed) NVFP4 encodings with E4M3 scales, RNE, Four-Over-Six, both 4/6
+bitmaps and both dequantised tensors. Other --config values time the other
+workloads (see WORKLOADS); --config 13 measures the 4/6 overhead of the row
+quantiser.
 
-One JSON line is printed by rank 0. `value` is algorithmic HBM bytes / time
-(GB/s) summed over all ranks; `roofline` relates the dominant kernel's own
-CUDA-event time to the measured HBM copy bandwidth; `e2e` repeats the metric
-through the same C ABI with host buffers (pinned host -> device copy of the
-input and device -> host copy of every output inside the timed region);
-`cpu_baseline` is the plain C oracle on the host cores (a baseline, not the
-target). With --impl reference the oracle itself is the timed arm.
+The K steps run as a pass bracketed by CUDA events; passes repeat back to
+back until at least --min-seconds of device time have run and the median pass
+is reported. One JSON line is printed by rank 0. `value` is algorithmic HBM
+bytes / time (GB/s) summed over all ranks; `roofline` relates the dominant
+kernel's own CUDA-event time to the measured HBM copy bandwidth (and, where a
+committed ncu count exists, to the instruction-issue bound); `e2e` repeats the
+metric through the same C ABI with host buffers (pinned host -> device copy of
+the input and device -> host copy of every output inside the timed region);
+`cpu_baseline` is the plain C oracle on the host cores, one core and all cores
+(a baseline, not the target). With --impl reference the oracle itself is the
+timed arm.
 """
 from __future__ import annotations
 
@@ -54,10 +60,27 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-# ALU roofline for a kernel bound by arithmetic by definition: simple fp32
-# operations per second of the whole GPU, 152 SMs x 128 fp32 lanes x the
-# 2070 MHz maximum SM clock (an fma counted as one operation).
-ALU_PEAK_TOPS = 152 * 128 * 2.070e9 / 1e12
+def sm_max_mhz() -> float:
+    """The maximum SM clock: the generated peaks file, else 2070 MHz
+    (GB300's maximum SM clock)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["sm_max_mhz"])
+    except Exception:
+        return 2070.0
+
+
+def alu_peak_tops(sms: int, mhz: float) -> float:
+    """ALU roofline of a kernel bound by arithmetic by definition: simple fp32
+    operations per second of the whole GPU, SMs x 128 fp32 lanes x the
+    maximum SM clock (an fma counted as one operation)."""
+    return sms * 128 * mhz * 1e6 / 1e12
+
+
+def issue_peak_ginst(sms: int, mhz: float) -> float:
+    """Instruction issue rate of the whole GPU: every SM has four schedulers,
+    each issuing at most one warp instruction per cycle."""
+    return sms * 4 * mhz * 1e6 / 1e9
 
 
 
@@ -166,10 +189,19 @@ class Activation(Workload):
         self.amax = [torch.empty(1, dtype=torch.float32, device=device) for _ in range(self.nsets)]
         self.out = [nv.alloc_encoding(1, rows, cols, device, bool(fos)) for _ in range(self.nsets)]
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
-        self.q_bytes = self.elements * (2 + 0.5 + 1 / 16 + 2) + (self.elements / 128 if fos else 0)
-        self.a_bytes = self.elements * 2
+        bpe = Activation.call_bpe(dict(fos=fos, cols=cols))
+        self.q_bytes = self.elements * bpe["quantize_row"]
+        self.a_bytes = self.elements * bpe["amax"]
         self.working_set = per_set * self.nsets
         self._prep(device)
+
+    @staticmethod
+    def call_bpe(kw):
+        """Algorithmic HBM bytes per element of each call of a step: the amax
+        pass reads x; the quantiser reads x and writes codes (1/2), scale
+        bytes (1/16), the 4/6 bitmap (1/128) and the bf16 dequant (2)."""
+        return {"amax": 2.0,
+                "quantize_row": 2 + 0.5 + 1 / 16 + 2 + (1 / 128 if kw["fos"] else 0)}
 
     def _prep(self, device):
         L = nv.lib()
@@ -253,8 +285,9 @@ class ScaleLearning(Workload):
                                   xq=torch.empty_like(w), gx=torch.empty_like(w),
                                   gsp=torch.empty_like(sp), gso=torch.empty_like(sp)))
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
-        self.f_bytes = self.elements * 4.5
-        self.b_bytes = self.elements * 7.0
+        bpe = ScaleLearning.call_bpe({})
+        self.f_bytes = self.elements * bpe["fakequant_fwd"]
+        self.b_bytes = self.elements * bpe["scale_grad_bwd"]
         self.working_set = per_set * self.nsets
         L = nv.lib()
         st = torch.cuda.current_stream(device).cuda_stream
@@ -273,6 +306,13 @@ class ScaleLearning(Workload):
                                           d["gx"].data_ptr(), d["gsp"].data_ptr(),
                                           d["gso"].data_ptr(), self.status.data_ptr(), st)
         self._fwd, self._bwd = fwd, bwd
+
+    @staticmethod
+    def call_bpe(kw):
+        """Forward: x (2), s_pre and s_post (2 x 4 / 16), x~ (2). Backward: x and
+        dL/dx~ (2 + 2), both scales (0.5), dL/dx (2), dL/ds_pre and dL/ds_post
+        (0.5)."""
+        return {"fakequant_fwd": 4.5, "scale_grad_bwd": 7.0}
 
     def kernels(self, k, i):
         return [Kernel("fakequant_fwd", self.f_bytes, lambda: self._fwd(i)),
@@ -320,8 +360,9 @@ class DriftingGradient(Workload):
         self.out = [nv.alloc_encoding(1, rows, cols, device, False, dequant=False)
                     for _ in range(2)]
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
-        self.q_bytes = self.elements * (2 + 0.5 + 1 / 16)
-        self.a_bytes = self.elements * 2
+        bpe = self.call_bpe({})
+        self.q_bytes = self.elements * bpe["quantize_row_sr"]
+        self.a_bytes = self.elements * bpe["amax"]
         self.working_set = self.elements * 2 * nsteps
         L = nv.lib()
         st = torch.cuda.current_stream(device).cuda_stream
@@ -338,6 +379,12 @@ class DriftingGradient(Workload):
                                     self.amax.data_ptr(), C.byref(self._outs[t % 2]), None,
                                     self.status.data_ptr(), st)
         self._amax, self._quant = amax, quant
+
+    @staticmethod
+    def call_bpe(kw):
+        """amax on refresh steps (x, 2); every step x (2), codes (1/2), scale
+        bytes (1/16); no dequant."""
+        return {"amax": 2.0, "quantize_row_sr": 2 + 0.5 + 1 / 16}
 
     def kernels(self, k, i):
         t = k % self.nsets
@@ -393,8 +440,9 @@ class MoeExperts(Workload):
         self.cfg = nv.Config(blocks=3, four_over_six=1)
         self._c = self.cfg.c()
         self._r, self._cc = nv._out(self.row), nv._out(self.col)
-        self.d_bytes = self.elements * (2 + 2 * (0.5 + 1 / 16 + 1 / 128 + 2))
-        self.a_bytes = self.elements * 2
+        bpe = self.call_bpe({})
+        self.d_bytes = self.elements * bpe["quantize_dual"]
+        self.a_bytes = self.elements * bpe["amax"]
         self.nsets = 1
         self.working_set = self.elements * (2 + 2 * 4.57)
         L = nv.lib()
@@ -409,6 +457,13 @@ class MoeExperts(Workload):
                                     self.amax.data_ptr(), C.byref(self._r), C.byref(self._cc),
                                     self.status.data_ptr(), st)
         self._amax, self._dual = amax, dual
+
+    @staticmethod
+    def call_bpe(kw):
+        """amax reads x (2); the dual pass reads x once (2) and writes, for each
+        of the row and column encodings, codes (1/2), scale bytes (1/16), the
+        4/6 bitmap (1/128) and the bf16 dequant (2)."""
+        return {"amax": 2.0, "quantize_dual": 2 + 2 * (0.5 + 1 / 16 + 1 / 128 + 2)}
 
     def kernels(self, k, i):
         return [Kernel("amax", self.a_bytes, self._amax, 2),
@@ -456,13 +511,19 @@ class PerTokenActivation(Activation):
                          for _ in range(self.nsets)]
         self.out = [nv.alloc_encoding(R, 1, Cc, device, bool(self.fos)) for _ in range(self.nsets)]
         self._touts = [nv._out(o) for o in self.out]
-        self.t_bytes = self.q_bytes + R * 4
+        self.t_bytes = self.elements * PerTokenActivation.call_bpe(dict(cols=Cc))["quantize_per_token"]
 
         def tok(i):
             return L.nvfp4_quantize_per_token(C.byref(self._c), self.x[i].data_ptr(), R, Cc,
                                               self.row_amax[i].data_ptr(),
                                               C.byref(self._touts[i]), self.status.data_ptr(), st)
         self._tok = tok
+
+    @staticmethod
+    def call_bpe(kw):
+        """The row quantiser's bytes with 4/6 and dequant, plus the fp32 row
+        amax (4 bytes per row of `cols` elements)."""
+        return {"quantize_per_token": 2 + 0.5 + 1 / 16 + 1 / 128 + 2 + 4 / kw["cols"]}
 
     def kernels(self, k, i):
         return [Kernel("quantize_per_token", self.t_bytes, lambda: self._tok(i))]
@@ -510,7 +571,7 @@ class RequantActivation(Workload):
         self.out = [nv.alloc_requant(1, rows, cols, device, target, target == 1)
                     for _ in range(self.nsets)]
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
-        self.r_bytes = in_bytes + out_bytes
+        self.r_bytes = self.elements * sum(self.call_bpe(dict(target=target)).values())
         self.working_set = per_set * self.nsets
         L = nv.lib()
         st = torch.cuda.current_stream(device).cuda_stream
@@ -526,6 +587,15 @@ class RequantActivation(Workload):
                                              C.byref(self._outs[i]), self.status.data_ptr(), st)
         self._rq = rq
         self.dominant = "requant_mxfp8_sr" if target == 0 else "requant_nvfp4_sr"
+
+    @staticmethod
+    def call_bpe(kw):
+        """Reads the source codes (1/2) and scale bytes (1/16); writes MXFP8
+        codes (1) and E8M0 scales (1/32), or NVFP4 codes (1/2), scale bytes
+        (1/16) and the 4/6 bitmap (1/128)."""
+        if kw["target"] == 0:
+            return {"requant_mxfp8_sr": 0.5 + 1 / 16 + 1 + 1 / 32}
+        return {"requant_nvfp4_sr": 0.5 + 1 / 16 + 0.5 + 1 / 16 + 1 / 128}
 
     def kernels(self, k, i):
         return [Kernel(self.dominant, self.r_bytes, lambda: self._rq(i), 2 if self.target == 1 else 1)]
@@ -590,6 +660,11 @@ class ScaleLearningFp8(ScaleLearning):
                 d["gsp"].data_ptr(), d["gso"].data_ptr(), self.status.data_ptr(), st)
         self._fwd, self._bwd = fwd, bwd
 
+    @staticmethod
+    def call_bpe(kw):
+        """As the fp32-scale step (the FP8 outer amax is one float)."""
+        return {"fakequant_fwd_fp8": 4.5, "scale_grad_bwd_fp8": 7.0}
+
     def kernels(self, k, i):
         return [Kernel("fakequant_fwd_fp8", self.f_bytes, lambda: self._fwd(i)),
                 Kernel("scale_grad_bwd_fp8", self.b_bytes, lambda: self._bwd(i))]
@@ -631,8 +706,9 @@ class ScaleInitExport(ScaleLearningFp8):
             d["enc"] = nv.alloc_encoding(1, R, Cc, device, False, dequant=False)
             d["eo"] = nv._Out(d["enc"]["codes"].data_ptr(), d["enc"]["scales"].data_ptr(), None,
                               None)
-        self.i_bytes = self.elements * (2 + 1 / 16 + 4 / 16)
-        self.e_bytes = self.elements * (2 + 0.5 + 0.5 + 1 / 16)
+        bpe = self.call_bpe({})
+        self.i_bytes = self.elements * bpe["scale_init_mse"]
+        self.e_bytes = self.elements * bpe["export_scales"]
 
         def init(i):
             d = self.sets[i]
@@ -646,6 +722,12 @@ class ScaleInitExport(ScaleLearningFp8):
                                          d["so"].data_ptr(), self.gamax.data_ptr(),
                                          C.byref(d["eo"]), self.status.data_ptr(), st)
         self._init, self._export = init, export
+
+    @staticmethod
+    def call_bpe(kw):
+        """Sweep: x (2), scale codes (1/16), fp32 scales (4/16). Export: x (2),
+        both fp32 scales (0.5), codes (1/2), scale bytes (1/16)."""
+        return {"scale_init_mse": 2 + 1 / 16 + 4 / 16, "export_scales": 2 + 0.5 + 0.5 + 1 / 16}
 
     def kernels(self, k, i):
         return [Kernel("scale_init_mse", self.i_bytes, lambda: self._init(i)),
@@ -708,8 +790,9 @@ class TileWeight(Workload):
         self.row = [nv.alloc_encoding(1, rows, cols, device, False) for _ in range(self.nsets)]
         self.col = [nv.alloc_encoding(1, cols, rows, device, False) for _ in range(self.nsets)]
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
-        self.t_bytes = self.elements * (2 + 2 * (0.5 + 1 / 16 + 2))
-        self.a_bytes = self.elements * 2
+        bpe = self.call_bpe({})
+        self.t_bytes = self.elements * bpe["quantize_tile16"]
+        self.a_bytes = self.elements * bpe["amax"]
         self.working_set = per_set * self.nsets
         L = nv.lib()
         st = torch.cuda.current_stream(device).cuda_stream
@@ -726,6 +809,13 @@ class TileWeight(Workload):
                                     self.amax[i].data_ptr(), C.byref(self._ro[i]),
                                     C.byref(self._co[i]), self.status.data_ptr(), st)
         self._amax, self._tile = amax, tile
+
+    @staticmethod
+    def call_bpe(kw):
+        """amax (2); the tile pass reads x (2) and writes, for the row encoding
+        and its transpose, codes (1/2), a scale byte per 16 (1/16: a tile's
+        scale is stored once per 16-value row block) and the dequant (2)."""
+        return {"amax": 2.0, "quantize_tile16": 2 + 2 * (0.5 + 1 / 16 + 2)}
 
     def kernels(self, k, i):
         return [Kernel("amax", self.a_bytes, lambda: self._amax(i), 2),
@@ -766,7 +856,7 @@ class GradientMx(Workload):
         gen = synth.DriftingGradient(rows, cols, seed=seed)
         self.rows, self.cols = rows, cols
         self.elements = rows * cols
-        self.m_bytes = self.elements * (2 + 2 * (1 + 1 / 32))
+        self.m_bytes = self.elements * self.call_bpe({})["mx_quantize_sr"]
         self.nsets = max(2, int(np.ceil(2.5 * L2_BYTES / self.m_bytes)))
         self.host0 = gen.step(0)
         self.x = [torch.from_numpy(gen.step(t).view(np.int16)).to(device)
@@ -789,6 +879,11 @@ class GradientMx(Workload):
                                        cols, C.byref(self._ro[i]), C.byref(self._co[i]),
                                        self.status.data_ptr(), st)
         self._mx = mx
+
+    @staticmethod
+    def call_bpe(kw):
+        """x (2); rows and transpose: E4M3 codes (1) and E8M0 scales (1/32) each."""
+        return {"mx_quantize_sr": 2 + 2 * (1 + 1 / 32)}
 
     def kernels(self, k, i):
         return [Kernel("mx_quantize_sr", self.m_bytes, lambda: self._mx(k, i))]
@@ -864,10 +959,73 @@ def describe_workload(config, args):
     return stub.workload
 
 
+# Four-Over-Six overhead of the row quantiser: the 4/6 pages' one published
+# figure for this path is an overhead below 2 % at S <= 2048 tokens and below
+# 15 % at S = 8192 on their Blackwell kernel.
+FOS_OVERHEAD = 13
+FOS_PAGES = "4/6 overhead < 2 % at S <= 2048 and < 15 % at S = 8192 (Four Over Six, Blackwell)"
+
+
+def fos_overhead(args, device):
+    """Row quantiser on activations [S x 4096] (0.5 * Student-t(3)), S = 2048
+    and 8192, with and without the dequantised output, 4/6 off and on: each
+    variant timed alone as back-to-back calls over rotating buffer sets larger
+    than L2 (median of repeated passes, events at the pass ends only)."""
+    import math
+    steps = args.steps or 50
+    out, tot_b, tot_ms = [], 0.0, 0.0
+    for rows in (2048, 8192):
+        for dq in (True, False):
+            us = {}
+            for fos in (0, 1):
+                wl = Activation(device, rows=rows, fos=fos)
+                if not dq:
+                    for o in wl._outs:
+                        o.dequant = None
+                def call(i, wl=wl):
+                    return wl._quant(i)
+                for k in range(args.warmup):
+                    call(k % wl.nsets)
+                torch.cuda.synchronize()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                passes, npass = [], None
+                while npass is None or len(passes) < npass:
+                    torch.cuda.synchronize()
+                    a.record()
+                    for k in range(steps):
+                        rc = call(k % wl.nsets)
+                        if rc != 0:
+                            raise nv.Nvfp4Error("quantize_row", rc)
+                    b.record()
+                    torch.cuda.synchronize()
+                    passes.append(a.elapsed_time(b))
+                    if npass is None:
+                        npass = min(max(3, math.ceil(0.25e3 / max(passes[0], 1e-3))), 2000)
+                if int(wl.status.item()) != 0:
+                    raise RuntimeError("device status set")
+                ms = statistics.median(passes) / steps
+                bpe = 2 + 0.5 + 1 / 16 + (2 if dq else 0) + (1 / 128 if fos else 0)
+                tot_b += bpe * wl.elements
+                tot_ms += ms
+                us[fos] = 1e3 * ms
+                del wl
+                torch.cuda.empty_cache()
+            out.append({"rows": rows, "cols": 4096, "dequant": dq, "us_4over6_off": round(us[0], 2),
+                        "us_4over6_on": round(us[1], 2),
+                        "overhead_pct": round(100 * (us[1] / us[0] - 1), 1)})
+    return {"metric": METRIC, "value": round(tot_b / (tot_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "n_gpus": 1, "steps": steps, "warmup": args.warmup, "higher_is_better": True,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "Four-Over-Six overhead of the 1x16 row quantiser (E4M3, "
+                                   "RNE) on activations S x 4096, S = 2048 and 8192, with and "
+                                   "without dequant output"},
+            "fos_overhead": out, "pages": FOS_PAGES}
+
+
 # --------------------------------------------------------------- clocks --
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -881,7 +1039,20 @@ class ClockSampler:
         except Exception:
             self.proc = None
 
-    def stop(self):
+    @staticmethod
+    def _when(stamp: str):
+        import datetime
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(stamp, fmt).timestamp()
+            except ValueError:
+                pass
+        return None
+
+    def stop(self, t0: float | None = None, t1: float | None = None):
+        """Median SM clock, maximum clock and throttle reasons of the samples
+        taken between host times t0 and t1 (the timed passes); all samples
+        when their timestamps cannot be read."""
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -890,25 +1061,26 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        sm, mx, reasons, n = [], 0.0, set(), 0
-        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        rows = []
         for line in out.strip().splitlines():
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1]))
-                mx = max(mx, float(f[2]))
+                rows.append((self._when(f[0]), float(f[2]), float(f[3]), f[6:10]))
             except ValueError:
                 continue
-            n += 1
-            for name, v in zip(names, f[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(name)
-        if not sm:
+        inside = [r for r in rows if r[0] is not None and t0 is not None and t0 <= r[0] <= t1]
+        window = "timed passes" if inside else "whole run"
+        use = inside or rows
+        if not use:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": n}
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = {name for r in use for name, v in zip(names, r[3])
+                   if v.lower().startswith("active")}
+        return {"sm_mhz": statistics.median(r[1] for r in use),
+                "sm_max_mhz": max(r[2] for r in use), "reasons": sorted(reasons),
+                "samples": len(use), "window": window}
 
 
 # --------------------------------------------------------------- timing --
@@ -974,11 +1146,14 @@ def run_steps(wl, k0, K, events=None):
 
 
 def time_ours(wl, args, world, local):
-    """Two timed passes over the same K steps. The step time comes from a pass
-    with one CUDA event at each end of the timed region (an event record
-    between kernels costs the device about a microsecond and a half); the
-    per-kernel durations behind the roofline come from a second pass with an
-    event after every kernel."""
+    """Timed passes over the same K steps, each bracketed by a barrier, a
+    device synchronisation and one CUDA event at either end, repeated back to
+    back until at least --min-seconds of device time have run, so that the
+    clock samples cover the kernels under load; the median pass is the step
+    time. A last pass with an event after every call (an event record between
+    kernels costs the device about a microsecond and a half) gives the
+    per-kernel durations behind the roofline."""
+    import math
     run_steps(wl, 0, args.warmup)
     torch.cuda.synchronize()
     nk = sum(len(wl.kernels(k, k % wl.nsets)) for k in range(args.warmup, args.warmup + args.steps))
@@ -987,28 +1162,40 @@ def time_ours(wl, args, world, local):
     barrier(world)
     torch.cuda.synchronize()
     clocks = ClockSampler(_smi_id(local))
-    time.sleep(0.3)
+    time.sleep(0.3)  # the sampler's first line
+    t0 = time.time()
     wall0 = time.perf_counter()
-    a.record()
-    run_steps(wl, args.warmup, args.steps)
-    b.record()
-    torch.cuda.synchronize()
+    passes, npass = [], None
+    while npass is None or len(passes) < npass:
+        barrier(world)
+        torch.cuda.synchronize()
+        a.record()
+        run_steps(wl, args.warmup, args.steps)
+        b.record()
+        torch.cuda.synchronize()
+        passes.append(a.elapsed_time(b))
+        if npass is None:
+            want = math.ceil(args.min_seconds * 1e3 / max(passes[0], 1e-3))
+            npass = int(max_over_ranks(float(min(max(3, want), args.max_passes)), world))
     wall = time.perf_counter() - wall0
     barrier(world)
     torch.cuda.synchronize()
     evs = run_steps(wl, args.warmup, args.steps, events)
     torch.cuda.synchronize()
+    t1 = time.time()
     barrier(world)
     torch.cuda.synchronize()
-    clk = clocks.stop()
-    total_ms = a.elapsed_time(b)
+    clk = clocks.stop(t0, t1)
     per_kernel = {}
     for kern, e0, e1 in evs:
         d = per_kernel.setdefault(kern.name, {"ms": 0.0, "n": 0, "bytes": kern.nbytes,
                                               "launches": kern.launches})
         d["ms"] += e0.elapsed_time(e1)
         d["n"] += 1
-    return total_ms, per_kernel, clk, wall
+    stats = {"passes": len(passes), "device_s": round(sum(passes) / 1e3, 3),
+             "median_ms": round(statistics.median(passes), 4), "min_ms": round(min(passes), 4),
+             "max_ms": round(max(passes), 4)}
+    return statistics.median(passes), stats, per_kernel, clk, wall
 
 
 def time_e2e(wl, steps, device):
@@ -1082,25 +1269,70 @@ def time_e2e(wl, steps, device):
     return a.elapsed_time(b), bi, bo
 
 
-def cores_used() -> int:
-    return 1
+def cpu_model() -> str:
+    """The host CPU's model name (Linux /proc/cpuinfo; the Arm machines give a
+    part number instead)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+    except OSError:
+        return "unknown"
+    for key in ("model name", "Model Name", "Hardware", "CPU part"):
+        for line in info.splitlines():
+            if line.split(":")[0].strip() == key:
+                val = line.split(":", 1)[1].strip()
+                return val if key != "CPU part" else f"Arm CPU part {val}"
+    return "unknown"
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(wl, budget_s):
+    """The oracle on the host: one core (the single-threaded build) and all
+    cores (the OpenMP build of the same source), each on a bounded sample of
+    the workload; `value` is the all-core leg."""
+    import oracle
+    legs = []
+    for n in (1, host_cores()):
+        used = oracle.set_threads(n)
+        try:
+            e, dt, sample = wl.cpu_sample(budget_s)
+        finally:
+            oracle.set_threads(1)
+        legs.append({"cores": used, "value": round(e * wl.bytes_per_elem / dt / 1e9, 5),
+                     "gelem_per_s": round(e / dt / 1e9, 6), "sample": sample})
+    best = legs[-1]
+    return {"value": best["value"], "unit": "GB/s", "cores": best["cores"], "kind": "oracle",
+            "sample": best["sample"], "gelem_per_s": best["gelem_per_s"],
+            "cpu_model": cpu_model(), "nproc": host_cores(), "legs": legs}
 
 
 def reference_arm(args, world, rank):
-    """The oracle, as it stands, timed on the host cores: each step is a bounded
-    sample of the chosen workload, reported with our arm's metric and unit."""
+    """The oracle, as it stands, timed on all host cores (its OpenMP build):
+    each step is a bounded sample of the chosen workload, charged with the
+    same per-call algorithmic bytes as our arm, reported in our arm's metric
+    and unit."""
     if rank != 0:
         return
     import oracle
     oracle.build()
-    desc, bpe, sample_text, step = _reference_sample(args)
-    secs, total_e = 0.0, 0
+    bpe = WORKLOADS[args.config].call_bpe(_ctor_args(args.config, args))
+    desc, sample_text, step = _reference_sample(args)
+    cores = oracle.set_threads(host_cores())
+    secs, total_e, total_b = 0.0, 0, 0.0
     for k in range(args.warmup + args.steps):
-        e, dt = step()
+        e, calls, dt = step(k)
         if k >= args.warmup:
             secs += dt
             total_e += e
-    value = total_e * bpe / secs / 1e9
+            total_b += e * sum(bpe[c] for c in calls)
+    oracle.set_threads(1)
+    value = total_b / secs / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "GB/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -1109,136 +1341,152 @@ def reference_arm(args, world, rank):
         "config": {"workload": describe_workload(args.config, args), "sample": sample_text,
                    "oracle_workload": desc},
         "gelem_per_s": round(total_e / secs / 1e9, 6),
-        "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": cores_used(),
-                         "kind": "oracle", "sample": sample_text},
+        "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": cores,
+                         "kind": "oracle", "sample": sample_text, "cpu_model": cpu_model(),
+                         "nproc": host_cores()},
         "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
+def _timed(fn):
+    t0 = time.perf_counter()
+    fn()
+    return time.perf_counter() - t0
+
+
 def _reference_sample(args):
-    """(workload text, algorithmic bytes/elem, sample text, -, step fn) for the
-    reference arm. Each step runs the oracle on the same rows of the workload."""
+    """(workload text, sample text, step) for the reference arm. step(k) runs
+    the oracle on the same rows of the workload for step k and returns
+    (elements, names of the calls it ran, seconds); the calls' bytes per
+    element come from the workload's call_bpe, as in our arm."""
     import oracle
+    n = args.ref_rows
     if args.config in (1, 2):
         rows, cols = (1024, 1024) if args.config == 1 else (8192, 4096)
         fos = 0 if args.config == 1 else 1
         xb = (synth.outlier_normal(rows, cols, seed=0) if args.config == 1
               else synth.student_t(rows, cols, seed=1))
-        sub = xb[:args.ref_rows]
-        bpe = 2 + 2 + 0.5 + 1 / 16 + (1 / 128 if fos else 0)
+        sub = xb[:n]
 
-        def step():
-            t0 = time.perf_counter()
+        def run():
             a, _ = oracle.global_amax(sub)
             oracle.quantize(sub, a, four_over_six=fos)
-            return sub.size, time.perf_counter() - t0
+
+        def step(k):
+            return sub.size, ("amax", "quantize_row"), _timed(run)
         wl = "activation 8192x4096 bf16 0.5*Student-t(3), amax + row 4/6" if args.config == 2 \
             else "1024x1024 bf16 N(0,1) 0.1% x20, amax + row"
-        return wl, bpe, f"first {sub.shape[0]} rows of {rows} per step", step
-    if args.config == 3:
+        return wl, f"first {sub.shape[0]} rows of {rows} per step", step
+    if args.config in (3, 9):
         wb, gb, s = synth.scale_learning(seed=2)
-        n = args.ref_rows
+        names = ("fakequant_fwd", "scale_grad_bwd") if args.config == 3 else \
+            ("fakequant_fwd_fp8", "scale_grad_bwd_fp8")
+        gam = float(np.abs(synth.bf16_bits_to_f32(wb)).max()) * 1.5
 
-        def step():
-            t0 = time.perf_counter()
-            oracle.fakequant_fwd(wb[:n], s[:n], s[:n])
-            oracle.scale_grad_bwd(wb[:n], gb[:n], s[:n], s[:n])
-            return n * wb.shape[1], time.perf_counter() - t0
-        return "scale-learning step 14336x4096", 11.5, f"first {n} of 14336 rows per step", step
+        def run():
+            if args.config == 3:
+                oracle.fakequant_fwd(wb[:n], s[:n], s[:n])
+                oracle.scale_grad_bwd(wb[:n], gb[:n], s[:n], s[:n])
+            else:
+                oracle.fakequant_fwd_fp8(wb[:n], s[:n], s[:n], gam)
+                oracle.scale_grad_bwd_fp8(wb[:n], gb[:n], s[:n], s[:n], gam)
+
+        def step(k):
+            return n * wb.shape[1], names, _timed(run)
+        return ("scale-learning step 14336x4096" + (", FP8 scales" if args.config == 9 else "")), \
+            f"first {n} of 14336 rows per step", step
     if args.config == 4:
-        xb = synth.DriftingGradient().step(0)
-        sub = xb[:args.ref_rows]
-        a, _ = oracle.global_amax(sub)
+        gen = synth.DriftingGradient()
+        period = _ctor_args(4, args)["period"]
+        subs = [gen.step(t)[:n] for t in range(2)]
+        amax = [None]
 
-        def step():
-            t0 = time.perf_counter()
-            oracle.quantize(sub, a, scale_fmt=1, rounding=1, seed=3, step=0, dequant=False)
-            return sub.size, time.perf_counter() - t0
-        return "gradient 16384x4096 UE5M3 SR periodic", 2.5625 + 2 / 16, \
-            f"first {sub.shape[0]} of 16384 rows per step", step
+        def step(k):
+            sub = subs[k % 2]
+            t = time.perf_counter()
+            calls = ("quantize_row_sr",)
+            if amax[0] is None or k % period == 0:  # periodic tensor scaling
+                amax[0], _ = oracle.global_amax(sub)
+                calls = ("amax", "quantize_row_sr")
+            oracle.quantize(sub, amax[0], scale_fmt=1, rounding=1, seed=3, step=k,
+                            dequant=False)
+            return sub.size, calls, time.perf_counter() - t
+        return "gradient 16384x4096 UE5M3 SR periodic", \
+            f"first {n} of 16384 rows per step (amax every {period} steps)", step
     if args.config == 6:
         xb = synth.student_t(8192, 4096, seed=1)
-        sub = xb[:args.ref_rows].reshape(-1, 1, 4096)
+        sub = xb[:n].reshape(-1, 1, 4096)
 
-        def step():
-            t0 = time.perf_counter()
+        def run():
             a, _ = oracle.global_amax(sub, sub.shape[0])
             oracle.quantize(sub, a, four_over_six=1)
-            return sub.size, time.perf_counter() - t0
+
+        def step(k):
+            return sub.size, ("quantize_per_token",), _timed(run)
         return "activation 8192x4096 per-token outer scales, row 4/6", \
-            2 + 0.5 + 1 / 16 + 1 / 128 + 2 + 4 / 4096, \
             f"first {sub.shape[0]} of 8192 rows per step", step
     if args.config in (7, 8):
         target = args.config - 7
         xb = synth.student_t(8192, 4096, seed=1)
         a, _ = oracle.global_amax(xb)
-        n = max(32, args.ref_rows - args.ref_rows % 32) // 4
-        n -= n % 32
-        q = oracle.quantize(xb[:n], a, four_over_six=1, dequant=False)
+        m = max(32, (n // 4) - (n // 4) % 32)
+        q = oracle.quantize(xb[:m], a, four_over_six=1, dequant=False)
+        name = "requant_mxfp8_sr" if target == 0 else "requant_nvfp4_sr"
 
-        def step():
-            t0 = time.perf_counter()
+        def run():
             oracle.requant(q["row_codes"], q["row_scales"], a, target=target, rounding=1,
                            seed=7, src_fos=1, dst_fos=target)
-            return n * 4096, time.perf_counter() - t0
-        bpe = 0.5 + 1 / 16 + ((1 + 1 / 32) if target == 0 else (0.5 + 1 / 16 + 1 / 128))
+
+        def step(k):
+            return m * 4096, (name,), _timed(run)
         return ("activation 8192x4096 NVFP4 (4/6) re-quantised, transposed, SR to "
-                + ("MXFP8" if target == 0 else "NVFP4")), bpe, \
-            f"first {n} of 8192 source rows per step", step
+                + ("MXFP8" if target == 0 else "NVFP4")), \
+            f"first {m} of 8192 source rows per step", step
     if args.config == 11:
         wb, _, _ = synth.scale_learning(seed=2)
-        n = max(16, args.ref_rows - args.ref_rows % 16)
+        m = max(16, n - n % 16)
 
-        def step():
-            t0 = time.perf_counter()
-            a, _ = oracle.global_amax(wb[:n])
-            oracle.quantize_tile16(wb[:n], a)
-            return n * wb.shape[1], time.perf_counter() - t0
-        return "weight 14336x4096 16x16 tile scale + transpose", 2 + 2 + 2 * (0.5 + 1 / 16 + 2), \
-            f"first {n} of 14336 rows per step", step
+        def run():
+            a, _ = oracle.global_amax(wb[:m])
+            oracle.quantize_tile16(wb[:m], a)
+
+        def step(k):
+            return m * wb.shape[1], ("amax", "quantize_tile16"), _timed(run)
+        return "weight 14336x4096 16x16 tile scale + transpose", \
+            f"first {m} of 14336 rows per step", step
     if args.config == 12:
         xb = synth.DriftingGradient(seed=3).step(0)
-        n = max(32, args.ref_rows - args.ref_rows % 32)
+        m = max(32, n - n % 32)
 
-        def step():
-            t0 = time.perf_counter()
-            oracle.mx_quantize(xb[:n], blocks=3, rounding=1, seed=12, step=0)
-            return n * xb.shape[1], time.perf_counter() - t0
-        return "gradient 16384x4096 MXFP8 rows + transpose, SR", 2 + 2 * (1 + 1 / 32), \
-            f"first {n} of 16384 rows per step", step
-    if args.config in (9, 10):
-        wb, gb, s = synth.scale_learning(seed=2)
+        def step(k):
+            return m * xb.shape[1], ("mx_quantize_sr",), _timed(
+                lambda: oracle.mx_quantize(xb[:m], blocks=3, rounding=1, seed=12, step=k))
+        return "gradient 16384x4096 MXFP8 rows + transpose, SR", \
+            f"first {m} of 16384 rows per step", step
+    if args.config == 10:
+        wb, _, s = synth.scale_learning(seed=2)
         gam = float(np.abs(synth.bf16_bits_to_f32(wb)).max()) * 1.5
-        if args.config == 9:
-            n = args.ref_rows
+        m = max(1, n // 64)
 
-            def step():
-                t0 = time.perf_counter()
-                oracle.fakequant_fwd_fp8(wb[:n], s[:n], s[:n], gam)
-                oracle.scale_grad_bwd_fp8(wb[:n], gb[:n], s[:n], s[:n], gam)
-                return n * wb.shape[1], time.perf_counter() - t0
-            return "scale-learning step 14336x4096, FP8 scales", 11.5, \
-                f"first {n} of 14336 rows per step", step
-        n = max(1, args.ref_rows // 64)
+        def run():
+            oracle.scale_init_mse(wb[:m], gam)
+            oracle.export_scales(wb[:m], s[:m], s[:m], gam)
 
-        def step():
-            t0 = time.perf_counter()
-            oracle.scale_init_mse(wb[:n], gam)
-            oracle.export_scales(wb[:n], s[:n], s[:n], gam)
-            return n * wb.shape[1], time.perf_counter() - t0
-        return "MSE scale sweep + export 14336x4096", 2 + 1 / 16 + 4 / 16 + 2 + 0.5 + 0.5 + 1 / 16, \
-            f"first {n} of 14336 rows per step", step
+        def step(k):
+            return m * wb.shape[1], ("scale_init_mse", "export_scales"), _timed(run)
+        return "MSE scale sweep + export 14336x4096", f"first {m} of 14336 rows per step", step
     xb = synth.moe_experts(1, 2048, 7168, seed=4)[0]
-    sub = xb[:max(16, args.ref_rows - args.ref_rows % 16)]
+    sub = xb[:max(16, n - n % 16)]
 
-    def step():
-        t0 = time.perf_counter()
+    def run():
         a, _ = oracle.global_amax(sub)
         oracle.quantize(sub, a, blocks=3, four_over_six=1)
-        return sub.size, time.perf_counter() - t0
-    return "MoE 64x2048x7168 dual 4/6", 2 + 2 + 2 * (0.5 + 1 / 16 + 1 / 128 + 2), \
+
+    def step(k):
+        return sub.size, ("amax", "quantize_dual"), _timed(run)
+    return "MoE 64x2048x7168 dual 4/6", \
         f"first {sub.shape[0]} rows of one expert per step", step
 
 
@@ -1247,7 +1495,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=2, choices=sorted(WORKLOADS))
+    ap.add_argument("--config", type=int, default=5, choices=sorted(WORKLOADS) + [FOS_OVERHEAD])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -1255,6 +1503,9 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--experts", type=int, default=64, help="MoE workload: number of experts")
+    ap.add_argument("--min-seconds", type=float, default=2.0,
+                    help="device time the repeated timed passes run for at least")
+    ap.add_argument("--max-passes", type=int, default=5000)
     ap.add_argument("--sr-steps", type=int, default=32,
                     help="drifting-gradient workload: distinct step inputs held on the device")
     args = ap.parse_args()
@@ -1264,20 +1515,23 @@ def main():
     world, rank, local = dist_setup(args) if args.impl == "ours" else (
         int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), 0)
     if args.impl == "reference":
+        if args.config == FOS_OVERHEAD:
+            ap.error("--config 13 (the 4/6 overhead) has no reference arm")
         args.steps = args.steps or 3
         reference_arm(args, world, rank)
         return
 
     device = torch.device("cuda", local)
     nv.build()
+    if args.config == FOS_OVERHEAD:
+        if rank == 0:
+            print(json.dumps(fos_overhead(args, device)), flush=True)
+        return
     extra = {5: dict(experts=args.experts), 4: dict(nsteps=args.sr_steps)}.get(args.config, {})
     wl = WORKLOADS[args.config](device, **extra)
-    if args.steps is None:
-        # about two seconds of device time, so the clock samples cover the run
-        args.steps = {1: 20000, 2: 40000, 3: 10000, 4: 16000, 5: 150, 6: 50000, 7: 40000,
-                      8: 40000, 9: 10000, 10: 300, 11: 8000, 12: 30000}[args.config]
-    total_ms, per_kernel, clk, wall = time_ours(wl, args, world, local)
-    total_ms = max_over_ranks(total_ms, world)
+    args.steps = args.steps or 20
+    pass_ms, pass_stats, per_kernel, clk, wall = time_ours(wl, args, world, local)
+    total_ms = max_over_ranks(pass_ms, world)
     units = wl.elements * args.steps * world
     alg_bytes = sum(d["bytes"] * d["n"] for d in per_kernel.values()) * world
     value = alg_bytes / (total_ms * 1e-3) / 1e9
@@ -1286,21 +1540,49 @@ def main():
         raise RuntimeError(f"device status {st} during the benchmark")
 
     peak, peak_kind = measured_peak()
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    mhz = float(clk["sm_max_mhz"]) if clk and clk.get("sm_max_mhz") else sm_max_mhz()
     dom = per_kernel[wl.dominant]
     if len(per_kernel) == 1 and dom["n"] == args.steps:
-        # one call per step: the clean pass's events bracket exactly the K calls
-        dom_ms, dur_src = total_ms / args.steps, "step events, one call per step"
+        # one call per step: the clean passes' events bracket exactly the K calls
+        dom_ms, dur_src = total_ms / args.steps, "median pass, one call per step"
     else:
         dom_ms, dur_src = dom["ms"] / dom["n"], "an event after every call"
     achieved = dom["bytes"] / (dom_ms * 1e-3) / 1e9
-    traffic = _committed_traffic(args.config, wl.dominant)
+    traffic = _committed_counts(args.config, wl.dominant, "traffic.json", "bytes")
     alu_ops = getattr(wl, "alu_ops_per_elem", {}).get(wl.dominant)
+    elems_per_call = dom["bytes"] / wl.call_bpe(_wl_kw(wl))[wl.dominant]
     kernels = {name: {"calls": d["n"], "kernels_per_call": d["launches"],
                       "avg_us": round(1e3 * d["ms"] / d["n"], 3),
                       "alg_bytes": int(d["bytes"]),
                       "gbs": round(d["bytes"] / (d["ms"] / d["n"] * 1e-3) / 1e9, 1),
                       "frac_of_peak": round(d["bytes"] / (d["ms"] / d["n"] * 1e-3) / 1e9 / peak, 4)}
                for name, d in per_kernel.items()}
+    if alu_ops is None:
+        roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                    "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                    "kernel": wl.dominant, "peak_source": f"{peak_kind} HBM copy bandwidth",
+                    "duration_from": dur_src}
+    else:
+        alu_peak = alu_peak_tops(sms, mhz)
+        alu = alu_ops * elems_per_call / (dom_ms * 1e-3) / 1e12
+        roofline = {"bound": "alu", "achieved": round(alu, 2), "peak": round(alu_peak, 2),
+                    "unit": "Top/s", "frac": round(alu / alu_peak, 4), "traffic": traffic,
+                    "kernel": wl.dominant,
+                    "peak_source": f"{sms} SMs x 128 fp32 lanes x {mhz:.0f} MHz (derived)",
+                    "ops_per_element": alu_ops, "duration_from": dur_src}
+    ipe = _committed_counts(args.config, wl.dominant, "inst.json", "warp_inst_per_elem")
+    if ipe is not None:
+        # the same kernel against its instruction-issue bound
+        rate = ipe * elems_per_call / (dom_ms * 1e-3) / 1e9
+        ipeak = issue_peak_ginst(sms, mhz)
+        roofline["issue"] = {"warp_inst_per_elem": round(ipe, 4),
+                             "thread_inst_per_elem": round(32 * ipe, 2),
+                             "achieved": round(rate, 1), "peak": round(ipeak, 1),
+                             "unit": "Gwarp-inst/s", "frac": round(rate / ipeak, 4),
+                             "peak_source": f"{sms} SMs x 4 schedulers x {mhz:.0f} MHz",
+                             "count_from": "ncu smsp__inst_executed.sum of one launch "
+                                           "(profiles/inst.json)"}
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
@@ -1311,20 +1593,11 @@ def main():
                    "l2": (f"inputs larger than L2: {wl.nsets} rotating input/output sets, "
                           f"{wl.working_set / 2 ** 20:.0f} MiB > {L2_BYTES / 2 ** 20:.0f} MiB L2")},
         "gelem_per_s": round(units / (total_ms * 1e-3) / 1e9, 3),
-        "roofline": ({"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
-                      "unit": "GB/s", "frac": round(achieved / peak, 4),
-                      "traffic": traffic, "kernel": wl.dominant,
-                      "peak_source": f"{peak_kind} HBM copy bandwidth",
-                      "duration_from": dur_src} if alu_ops is None else
-                     {"bound": "alu",
-                      "achieved": round(alu_ops * wl.elements / (dom_ms * 1e-3) / 1e12, 2),
-                      "peak": round(ALU_PEAK_TOPS, 2), "unit": "Top/s",
-                      "frac": round(alu_ops * wl.elements / (dom_ms * 1e-3) / 1e12
-                                    / ALU_PEAK_TOPS, 4),
-                      "traffic": traffic, "kernel": wl.dominant,
-                      "peak_source": "152 SMs x 128 fp32 lanes x 2070 MHz (derived)",
-                      "ops_per_element": alu_ops, "duration_from": dur_src}),
+        "roofline": roofline,
         "kernels": kernels,
+        "timing": dict(pass_stats, steps_per_pass=args.steps,
+                       rule="median of the timed passes (barrier + synchronize + events around "
+                            "each pass of K steps)"),
         "gpu_launches": sum(d["n"] * d["launches"] for d in per_kernel.values()),
         "clocks": clk,
         "host_wall_s": round(wall, 3),
@@ -1336,10 +1609,7 @@ def main():
                        "unit": "GB/s", "h2d_bytes_per_step": int(bi),
                        "d2h_bytes_per_step": int(bo)}
     if rank == 0 and not args.no_cpu:
-        e, dt, sample = wl.cpu_sample(args.cpu_seconds)
-        line["cpu_baseline"] = {"value": round(e * wl.bytes_per_elem / dt / 1e9, 5),
-                                "unit": "GB/s", "cores": cores_used(), "kind": "oracle",
-                                "sample": sample, "gelem_per_s": round(e / dt / 1e9, 6)}
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -1386,20 +1656,27 @@ def kernel_source_hash(kernel: str | None = None) -> str:
     return h.hexdigest()[:16]
 
 
-def _committed_traffic(config: int, kernel: str):
-    """DRAM bytes (read + write) per launch of `kernel` from the committed ncu
-    summary (profiles/traffic.json), or None when absent or taken from other
-    sources of that kernel than the ones built now."""
-    p = os.path.join(ROOT, "profiles", "traffic.json")
+def _committed_counts(config: int, kernel: str, fname: str, key: str):
+    """A per-launch ncu figure of `kernel` on workload `config` from a
+    committed summary under profiles/ (traffic.json: DRAM bytes read + written;
+    inst.json: warp instructions per element), or None when absent or taken
+    from other sources of that kernel than the ones built now."""
+    p = os.path.join(ROOT, "profiles", fname)
     try:
         with open(p) as f:
             d = json.load(f)
         e = d.get("workloads", {}).get(str(config), {}).get(kernel)
         if not e or e.get("source_sha") != kernel_source_hash(kernel):
             return None
-        return float(e["bytes"])
+        return float(e[key])
     except Exception:
         return None
+
+
+def _wl_kw(wl) -> dict:
+    """The constructor options a workload's call_bpe reads."""
+    return {"fos": getattr(wl, "fos", 1), "cols": getattr(wl, "cols", None),
+            "target": getattr(wl, "target", 0)}
 
 
 if __name__ == "__main__":

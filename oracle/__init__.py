@@ -6,7 +6,9 @@ library never loads it and shares no code with it.
 
 The arithmetic lives in ``nvfp4_oracle.c`` (plain single-threaded C, fp32
 round-to-nearest, no contraction); this module only compiles it with gcc and
-marshals numpy arrays through ctypes.
+marshals numpy arrays through ctypes. A second build of the same source with
+OpenMP (``set_threads(n)``, n > 1) runs its independent loops on n host
+threads, only to time the oracle on all cores; it returns the same bytes.
 """
 from __future__ import annotations
 
@@ -20,8 +22,11 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "nvfp4_oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
+_LIB_OMP = os.path.join(_HERE, "liboracle_omp.so")
 _lock = threading.Lock()
 _lib = None
+_lib_omp = None
+_threads = 1
 
 ST_NONFINITE_INPUT = 1
 ST_BAD_SCALE = 2
@@ -30,24 +35,47 @@ ST_BAD_AMAX = 4
 CFLAGS = ["-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
 
 
+def _compile(out: str, extra: list) -> None:
+    tmp = out + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", *CFLAGS, *extra, _SRC, "-o", tmp, "-lm"], check=True)
+    os.replace(tmp, out)
+
+
 def build(force: bool = False) -> str:
-    """Compile the oracle into ``oracle/liboracle.so`` (skipped when up to date)."""
-    if (not force and os.path.exists(_LIB)
-            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
-        return _LIB
-    tmp = _LIB + f".tmp{os.getpid()}"
-    subprocess.run(["gcc", *CFLAGS, _SRC, "-o", tmp, "-lm"], check=True)
-    os.replace(tmp, _LIB)
+    """Compile the oracle into ``oracle/liboracle.so`` (one thread) and
+    ``oracle/liboracle_omp.so`` (the same source with OpenMP, used only to
+    time the oracle on all host cores); skipped when up to date."""
+    for out, extra in ((_LIB, []), (_LIB_OMP, ["-fopenmp"])):
+        if force or not os.path.exists(out) or os.path.getmtime(out) < os.path.getmtime(_SRC):
+            _compile(out, extra)
     return _LIB
 
 
+def set_threads(n: int) -> int:
+    """Run the following oracle calls on n host threads: 1 selects the
+    single-threaded build, more the OpenMP build of the same source. Returns
+    the thread count in use."""
+    global _threads
+    with _lock:
+        _threads = max(1, int(n))
+    return lib().orc_set_threads(_threads) if _threads > 1 else 1
+
+
+def threads() -> int:
+    return _threads
+
+
 def lib() -> C.CDLL:
-    global _lib
+    global _lib, _lib_omp
     with _lock:
         if _lib is None:
-            _lib = C.CDLL(build())
+            build()
+            _lib = C.CDLL(_LIB)
             _declare(_lib)
-    return _lib
+        if _threads > 1 and _lib_omp is None:
+            _lib_omp = C.CDLL(_LIB_OMP)
+            _declare(_lib_omp)
+        return _lib_omp if _threads > 1 else _lib
 
 
 _u8p = C.POINTER(C.c_uint8)
@@ -58,6 +86,8 @@ _i64 = C.c_int64
 
 
 def _declare(L):
+    L.orc_set_threads.restype = C.c_int
+    L.orc_set_threads.argtypes = [C.c_int]
     L.orc_bf16_to_f32.restype = C.c_float
     L.orc_bf16_to_f32.argtypes = [C.c_uint16]
     L.orc_f32_to_bf16.restype = C.c_uint16

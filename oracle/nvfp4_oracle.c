@@ -2,6 +2,14 @@
  * nvfp4_oracle.c -- plain, single-threaded CPU oracle for NVFP4 block-scaled
  * quantization of bf16 tensors and for the scale-learning STE backward.
  *
+ * The loops over independent blocks, rows or elements carry OpenMP pragmas.
+ * The default build ignores them and runs on one thread; a second build
+ * (-fopenmp) runs the same loops on all host cores, only to time the oracle
+ * as an all-core CPU baseline. Every parallel iteration writes outputs that
+ * no other iteration touches (4/6 bitmaps are built one 32-block word per
+ * iteration), and status bits are OR-reduced, so both builds give the same
+ * bytes.
+ *
  * TEST INFRASTRUCTURE. This file is the yardstick the CUDA library is checked
  * against; it is not part of the product. Only the tests, the smoke check and
  * the benchmark's CPU-baseline leg load it. It shares no source, header, table
@@ -65,11 +73,26 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 /* ---- status bits returned by the oracle (meaning mirrors the C-ABI) ----- */
 #define ORC_ST_NONFINITE_INPUT 1 /* a NaN or Inf element in x            */
 #define ORC_ST_BAD_SCALE 2       /* an STE scale that is not usable      */
 #define ORC_ST_BAD_AMAX 4        /* a global amax that is NaN/Inf/< 0    */
+
+/* Threads of the OpenMP build (n > 0 sets them); returns the count in use,
+ * 1 for the default build. */
+int orc_set_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+  return omp_get_max_threads();
+#else
+  (void)n;
+  return 1;
+#endif
+}
 
 /* ---------------------------------------------------------------- bits -- */
 static uint32_t f2u(float f) { uint32_t u; memcpy(&u, &f, 4); return u; }
@@ -356,7 +379,9 @@ static int encode_rows(const float* xs, int64_t S, int64_t Rm, int64_t Cm,
   int64_t B = Rm * Cm / 16, W = (B + 31) / 32;
   if (choice) memset(choice, 0, (size_t)(S * W) * sizeof(uint32_t));
   for (int64_t s = 0; s < S; ++s) {
-    for (int64_t b = 0; b < B; ++b) {
+#pragma omp parallel for schedule(static)
+    for (int64_t w = 0; w < W; ++w)
+    for (int64_t b = 32 * w; b < B && b < 32 * w + 32; ++b) {
       int64_t e0 = s * Rm * Cm + b * 16;
       uint8_t q[16], sc, ch;
       uint16_t d16[16];
@@ -381,6 +406,7 @@ int orc_global_amax(const uint16_t* x, int64_t S, int64_t n, float* amax) {
   int st = 0;
   for (int64_t s = 0; s < S; ++s) {
     uint16_t m = 0;
+#pragma omp parallel for schedule(static) reduction(max : m) reduction(| : st)
     for (int64_t i = 0; i < n; ++i) {
       uint16_t a = x[s * n + i] & 0x7FFFu;
       if (a >= 0x7F80u) st |= ORC_ST_NONFINITE_INPUT;
@@ -404,6 +430,7 @@ int orc_quantize(int blocks, int fmt, int rounding, int fos, int rule, float sca
   float* g = (float*)malloc((size_t)(S > 0 ? S : 1) * sizeof(float));
   float* xf = (float*)malloc((size_t)(N > 0 ? N : 1) * sizeof(float));
   for (int64_t s = 0; s < S; ++s) st |= global_decode_scale(gamax[s], M, &g[s]);
+#pragma omp parallel for schedule(static) reduction(| : st)
   for (int64_t i = 0; i < N; ++i) {
     if ((x[i] & 0x7FFFu) >= 0x7F80u) st |= ORC_ST_NONFINITE_INPUT;
     xf[i] = orc_bf16_to_f32(x[i]);
@@ -414,6 +441,7 @@ int orc_quantize(int blocks, int fmt, int rounding, int fos, int rule, float sca
   if (blocks & 2) {
     float* xt = (float*)malloc((size_t)(N > 0 ? N : 1) * sizeof(float));
     for (int64_t s = 0; s < S; ++s)
+#pragma omp parallel for schedule(static)
       for (int64_t r = 0; r < R; ++r)
         for (int64_t c = 0; c < C; ++c)
           xt[s * R * C + c * R + r] = xf[s * R * C + r * C + c];
@@ -440,6 +468,7 @@ int orc_fakequant_fwd(const uint16_t* x, int64_t R, int64_t C, const float* s_pr
                       const float* s_post, uint16_t* xq) {
   int st = 0;
   int64_t nb = R * C / 16;
+#pragma omp parallel for schedule(static) reduction(| : st)
   for (int64_t b = 0; b < nb; ++b) {
     float sp = s_pre[b], so = s_post ? s_post[b] : s_pre[b];
     if (!scale_ok(sp, so)) st |= ORC_ST_BAD_SCALE;
@@ -470,6 +499,7 @@ int orc_scale_grad_bwd(const uint16_t* x, const uint16_t* gq, int64_t R, int64_t
   int st = 0;
   int64_t nb = R * C / 16;
   int tied = (s_post == NULL);
+#pragma omp parallel for schedule(static) reduction(| : st)
   for (int64_t b = 0; b < nb; ++b) {
     float sp = s_pre[b], so = tied ? sp : s_post[b];
     if (!scale_ok(sp, so)) st |= ORC_ST_BAD_SCALE;
@@ -599,6 +629,7 @@ int orc_dequant(int fmt, float scale_max, int fos, const uint8_t* codes,
   for (int64_t s = 0; s < S; ++s) {
     float g;
     st |= global_decode_scale(gamax[s], M, &g);
+#pragma omp parallel for schedule(static) reduction(| : st)
     for (int64_t i = 0; i < R * C; ++i) {
       int64_t e = s * R * C + i;
       float d = orc_scale_value(fmt, scales[e / 16]) * g;
@@ -624,10 +655,12 @@ int orc_requant(int src_fmt, float src_scale_max, int src_fos, const uint8_t* co
   float* xt = (float*)malloc((size_t)(N > 0 ? N : 1) * sizeof(float));
   int st = orc_dequant(src_fmt, src_scale_max, src_fos, codes, scales, S, R, C, gamax, xh);
   for (int64_t s = 0; s < S; ++s)
+#pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < R; ++r)
       for (int64_t c = 0; c < C; ++c) xt[s * R * C + c * R + r] = xh[s * R * C + r * C + c];
   if (target == 0) {
     for (int64_t s = 0; s < S; ++s)
+#pragma omp parallel for schedule(static)
       for (int64_t c = 0; c < C; ++c) {
         int64_t e0 = s * C * R + c * R;
         orc_mx_encode(xt + e0, R, rounding, seed, step, 2, (uint64_t)e0, out_codes + e0,
@@ -757,6 +790,7 @@ int orc_scale_init_mse(const uint16_t* x, int64_t R, int64_t C, float gamax, uin
   fp8_unit u;
   int st = fp8_scale_unit(gamax, &u);
   int64_t nb = R * C / 16;
+#pragma omp parallel for schedule(dynamic, 64) reduction(| : st)
   for (int64_t b = 0; b < nb; ++b) {
     float xb[16];
     for (int i = 0; i < 16; ++i) {
@@ -788,6 +822,7 @@ int orc_export_scales(const uint16_t* x, int64_t R, int64_t C, const float* s_pr
   int st = fp8_scale_unit(gamax, &u);
   float* sp = q8_array(s_pre, nb, &u);
   st |= fp8_scale_status(s_pre, s_post, nb, sp);
+#pragma omp parallel for schedule(static) reduction(| : st)
   for (int64_t b = 0; b < nb; ++b) {
     float inv = 1.0f / sp[b];
     float so = s_post ? s_post[b] : s_pre[b];
@@ -828,6 +863,7 @@ int orc_quantize_tile16(int fmt, int rounding, float scale_max, uint32_t seed, u
   for (int64_t s = 0; s < S; ++s) {
     float g;
     st |= global_decode_scale(gamax[s], M, &g);
+#pragma omp parallel for schedule(static) reduction(| : st)
     for (int64_t tr = 0; tr < R / 16; ++tr)
       for (int64_t tc = 0; tc < C / 16; ++tc) {
         float amax = 0.0f;
@@ -859,8 +895,9 @@ int orc_quantize_tile16(int fmt, int rounding, float scale_max, uint32_t seed, u
   }
   /* the column encoding: the row encoding transposed */
   for (int64_t s = 0; s < S; ++s)
-    for (int64_t r = 0; r < R; ++r)
-      for (int64_t c = 0; c < C; ++c) {
+#pragma omp parallel for schedule(static)
+    for (int64_t c = 0; c < C; ++c)
+      for (int64_t r = 0; r < R; ++r) {
         int64_t e = s * R * C + r * C + c, t = s * R * C + c * R + r;
         if (c_codes) {
           uint8_t q = (e & 1) ? (r_codes[e / 2] >> 4) : (r_codes[e / 2] & 15);
@@ -891,12 +928,14 @@ int orc_mx_quantize(int blocks, int rounding, uint32_t seed, uint32_t step, cons
   int st = 0;
   int64_t N = S * R * C;
   float* xf = (float*)malloc((size_t)(N > 0 ? N : 1) * sizeof(float));
+#pragma omp parallel for schedule(static) reduction(| : st)
   for (int64_t i = 0; i < N; ++i) {
     if ((x[i] & 0x7FFFu) >= 0x7F80u) st |= ORC_ST_NONFINITE_INPUT;
     xf[i] = orc_bf16_to_f32(x[i]);
   }
   if (blocks & 1)
     for (int64_t s = 0; s < S; ++s)
+#pragma omp parallel for schedule(static)
       for (int64_t r = 0; r < R; ++r) {
         int64_t e0 = s * R * C + r * C;
         orc_mx_encode(xf + e0, C, rounding, seed, step, 0, (uint64_t)e0, r_codes + e0,
@@ -905,9 +944,11 @@ int orc_mx_quantize(int blocks, int rounding, uint32_t seed, uint32_t step, cons
   if (blocks & 2) {
     float* xt = (float*)malloc((size_t)(N > 0 ? N : 1) * sizeof(float));
     for (int64_t s = 0; s < S; ++s)
+#pragma omp parallel for schedule(static)
       for (int64_t r = 0; r < R; ++r)
         for (int64_t c = 0; c < C; ++c) xt[s * R * C + c * R + r] = xf[s * R * C + r * C + c];
     for (int64_t s = 0; s < S; ++s)
+#pragma omp parallel for schedule(static)
       for (int64_t c = 0; c < C; ++c) {
         int64_t e0 = s * C * R + c * R;
         orc_mx_encode(xt + e0, R, rounding, seed, step, 1, (uint64_t)e0, c_codes + e0,

@@ -50,6 +50,50 @@ def test_description_matches_the_built_workload(bench, config):
     args = types.SimpleNamespace(experts=64, sr_steps=32)
     wl = bench.WORKLOADS[config](torch.device("cuda"))
     assert wl.workload == bench.describe_workload(config, args)
+    # every call's bytes are its elements times the per-call table's figure
+    bpe = wl.call_bpe(bench._wl_kw(wl))
+    for kern in wl.kernels(0, 0):
+        assert kern.nbytes == pytest.approx(wl.elements * bpe[kern.name], rel=1e-12)
+    assert wl.bytes_per_elem == pytest.approx(sum(bpe.values()), rel=1e-12)
+
+
+@pytest.mark.parametrize("config", list(range(1, 13)))
+def test_reference_arm_charges_the_calls_it_runs(bench, config):
+    """Each reference-arm step names the calls it ran, and those calls are
+    the ones the CUDA arm's workload charges bytes for."""
+    args = types.SimpleNamespace(config=config, ref_rows=32, experts=64, sr_steps=32)
+    _, sample, step = bench._reference_sample(args)
+    bpe = bench.WORKLOADS[config].call_bpe(bench._ctor_args(config, args))
+    e, calls, dt = step(0)
+    assert e > 0 and dt > 0 and calls and set(calls) <= set(bpe), (calls, bpe)
+    if config == 4:  # periodic scaling: the amax runs on refresh steps only
+        assert "amax" not in step(1)[1]
+
+
+def test_reference_arm_counts_the_dequant(bench):
+    """The activation step writes the bf16 dequant: amax (2) + x (2) + codes
+    (1/2) + scales (1/16) + 4/6 bitmap (1/128) + dequant (2) bytes."""
+    args = types.SimpleNamespace(config=2, ref_rows=32, experts=64, sr_steps=32)
+    bpe = bench.WORKLOADS[2].call_bpe(bench._ctor_args(2, args))
+    _, _, step = bench._reference_sample(args)
+    calls = step(0)[1]
+    assert sum(bpe[c] for c in calls) == pytest.approx(2 + 2 + 0.5 + 1 / 16 + 1 / 128 + 2)
+
+
+def test_host_description(bench):
+    assert bench.host_cores() >= 1
+    assert isinstance(bench.cpu_model(), str) and bench.cpu_model()
+    t = bench.ClockSampler._when("2026/12/02 15:31:00.123")
+    assert t is not None and bench.ClockSampler._when("garbage") is None
+
+
+def test_default_workload_is_the_largest(bench):
+    """Without --config the benchmark times the MoE dual pass (the largest
+    workload that fits one GPU)."""
+    src = open(os.path.join(ROOT, "bench.py")).read()
+    assert '"--config", type=int, default=5' in src
+    args = types.SimpleNamespace(experts=64, sr_steps=32)
+    assert "64 x 2048x7168" in bench.describe_workload(5, args)
 
 
 def _free_port():
