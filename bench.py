@@ -152,8 +152,9 @@ def sweep_candidates_per_block(w_bits: np.ndarray, gamax: float) -> float:
 
 class Kernel:
     """One call of the C ABI, its algorithmic HBM bytes and the number of our
-    kernels it launches (a zeroing kernel precedes the atomic amax and the
-    OR-ed 4/6 bitmaps of the column, dual and re-quantisation kernels)."""
+    kernels it launches (a zeroing kernel precedes the OR-ed 4/6 bitmaps of
+    the column, dual and re-quantisation kernels; the global amax is one
+    launch, nvfp4_amax_ws)."""
 
     def __init__(self, name, nbytes, fn, launches=1):
         self.name, self.nbytes, self.fn, self.launches = name, nbytes, fn, launches
@@ -210,9 +211,12 @@ class Activation(Workload):
         st = torch.cuda.current_stream(device).cuda_stream
         R, Cc = self.rows, self.cols
 
+        ws = nv.amax_workspace(1, self.x[0].device)
+        self._ws = ws
+
         def amax(i):
-            return L.nvfp4_amax(self.x[i].data_ptr(), 1, R, Cc, self.amax[i].data_ptr(),
-                                self.status.data_ptr(), st)
+            return L.nvfp4_amax_ws(self.x[i].data_ptr(), 1, R, Cc, self.amax[i].data_ptr(),
+                                   ws.data_ptr(), ws.numel() * 4, self.status.data_ptr(), st)
 
         def quant(i):
             return L.nvfp4_quantize(C.byref(self._c), self.x[i].data_ptr(), 1, R, Cc,
@@ -221,7 +225,7 @@ class Activation(Workload):
         self._amax, self._quant = amax, quant
 
     def kernels(self, k, i):
-        return [Kernel("amax", self.a_bytes, lambda: self._amax(i), 2),
+        return [Kernel("amax", self.a_bytes, lambda: self._amax(i)),
                 Kernel("quantize_row", self.q_bytes, lambda: self._quant(i))]
 
     def e2e_io(self, k, i):
@@ -370,9 +374,12 @@ class DriftingGradient(Workload):
         self._cfgs = [nv.Config(scale_fmt=1, rounding=1, scale_max=448.0, seed=3, step=t).c()
                       for t in range(nsteps)]
 
+        ws = nv.amax_workspace(1, device)
+        self._ws = ws
+
         def amax(t):
-            return L.nvfp4_amax(self.x[t].data_ptr(), 1, rows, cols, self.amax.data_ptr(),
-                                self.status.data_ptr(), st)
+            return L.nvfp4_amax_ws(self.x[t].data_ptr(), 1, rows, cols, self.amax.data_ptr(),
+                                   ws.data_ptr(), ws.numel() * 4, self.status.data_ptr(), st)
 
         def quant(t):
             return L.nvfp4_quantize(C.byref(self._cfgs[t]), self.x[t].data_ptr(), 1, rows, cols,
@@ -390,7 +397,7 @@ class DriftingGradient(Workload):
         t = k % self.nsets
         ks = []
         if t % self.period == 0:
-            ks.append(Kernel("amax", self.a_bytes, lambda: self._amax(t), 2))
+            ks.append(Kernel("amax", self.a_bytes, lambda: self._amax(t)))
         ks.append(Kernel("quantize_row_sr", self.q_bytes, lambda: self._quant(t)))
         return ks
 
@@ -448,9 +455,12 @@ class MoeExperts(Workload):
         L = nv.lib()
         st = torch.cuda.current_stream(device).cuda_stream
 
+        ws = nv.amax_workspace(experts, device)
+        self._ws = ws
+
         def amax():
-            return L.nvfp4_amax(self.x.data_ptr(), experts, rows, cols, self.amax.data_ptr(),
-                                self.status.data_ptr(), st)
+            return L.nvfp4_amax_ws(self.x.data_ptr(), experts, rows, cols, self.amax.data_ptr(),
+                                   ws.data_ptr(), ws.numel() * 4, self.status.data_ptr(), st)
 
         def dual():
             return L.nvfp4_quantize(C.byref(self._c), self.x.data_ptr(), experts, rows, cols,
@@ -466,7 +476,7 @@ class MoeExperts(Workload):
         return {"amax": 2.0, "quantize_dual": 2 + 2 * (0.5 + 1 / 16 + 1 / 128 + 2)}
 
     def kernels(self, k, i):
-        return [Kernel("amax", self.a_bytes, self._amax, 2),
+        return [Kernel("amax", self.a_bytes, self._amax),
                 Kernel("quantize_dual", self.d_bytes, self._dual, 3)]
 
     def e2e_io(self, k, i):
@@ -800,9 +810,12 @@ class TileWeight(Workload):
         self._ro = [nv._out(o) for o in self.row]
         self._co = [nv._out(o) for o in self.col]
 
+        ws = nv.amax_workspace(1, device)
+        self._ws = ws
+
         def amax(i):
-            return L.nvfp4_amax(self.x[i].data_ptr(), 1, rows, cols, self.amax[i].data_ptr(),
-                                self.status.data_ptr(), st)
+            return L.nvfp4_amax_ws(self.x[i].data_ptr(), 1, rows, cols, self.amax[i].data_ptr(),
+                                   ws.data_ptr(), ws.numel() * 4, self.status.data_ptr(), st)
 
         def tile(i):
             return L.nvfp4_quantize(C.byref(self._c), self.x[i].data_ptr(), 1, rows, cols,
@@ -818,7 +831,7 @@ class TileWeight(Workload):
         return {"amax": 2.0, "quantize_tile16": 2 + 2 * (0.5 + 1 / 16 + 2)}
 
     def kernels(self, k, i):
-        return [Kernel("amax", self.a_bytes, lambda: self._amax(i), 2),
+        return [Kernel("amax", self.a_bytes, lambda: self._amax(i)),
                 Kernel("quantize_tile16", self.t_bytes, lambda: self._tile(i))]
 
     def e2e_io(self, k, i):

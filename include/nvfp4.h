@@ -35,6 +35,7 @@
 #ifndef NVFP4_H
 #define NVFP4_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #if defined(__GNUC__)
@@ -116,6 +117,28 @@ typedef struct {
  * Errors: NULL x/amax, negative sizes, misaligned x. */
 NVFP4_API nvfp4_status nvfp4_amax(const void* x, int64_t slices, int64_t rows, int64_t cols,
                         float* amax, int32_t* status, void* stream);
+
+/* Bytes of device workspace nvfp4_amax_ws needs for `slices` slices: two
+ * 32-bit words per slice (0 for slices <= 0). */
+NVFP4_API size_t nvfp4_amax_ws_bytes(int64_t slices);
+
+/* The global amax of nvfp4_amax (same passages, same result) in ONE kernel
+ * launch: nvfp4_amax zeroes amax[] with a kernel of its own before the
+ * reduction's atomic max; here every CTA folds its maximum into a workspace
+ * word and takes a ticket, and the CTA holding a slice's last ticket writes
+ * amax[s] and returns the slice's two words to zero. No CTA waits for another.
+ * x: bf16 [slices][rows][cols]; amax: fp32 [slices], overwritten.
+ * workspace: device memory owned by the caller, >= nvfp4_amax_ws_bytes(slices)
+ * bytes (ws_bytes), 4-byte aligned, ALL ZERO before its first use (e.g. one
+ * cudaMemsetAsync when it is allocated); every call leaves it zero again. A
+ * workspace serves one call at a time: calls that may run at the same time
+ * (other streams) need their own workspaces.
+ * Errors: those of nvfp4_amax; NVFP4_ERR_NULL for a NULL workspace,
+ * NVFP4_ERR_SHAPE for ws_bytes below nvfp4_amax_ws_bytes(slices),
+ * NVFP4_ERR_ALIGN for a misaligned workspace. */
+NVFP4_API nvfp4_status nvfp4_amax_ws(const void* x, int64_t slices, int64_t rows, int64_t cols,
+                                     float* amax, void* workspace, size_t ws_bytes,
+                                     int32_t* status, void* stream);
 
 /* NVFP4 quantisation of x: bf16 [slices][rows][cols] (End-to-End 4-Bit
  * Training, "Low-precision formats on Blackwell" and "Block-scaled backward

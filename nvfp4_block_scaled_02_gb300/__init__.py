@@ -13,6 +13,7 @@ library is not built or no CUDA device is present.
 from __future__ import annotations
 
 import ctypes as C
+import functools
 import os
 import threading
 from dataclasses import dataclass
@@ -101,6 +102,9 @@ def lib() -> C.CDLL:
                     "(python -m nvfp4_block_scaled_02_gb300.buildlib)")
             L = C.CDLL(LIB_PATH)
             L.nvfp4_amax.argtypes = [_vp, _i64, _i64, _i64, _vp, _vp, _vp]
+            L.nvfp4_amax_ws.argtypes = [_vp, _i64, _i64, _i64, _vp, _vp, C.c_size_t, _vp, _vp]
+            L.nvfp4_amax_ws_bytes.argtypes = [_i64]
+            L.nvfp4_amax_ws_bytes.restype = C.c_size_t
             L.nvfp4_quantize.argtypes = [C.POINTER(_Config), _vp, _i64, _i64, _i64, _vp,
                                          C.POINTER(_Out), C.POINTER(_Out), _vp, _vp]
             L.nvfp4_quantize_per_token.argtypes = [C.POINTER(_Config), _vp, _i64, _i64, _vp,
@@ -124,7 +128,7 @@ def lib() -> C.CDLL:
             L.nvfp4_sr_bits.argtypes = [_u32, _u32, _u32, C.c_uint64, _i64, _vp, _vp]
             L.nvfp4_status_string.restype = C.c_char_p
             L.nvfp4_status_string.argtypes = [C.c_int]
-            for name in ("nvfp4_amax", "nvfp4_quantize", "nvfp4_quantize_per_token",
+            for name in ("nvfp4_amax", "nvfp4_amax_ws", "nvfp4_quantize", "nvfp4_quantize_per_token",
                          "nvfp4_requant_transpose", "nvfp4_fakequant_fwd",
                          "nvfp4_fakequant_fwd_fp8scale", "nvfp4_scale_grad_bwd_fp8scale",
                          "nvfp4_scale_init_mse", "nvfp4_export_scales", "nvfp4_mx_quantize",
@@ -143,7 +147,25 @@ def _dev(t: torch.Tensor | None, name: str) -> int | None:
         raise ValueError(f"{name} must be a CUDA tensor (this library has no CPU path)")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name} is on {t.device} but the call runs on "
+                         f"cuda:{torch.cuda.current_device()}: every buffer of a call must "
+                         "be on one device")
     return t.data_ptr()
+
+
+def _on_input_device(fn):
+    """Run an entry point with the device of its first tensor argument
+    current: the library launches on the current CUDA device and sizes its
+    grids for that device's SM count."""
+    @functools.wraps(fn)
+    def wrapper(*args, **kwargs):
+        dev = next((a.device for a in args if isinstance(a, torch.Tensor)), None)
+        if dev is None or dev.type != "cuda":
+            return fn(*args, **kwargs)
+        with torch.cuda.device(dev):
+            return fn(*args, **kwargs)
+    return wrapper
 
 
 def _bf16(t: torch.Tensor, name: str) -> int:
@@ -200,6 +222,7 @@ def _shape3(x: torch.Tensor):
 
 # ---------------------------------------------------------------- entries --
 
+@_on_input_device
 def nvfp4_amax(x: torch.Tensor, amax: torch.Tensor | None = None,
                status: torch.Tensor | None = None) -> torch.Tensor:
     """Per-slice max |x| of a bf16 [rows, cols] or [slices, rows, cols] tensor."""
@@ -210,6 +233,29 @@ def nvfp4_amax(x: torch.Tensor, amax: torch.Tensor | None = None,
         amax = torch.empty(S, dtype=torch.float32, device=x.device)
     _check("nvfp4_amax", lib().nvfp4_amax(_bf16(x, "x"), S, R, Cc, _dev(amax, "amax"),
                                           _dev(status, "status"), _stream(x.device)))
+    return amax
+
+
+def amax_workspace(slices: int, device) -> torch.Tensor:
+    """A zeroed workspace for nvfp4_amax_ws (two 32-bit words per slice); every
+    call leaves it zero, so it is allocated and cleared once."""
+    return torch.zeros(max(2 * int(slices), 1), dtype=torch.int32, device=device)
+
+
+@_on_input_device
+def nvfp4_amax_ws(x: torch.Tensor, workspace: torch.Tensor, amax: torch.Tensor | None = None,
+                  status: torch.Tensor | None = None) -> torch.Tensor:
+    """nvfp4_amax in one kernel launch, with a caller-owned zeroed workspace
+    (amax_workspace) that serves one call at a time."""
+    S, R, Cc = _shape3(x)
+    _need(amax, "amax", S, "f32")
+    _need(status, "status", 1, "i32")
+    _need(workspace, "workspace", 2 * S, "i32")
+    if amax is None:
+        amax = torch.empty(S, dtype=torch.float32, device=x.device)
+    _check("nvfp4_amax_ws", lib().nvfp4_amax_ws(
+        _bf16(x, "x"), S, R, Cc, _dev(amax, "amax"), _dev(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _dev(status, "status"), _stream(x.device)))
     return amax
 
 
@@ -236,6 +282,7 @@ def _out(enc: dict | None) -> _Out | None:
                 _dev(enc.get("choice"), "choice"), _dev(enc.get("dequant"), "dequant"))
 
 
+@_on_input_device
 def nvfp4_quantize(x: torch.Tensor, global_amax: torch.Tensor, cfg: Config | None = None,
                    row: dict | None = None, col: dict | None = None,
                    status: torch.Tensor | None = None, dequant: bool = True) -> dict:
@@ -272,6 +319,7 @@ def nvfp4_quantize(x: torch.Tensor, global_amax: torch.Tensor, cfg: Config | Non
     return {"row": row if cfg.blocks & 1 else None, "col": col if cfg.blocks & 2 else None}
 
 
+@_on_input_device
 def nvfp4_quantize_per_token(x: torch.Tensor, cfg: Config | None = None, out: dict | None = None,
                              row_amax: torch.Tensor | None = None,
                              status: torch.Tensor | None = None, dequant: bool = True) -> dict:
@@ -311,6 +359,7 @@ def alloc_requant(slices: int, rows: int, cols: int, device, target: int,
     return alloc_encoding(slices, cols, rows, device, four_over_six, dequant=False)
 
 
+@_on_input_device
 def nvfp4_requant_transpose(codes: torch.Tensor, scales: torch.Tensor,
                             global_amax: torch.Tensor, src: Config | None = None,
                             dst: Config | None = None, target: int = TARGET_MXFP8,
@@ -362,6 +411,7 @@ def alloc_mx(slices: int, rows: int, cols: int, device) -> dict:
             "scales": torch.empty((slices, rows, cols // 32), dtype=torch.uint8, device=device)}
 
 
+@_on_input_device
 def nvfp4_mx_quantize(x: torch.Tensor, cfg: Config | None = None, row: dict | None = None,
                       col: dict | None = None, status: torch.Tensor | None = None) -> dict:
     """MXFP8-encode a bf16 tensor (E8M0 scale per 32 values, E4M3 elements):
@@ -390,6 +440,7 @@ def nvfp4_mx_quantize(x: torch.Tensor, cfg: Config | None = None, row: dict | No
     return {"row": row if cfg.blocks & 1 else None, "col": col if cfg.blocks & 2 else None}
 
 
+@_on_input_device
 def nvfp4_fakequant_fwd(x: torch.Tensor, s_pre: torch.Tensor, s_post: torch.Tensor | None = None,
                         out: torch.Tensor | None = None,
                         status: torch.Tensor | None = None) -> torch.Tensor:
@@ -406,6 +457,7 @@ def nvfp4_fakequant_fwd(x: torch.Tensor, s_pre: torch.Tensor, s_post: torch.Tens
     return out
 
 
+@_on_input_device
 def nvfp4_scale_grad_bwd(x: torch.Tensor, gq: torch.Tensor, s_pre: torch.Tensor,
                          s_post: torch.Tensor | None = None, want_gx: bool = True,
                          gx: torch.Tensor | None = None, gs_pre: torch.Tensor | None = None,
@@ -434,6 +486,7 @@ def nvfp4_scale_grad_bwd(x: torch.Tensor, gq: torch.Tensor, s_pre: torch.Tensor,
             "gs_post": gs_post if s_post is not None else None}
 
 
+@_on_input_device
 def nvfp4_fakequant_fwd_fp8scale(x: torch.Tensor, s_pre: torch.Tensor,
                                  s_post: torch.Tensor | None, global_amax: torch.Tensor,
                                  out: torch.Tensor | None = None,
@@ -454,6 +507,7 @@ def nvfp4_fakequant_fwd_fp8scale(x: torch.Tensor, s_pre: torch.Tensor,
     return out
 
 
+@_on_input_device
 def nvfp4_scale_grad_bwd_fp8scale(x: torch.Tensor, gq: torch.Tensor, s_pre: torch.Tensor,
                                   s_post: torch.Tensor | None, global_amax: torch.Tensor,
                                   want_gx: bool = True,
@@ -476,6 +530,7 @@ def nvfp4_scale_grad_bwd_fp8scale(x: torch.Tensor, gq: torch.Tensor, s_pre: torc
     return {"gx": gx, "gs_pre": gs_pre, "gs_post": gs_post}
 
 
+@_on_input_device
 def nvfp4_scale_init_mse(x: torch.Tensor, global_amax: torch.Tensor,
                          status: torch.Tensor | None = None) -> dict:
     """MSE scale setting over every E4M3 scale per 1x16 block: {"codes", "s"}."""
@@ -490,6 +545,7 @@ def nvfp4_scale_init_mse(x: torch.Tensor, global_amax: torch.Tensor,
     return {"codes": codes, "s": s}
 
 
+@_on_input_device
 def nvfp4_export_scales(x: torch.Tensor, s_pre: torch.Tensor, s_post: torch.Tensor | None,
                         global_amax: torch.Tensor, out: dict | None = None,
                         status: torch.Tensor | None = None) -> dict:
@@ -513,6 +569,7 @@ def nvfp4_export_scales(x: torch.Tensor, s_pre: torch.Tensor, s_post: torch.Tens
     return out
 
 
+@_on_input_device
 def nvfp4_codec_probe(op: int, inp: torch.Tensor, aux: torch.Tensor | None = None,
                       out: torch.Tensor | None = None) -> torch.Tensor:
     _need(inp, "in", inp.numel(), "f32")
@@ -529,9 +586,10 @@ def nvfp4_sr_bits(seed: int, step: int, direction: int, idx0: int, n: int,
                   device="cuda", out: torch.Tensor | None = None) -> torch.Tensor:
     _need(out, "out", n, "i32")
     out = torch.empty(n, dtype=torch.int32, device=device) if out is None else out
-    _check("nvfp4_sr_bits", lib().nvfp4_sr_bits(seed & 0xFFFFFFFF, step & 0xFFFFFFFF, direction,
-                                                idx0, n, _dev(out, "out"),
-                                                _stream(out.device)))
+    with torch.cuda.device(out.device):
+        _check("nvfp4_sr_bits", lib().nvfp4_sr_bits(seed & 0xFFFFFFFF, step & 0xFFFFFFFF,
+                                                    direction, idx0, n, _dev(out, "out"),
+                                                    _stream(out.device)))
     return out
 
 

@@ -5,8 +5,9 @@
 // Pure read stream: 128-bit loads, |x| as the integer bf16 pattern & 0x7FFF
 // (the ordering of non-negative floats is the ordering of their bits), packed
 // u16x2 max, a warp max (redux), a CTA max, and one atomicMax per CTA on the
-// fp32 bit pattern of the result. MAX is exact and order-free, so the result
-// does not depend on the schedule.
+// fp32 bit pattern of the result (after a zeroing kernel), or, with a
+// caller's workspace, one launch whose last CTA per slice writes the result.
+// MAX is exact and order-free, so the result does not depend on the schedule.
 #include "device.cuh"
 #include "launch.h"
 
@@ -17,11 +18,9 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kUnroll = 4;
 
-__global__ void __launch_bounds__(kThreads) amax_kernel(const uint16_t* __restrict__ x, int64_t n,
-                                                        uint32_t* amax_bits, int32_t* status) {
-  pdl_begin();
-  const int64_t s = blockIdx.y;
-  const uint16_t* base = x + s * n;
+// The CTA's part of one slice's max |x| as a bf16 bit pattern (in thread 0;
+// the other threads return garbage), from 128-bit streaming loads.
+__device__ __forceinline__ uint32_t cta_absmax(const uint16_t* __restrict__ base, int64_t n) {
   const int64_t head0 = ((16 - ((uintptr_t)base & 15)) & 15) / 2;
   const int64_t head = head0 < n ? head0 : n;
   const uint4* v = reinterpret_cast<const uint4*>(base + head);
@@ -49,10 +48,41 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const uint16_t* __restri
   __shared__ uint32_t wmax[kThreads / 32];
   if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0)
     for (int w = 1; w < kThreads / 32; ++w) m = max(m, wmax[w]);
+  return m;
+}
+
+__global__ void __launch_bounds__(kThreads) amax_kernel(const uint16_t* __restrict__ x, int64_t n,
+                                                        uint32_t* amax_bits, int32_t* status) {
+  pdl_begin();
+  const uint32_t m = cta_absmax(x + blockIdx.y * n, n);
+  if (threadIdx.x == 0) {
     if (m >= 0x7F80u) flag(status, NVFP4_DEV_NONFINITE_INPUT_BIT);
-    if (m) atomicMax(amax_bits + s, m << 16);
+    if (m) atomicMax(amax_bits + blockIdx.y, m << 16);
+  }
+}
+
+// The same in one launch, without a zeroed output: each CTA folds its maximum
+// into workspace word 2s with an atomic max, makes that visible, and takes a
+// ticket from word 2s + 1; the CTA holding the slice's last ticket reads the
+// maximum back (an atomic exchange, so it sees every other CTA's), writes
+// amax[s] and returns both words to zero for the next call. No CTA waits.
+__global__ void __launch_bounds__(kThreads) amax_ticket_kernel(const uint16_t* __restrict__ x,
+                                                               int64_t n, float* amax,
+                                                               uint32_t* ws, int32_t* status) {
+  pdl_begin();
+  const uint32_t m = cta_absmax(x + blockIdx.y * n, n);
+  if (threadIdx.x == 0) {
+    uint32_t* w = ws + 2 * blockIdx.y;
+    if (m >= 0x7F80u) flag(status, NVFP4_DEV_NONFINITE_INPUT_BIT);
+    if (m) atomicMax(w, m);
+    __threadfence();
+    if (atomicAdd(w + 1, 1u) == gridDim.x - 1) {
+      const uint32_t v = atomicExch(w, 0u);
+      atomicExch(w + 1, 0u);
+      amax[blockIdx.y] = __uint_as_float(v << 16);
+    }
   }
 }
 
@@ -74,16 +104,34 @@ cudaError_t launch_zero_words(uint32_t* p, int64_t n, cudaStream_t st) {
                     n);
 }
 
+// Grid of the amax kernels: CTAs per slice, enough to fill the GPU.
+static int64_t amax_ctas(int64_t S, int64_t n) {
+  const int64_t nvec = n / 8 + 1;
+  const int64_t want = (nvec + kThreads * kUnroll - 1) / (kThreads * kUnroll);
+  const int64_t cap = std::max<int64_t>(1, (int64_t)sm_count() * 8 / std::max<int64_t>(1, S));
+  return std::min(want, cap);
+}
+
+cudaError_t launch_amax_ticket(const uint16_t* x, int64_t S, int64_t n, float* amax,
+                               uint32_t* ws, int32_t* status, cudaStream_t st) {
+  const int64_t ctas = amax_ctas(S, n);
+  for (int64_t s0 = 0; s0 < S; s0 += 65535) {
+    dim3 grid((unsigned)ctas, (unsigned)std::min<int64_t>(S - s0, 65535));
+    const cudaError_t e = launch_pdl(amax_ticket_kernel, grid, dim3(kThreads), st, x + s0 * n, n,
+                                     amax + s0, ws + 2 * s0, status);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
 cudaError_t launch_amax(const uint16_t* x, int64_t S, int64_t n, float* amax, int32_t* status,
                         cudaStream_t st) {
   cudaError_t e = launch_zero_words(reinterpret_cast<uint32_t*>(amax), S, st);  // for the atomic max
   if (e != cudaSuccess) return e;
   if (n == 0) return cudaSuccess;
-  const int64_t nvec = n / 8 + 1;
-  const int64_t want = (nvec + kThreads * kUnroll - 1) / (kThreads * kUnroll);
-  const int64_t cap = std::max<int64_t>(1, (int64_t)sm_count() * 8 / std::max<int64_t>(1, S));
+  const int64_t ctas = amax_ctas(S, n);
   for (int64_t s0 = 0; s0 < S; s0 += 65535) {
-    dim3 grid((unsigned)std::min(want, cap), (unsigned)std::min<int64_t>(S - s0, 65535));
+    dim3 grid((unsigned)ctas, (unsigned)std::min<int64_t>(S - s0, 65535));
     e = launch_pdl(amax_kernel, grid, dim3(kThreads), st, x + s0 * n, n,
                    reinterpret_cast<uint32_t*>(amax + s0), status);
     if (e != cudaSuccess) return e;

@@ -109,6 +109,25 @@ nvfp4_status nvfp4_amax(const void* x, int64_t slices, int64_t rows, int64_t col
                                         status, static_cast<cudaStream_t>(stream)));
 }
 
+size_t nvfp4_amax_ws_bytes(int64_t slices) {
+  return slices > 0 ? (size_t)slices * 2 * sizeof(uint32_t) : 0;
+}
+
+nvfp4_status nvfp4_amax_ws(const void* x, int64_t slices, int64_t rows, int64_t cols, float* amax,
+                           void* workspace, size_t ws_bytes, int32_t* status, void* stream) {
+  if (slices < 0 || rows < 0 || cols < 0) return NVFP4_ERR_SHAPE;
+  if (slices == 0) return NVFP4_OK;
+  if (!amax || !workspace) return NVFP4_ERR_NULL;
+  if (rows * cols != 0 && !x) return NVFP4_ERR_NULL;
+  if (ws_bytes < nvfp4_amax_ws_bytes(slices)) return NVFP4_ERR_SHAPE;
+  if (!aligned(x, 16) || !aligned(amax, 4) || !aligned(workspace, 4) || !aligned(status, 4))
+    return NVFP4_ERR_ALIGN;
+  return cuda_status(nvfp4::launch_amax_ticket(static_cast<const uint16_t*>(x), slices,
+                                               rows * cols, amax,
+                                               static_cast<uint32_t*>(workspace), status,
+                                               static_cast<cudaStream_t>(stream)));
+}
+
 nvfp4_status nvfp4_quantize(const nvfp4_config* cfg, const void* x, int64_t slices, int64_t rows,
                             int64_t cols, const float* global_amax, const nvfp4_out* row,
                             const nvfp4_out* col, int32_t* status, void* stream) {

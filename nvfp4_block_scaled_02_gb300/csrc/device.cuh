@@ -293,6 +293,13 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
 }
+// The same with the source byte count given: 0 writes 16 zero bytes and reads
+// nothing (a tile chunk past the tensor's edge).
+__device__ __forceinline__ void cp_async16_zfill(void* smem, const void* gmem, uint32_t bytes) {
+  const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(s), "l"(gmem), "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
@@ -311,6 +318,20 @@ __device__ __forceinline__ void cp_async_wait() {
 __device__ __forceinline__ void pdl_begin() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ------------------------------------------------ division by a constant --
+// n / d for 32-bit unsigned n and a divisor fixed at launch, by the
+// multiply-high method of Granlund and Montgomery ("Division by invariant
+// integers using multiplication", PLDI 1994, figure 4.1): with
+// l = ceil(log2 d) and m = floor(2^32 (2^l - d) / d) + 1,
+// t = mulhi(m, n), n / d = (t + ((n - t) >> min(l, 1))) >> max(l - 1, 0).
+struct FastDiv {
+  uint32_t m, s1, s2;
+};
+__device__ __forceinline__ uint32_t fastdiv(uint32_t n, const FastDiv& f) {
+  const uint32_t t = __umulhi(n, f.m);
+  return (t + ((n - t) >> f.s1)) >> f.s2;
 }
 
 // ---------------------------------------------------------- status word ---

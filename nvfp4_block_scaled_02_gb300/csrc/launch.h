@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/nvfp4.h"
+#include "device.cuh"
 
 #define NVFP4_DEV_NONFINITE_INPUT_BIT NVFP4_DEV_NONFINITE_INPUT
 #define NVFP4_DEV_BAD_SCALE_BIT NVFP4_DEV_BAD_SCALE
@@ -14,6 +15,17 @@
 namespace nvfp4 {
 
 int sm_count();
+
+// Host side of FastDiv (device.cuh): the constants for divisor d >= 1.
+inline FastDiv make_fastdiv(uint32_t d) {
+  uint32_t l = 0;
+  while ((1ull << l) < d) ++l;
+  FastDiv f;
+  f.m = (uint32_t)(((1ull << 32) * ((1ull << l) - d)) / d + 1);
+  f.s1 = l < 1 ? l : 1;
+  f.s2 = l > 0 ? l - 1 : 0;
+  return f;
+}
 
 // CTAs of `kernel` (with `threads` threads and `smem` dynamic shared memory)
 // that fit on one SM at once, at least 1: sizes persistent grids to a single
@@ -147,6 +159,10 @@ cudaError_t launch_zero_words(uint32_t* p, int64_t n, cudaStream_t st);
 // Per-slice global amax.
 cudaError_t launch_amax(const uint16_t* x, int64_t S, int64_t n, float* amax, int32_t* status,
                         cudaStream_t st);
+// The same in one launch with a workspace of 2 words per slice (zero before,
+// zero after).
+cudaError_t launch_amax_ticket(const uint16_t* x, int64_t S, int64_t n, float* amax,
+                               uint32_t* ws, int32_t* status, cudaStream_t st);
 
 // Scale-learning fake quantisation and STE backward (row blocks).
 struct SteParams {

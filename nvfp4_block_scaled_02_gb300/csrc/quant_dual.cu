@@ -4,23 +4,23 @@
 // operand groups each value with the 15 values above/below it instead).
 //
 // One CTA (256 threads) per 64 x 128 tile of one slice:
-//  1. every thread loads 4 chunks of 8 bf16 (128-bit loads, a warp covers two
-//     full 256 B tile rows) and, in BOTH mode, encodes the row blocks straight
-//     from registers (lane pairs hold the two halves of a block);
-//  2. the chunks go to a 16 KiB shared tile of 32-bit words (two columns
-//     each), word w of row r stored at w ^ (((r >> 4) & 3) << 3);
+//  1. every thread loads 4 chunks of 8 bf16 (128-bit loads; a warp covers two
+//     full 256 B tile rows) and stores them into a 16 KiB shared tile of
+//     32-bit words (two columns each), word w of row r kept at
+//     w ^ (((r >> 4) & 3) << 3);
+//  2. in BOTH mode the row blocks are encoded straight from the registers,
+//     lanes 2m and 2m+1 holding the two halves of a block (encode_half8);
 //  3. lane (cp, q) = (lane >> 2, lane & 3) of warp w takes column pair
-//     8w + cp in the 16-row band q: it reads one word per row (with the
+//     8 w + cp in the 16-row band q: it reads one word per row (with the
 //     swizzle the 32 lanes hit 32 distinct banks) and encodes the two column
-//     blocks it now holds.
-// Column outputs are the row encoding of X^T. The four bands of a column sit
-// in four adjacent lanes, so each column's 64 rows go out contiguously from
-// one store instruction: 32 code bytes, 4 scale bytes, 128 B of dequant (two
-// instructions). Scattering a column's bands over four warps instead costs
-// several partial-sector writes per sector.
-// 4/6 bits are gathered per tile row (a ballot) and per column (a ballot over
-// the four band lanes) and OR-ed into the (pre-zeroed) bitmaps, since a
-// tile's bits share words with other tiles.
+//     blocks it now holds, one lane per block (encode_block). The four bands
+//     of a column are adjacent lanes, so each column's 64 rows of codes
+//     (32 B), scales (4 B) and dequant (128 B, two instructions) leave from
+//     one store instruction.
+// The 4/6 bits of the tile are gathered in shared memory (one ballot per warp
+// and half-block) and OR-ed into the pre-zeroed bitmaps once per tile: a
+// tile's bits share words with other tiles. Non-finite inputs are gathered
+// per thread and flagged once.
 #include "encode.cuh"
 #include "launch.h"
 
@@ -31,13 +31,14 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int TR = 64;    // tile rows
 constexpr int TC = 128;   // tile columns
-constexpr int kChunksPerRow = TC / 8;
 constexpr int kWords = TC / 2;  // 32-bit words (column pairs) per tile row
 
 __device__ __forceinline__ int word_of(int r, int w) {
   return r * kWords + (w ^ (((r >> 4) & 3) << 3));
 }
 
+// OR `nbits` bits into a bitmap at bit position bit0 (they may straddle two
+// words).
 __device__ __forceinline__ void or_bits(uint32_t* words, int64_t bit0, uint32_t bits, int nbits) {
   if (bits == 0) return;
   const int64_t w = bit0 >> 5;
@@ -46,163 +47,284 @@ __device__ __forceinline__ void or_bits(uint32_t* words, int64_t bit0, uint32_t 
   if (off + nbits > 32) atomicOr(words + w + 1, bits >> (32 - off));
 }
 
-__device__ __forceinline__ uint32_t even_bits8(uint32_t b) {  // lanes 0,2,..,14 -> 8 bits
-  b &= 0x5555u;
-  b = (b | (b >> 1)) & 0x3333u;
-  b = (b | (b >> 2)) & 0x0F0Fu;
-  b = (b | (b >> 4)) & 0x00FFu;
-  return b;
+// The bits at even positions 0, 2, .., 2n-2 of b, packed into n bits.
+__device__ __forceinline__ uint32_t even_bits(uint32_t b) {
+  b &= 0x55555555u;
+  b = (b | (b >> 1)) & 0x33333333u;
+  b = (b | (b >> 2)) & 0x0F0F0F0Fu;
+  b = (b | (b >> 4)) & 0x00FF00FFu;
+  return (b | (b >> 8)) & 0x0000FFFFu;
 }
 
+// Block amax as bf16 bits from the magnitude maximum m of this lane's half
+// (both halves of m) and of its partner's.
+__device__ __forceinline__ uint32_t pair_amax(uint32_t m) {
+  m = bmax_abs2(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+  return m;
+}
+
+// Launch geometry, computed once on the host. Tiles are numbered slice by
+// slice, row of tiles by row of tiles, and CTA b takes the kTilesPerCta
+// consecutive tiles from b * kTilesPerCta: while it encodes one the next one
+// loads, and since CTAs start in order as earlier ones finish, the tiles in
+// flight stay a compact run of neighbours whose rows share DRAM pages. (One
+// CTA per SM slot looping over the whole tensor lets the CTAs drift apart,
+// and the spread of the tiles in flight slows DRAM down as the tensor grows.)
+constexpr uint32_t kTilesPerCta = 8;
+struct DualGeom {
+  FastDiv by_tiles_c, by_tiles_slice;
+  uint32_t tiles_c, tiles_slice;
+  uint32_t n_tiles;
+  int64_t slice_elems;   // R * C
+  int64_t words;         // 4/6 bitmap words per slice
+};
+
 template <int FMT, bool SR, int FOS, bool ROWS>
-__global__ void __launch_bounds__(kThreads) quant_dual_kernel(const DualParams p, int64_t tiles_r,
-                                                              int64_t tiles_c) {
+__global__ void __launch_bounds__(kThreads, SR ? (FOS != 0 ? 2 : 3) : (FOS == 2 ? 3 : 4))
+    quant_dual_kernel(const DualParams p, const DualGeom geo) {
   pdl_begin();
-  __shared__ __align__(16) uint32_t tile[TR * kWords];
-  __shared__ float s_d[256], s_inv[256];
+  __shared__ __align__(16) uint32_t tile[2][TR * kWords];
+  __shared__ float2 s_tab[2][256];  // block-scale table of the tile in each buffer
+  __shared__ float s_rden[2][2];    // its 1 / (6 g), 1 / (4 g)
+  // 4/6 bits of the tile in each buffer: row ballots (one word per two tile
+  // rows) and column ballots (one word per warp and column parity)
+  __shared__ uint32_t s_rbits[2][TR / 2], s_cbits[2][16];
 
   const int64_t R = p.R, C = p.C;
-  const int64_t bid = blockIdx.x;
-  const int64_t tc = bid % tiles_c;
-  const int64_t tr = (bid / tiles_c) % tiles_r;
-  const int64_t s = bid / (tiles_c * tiles_r);
-  const int64_t r0 = tr * TR, c0 = tc * TC;
-  const int64_t slice_elems = R * C;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-
-  const SliceScale ss = slice_scale(p.gamax[s], p.M);
-  if (ss.bad && threadIdx.x == 0 && tr == 0 && tc == 0) flag(p.status, NVFP4_DEV_BAD_AMAX_BIT);
-  build_scale_table<FMT>(s_d, s_inv, ss.g);
-
-  // ---- 1 + 2: load, row-encode, stage ------------------------------------
-  const uint16_t* xs = p.x + s * slice_elems;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int rule = FOS == 2 ? p.rule : 0;
   const bool vec = (C % 8) == 0;
-  uint4 v[4];
-  bool ok[4];
+  const int lr0 = t >> 4, lq = t & 15;  // thread t's chunks: rows 16 k + lr0, columns 8 lq ..
+  constexpr int kTab = FMT == 0 ? 128 : 256;
+
+  // Where tile T lies.
+  struct Where {
+    int64_t s, r0, c0;
+    int nr, nc;
+    bool first;  // the slice's first tile
+  };
+  auto where = [&](uint32_t T) {
+    Where w;
+    const uint32_t s = fastdiv(T, geo.by_tiles_slice), u = T - s * geo.tiles_slice;
+    const uint32_t tr = fastdiv(u, geo.by_tiles_c), tc = u - tr * geo.tiles_c;
+    w.s = s;
+    w.r0 = (int64_t)tr * TR;
+    w.c0 = (int64_t)tc * TC;
+    w.nr = (int)(R - w.r0 < TR ? R - w.r0 : TR);
+    w.nc = (int)(C - w.c0 < TC ? C - w.c0 : TC);
+    w.first = u == 0;
+    return w;
+  };
+  // Copy tile `at` into buffer `buf` (one 16-byte cp.async per chunk; chunks
+  // past the tensor's edge are zero-filled).
+  auto fetch = [&](const Where& at, int buf) {
+    const uint16_t* xt = p.x + at.s * geo.slice_elems + at.r0 * C + at.c0;
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int chunk = k * kThreads + threadIdx.x;
-    const int lr = chunk / kChunksPerRow, lc = (chunk % kChunksPerRow) * 8;
-    const int64_t r = r0 + lr, c = c0 + lc;
-    ok[k] = r < R && c < C;
-    v[k] = make_uint4(0, 0, 0, 0);
-    if (ok[k]) {
+    for (int k = 0; k < 4; ++k) {
+      const int lr = 16 * k + lr0, lc = 8 * lq;
+      const bool ok = lr < at.nr && lc < at.nc;
+      uint32_t* dst = &tile[buf][word_of(lr, 4 * lq)];
+      const uint16_t* src = xt + (int64_t)lr * C + lc;
       if (vec) {
-        v[k] = __ldcs(reinterpret_cast<const uint4*>(xs + r * C + c));
+        cp_async16_zfill(dst, ok ? src : p.x, ok ? 16u : 0u);
       } else {  // column-only encoding of a tensor whose rows are not 16 B multiples
         uint32_t h[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) h[i] = (c + i < C) ? xs[r * C + c + i] : 0u;
-        v[k] = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
-                          h[6] | (h[7] << 16));
+        for (int i = 0; i < 8; ++i) h[i] = (ok && lc + i < at.nc) ? src[i] : 0u;
+        *reinterpret_cast<uint4*>(dst) = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16),
+                                                    h[4] | (h[5] << 16), h[6] | (h[7] << 16));
       }
     }
-  }
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int chunk = k * kThreads + threadIdx.x;
-    const int lr = chunk / kChunksPerRow, lw = (chunk % kChunksPerRow) * 4;
-    *reinterpret_cast<uint4*>(&tile[word_of(lr, lw)]) = v[k];
-  }
-  __syncthreads();  // tables and tile ready
-
-  if constexpr (ROWS) {
-    const bool want_dq = p.r_dq != nullptr;
-    const int64_t Bs = slice_elems / 16, W = (Bs + 31) / 32;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int chunk = k * kThreads + threadIdx.x;
-      const int lr = chunk / kChunksPerRow, lc = (chunk % kChunksPerRow) * 8;
-      const int64_t r = r0 + lr, c = c0 + lc;
-      f2 x[4];
-      unpack8(v[k], x);
-      uint32_t m = absmax_bits4(v[k]);
-      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-      if (ok[k] && m >= 0x7F80u) flag(p.status, NVFP4_DEV_NONFINITE_INPUT_BIT);
-      const int64_t e = s * slice_elems + r * C + c;  // flat row-layout index
-      uint4 rb = make_uint4(0, 0, 0, 0);
-      if constexpr (SR) rb = sr_group_bits(p.seed, p.step, 0u, (uint64_t)e);
-      const HalfResult hr = encode_half<FMT, SR, FOS != 0>(x, m, ss, s_d, s_inv, rb, want_dq,
-                                                              FOS == 2 ? p.rule : 0);
-      if (ok[k]) {
-        reinterpret_cast<uint32_t*>(p.r_codes)[e / 8] = hr.codes;
-        if (want_dq) __stcs(reinterpret_cast<uint4*>(p.r_dq + e), hr.dq);
-        if ((lane & 1) == 0) p.r_scales[e / 16] = (uint8_t)hr.scale;
-      }
-      if constexpr (FOS) {
-        const uint32_t b = __ballot_sync(0xFFFFFFFFu, ok[k] && hr.pick4);
-        if ((lane & 15) == 0 && ok[k]) {
-          const uint32_t bits = even_bits8(b >> (lane & 16));
-          const int64_t blk = (r * C + c) / 16;  // block index within the slice
-          const int64_t nb = (C - c) / 16 < 8 ? (C - c) / 16 : 8;
-          or_bits(p.r_choice + s * W, blk, bits, (int)nb);
-        }
+    cp_async_commit();
+  };
+  // The scale table and outer-scale reciprocals of a slice with global amax
+  // gamax into buffer `buf` (threads 0..kTab-1; thread 0 also flags a bad
+  // amax, once per slice).
+  auto tables = [&](float gamax, bool first, int buf) {
+    if (t < kTab) {
+      const SliceScale ss = slice_scale(gamax, p.M);
+      float d, inv;
+      scale_entry<FMT>((uint32_t)t, ss.g, d, inv);
+      s_tab[buf][t] = make_float2(d, inv);
+      if (t == 0) {
+        s_rden[buf][0] = ss.rden6;
+        s_rden[buf][1] = ss.rden4;
+        if (ss.bad && first) flag(p.status, NVFP4_DEV_BAD_AMAX_BIT);
       }
     }
-  }
+  };
 
-  // ---- 3: column blocks ---------------------------------------------------
-  {
-    const bool want_dq = p.c_dq != nullptr;
-    const int q = lane & 3, cpl = warp * 8 + (lane >> 2);  // band, column pair
-    const int64_t c = c0 + 2 * cpl, r = r0 + 16 * q;
-    uint32_t w[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) w[i] = tile[word_of(16 * q + i, cpl)];
-    uint32_t mm = 0;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) mm = __vmaxu2(mm, w[i] & 0x7FFF7FFFu);
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {  // column c + j
-      const uint32_t m = j ? (mm >> 16) : (mm & 0xFFFFu);
-      f2 lo[4], hi[4];
+  // Thread offsets within a tile, in units of 8 (rows) or 16 (columns) values.
+  const int64_t R16 = R >> 4;
+  const int64_t ro0 = (int64_t)lr0 * (C >> 3) + lq;  // row chunk k: ro0 + 2 C k
+  const int cq = lane & 3, cpl = 8 * warp + (lane >> 2);  // column band, column pair
+  const int64_t co0 = (int64_t)(2 * cpl) * R16 + cq;   // column 2 cpl + j: co0 + j R16
+
+  // OR the 4/6 bits a finished tile left in s_[rc]bits[buf] into the bitmaps
+  // (rows by threads 0..63, columns by threads 128..255): tile rows' blocks
+  // are 8 consecutive bits, tile columns' bands 4.
+  auto flush = [&](int buf, const Where& at) {
+    if (ROWS && t < at.nr) {
+      const int nb = at.nc / 16;
+      const uint32_t bits = even_bits(s_rbits[buf][t >> 1] >> (16 * (t & 1))) & 0xFFu;
+      or_bits(p.r_choice + at.s * geo.words, (at.r0 + t) * (C >> 4) + (at.c0 >> 4),
+              bits & ((1u << nb) - 1u), nb);
+    }
+    if (t >= 128 && t - 128 < at.nc) {
+      const int cc = t - 128, cp = cc >> 1, nb = at.nr / 16;
+      const uint32_t bits = (s_cbits[buf][(cc & 1) * 8 + (cp >> 3)] >> (4 * (cp & 7))) & 0xFu;
+      or_bits(p.c_choice + at.s * geo.words, (at.c0 + cc) * R16 + (at.r0 >> 4),
+              bits & ((1u << nb) - 1u), nb);
+    }
+  };
+
+  const uint32_t T0 = blockIdx.x * kTilesPerCta;
+  const uint32_t T1 = T0 + kTilesPerCta < geo.n_tiles ? T0 + kTilesPerCta : geo.n_tiles;
+  Where cur = where(T0), prev = cur;
+  fetch(cur, 0);
+  tables(t < kTab ? p.gamax[cur.s] : 0.0f, cur.first, 0);
+  uint32_t seen = 0;  // magnitude maximum of every value this thread encodes
+  int buf = 0;
+  for (uint32_t T = T0; T < T1; ++T, buf ^= 1) {
+    cp_async_wait<0>();  // this thread's copies of tile T have landed
+    __syncthreads();     // everyone's have, and its tables are built; the
+                         // previous tile is done with the other buffers
+    const bool more = T + 1 < T1;
+    const Where nx = more ? where(T + 1) : cur;
+    if (more) fetch(nx, buf ^ 1);  // in flight while this tile is encoded
+    const bool new_slice = more && nx.s != cur.s;
+    const float gam_next = new_slice && t < kTab ? p.gamax[nx.s] : 0.0f;
+    if (FOS != 0 && T != T0) flush(buf ^ 1, prev);
+    SliceScale ss;
+    ss.rden6 = s_rden[buf][0];
+    ss.rden4 = s_rden[buf][1];
+    const float2* tab = s_tab[buf];
+    const int64_t s = cur.s, r0 = cur.r0, c0 = cur.c0;
+    const int nr = cur.nr, nc = cur.nc;
+    const int64_t slice0 = s * geo.slice_elems;
+    const uint32_t* tl = tile[buf];
+    // ---- row blocks: chunks from the staged tile ----------------------------
+    if constexpr (ROWS) {
+      const bool want_dq = p.r_dq != nullptr;
+      const int64_t tile0 = slice0 + r0 * C + c0;  // row-layout index of the tile origin
+      uint32_t* rcodes = reinterpret_cast<uint32_t*>(p.r_codes) + (tile0 >> 3);
+      uint4* rdq = reinterpret_cast<uint4*>(p.r_dq + tile0);
+      uint8_t* rscales = p.r_scales + (tile0 >> 4);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        lo[k] = j ? make_float2(bf16_hi(w[2 * k]), bf16_hi(w[2 * k + 1]))
-                  : make_float2(bf16_lo(w[2 * k]), bf16_lo(w[2 * k + 1]));
-        hi[k] = j ? make_float2(bf16_hi(w[8 + 2 * k]), bf16_hi(w[9 + 2 * k]))
-                  : make_float2(bf16_lo(w[8 + 2 * k]), bf16_lo(w[9 + 2 * k]));
-      }
-      const bool okc = c + j < C && r < R;
-      if (okc && m >= 0x7F80u) flag(p.status, NVFP4_DEV_NONFINITE_INPUT_BIT);
-      const int64_t e = s * slice_elems + (c + j) * R + r;  // flat column-layout index
-      uint4 rb0 = make_uint4(0, 0, 0, 0), rb1 = rb0;
-      if constexpr (SR) {
-        rb0 = sr_group_bits(p.seed, p.step, 1u, (uint64_t)e);
-        rb1 = sr_group_bits(p.seed, p.step, 1u, (uint64_t)e + 8);
-      }
-      const BlockResult br =
-          encode_block<FMT, SR, FOS != 0>(lo, hi, m, ss, TableScales{s_d, s_inv}, rb0, rb1,
-                                          want_dq, FOS == 2 ? p.rule : 0);
-      if (okc) {
-        *reinterpret_cast<uint2*>(p.c_codes + e / 2) = make_uint2(br.codes[0], br.codes[1]);
-        p.c_scales[e / 16] = (uint8_t)br.scale;
-        if (want_dq) {
-          __stcs(reinterpret_cast<uint4*>(p.c_dq + e), br.dq[0]);
-          __stcs(reinterpret_cast<uint4*>(p.c_dq + e) + 1, br.dq[1]);
+        const int lr = 16 * k + lr0;
+        const bool ok = lr < nr && 8 * lq < nc;
+        const int64_t o = ro0 + k * (2 * C);
+        const uint4 v = *reinterpret_cast<const uint4*>(&tl[word_of(lr, 4 * lq)]);
+        const uint32_t m = pair_amax(bmax_abs2(bmax_abs2(v.x, v.y), bmax_abs2(v.z, v.w)));
+        seen = bmax_abs2(seen, m);
+        const uint32_t amax_bits = max(m & 0x7FFFu, (m >> 16) & 0x7FFFu);
+        f2 x[4];
+        unpack8(v, x);
+        uint4 rb = make_uint4(0, 0, 0, 0);
+        if constexpr (SR) rb = sr_group_bits(p.seed, p.step, 0u, (uint64_t)(tile0 + 8 * o));
+        const HalfOut h = encode_half8<FMT, SR, FOS>(x, amax_bits, ss, tab, rb, want_dq, rule);
+        if (ok) {
+          rcodes[o] = h.codes;
+          if (want_dq) __stcs(rdq + o, h.dq);
+          if ((lane & 1) == 0) rscales[o >> 1] = (uint8_t)h.scale;
         }
-      }
-      if constexpr (FOS) {
-        // bands 0..3 of this column are lanes 4cp .. 4cp+3: its 4 bits
-        const uint32_t b = __ballot_sync(0xFFFFFFFFu, okc && br.pick4);
-        if (q == 0 && c + j < C) {
-          const int64_t Bs = slice_elems / 16, W = (Bs + 31) / 32;
-          const int64_t nb = (R - r0) / 16 < 4 ? (R - r0) / 16 : 4;
-          or_bits(p.c_choice + s * W, (c + j) * (R / 16) + r0 / 16, (b >> (lane & ~3)) & 15u,
-                  (int)nb);
+        if constexpr (FOS != 0) {
+          // lanes 0..15: tile row lr (even), lanes 16..31: row lr + 1
+          const uint32_t bb = __ballot_sync(0xFFFFFFFFu, ok && h.pick4);
+          if (lane == 0) s_rbits[buf][lr >> 1] = bb;
         }
       }
     }
+
+    // ---- column blocks ----------------------------------------------------------
+    {
+      const bool want_dq = p.c_dq != nullptr;
+      const int q = cq;
+      const bool rows_ok = 16 * q < nr;
+      const int64_t tile0 = slice0 + c0 * R + r0;  // column-layout index of the tile origin
+      uint2* ccodes = reinterpret_cast<uint2*>(p.c_codes) + (tile0 >> 4);
+      uint4* cdq = reinterpret_cast<uint4*>(p.c_dq + tile0);
+      uint8_t* cscales = p.c_scales + (tile0 >> 4);
+      uint32_t w[16];
+#pragma unroll
+      for (int i2 = 0; i2 < 16; ++i2) w[i2] = tl[word_of(16 * q + i2, cpl)];
+      uint32_t m = 0;
+#pragma unroll
+      for (int i2 = 0; i2 < 16; ++i2) m = bmax_abs2(m, w[i2]);  // both columns' block amax
+      seen = bmax_abs2(seen, m);
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {  // column 2 cpl + j
+        const bool okc = 2 * cpl + j < nc && rows_ok;
+        const int64_t o = co0 + j * R16;
+        f2 lo[4], hi[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          lo[k] = j ? make_float2(bf16_hi(w[2 * k]), bf16_hi(w[2 * k + 1]))
+                    : make_float2(bf16_lo(w[2 * k]), bf16_lo(w[2 * k + 1]));
+          hi[k] = j ? make_float2(bf16_hi(w[8 + 2 * k]), bf16_hi(w[9 + 2 * k]))
+                    : make_float2(bf16_lo(w[8 + 2 * k]), bf16_lo(w[9 + 2 * k]));
+        }
+        const uint32_t amax_bits = j ? (m >> 16) & 0x7FFFu : m & 0x7FFFu;
+        uint4 rb0 = make_uint4(0, 0, 0, 0), rb1 = rb0;
+        if constexpr (SR) {
+          rb0 = sr_group_bits(p.seed, p.step, 1u, (uint64_t)(tile0 + 16 * o));
+          rb1 = sr_group_bits(p.seed, p.step, 1u, (uint64_t)(tile0 + 16 * o + 8));
+        }
+        const BlockResult br = encode_block<FMT, SR, FOS != 0>(
+            lo, hi, amax_bits, ss, TableScales2{tab}, rb0, rb1, want_dq, rule);
+        if (okc) {
+          ccodes[o] = make_uint2(br.codes[0], br.codes[1]);
+          cscales[o] = (uint8_t)br.scale;
+          if (want_dq) {
+            __stcs(cdq + 2 * o, br.dq[0]);
+            __stcs(cdq + 2 * o + 1, br.dq[1]);
+          }
+        }
+        if constexpr (FOS != 0) {
+          // bit 4 cp + q = band q of the warp's column pair cp, column j
+          const uint32_t bb = __ballot_sync(0xFFFFFFFFu, okc && br.pick4);
+          if (lane == 0) s_cbits[buf][j * 8 + warp] = bb;
+        }
+      }
+    }
+    // the next tile's tables, ready by the next barrier (built after this
+    // tile's work, so reading the slice's amax costs no wait)
+    if (more) {
+      if (new_slice) {
+        tables(gam_next, nx.first, buf ^ 1);
+      } else if (t < kTab) {
+        s_tab[buf ^ 1][t] = tab[t];
+        if (t < 2) s_rden[buf ^ 1][t] = s_rden[buf][t];
+      }
+    }
+    prev = cur;
+    cur = nx;
   }
+  if (FOS != 0) {  // the last tile's bits
+    __syncthreads();
+    flush(buf ^ 1, prev);
+  }
+  if (((seen & 0x7FFFu) >= 0x7F80u || ((seen >> 16) & 0x7FFFu) >= 0x7F80u))
+    flag(p.status, NVFP4_DEV_NONFINITE_INPUT_BIT);
 }
 
 template <int FMT, bool SR, int FOS, bool ROWS>
 cudaError_t launch_t(const DualParams& p, int64_t S, cudaStream_t st) {
   const int64_t tiles_r = (p.R + TR - 1) / TR, tiles_c = (p.C + TC - 1) / TC;
-  const int64_t n = S * tiles_r * tiles_c;
+  const int64_t per_slice = tiles_r * tiles_c, n = S * per_slice;
   if (n > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
-  return launch_pdl(quant_dual_kernel<FMT, SR, FOS, ROWS>, dim3((unsigned)n), dim3(kThreads), st,
-                    p, tiles_r, tiles_c);
+  const int64_t grid = (n + kTilesPerCta - 1) / kTilesPerCta;
+  DualGeom geo;
+  geo.by_tiles_c = make_fastdiv((uint32_t)tiles_c);
+  geo.by_tiles_slice = make_fastdiv((uint32_t)per_slice);
+  geo.tiles_c = (uint32_t)tiles_c;
+  geo.tiles_slice = (uint32_t)per_slice;
+  geo.n_tiles = (uint32_t)n;
+  geo.slice_elems = p.R * p.C;
+  geo.words = (p.R * p.C / 16 + 31) / 32;
+  return launch_pdl(quant_dual_kernel<FMT, SR, FOS, ROWS>, dim3((unsigned)grid), dim3(kThreads),
+                    st, p, geo);
 }
 
 }  // namespace

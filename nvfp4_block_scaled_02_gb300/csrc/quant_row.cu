@@ -26,11 +26,11 @@ __global__ void __launch_bounds__(kThreads) quant_row_kernel(const RowParams p) 
   // stage[slot][w][c]: chunk c (0..63) of warp w's tile; chunk c holds values
   // 8c .. 8c+7 of the tile, i.e. half c%2 of block c/2.
   __shared__ __align__(16) uint4 stage[kStages][kWarps][64];
-  __shared__ float s_d[256], s_inv[256];
+  __shared__ float2 s_tab[256];
   const int64_t s = p.slice0 + blockIdx.y;
   const SliceScale ss = slice_scale(p.gamax[s], p.M);
   if (ss.bad && threadIdx.x == 0 && blockIdx.x == 0) flag(p.status, NVFP4_DEV_BAD_AMAX_BIT);
-  build_scale_table<FMT>(s_d, s_inv, ss.g);
+  build_scale_table2<FMT>(s_tab, ss.g);
   __syncthreads();
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(kThreads) quant_row_kernel(const RowParams p) 
       rb1 = sr_group_bits(p.seed, p.step, 0u, (uint64_t)gblk * 16 + 8);
     }
     const BlockResult r =
-        encode_block<FMT, SR, FOS != 0>(lo, hi, m, ss, TableScales{s_d, s_inv}, rb0, rb1, want_dq,
+        encode_block<FMT, SR, FOS != 0>(lo, hi, m, ss, TableScales2{s_tab}, rb0, rb1, want_dq,
                                         FOS == 2 ? p.rule : 0);
     if (ok) {
       __stcs(reinterpret_cast<uint2*>(p.codes) + gblk, make_uint2(r.codes[0], r.codes[1]));

@@ -221,6 +221,19 @@ def test_fp8_scale_learning_argument_errors(L):
     assert ex(FAKE, 4, 32, FAKE, None, None, C.byref(_out(dq=0)), None, None) == 1
 
 
+def test_amax_ws_argument_errors(L):
+    ws = L.nvfp4_amax_ws
+    assert L.nvfp4_amax_ws_bytes(3) == 24 and L.nvfp4_amax_ws_bytes(0) == 0
+    assert ws(FAKE, 2, 4, 4, FAKE, None, 16, None, None) == 1        # no workspace
+    assert ws(FAKE, 2, 4, 4, FAKE, FAKE, 15, None, None) == 2        # workspace too small
+    assert ws(FAKE, 2, 4, 4, None, FAKE, 16, None, None) == 1        # no output
+    assert ws(None, 2, 4, 4, FAKE, FAKE, 16, None, None) == 1        # no input
+    assert ws(FAKE, -1, 4, 4, FAKE, FAKE, 16, None, None) == 2
+    assert ws(FAKE + 2, 2, 4, 4, FAKE, FAKE, 16, None, None) == 3    # misaligned x
+    assert ws(FAKE, 2, 4, 4, FAKE, FAKE + 2, 16, None, None) == 3    # misaligned workspace
+    assert ws(None, 0, 4, 4, None, None, 0, None, None) == 0         # empty: nothing enqueued
+
+
 def test_amax_argument_errors(L):
     assert L.nvfp4_amax(FAKE, -1, 4, 4, FAKE, None, None) == 2
     assert L.nvfp4_amax(FAKE, 1, 4, 4, None, None, None) == 1
