@@ -140,6 +140,34 @@ NVFP4_API nvfp4_status nvfp4_amax_ws(const void* x, int64_t slices, int64_t rows
                                      float* amax, void* workspace, size_t ws_bytes,
                                      int32_t* status, void* stream);
 
+/* The one-launch global amax for callers that cannot allocate device memory.
+ * The pages have no counterpart: this entry point exists for callers that may
+ * not call cudaMalloc or cudaFree, or hold no spare buffer to lend: an
+ * operator hook inside another framework that hands out no workspace, a
+ * serving or real-time loop that fixes all of its memory at start-up, code
+ * that must not let an allocation synchronise the device. It computes what
+ * nvfp4_amax_ws computes, bit for bit, taking its scratch (two 32-bit words
+ * per slice) from a fixed array in the library's own device image instead of
+ * a caller's workspace; it allocates nothing.
+ * x: bf16 [slices][rows][cols]; amax: fp32 [slices], overwritten.
+ * - At most NVFP4_AMAX_NOALLOC_MAX_SLICES (4096) slices; more returns
+ *   NVFP4_ERR_SHAPE. The array (32 KiB) is held by every GPU that loads the
+ *   library until the process exits.
+ * - The first call on a device looks up the array's device address (with that
+ *   device current) and keeps it; make that first call before any stream
+ *   capture.
+ * - Each call clears the words it uses (a small zeroing kernel) and then runs
+ *   the amax kernel: two launches on `stream`.
+ * - Every call shares the one array per device: calls that overlap on the GPU
+ *   (on different streams, or from different host threads without ordering)
+ *   race on it and may return wrong maxima. Order them (one stream, or events).
+ * Errors: those of nvfp4_amax, plus NVFP4_ERR_SHAPE above the slice limit and
+ * NVFP4_ERR_CUDA when the array's address cannot be looked up. */
+#define NVFP4_AMAX_NOALLOC_MAX_SLICES 4096
+NVFP4_API nvfp4_status nvfp4_amax_noalloc(const void* x, int64_t slices, int64_t rows,
+                                          int64_t cols, float* amax, int32_t* status,
+                                          void* stream);
+
 /* NVFP4 quantisation of x: bf16 [slices][rows][cols] (End-to-End 4-Bit
  * Training, "Low-precision formats on Blackwell" and "Block-scaled backward
  * passes"; UE5M3 blog, math derivation and stochastic rounding; "Four Over

@@ -103,6 +103,7 @@ def lib() -> C.CDLL:
             L = C.CDLL(LIB_PATH)
             L.nvfp4_amax.argtypes = [_vp, _i64, _i64, _i64, _vp, _vp, _vp]
             L.nvfp4_amax_ws.argtypes = [_vp, _i64, _i64, _i64, _vp, _vp, C.c_size_t, _vp, _vp]
+            L.nvfp4_amax_noalloc.argtypes = [_vp, _i64, _i64, _i64, _vp, _vp, _vp]
             L.nvfp4_amax_ws_bytes.argtypes = [_i64]
             L.nvfp4_amax_ws_bytes.restype = C.c_size_t
             L.nvfp4_quantize.argtypes = [C.POINTER(_Config), _vp, _i64, _i64, _i64, _vp,
@@ -128,7 +129,7 @@ def lib() -> C.CDLL:
             L.nvfp4_sr_bits.argtypes = [_u32, _u32, _u32, C.c_uint64, _i64, _vp, _vp]
             L.nvfp4_status_string.restype = C.c_char_p
             L.nvfp4_status_string.argtypes = [C.c_int]
-            for name in ("nvfp4_amax", "nvfp4_amax_ws", "nvfp4_quantize", "nvfp4_quantize_per_token",
+            for name in ("nvfp4_amax", "nvfp4_amax_ws", "nvfp4_amax_noalloc", "nvfp4_quantize", "nvfp4_quantize_per_token",
                          "nvfp4_requant_transpose", "nvfp4_fakequant_fwd",
                          "nvfp4_fakequant_fwd_fp8scale", "nvfp4_scale_grad_bwd_fp8scale",
                          "nvfp4_scale_init_mse", "nvfp4_export_scales", "nvfp4_mx_quantize",
@@ -256,6 +257,25 @@ def nvfp4_amax_ws(x: torch.Tensor, workspace: torch.Tensor, amax: torch.Tensor |
     _check("nvfp4_amax_ws", lib().nvfp4_amax_ws(
         _bf16(x, "x"), S, R, Cc, _dev(amax, "amax"), _dev(workspace, "workspace"),
         workspace.numel() * workspace.element_size(), _dev(status, "status"), _stream(x.device)))
+    return amax
+
+
+AMAX_NOALLOC_MAX_SLICES = 4096
+
+
+@_on_input_device
+def nvfp4_amax_noalloc(x: torch.Tensor, amax: torch.Tensor | None = None,
+                       status: torch.Tensor | None = None) -> torch.Tensor:
+    """The one-launch amax for callers that cannot allocate device memory: the
+    library's own fixed scratch array stands in for the workspace (at most
+    AMAX_NOALLOC_MAX_SLICES slices; calls that overlap on the GPU race on it)."""
+    S, R, Cc = _shape3(x)
+    _need(amax, "amax", S, "f32")
+    _need(status, "status", 1, "i32")
+    if amax is None:
+        amax = torch.empty(S, dtype=torch.float32, device=x.device)
+    _check("nvfp4_amax_noalloc", lib().nvfp4_amax_noalloc(
+        _bf16(x, "x"), S, R, Cc, _dev(amax, "amax"), _dev(status, "status"), _stream(x.device)))
     return amax
 
 

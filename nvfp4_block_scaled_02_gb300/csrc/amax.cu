@@ -8,6 +8,8 @@
 // fp32 bit pattern of the result (after a zeroing kernel), or, with a
 // caller's workspace, one launch whose last CTA per slice writes the result.
 // MAX is exact and order-free, so the result does not depend on the schedule.
+#include <atomic>
+
 #include "device.cuh"
 #include "launch.h"
 
@@ -137,6 +139,39 @@ cudaError_t launch_amax(const uint16_t* x, int64_t S, int64_t n, float* amax, in
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+// ---- the amax without any caller memory but its input and output ---------
+// Some callers cannot allocate device memory: an operator hook inside another
+// framework that hands out no workspace, a serving or real-time loop that
+// fixes all its memory at start-up, code that must not call cudaMalloc or
+// cudaFree because those can synchronise the device. For them the one-launch
+// amax takes its two scratch words per slice from a fixed array in this
+// library's own device image (every GPU that loads the library holds it until
+// the process exits). In host code the array's name is only a stand-in, not
+// a device address: its address is looked up once per device.
+static __device__ __align__(256) uint32_t g_amax_scratch[2 * kAmaxNoAllocMaxSlices];
+static std::atomic<uint32_t*> g_amax_scratch_at[64];  // its device address, per device
+
+cudaError_t launch_amax_noalloc(const uint16_t* x, int64_t S, int64_t n, float* amax,
+                                int32_t* status, cudaStream_t st) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  uint32_t* ws = g_amax_scratch_at[dev].load(std::memory_order_acquire);
+  if (ws == nullptr) {  // first call on this device (that device is current)
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_amax_scratch);
+    if (e != cudaSuccess) return e;
+    ws = static_cast<uint32_t*>(p);
+    g_amax_scratch_at[dev].store(ws, std::memory_order_release);
+  }
+  // the words of this call's slices start at zero whatever an earlier call
+  // (one that overlapped another on the GPU, say) left in them
+  e = launch_zero_words(ws, 2 * S, st);
+  if (e != cudaSuccess) return e;
+  return launch_amax_ticket(x, S, n, amax, ws, status, st);
 }
 
 }  // namespace nvfp4

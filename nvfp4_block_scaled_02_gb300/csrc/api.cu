@@ -128,6 +128,19 @@ nvfp4_status nvfp4_amax_ws(const void* x, int64_t slices, int64_t rows, int64_t 
                                                static_cast<cudaStream_t>(stream)));
 }
 
+nvfp4_status nvfp4_amax_noalloc(const void* x, int64_t slices, int64_t rows, int64_t cols,
+                                float* amax, int32_t* status, void* stream) {
+  if (slices < 0 || rows < 0 || cols < 0) return NVFP4_ERR_SHAPE;
+  if (slices > NVFP4_AMAX_NOALLOC_MAX_SLICES) return NVFP4_ERR_SHAPE;
+  if (slices == 0) return NVFP4_OK;
+  if (!amax) return NVFP4_ERR_NULL;
+  if (rows * cols != 0 && !x) return NVFP4_ERR_NULL;
+  if (!aligned(x, 16) || !aligned(amax, 4) || !aligned(status, 4)) return NVFP4_ERR_ALIGN;
+  return cuda_status(nvfp4::launch_amax_noalloc(static_cast<const uint16_t*>(x), slices,
+                                                rows * cols, amax, status,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
 nvfp4_status nvfp4_quantize(const nvfp4_config* cfg, const void* x, int64_t slices, int64_t rows,
                             int64_t cols, const float* global_amax, const nvfp4_out* row,
                             const nvfp4_out* col, int32_t* status, void* stream) {

@@ -163,6 +163,11 @@ cudaError_t launch_amax(const uint16_t* x, int64_t S, int64_t n, float* amax, in
 // zero after).
 cudaError_t launch_amax_ticket(const uint16_t* x, int64_t S, int64_t n, float* amax,
                                uint32_t* ws, int32_t* status, cudaStream_t st);
+// The same with the library's own fixed scratch array (at most
+// kAmaxNoAllocMaxSlices slices): no memory of the caller's beyond x and amax.
+constexpr int64_t kAmaxNoAllocMaxSlices = NVFP4_AMAX_NOALLOC_MAX_SLICES;
+cudaError_t launch_amax_noalloc(const uint16_t* x, int64_t S, int64_t n, float* amax,
+                                int32_t* status, cudaStream_t st);
 
 // Scale-learning fake quantisation and STE backward (row blocks).
 struct SteParams {

@@ -234,6 +234,16 @@ def test_amax_ws_argument_errors(L):
     assert ws(None, 0, 4, 4, None, None, 0, None, None) == 0         # empty: nothing enqueued
 
 
+def test_amax_noalloc_argument_errors(L):
+    na = L.nvfp4_amax_noalloc
+    assert na(FAKE, 4097, 4, 4, FAKE, None, None) == 2      # above the fixed scratch's limit
+    assert na(FAKE, -1, 4, 4, FAKE, None, None) == 2
+    assert na(FAKE, 2, 4, 4, None, None, None) == 1
+    assert na(None, 2, 4, 4, FAKE, None, None) == 1
+    assert na(FAKE + 2, 2, 4, 4, FAKE, None, None) == 3
+    assert na(None, 0, 4, 4, None, None, None) == 0         # empty: nothing enqueued
+
+
 def test_amax_argument_errors(L):
     assert L.nvfp4_amax(FAKE, -1, 4, 4, FAKE, None, None) == 2
     assert L.nvfp4_amax(FAKE, 1, 4, 4, None, None, None) == 1
