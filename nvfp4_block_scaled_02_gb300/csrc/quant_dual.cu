@@ -90,12 +90,22 @@ __global__ void __launch_bounds__(kThreads, SR ? (FOS != 0 ? 2 : 3) : (FOS == 2 
   // rows) and column ballots (one word per warp and column parity)
   __shared__ uint32_t s_rbits[2][TR / 2], s_cbits[2][16];
 
-  const int64_t R = p.R, C = p.C;
+  const int64_t R = p.R, C = p.C, R16 = R >> 4, C16 = C >> 4;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int rule = FOS == 2 ? p.rule : 0;
   const bool vec = (C % 8) == 0;
   const int lr0 = t >> 4, lq = t & 15;  // thread t's chunks: rows 16 k + lr0, columns 8 lq ..
+  const int cq = lane & 3, cpl = 8 * warp + (lane >> 2);  // column band q, column pair
   constexpr int kTab = FMT == 0 ? 128 : 256;
+
+  // Offsets of this thread's outputs within any tile, fixed for the kernel:
+  // row chunk k at (16 k + lr0) C / 8 + lq + 2 C k groups of 8 values from the
+  // tile's first; column 2 cpl + j, band q at (2 cpl + j) R / 16 + q groups of
+  // 16; the row / column 4/6 bits of tile row t / column t - 128 at
+  // t C/16 / (t - 128) R/16 bits from the tile's first.
+  const int64_t ro8 = (int64_t)lr0 * (C >> 3) + lq;
+  const int64_t co16 = (int64_t)(2 * cpl) * R16 + cq;
+  const int64_t rbit_t = (int64_t)t * C16, cbit_t = (int64_t)(t - 128) * R16;
 
   // Where tile T lies.
   struct Where {
@@ -153,34 +163,31 @@ __global__ void __launch_bounds__(kThreads, SR ? (FOS != 0 ? 2 : 3) : (FOS == 2 
       }
     }
   };
-
-  // Thread offsets within a tile, in units of 8 (rows) or 16 (columns) values.
-  const int64_t R16 = R >> 4;
-  const int64_t ro0 = (int64_t)lr0 * (C >> 3) + lq;  // row chunk k: ro0 + 2 C k
-  const int cq = lane & 3, cpl = 8 * warp + (lane >> 2);  // column band, column pair
-  const int64_t co0 = (int64_t)(2 * cpl) * R16 + cq;   // column 2 cpl + j: co0 + j R16
-
-  // OR the 4/6 bits a finished tile left in s_[rc]bits[buf] into the bitmaps
-  // (rows by threads 0..63, columns by threads 128..255): tile rows' blocks
-  // are 8 consecutive bits, tile columns' bands 4.
-  auto flush = [&](int buf, const Where& at) {
-    if (ROWS && t < at.nr) {
-      const int nb = at.nc / 16;
-      const uint32_t bits = even_bits(s_rbits[buf][t >> 1] >> (16 * (t & 1))) & 0xFFu;
-      or_bits(p.r_choice + at.s * geo.words, (at.r0 + t) * (C >> 4) + (at.c0 >> 4),
-              bits & ((1u << nb) - 1u), nb);
+  // A finished tile's 4/6 bits (left in s_[rc]bits[buf]) still to be OR-ed
+  // into the bitmaps: tile row t's 8 blocks are bits rbit + t C/16 ..,
+  // tile column cc's 4 bands bits cbit + cc R/16 ..
+  struct Pending {
+    uint32_t *rw, *cw;
+    int64_t rbit, cbit;
+    int nr, nc;
+  };
+  auto flush = [&](int buf, const Pending& f) {
+    if (ROWS && t < f.nr) {  // threads 0..63
+      const int nb = f.nc >> 4;
+      const uint32_t bits = even_bits(s_rbits[buf][t >> 1] >> (16 * (t & 1)));
+      or_bits(f.rw, f.rbit + rbit_t, bits & ((1u << nb) - 1u), nb);
     }
-    if (t >= 128 && t - 128 < at.nc) {
-      const int cc = t - 128, cp = cc >> 1, nb = at.nr / 16;
-      const uint32_t bits = (s_cbits[buf][(cc & 1) * 8 + (cp >> 3)] >> (4 * (cp & 7))) & 0xFu;
-      or_bits(p.c_choice + at.s * geo.words, (at.c0 + cc) * R16 + (at.r0 >> 4),
-              bits & ((1u << nb) - 1u), nb);
+    if (t >= 128 && t - 128 < f.nc) {  // threads 128..255
+      const int cc = t - 128, cp = cc >> 1, nb = f.nr >> 4;
+      const uint32_t bits = s_cbits[buf][(cc & 1) * 8 + (cp >> 3)] >> (4 * (cp & 7));
+      or_bits(f.cw, f.cbit + cbit_t, bits & ((1u << nb) - 1u), nb);
     }
   };
 
   const uint32_t T0 = blockIdx.x * kTilesPerCta;
   const uint32_t T1 = T0 + kTilesPerCta < geo.n_tiles ? T0 + kTilesPerCta : geo.n_tiles;
-  Where cur = where(T0), prev = cur;
+  Where cur = where(T0);
+  Pending pend{};
   fetch(cur, 0);
   tables(t < kTab ? p.gamax[cur.s] : 0.0f, cur.first, 0);
   uint32_t seen = 0;  // magnitude maximum of every value this thread encodes
@@ -194,27 +201,27 @@ __global__ void __launch_bounds__(kThreads, SR ? (FOS != 0 ? 2 : 3) : (FOS == 2 
     if (more) fetch(nx, buf ^ 1);  // in flight while this tile is encoded
     const bool new_slice = more && nx.s != cur.s;
     const float gam_next = new_slice && t < kTab ? p.gamax[nx.s] : 0.0f;
-    if (FOS != 0 && T != T0) flush(buf ^ 1, prev);
+    if (FOS != 0 && T != T0) flush(buf ^ 1, pend);
     SliceScale ss;
     ss.rden6 = s_rden[buf][0];
     ss.rden4 = s_rden[buf][1];
     const float2* tab = s_tab[buf];
-    const int64_t s = cur.s, r0 = cur.r0, c0 = cur.c0;
-    const int nr = cur.nr, nc = cur.nc;
-    const int64_t slice0 = s * geo.slice_elems;
     const uint32_t* tl = tile[buf];
+    const int64_t slice0 = cur.s * geo.slice_elems;
+    const int nr = cur.nr, nc = cur.nc;
+
     // ---- row blocks: chunks from the staged tile ----------------------------
     if constexpr (ROWS) {
       const bool want_dq = p.r_dq != nullptr;
-      const int64_t tile0 = slice0 + r0 * C + c0;  // row-layout index of the tile origin
-      uint32_t* rcodes = reinterpret_cast<uint32_t*>(p.r_codes) + (tile0 >> 3);
-      uint4* rdq = reinterpret_cast<uint4*>(p.r_dq + tile0);
-      uint8_t* rscales = p.r_scales + (tile0 >> 4);
+      const int64_t tile0 = slice0 + cur.r0 * C + cur.c0;  // row-layout index of the tile origin
+      const int64_t g8 = (tile0 >> 3) + ro8;               // chunk 0, in groups of 8 values
+      uint32_t* const rc = reinterpret_cast<uint32_t*>(p.r_codes) + g8;
+      uint4* const rd = reinterpret_cast<uint4*>(p.r_dq) + g8;
+      uint8_t* const rs = p.r_scales + (g8 >> 1);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int lr = 16 * k + lr0;
         const bool ok = lr < nr && 8 * lq < nc;
-        const int64_t o = ro0 + k * (2 * C);
         const uint4 v = *reinterpret_cast<const uint4*>(&tl[word_of(lr, 4 * lq)]);
         const uint32_t m = pair_amax(bmax_abs2(bmax_abs2(v.x, v.y), bmax_abs2(v.z, v.w)));
         seen = bmax_abs2(seen, m);
@@ -222,13 +229,12 @@ __global__ void __launch_bounds__(kThreads, SR ? (FOS != 0 ? 2 : 3) : (FOS == 2 
         f2 x[4];
         unpack8(v, x);
         uint4 rb = make_uint4(0, 0, 0, 0);
-        if constexpr (SR) rb = sr_group_bits(p.seed, p.step, 0u, (uint64_t)(tile0 + 8 * o));
+        if constexpr (SR)
+          rb = sr_group_bits(p.seed, p.step, 0u, (uint64_t)(8 * (g8 + k * (2 * C))));
         const HalfOut h = encode_half8<FMT, SR, FOS>(x, amax_bits, ss, tab, rb, want_dq, rule);
-        if (ok) {
-          rcodes[o] = h.codes;
-          if (want_dq) __stcs(rdq + o, h.dq);
-          if ((lane & 1) == 0) rscales[o >> 1] = (uint8_t)h.scale;
-        }
+        if (ok) rc[k * (2 * C)] = h.codes;
+        if (ok && want_dq) __stcs(rd + k * (2 * C), h.dq);
+        if (ok && (lane & 1) == 0) rs[k * C] = (uint8_t)h.scale;
         if constexpr (FOS != 0) {
           // lanes 0..15: tile row lr (even), lanes 16..31: row lr + 1
           const uint32_t bb = __ballot_sync(0xFFFFFFFFu, ok && h.pick4);
@@ -240,15 +246,15 @@ __global__ void __launch_bounds__(kThreads, SR ? (FOS != 0 ? 2 : 3) : (FOS == 2 
     // ---- column blocks ----------------------------------------------------------
     {
       const bool want_dq = p.c_dq != nullptr;
-      const int q = cq;
-      const bool rows_ok = 16 * q < nr;
-      const int64_t tile0 = slice0 + c0 * R + r0;  // column-layout index of the tile origin
-      uint2* ccodes = reinterpret_cast<uint2*>(p.c_codes) + (tile0 >> 4);
-      uint4* cdq = reinterpret_cast<uint4*>(p.c_dq + tile0);
-      uint8_t* cscales = p.c_scales + (tile0 >> 4);
+      const bool rows_ok = 16 * cq < nr;
+      const int64_t tile0 = slice0 + cur.c0 * R + cur.r0;  // column-layout index of the tile origin
+      const int64_t g16 = (tile0 >> 4) + co16;             // column 2 cpl, in groups of 16 values
+      uint2* const ccodes = reinterpret_cast<uint2*>(p.c_codes) + g16;
+      uint4* const cdq = reinterpret_cast<uint4*>(p.c_dq) + 2 * g16;
+      uint8_t* const cscales = p.c_scales + g16;
       uint32_t w[16];
 #pragma unroll
-      for (int i2 = 0; i2 < 16; ++i2) w[i2] = tl[word_of(16 * q + i2, cpl)];
+      for (int i2 = 0; i2 < 16; ++i2) w[i2] = tl[word_of(16 * cq + i2, cpl)];
       uint32_t m = 0;
 #pragma unroll
       for (int i2 = 0; i2 < 16; ++i2) m = bmax_abs2(m, w[i2]);  // both columns' block amax
@@ -256,7 +262,6 @@ __global__ void __launch_bounds__(kThreads, SR ? (FOS != 0 ? 2 : 3) : (FOS == 2 
 #pragma unroll
       for (int j = 0; j < 2; ++j) {  // column 2 cpl + j
         const bool okc = 2 * cpl + j < nc && rows_ok;
-        const int64_t o = co0 + j * R16;
         f2 lo[4], hi[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -268,18 +273,17 @@ __global__ void __launch_bounds__(kThreads, SR ? (FOS != 0 ? 2 : 3) : (FOS == 2 
         const uint32_t amax_bits = j ? (m >> 16) & 0x7FFFu : m & 0x7FFFu;
         uint4 rb0 = make_uint4(0, 0, 0, 0), rb1 = rb0;
         if constexpr (SR) {
-          rb0 = sr_group_bits(p.seed, p.step, 1u, (uint64_t)(tile0 + 16 * o));
-          rb1 = sr_group_bits(p.seed, p.step, 1u, (uint64_t)(tile0 + 16 * o + 8));
+          const uint64_t e = (uint64_t)(16 * (g16 + j * R16));
+          rb0 = sr_group_bits(p.seed, p.step, 1u, e);
+          rb1 = sr_group_bits(p.seed, p.step, 1u, e + 8);
         }
         const BlockResult br = encode_block<FMT, SR, FOS != 0>(
             lo, hi, amax_bits, ss, TableScales2{tab}, rb0, rb1, want_dq, rule);
-        if (okc) {
-          ccodes[o] = make_uint2(br.codes[0], br.codes[1]);
-          cscales[o] = (uint8_t)br.scale;
-          if (want_dq) {
-            __stcs(cdq + 2 * o, br.dq[0]);
-            __stcs(cdq + 2 * o + 1, br.dq[1]);
-          }
+        if (okc) ccodes[j * R16] = make_uint2(br.codes[0], br.codes[1]);
+        if (okc) cscales[j * R16] = (uint8_t)br.scale;
+        if (okc && want_dq) {
+          __stcs(cdq + 2 * j * R16, br.dq[0]);
+          __stcs(cdq + 2 * j * R16 + 1, br.dq[1]);
         }
         if constexpr (FOS != 0) {
           // bit 4 cp + q = band q of the warp's column pair cp, column j
@@ -287,6 +291,14 @@ __global__ void __launch_bounds__(kThreads, SR ? (FOS != 0 ? 2 : 3) : (FOS == 2 
           if (lane == 0) s_cbits[buf][j * 8 + warp] = bb;
         }
       }
+    }
+    if constexpr (FOS != 0) {
+      pend.rw = p.r_choice + cur.s * geo.words;
+      pend.cw = p.c_choice + cur.s * geo.words;
+      pend.rbit = cur.r0 * C16 + (cur.c0 >> 4);
+      pend.cbit = cur.c0 * R16 + (cur.r0 >> 4);
+      pend.nr = nr;
+      pend.nc = nc;
     }
     // the next tile's tables, ready by the next barrier (built after this
     // tile's work, so reading the slice's amax costs no wait)
@@ -298,12 +310,11 @@ __global__ void __launch_bounds__(kThreads, SR ? (FOS != 0 ? 2 : 3) : (FOS == 2 
         if (t < 2) s_rden[buf ^ 1][t] = s_rden[buf][t];
       }
     }
-    prev = cur;
     cur = nx;
   }
   if (FOS != 0) {  // the last tile's bits
     __syncthreads();
-    flush(buf ^ 1, prev);
+    flush(buf ^ 1, pend);
   }
   if (((seen & 0x7FFFu) >= 0x7F80u || ((seen >> 16) & 0x7FFFu) >= 0x7F80u))
     flag(p.status, NVFP4_DEV_NONFINITE_INPUT_BIT);
