@@ -997,6 +997,9 @@ def fos_overhead(args, device):
                         o.dequant = None
                 def call(i, wl=wl):
                     return wl._quant(i)
+                for i in range(wl.nsets):  # each set's global amax, once (untimed)
+                    if wl._amax(i) != 0:
+                        raise nv.Nvfp4Error("amax", 1)
                 for k in range(args.warmup):
                     call(k % wl.nsets)
                 torch.cuda.synchronize()

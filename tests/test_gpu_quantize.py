@@ -86,6 +86,21 @@ def test_column_and_dual_blocks(shape, blocks, fmt, rounding, fos):
     run_both(xb, gamax, blocks=blocks, fmt=fmt, rounding=rounding, fos=fos, seed=5, step=9)
 
 
+@pytest.mark.parametrize("blocks", [2, 3])
+@pytest.mark.parametrize("rounding", [0, 1])
+@pytest.mark.parametrize("shape", [(19, 16, 48), (11, 80, 32), (9, 64, 128)])
+def test_dual_runs_across_many_slices(shape, blocks, rounding):
+    """Slices of one or a few tiles each, every slice a different magnitude:
+    a CTA's run of consecutive tiles crosses slices (each needs its own outer
+    scale and scale table) and most tiles are partial."""
+    S, R, C = shape
+    f = synth.bf16_bits_to_f32(synth.student_t(S * R, C, seed=12)).reshape(S, R, C)
+    f = f * (2.0 ** (np.arange(S, dtype=np.float32) - S // 2))[:, None, None]
+    xb = synth.to_bf16_bits(f)
+    gamax, _ = oracle.global_amax(xb, S)
+    run_both(xb, gamax, blocks=blocks, fos=1, rounding=rounding, seed=3, step=4)
+
+
 @pytest.mark.parametrize("shape", [(1, 32, 24), (2, 48, 40), (1, 16, 7)])
 def test_column_blocks_with_unaligned_rows(shape):
     """Column-only encoding needs rows % 16 only; rows of the input may be any
