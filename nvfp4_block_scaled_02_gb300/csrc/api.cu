@@ -67,8 +67,7 @@ nvfp4_status quantize_tile16(const nvfp4_config* cfg, const void* x, int64_t sli
   p.C = cols;
   p.gamax = global_amax;
   p.M = cfg->scale_max > 0.0f ? cfg->scale_max : 448.0f;
-  p.seed = cfg->seed;
-  p.step = cfg->step;
+  p.key = nvfp4::make_sr_key(cfg->seed, cfg->step);
   p.r_codes = reinterpret_cast<uint32_t*>(row->codes);
   p.r_scales = row->scales;
   p.r_dq = static_cast<uint4*>(row->dequant);
@@ -180,8 +179,7 @@ nvfp4_status nvfp4_quantize(const nvfp4_config* cfg, const void* x, int64_t slic
     p.W = W;
     p.gamax = global_amax;
     p.M = M;
-    p.seed = cfg->seed;
-    p.step = cfg->step;
+    p.key = nvfp4::make_sr_key(cfg->seed, cfg->step);
     p.codes = reinterpret_cast<uint32_t*>(row->codes);
     p.scales = row->scales;
     p.choice = fos ? row->choice : nullptr;
@@ -205,8 +203,7 @@ nvfp4_status nvfp4_quantize(const nvfp4_config* cfg, const void* x, int64_t slic
   p.C = cols;
   p.gamax = global_amax;
   p.M = M;
-  p.seed = cfg->seed;
-  p.step = cfg->step;
+  p.key = nvfp4::make_sr_key(cfg->seed, cfg->step);
   if (do_row) {
     p.r_codes = row->codes;
     p.r_scales = row->scales;
@@ -244,8 +241,7 @@ nvfp4_status nvfp4_quantize_per_token(const nvfp4_config* cfg, const void* x, in
   p.R = rows;
   p.C = cols;
   p.M = cfg->scale_max > 0.0f ? cfg->scale_max : (fos ? 256.0f : 448.0f);
-  p.seed = cfg->seed;
-  p.step = cfg->step;
+  p.key = nvfp4::make_sr_key(cfg->seed, cfg->step);
   p.row_amax = row_amax;
   p.codes = reinterpret_cast<uint32_t*>(out->codes);
   p.scales = out->scales;
@@ -303,8 +299,7 @@ nvfp4_status nvfp4_requant_transpose(const nvfp4_config* src, const nvfp4_config
   p.src_fmt = src->scale_fmt;
   p.M_src = src->scale_max > 0.0f ? src->scale_max : (src->four_over_six ? 256.0f : 448.0f);
   p.M_dst = dst->scale_max > 0.0f ? dst->scale_max : (fos ? 256.0f : 448.0f);
-  p.seed = dst->seed;
-  p.step = dst->step;
+  p.key = nvfp4::make_sr_key(dst->seed, dst->step);
   p.out_codes = out->codes;
   p.out_scales = out->scales;
   p.out_choice = fos ? out->choice : nullptr;
@@ -338,8 +333,7 @@ nvfp4_status nvfp4_mx_quantize(const nvfp4_config* cfg, const void* x, int64_t s
   p.S = slices;
   p.R = rows;
   p.C = cols;
-  p.seed = cfg->seed;
-  p.step = cfg->step;
+  p.key = nvfp4::make_sr_key(cfg->seed, cfg->step);
   if (do_row) {
     p.r_codes = row->codes;
     p.r_scales = row->scales;

@@ -139,25 +139,37 @@ __device__ __forceinline__ void scale_entry(uint32_t code, float g, float& d, fl
 
 // --------------------------------------------------------------- Philox ---
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of two
-// 32x32 -> 64 multiplies, key bumped by the Weyl constants between rounds.
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+// 32x32 -> 64 multiplies, key (seed, step) bumped by the Weyl constants
+// between rounds. The ten round keys are the same for every element of a
+// launch, so the host computes them once and the kernels take them as launch
+// parameters: each round's key XOR then reads a launch constant instead of
+// re-deriving the key schedule for every group of 8 elements.
+struct SrKey {
+  uint32_t k0[10], k1[10];
+};
+__host__ __device__ inline SrKey make_sr_key(uint32_t seed, uint32_t step) {
+  SrKey k;
+  for (int r = 0; r < 10; ++r) {
+    k.k0[r] = seed + (uint32_t)r * 0x9E3779B9u;
+    k.k1[r] = step + (uint32_t)r * 0xBB67AE85u;
+  }
+  return k;
+}
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, const SrKey& key) {
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
     const uint64_t p0 = (uint64_t)0xD2511F53u * c.x;  // one 32x32 -> 64 multiply
     const uint64_t p1 = (uint64_t)0xCD9E8D57u * c.z;
-    c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ k0, (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c.w ^ k1,
-                   (uint32_t)p0);
-    k0 += 0x9E3779B9u;
-    k1 += 0xBB67AE85u;
+    c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ key.k0[r], (uint32_t)p1,
+                   (uint32_t)(p0 >> 32) ^ c.w ^ key.k1[r], (uint32_t)p0);
   }
   return c;
 }
 // The 128 random bits of the group of 8 elements starting at flat index
 // idx0 (idx0 % 8 == 0) of an encoding in direction dir (0 rows, 1 columns).
-__device__ __forceinline__ uint4 sr_group_bits(uint32_t seed, uint32_t step, uint32_t dir,
-                                               uint64_t idx0) {
+__device__ __forceinline__ uint4 sr_group_bits(const SrKey& key, uint32_t dir, uint64_t idx0) {
   uint64_t j = idx0 >> 3;
-  return philox4x32_10(make_uint4((uint32_t)j, (uint32_t)(j >> 32), dir, 0u), seed, step);
+  return philox4x32_10(make_uint4((uint32_t)j, (uint32_t)(j >> 32), dir, 0u), key);
 }
 // Random bits of element k (0..7) of a group.
 __device__ __forceinline__ uint32_t sr_bits_of(const uint4& w, int k) {

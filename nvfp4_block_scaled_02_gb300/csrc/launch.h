@@ -65,7 +65,7 @@ struct RowParams {
   int64_t W;            // 4/6 bitmap words per slice = ceil(Bs / 32)
   const float* gamax;   // [S]
   float M;              // outer-scale FP8 maximum
-  uint32_t seed, step;  // stochastic rounding key
+  SrKey key;            // stochastic rounding: Philox round keys of (seed, step)
   uint32_t* codes;      // 8 codes (one uint32) per chunk of 8 values
   uint8_t* scales;      // one byte per block
   uint32_t* choice;     // 4/6 bitmap (may be null when 4/6 is off)
@@ -84,7 +84,7 @@ struct DualParams {
   int64_t S, R, C;
   const float* gamax;
   float M;
-  uint32_t seed, step;
+  SrKey key;            // Philox round keys of (seed, step)
   // row encoding (used when the kernel writes both)
   uint8_t* r_codes;
   uint8_t* r_scales;
@@ -107,7 +107,7 @@ struct Tile16Params {
   int64_t S, R, C;
   const float* gamax;   // [S]
   float M;
-  uint32_t seed, step;
+  SrKey key;            // Philox round keys of (seed, step)
   uint32_t* r_codes;    // 8 codes per word, row layout
   uint8_t* r_scales;
   uint4* r_dq;          // may be null
@@ -123,7 +123,7 @@ struct TokenParams {
   const uint4* x;       // bf16 [R][C], C % 16 == 0
   int64_t R, C;
   float M;
-  uint32_t seed, step;
+  SrKey key;            // Philox round keys of (seed, step)
   float* row_amax;      // [R], written
   uint32_t* codes;      // as RowParams
   uint8_t* scales;
@@ -142,7 +142,7 @@ struct RequantParams {
   const float* gamax;     // [S], the forward encoding's global amax
   int src_fmt;            // source block-scale format
   float M_src, M_dst;     // outer-scale FP8 maxima of the source and target
-  uint32_t seed, step;
+  SrKey key;            // Philox round keys of (seed, step)
   uint8_t* out_codes;     // MX: [S][C][R] E4M3; NVFP4: [S][C][R/2]
   uint8_t* out_scales;    // MX: [S][C][R/32] E8M0; NVFP4: [S][C][R/16]
   uint32_t* out_choice;   // NVFP4 with 4/6: pre-zeroed bitmap

@@ -55,12 +55,12 @@ __global__ void codec_probe_kernel(int op, const float* __restrict__ in,
   }
 }
 
-__global__ void sr_bits_kernel(uint32_t seed, uint32_t step, uint32_t dir, uint64_t idx0, int64_t n,
+__global__ void sr_bits_kernel(const SrKey key, uint32_t dir, uint64_t idx0, int64_t n,
                                uint32_t* __restrict__ out) {
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
     const uint64_t idx = idx0 + (uint64_t)i;
-    const uint4 w = sr_group_bits(seed, step, dir, idx & ~(uint64_t)7);
+    const uint4 w = sr_group_bits(key, dir, idx & ~(uint64_t)7);
     out[i] = sr_bits_of(w, (int)(idx & 7));
   }
 }
@@ -79,7 +79,7 @@ cudaError_t launch_codec_probe(int op, const float* in, const uint32_t* aux, int
 
 cudaError_t launch_sr_bits(uint32_t seed, uint32_t step, uint32_t dir, uint64_t idx0, int64_t n,
                            uint32_t* out, cudaStream_t st) {
-  sr_bits_kernel<<<grid_for(n), 256, 0, st>>>(seed, step, dir, idx0, n, out);
+  sr_bits_kernel<<<grid_for(n), 256, 0, st>>>(make_sr_key(seed, step), dir, idx0, n, out);
   return cudaGetLastError();
 }
 

@@ -80,7 +80,7 @@ struct DualGeom {
 };
 
 template <int FMT, bool SR, int FOS, bool ROWS>
-__global__ void __launch_bounds__(kThreads, SR ? (FOS != 0 ? 2 : 3) : (FOS == 2 ? 3 : 4))
+__global__ void __launch_bounds__(kThreads, SR ? (FOS != 0 ? 2 : 3) : (FOS != 0 ? 3 : 4))
     quant_dual_kernel(const DualParams p, const DualGeom geo) {
   pdl_begin();
   __shared__ __align__(16) uint32_t tile[2][TR * kWords];
@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, SR ? (FOS != 0 ? 2 : 3) : (FOS == 2 
         unpack8(v, x);
         uint4 rb = make_uint4(0, 0, 0, 0);
         if constexpr (SR)
-          rb = sr_group_bits(p.seed, p.step, 0u, (uint64_t)(8 * (g8 + k * (2 * C))));
+          rb = sr_group_bits(p.key, 0u, (uint64_t)(8 * (g8 + k * (2 * C))));
         const HalfOut h = encode_half8<FMT, SR, FOS>(x, amax_bits, ss, tab, rb, want_dq, rule);
         if (ok) rc[k * (2 * C)] = h.codes;
         if (ok && want_dq) __stcs(rd + k * (2 * C), h.dq);
@@ -274,8 +274,8 @@ __global__ void __launch_bounds__(kThreads, SR ? (FOS != 0 ? 2 : 3) : (FOS == 2 
         uint4 rb0 = make_uint4(0, 0, 0, 0), rb1 = rb0;
         if constexpr (SR) {
           const uint64_t e = (uint64_t)(16 * (g16 + j * R16));
-          rb0 = sr_group_bits(p.seed, p.step, 1u, e);
-          rb1 = sr_group_bits(p.seed, p.step, 1u, e + 8);
+          rb0 = sr_group_bits(p.key, 1u, e);
+          rb1 = sr_group_bits(p.key, 1u, e + 8);
         }
         const BlockResult br = encode_block<FMT, SR, FOS != 0>(
             lo, hi, amax_bits, ss, TableScales2{tab}, rb0, rb1, want_dq, rule);

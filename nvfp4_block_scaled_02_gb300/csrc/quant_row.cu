@@ -74,8 +74,8 @@ __global__ void __launch_bounds__(kThreads) quant_row_kernel(const RowParams p) 
     if (ok && m >= 0x7F80u) flag(p.status, NVFP4_DEV_NONFINITE_INPUT_BIT);
     uint4 rb0 = make_uint4(0, 0, 0, 0), rb1 = rb0;
     if constexpr (SR) {
-      rb0 = sr_group_bits(p.seed, p.step, 0u, (uint64_t)gblk * 16);
-      rb1 = sr_group_bits(p.seed, p.step, 0u, (uint64_t)gblk * 16 + 8);
+      rb0 = sr_group_bits(p.key, 0u, (uint64_t)gblk * 16);
+      rb1 = sr_group_bits(p.key, 0u, (uint64_t)gblk * 16 + 8);
     }
     const BlockResult r =
         encode_block<FMT, SR, FOS != 0>(lo, hi, m, ss, TableScales2{s_tab}, rb0, rb1, want_dq,

@@ -67,8 +67,8 @@ __global__ void __launch_bounds__(kThreads) quant_token_kernel(const TokenParams
       const uint32_t mb = max(absmax_bits4(v0), absmax_bits4(v1));
       uint4 rb0 = make_uint4(0, 0, 0, 0), rb1 = rb0;
       if constexpr (SR) {
-        rb0 = sr_group_bits(p.seed, p.step, 0u, (uint64_t)gblk * 16);
-        rb1 = sr_group_bits(p.seed, p.step, 0u, (uint64_t)gblk * 16 + 8);
+        rb0 = sr_group_bits(p.key, 0u, (uint64_t)gblk * 16);
+        rb1 = sr_group_bits(p.key, 0u, (uint64_t)gblk * 16 + 8);
       }
       const BlockResult r =
           encode_block<FMT, SR, FOS != 0>(lo, hi, mb, ss, scales, rb0, rb1, want_dq,
@@ -177,8 +177,8 @@ __global__ void __launch_bounds__(kThreads) quant_token_cta_kernel(const TokenPa
       const uint32_t mb = max(absmax_bits4(v[k][0]), absmax_bits4(v[k][1]));
       uint4 rb0 = make_uint4(0, 0, 0, 0), rb1 = rb0;
       if constexpr (SR) {
-        rb0 = sr_group_bits(p.seed, p.step, 0u, (uint64_t)gblk * 16);
-        rb1 = sr_group_bits(p.seed, p.step, 0u, (uint64_t)gblk * 16 + 8);
+        rb0 = sr_group_bits(p.key, 0u, (uint64_t)gblk * 16);
+        rb1 = sr_group_bits(p.key, 0u, (uint64_t)gblk * 16 + 8);
       }
       BlockResult r;
       if constexpr (kDirect)

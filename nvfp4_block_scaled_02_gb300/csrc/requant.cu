@@ -131,7 +131,7 @@ __device__ __forceinline__ void load_src(const RequantParams& p, bool valid, con
 
 template <bool SR>
 __device__ __forceinline__ uint4 sr_bits_or_zero(const RequantParams& p, uint64_t idx0) {
-  if constexpr (SR) return sr_group_bits(p.seed, p.step, 2u, idx0);
+  if constexpr (SR) return sr_group_bits(p.key, 2u, idx0);
   else return make_uint4(0, 0, 0, 0);
 }
 
@@ -269,8 +269,8 @@ __global__ void __launch_bounds__(kThreads, min_blocks(TARGET, SR, FOS)) requant
                          e4m3x4_rn(yc[8], yc[9], yc[10], yc[11]),
                          e4m3x4_rn(yc[12], yc[13], yc[14], yc[15]));
         } else {
-          const uint2 a = e4m3x8_sr(yc, sr_group_bits(p.seed, p.step, 2u, (uint64_t)e0));
-          const uint2 b = e4m3x8_sr(yc + 8, sr_group_bits(p.seed, p.step, 2u, (uint64_t)e0 + 8));
+          const uint2 a = e4m3x8_sr(yc, sr_group_bits(p.key, 2u, (uint64_t)e0));
+          const uint2 b = e4m3x8_sr(yc + 8, sr_group_bits(p.key, 2u, (uint64_t)e0 + 8));
           w = make_uint4(a.x, a.y, b.x, b.y);
         }
         if (ok) {
