@@ -150,9 +150,11 @@ __device__ __forceinline__ uint2 e4m3x8_sr(const float* y, const uint4& rb) {
 }
 
 // Resident CTAs per SM the register allocation is held to (the kernel is
-// latency-bound below this; none of these spill).
+// latency-bound below this). At these counts only the NVFP4 target with E4M3
+// scales, stochastic rounding and 4/6 off spills (4 bytes); the NVFP4 target
+// with stochastic rounding and a runtime 4/6 rule would spill at 3.
 constexpr int min_blocks(int target, bool sr, int fos) {
-  return target == 0 ? 4 : (sr && fos ? 2 : 3);
+  return target == 0 ? 4 : (sr && fos == 2 ? 2 : 3);
 }
 
 // TARGET 0: MXFP8; TARGET 1: NVFP4 with block-scale format DFMT and 4/6 mode
