@@ -431,42 +431,60 @@ class DriftingGradient(Workload):
 
 class MoeExperts(Workload):
     """64 experts x 2048 x 7168: per-expert amax + one pass emitting row and
-    column NVFP4 encodings with 4/6 and both dequants."""
+    column NVFP4 encodings with 4/6 and both dequants. The input is larger
+    than L2, so the device-timed steps use one buffer set; the end-to-end run
+    uses two (e2e_sets), so one step's copies overlap its neighbours'."""
+
+    e2e_sets = 2
 
     def __init__(self, device, experts=64, rows=2048, cols=7168, seed=4):
         xb = synth.moe_experts(experts, rows, cols, seed=seed)
         self.S, self.rows, self.cols = experts, rows, cols
         self.elements = experts * rows * cols
         self.host_x = xb
-        self.x = torch.from_numpy(xb.view(np.int16)).to(device)
-        del xb
-        self.amax = torch.empty(experts, dtype=torch.float32, device=device)
-        self.row = nv.alloc_encoding(experts, rows, cols, device, True)
-        self.col = nv.alloc_encoding(experts, cols, rows, device, True)
+        self.device = device
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         self.cfg = nv.Config(blocks=3, four_over_six=1)
         self._c = self.cfg.c()
-        self._r, self._cc = nv._out(self.row), nv._out(self.col)
+        self._ws = nv.amax_workspace(experts, device)
+        self._sets = [self._make_set(torch.from_numpy(xb.view(np.int16)).to(device))]
+        del xb
+        self.x, self.amax = self._sets[0]["x"], self._sets[0]["amax"]
+        self.row, self.col = self._sets[0]["row"], self._sets[0]["col"]
         bpe = self.call_bpe({})
         self.d_bytes = self.elements * bpe["quantize_dual"]
         self.a_bytes = self.elements * bpe["amax"]
         self.nsets = 1
         self.working_set = self.elements * (2 + 2 * 4.57)
-        L = nv.lib()
-        st = torch.cuda.current_stream(device).cuda_stream
 
-        ws = nv.amax_workspace(experts, device)
-        self._ws = ws
+    def _make_set(self, x):
+        """Device buffers of one step (input, per-expert amax, both encodings)
+        and its two calls through the C ABI."""
+        E, R, Cc = self.S, self.rows, self.cols
+        b = {"x": x, "amax": torch.empty(E, dtype=torch.float32, device=self.device),
+             "row": nv.alloc_encoding(E, R, Cc, self.device, True),
+             "col": nv.alloc_encoding(E, Cc, R, self.device, True)}
+        r, cc = nv._out(b["row"]), nv._out(b["col"])
+        L = nv.lib()
+        st = torch.cuda.current_stream(self.device).cuda_stream
+        ws = self._ws
 
         def amax():
-            return L.nvfp4_amax_ws(self.x.data_ptr(), experts, rows, cols, self.amax.data_ptr(),
-                                   ws.data_ptr(), ws.numel() * 4, self.status.data_ptr(), st)
+            return L.nvfp4_amax_ws(x.data_ptr(), E, R, Cc, b["amax"].data_ptr(), ws.data_ptr(),
+                                   ws.numel() * 4, self.status.data_ptr(), st)
 
         def dual():
-            return L.nvfp4_quantize(C.byref(self._c), self.x.data_ptr(), experts, rows, cols,
-                                    self.amax.data_ptr(), C.byref(self._r), C.byref(self._cc),
+            return L.nvfp4_quantize(C.byref(self._c), x.data_ptr(), E, R, Cc,
+                                    b["amax"].data_ptr(), C.byref(r), C.byref(cc),
                                     self.status.data_ptr(), st)
-        self._amax, self._dual = amax, dual
+        b["_refs"] = (r, cc)
+        b["amax_fn"], b["dual_fn"] = amax, dual
+        return b
+
+    def _set(self, i):
+        while len(self._sets) <= i:  # the end-to-end run's second set, made on first use
+            self._sets.append(self._make_set(torch.empty_like(self.x)))
+        return self._sets[i]
 
     @staticmethod
     def call_bpe(kw):
@@ -476,13 +494,15 @@ class MoeExperts(Workload):
         return {"amax": 2.0, "quantize_dual": 2 + 2 * (0.5 + 1 / 16 + 1 / 128 + 2)}
 
     def kernels(self, k, i):
-        return [Kernel("amax", self.a_bytes, self._amax),
-                Kernel("quantize_dual", self.d_bytes, self._dual, 3)]
+        b = self._set(i)
+        return [Kernel("amax", self.a_bytes, b["amax_fn"]),
+                Kernel("quantize_dual", self.d_bytes, b["dual_fn"], 3)]
 
     def e2e_io(self, k, i):
+        b = self._set(i)
         names = ("codes", "scales", "choice", "dequant")
-        outs = [self.row[n] for n in names] + [self.col[n] for n in names]
-        return [self.x], outs
+        outs = [b["row"][n] for n in names] + [b["col"][n] for n in names]
+        return [b["x"]], outs
 
     def cpu_sample(self, budget_s):
         import oracle
@@ -1214,16 +1234,17 @@ def time_ours(wl, args, world, local):
     return statistics.median(passes), stats, per_kernel, clk, wall
 
 
-def time_e2e(wl, steps, device):
+def time_e2e(wl, steps, device, sets=None):
     """The same metric through the C ABI with host buffers, as a user streaming
     tensors through it would run it: every step copies its inputs from pinned
     host memory to the device (copy-in stream), runs the kernels (the
     workload's stream) and copies every output back to pinned host memory
-    (copy-out stream). Step k uses device buffer set k % B (B = 2, or 1 when
-    the workload holds a single set); events order each buffer's reuse, so
+    (copy-out stream). Step k uses device buffer set k % B (B = `sets`, else
+    the workload's e2e_sets, else 2, or 1 when the workload holds a single
+    set); events order each buffer's reuse, so
     one step's copies overlap its neighbours' compute and copies. Events
     bracket the whole run on all three streams."""
-    B = 1 if wl.nsets == 1 else 2
+    B = sets or getattr(wl, "e2e_sets", 1 if wl.nsets == 1 else 2)
     ins0, outs0 = wl.e2e_io(0, 0)
     h_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in ins0]
     for h, t in zip(h_in, ins0):
@@ -1518,6 +1539,9 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=512)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-sets", type=int, default=None,
+                    help="device buffer sets the end-to-end run rotates through (default: the "
+                         "workload's)")
     ap.add_argument("--experts", type=int, default=64, help="MoE workload: number of experts")
     ap.add_argument("--min-seconds", type=float, default=2.0,
                     help="device time the repeated timed passes run for at least")
@@ -1619,7 +1643,7 @@ def main():
         "host_wall_s": round(wall, 3),
     }
     if rank == 0 and not args.no_e2e:
-        ms, bi, bo = time_e2e(wl, args.e2e_steps, device)
+        ms, bi, bo = time_e2e(wl, args.e2e_steps, device, args.e2e_sets)
         per_step_bytes = alg_bytes / world / args.steps
         line["e2e"] = {"value": round(per_step_bytes * args.e2e_steps / (ms * 1e-3) / 1e9, 2),
                        "unit": "GB/s", "h2d_bytes_per_step": int(bi),
