@@ -1243,7 +1243,9 @@ def time_e2e(wl, steps, device, sets=None):
     the workload's e2e_sets, else 2, or 1 when the workload holds a single
     set); events order each buffer's reuse, so
     one step's copies overlap its neighbours' compute and copies. Events
-    bracket the whole run on all three streams."""
+    bracket the whole run on all three streams. Afterwards the inputs' and
+    outputs' copies are timed alone, each direction by itself, for the host
+    link's rates in the same run. Returns (ms, bytes in, bytes out, link)."""
     B = sets or getattr(wl, "e2e_sets", 1 if wl.nsets == 1 else 2)
     ins0, outs0 = wl.e2e_io(0, 0)
     h_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in ins0]
@@ -1303,7 +1305,26 @@ def time_e2e(wl, steps, device, sets=None):
     comp.wait_event(last)
     b.record(comp)
     torch.cuda.synchronize()
-    return a.elapsed_time(b), bi, bo
+    ms = a.elapsed_time(b)
+    # the host link's rates at this moment, each direction alone, on the same
+    # buffers (best of 3): the bound the e2e figure is read against
+    ins, outs = wl.e2e_io(0, 0)
+
+    def copy_ms(pairs):
+        best = float("inf")
+        for _ in range(3):
+            torch.cuda.synchronize()
+            a.record(comp)
+            for dst, src in pairs:
+                dst.copy_(src, non_blocking=True)
+            b.record(comp)
+            torch.cuda.synchronize()
+            best = min(best, a.elapsed_time(b))
+        return best
+    link = {"copy_in_gbs": round(bi / (copy_ms(list(zip(ins, h_in))) * 1e-3) / 1e9, 1),
+            "copy_out_gbs": round(bo / (copy_ms(list(zip(h_out[0], outs))) * 1e-3) / 1e9, 1),
+            "device_sets": B}
+    return ms, bi, bo, link
 
 
 def cpu_model() -> str:
@@ -1643,11 +1664,15 @@ def main():
         "host_wall_s": round(wall, 3),
     }
     if rank == 0 and not args.no_e2e:
-        ms, bi, bo = time_e2e(wl, args.e2e_steps, device, args.e2e_sets)
+        ms, bi, bo, link = time_e2e(wl, args.e2e_steps, device, args.e2e_sets)
         per_step_bytes = alg_bytes / world / args.steps
-        line["e2e"] = {"value": round(per_step_bytes * args.e2e_steps / (ms * 1e-3) / 1e9, 2),
-                       "unit": "GB/s", "h2d_bytes_per_step": int(bi),
-                       "d2h_bytes_per_step": int(bo)}
+        # no step can take less than its larger copy at that direction's rate
+        bound_s = max(bi / (link["copy_in_gbs"] * 1e9), bo / (link["copy_out_gbs"] * 1e9))
+        link["bound_gbs"] = round(per_step_bytes / bound_s / 1e9, 1)
+        e2e = per_step_bytes * args.e2e_steps / (ms * 1e-3) / 1e9
+        link["frac_of_bound"] = round(e2e / link["bound_gbs"], 3)
+        line["e2e"] = {"value": round(e2e, 2), "unit": "GB/s", "h2d_bytes_per_step": int(bi),
+                       "d2h_bytes_per_step": int(bo), "host_link": link}
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
     if rank == 0:

@@ -67,7 +67,8 @@ nvfp4_status quantize_tile16(const nvfp4_config* cfg, const void* x, int64_t sli
   p.C = cols;
   p.gamax = global_amax;
   p.M = cfg->scale_max > 0.0f ? cfg->scale_max : 448.0f;
-  p.key = nvfp4::make_sr_key(cfg->seed, cfg->step);
+  p.seed = cfg->seed;
+  p.step = cfg->step;
   p.r_codes = reinterpret_cast<uint32_t*>(row->codes);
   p.r_scales = row->scales;
   p.r_dq = static_cast<uint4*>(row->dequant);
@@ -333,7 +334,8 @@ nvfp4_status nvfp4_mx_quantize(const nvfp4_config* cfg, const void* x, int64_t s
   p.S = slices;
   p.R = rows;
   p.C = cols;
-  p.key = nvfp4::make_sr_key(cfg->seed, cfg->step);
+  p.seed = cfg->seed;
+  p.step = cfg->step;
   if (do_row) {
     p.r_codes = row->codes;
     p.r_scales = row->scales;

@@ -141,9 +141,12 @@ __device__ __forceinline__ void scale_entry(uint32_t code, float g, float& d, fl
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of two
 // 32x32 -> 64 multiplies, key (seed, step) bumped by the Weyl constants
 // between rounds. The ten round keys are the same for every element of a
-// launch, so the host computes them once and the kernels take them as launch
-// parameters: each round's key XOR then reads a launch constant instead of
-// re-deriving the key schedule for every group of 8 elements.
+// launch, so for the row, dual, per-token and re-quantisation kernels the
+// host computes them once and passes them as launch parameters: each round's
+// key XOR then reads a launch constant instead of re-deriving the key
+// schedule for every group of 8 elements. The 16x16 tile and MXFP8
+// quantisers derive them in the kernel (make_sr_key), which measured faster
+// there: the larger parameter block changed their register allocation.
 struct SrKey {
   uint32_t k0[10], k1[10];
 };

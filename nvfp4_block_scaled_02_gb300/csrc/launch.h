@@ -107,7 +107,7 @@ struct Tile16Params {
   int64_t S, R, C;
   const float* gamax;   // [S]
   float M;
-  SrKey key;            // Philox round keys of (seed, step)
+  uint32_t seed, step;  // stochastic rounding key (round keys derived in the kernel)
   uint32_t* r_codes;    // 8 codes per word, row layout
   uint8_t* r_scales;
   uint4* r_dq;          // may be null

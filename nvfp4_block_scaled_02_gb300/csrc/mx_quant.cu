@@ -76,7 +76,7 @@ __device__ __forceinline__ void encode_rows(const MxParams& p, const uint4 (&v)[
     }
     uint2 codes;
     if constexpr (SR) {
-      codes = e4m3x8_sr_mag(y, sr_group_bits(p.key, 0u, (uint64_t)e[k]));
+      codes = e4m3x8_sr_mag(y, sr_group_bits(make_sr_key(p.seed, p.step), 0u, (uint64_t)e[k]));
       codes.x |= __byte_perm(v[k].x, v[k].y, 0x7531u) & 0x80808080u;  // signs of values 0..3
       codes.y |= __byte_perm(v[k].z, v[k].w, 0x7531u) & 0x80808080u;
     } else {
@@ -120,8 +120,8 @@ __device__ __forceinline__ void encode_cols(const MxParams& p, const uint32_t (&
     const int64_t e = ce + h * p.R;
     uint2 a, b;
     if constexpr (SR) {
-      a = e4m3x8_sr_mag(y, sr_group_bits(p.key, 1u, (uint64_t)e));
-      b = e4m3x8_sr_mag(y + 8, sr_group_bits(p.key, 1u, (uint64_t)e + 8));
+      a = e4m3x8_sr_mag(y, sr_group_bits(make_sr_key(p.seed, p.step), 1u, (uint64_t)e));
+      b = e4m3x8_sr_mag(y + 8, sr_group_bits(make_sr_key(p.seed, p.step), 1u, (uint64_t)e + 8));
       a.x |= sg[h][0];
       a.y |= sg[h][1];
       b.x |= sg[h][2];

@@ -4,14 +4,12 @@
 
 #include <cuda_runtime.h>
 
-#include "device.cuh"
-
 namespace nvfp4 {
 
 struct MxParams {
   const uint16_t* x;      // bf16 [S][R][C]
   int64_t S, R, C;
-  SrKey key;              // Philox round keys of (seed, step)
+  uint32_t seed, step;    // stochastic rounding key (round keys derived in the kernel)
   uint8_t* r_codes;       // E4M3 [S][R][C]
   uint8_t* r_scales;      // E8M0 [S][R][C/32]
   uint8_t* c_codes;       // E4M3 [S][C][R]

@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(kThreads, 6) quant_tile16_kernel(const Tile16P
     float d, inv;
     scale_entry<FMT>(code, ss.g, d, inv);
     uint4 rb = make_uint4(0, 0, 0, 0);
-    if constexpr (SR) rb = sr_group_bits(p.key, 0u, (uint64_t)e[k]);
+    if constexpr (SR) rb = sr_group_bits(make_sr_key(p.seed, p.step), 0u, (uint64_t)e[k]);
     f2 x[4];
     unpack8(v[k], x);
     const uint32_t w = round8<SR>(x, inv, rb);
