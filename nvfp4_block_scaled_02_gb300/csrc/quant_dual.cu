@@ -84,8 +84,10 @@ __global__ void __launch_bounds__(kThreads, SR ? (FOS != 0 ? 2 : 3) : (FOS != 0 
     quant_dual_kernel(const DualParams p, const DualGeom geo) {
   pdl_begin();
   __shared__ __align__(16) uint32_t tile[2][TR * kWords];
-  __shared__ float2 s_tab[2][256];  // block-scale table of the tile in each buffer
-  __shared__ float s_rden[2][2];    // its 1 / (6 g), 1 / (4 g)
+  // block-scale tables of the current slice and the next one (the two swap
+  // when a CTA's run crosses into a new slice) and their 1 / (6 g), 1 / (4 g)
+  __shared__ float2 s_tab[2][256];
+  __shared__ float s_rden[2][2];
   // 4/6 bits of the tile in each buffer: row ballots (one word per two tile
   // rows) and column ballots (one word per warp and column parity)
   __shared__ uint32_t s_rbits[2][TR / 2], s_cbits[2][16];
@@ -106,12 +108,21 @@ __global__ void __launch_bounds__(kThreads, SR ? (FOS != 0 ? 2 : 3) : (FOS != 0 
   const int64_t ro8 = (int64_t)lr0 * (C >> 3) + lq;
   const int64_t co16 = (int64_t)(2 * cpl) * R16 + cq;
   const int64_t rbit_t = (int64_t)t * C16, cbit_t = (int64_t)(t - 128) * R16;
+  // thread t's first chunk from the tile origin, and the step of 16 rows
+  const int64_t fo = (int64_t)lr0 * C + 8 * lq, C16x16 = 16 * C;
 
-  // Where tile T lies.
+  // Where tile T lies: slice, origin, extent, and the element index of its
+  // origin in the row layout (the input's, and the row encoding's) and in the
+  // column layout.
   struct Where {
     int64_t s, r0, c0;
+    int64_t ro, co;
     int nr, nc;
     bool first;  // the slice's first tile
+  };
+  auto finish = [&](Where& w) {
+    w.nr = (int)(R - w.r0 < TR ? R - w.r0 : TR);
+    w.nc = (int)(C - w.c0 < TC ? C - w.c0 : TC);
   };
   auto where = [&](uint32_t T) {
     Where w;
@@ -120,21 +131,44 @@ __global__ void __launch_bounds__(kThreads, SR ? (FOS != 0 ? 2 : 3) : (FOS != 0 
     w.s = s;
     w.r0 = (int64_t)tr * TR;
     w.c0 = (int64_t)tc * TC;
-    w.nr = (int)(R - w.r0 < TR ? R - w.r0 : TR);
-    w.nc = (int)(C - w.c0 < TC ? C - w.c0 : TC);
+    w.ro = w.s * geo.slice_elems + w.r0 * C + w.c0;
+    w.co = w.s * geo.slice_elems + w.c0 * R + w.r0;
     w.first = u == 0;
+    finish(w);
     return w;
+  };
+  // The tile after `w` in the numbering (the next one of this CTA's run):
+  // along a row of tiles the origins move by fixed steps.
+  auto advance = [&](const Where& w) {
+    Where n = w;
+    n.first = false;
+    n.c0 = w.c0 + TC;
+    n.ro = w.ro + TC;
+    n.co = w.co + TC * R;
+    if (n.c0 >= C) {
+      n.c0 = 0;
+      n.r0 = w.r0 + TR;
+      if (n.r0 >= R) {
+        n.r0 = 0;
+        n.s = w.s + 1;
+        n.first = true;
+      }
+      n.ro = n.s * geo.slice_elems + n.r0 * C;
+      n.co = n.s * geo.slice_elems + n.r0;
+    }
+    finish(n);
+    return n;
   };
   // Copy tile `at` into buffer `buf` (one 16-byte cp.async per chunk; chunks
   // past the tensor's edge are zero-filled).
   auto fetch = [&](const Where& at, int buf) {
-    const uint16_t* xt = p.x + at.s * geo.slice_elems + at.r0 * C + at.c0;
+    const uint16_t* xt = p.x + at.ro + fo;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int lr = 16 * k + lr0, lc = 8 * lq;
       const bool ok = lr < at.nr && lc < at.nc;
       uint32_t* dst = &tile[buf][word_of(lr, 4 * lq)];
-      const uint16_t* src = xt + (int64_t)lr * C + lc;
+      const uint16_t* src = xt + k * C16x16;
       if (vec) {
         cp_async16_zfill(dst, ok ? src : p.x, ok ? 16u : 0u);
       } else {  // column-only encoding of a tensor whose rows are not 16 B multiples
@@ -191,30 +225,28 @@ __global__ void __launch_bounds__(kThreads, SR ? (FOS != 0 ? 2 : 3) : (FOS != 0 
   fetch(cur, 0);
   tables(t < kTab ? p.gamax[cur.s] : 0.0f, cur.first, 0);
   uint32_t seen = 0;  // magnitude maximum of every value this thread encodes
-  int buf = 0;
+  int buf = 0, tb = 0;  // tile buffer, table buffer (flips with the slice)
   for (uint32_t T = T0; T < T1; ++T, buf ^= 1) {
     cp_async_wait<0>();  // this thread's copies of tile T have landed
     __syncthreads();     // everyone's have, and its tables are built; the
                          // previous tile is done with the other buffers
     const bool more = T + 1 < T1;
-    const Where nx = more ? where(T + 1) : cur;
+    const Where nx = more ? advance(cur) : cur;
     if (more) fetch(nx, buf ^ 1);  // in flight while this tile is encoded
     const bool new_slice = more && nx.s != cur.s;
     const float gam_next = new_slice && t < kTab ? p.gamax[nx.s] : 0.0f;
     if (FOS != 0 && T != T0) flush(buf ^ 1, pend);
     SliceScale ss;
-    ss.rden6 = s_rden[buf][0];
-    ss.rden4 = s_rden[buf][1];
-    const float2* tab = s_tab[buf];
+    ss.rden6 = s_rden[tb][0];
+    ss.rden4 = s_rden[tb][1];
+    const float2* tab = s_tab[tb];
     const uint32_t* tl = tile[buf];
-    const int64_t slice0 = cur.s * geo.slice_elems;
     const int nr = cur.nr, nc = cur.nc;
 
     // ---- row blocks: chunks from the staged tile ----------------------------
     if constexpr (ROWS) {
       const bool want_dq = p.r_dq != nullptr;
-      const int64_t tile0 = slice0 + cur.r0 * C + cur.c0;  // row-layout index of the tile origin
-      const int64_t g8 = (tile0 >> 3) + ro8;               // chunk 0, in groups of 8 values
+      const int64_t g8 = (cur.ro >> 3) + ro8;  // chunk 0, in groups of 8 values
       uint32_t* const rc = reinterpret_cast<uint32_t*>(p.r_codes) + g8;
       uint4* const rd = reinterpret_cast<uint4*>(p.r_dq) + g8;
       uint8_t* const rs = p.r_scales + (g8 >> 1);
@@ -247,8 +279,7 @@ __global__ void __launch_bounds__(kThreads, SR ? (FOS != 0 ? 2 : 3) : (FOS != 0 
     {
       const bool want_dq = p.c_dq != nullptr;
       const bool rows_ok = 16 * cq < nr;
-      const int64_t tile0 = slice0 + cur.c0 * R + cur.r0;  // column-layout index of the tile origin
-      const int64_t g16 = (tile0 >> 4) + co16;             // column 2 cpl, in groups of 16 values
+      const int64_t g16 = (cur.co >> 4) + co16;  // column 2 cpl, in groups of 16 values
       uint2* const ccodes = reinterpret_cast<uint2*>(p.c_codes) + g16;
       uint4* const cdq = reinterpret_cast<uint4*>(p.c_dq) + 2 * g16;
       uint8_t* const cscales = p.c_scales + g16;
@@ -300,15 +331,12 @@ __global__ void __launch_bounds__(kThreads, SR ? (FOS != 0 ? 2 : 3) : (FOS != 0 
       pend.nr = nr;
       pend.nc = nc;
     }
-    // the next tile's tables, ready by the next barrier (built after this
-    // tile's work, so reading the slice's amax costs no wait)
-    if (more) {
-      if (new_slice) {
-        tables(gam_next, nx.first, buf ^ 1);
-      } else if (t < kTab) {
-        s_tab[buf ^ 1][t] = tab[t];
-        if (t < 2) s_rden[buf ^ 1][t] = s_rden[buf][t];
-      }
+    // the next slice's tables in the other table buffer, ready by the next
+    // barrier (built after this tile's work, so reading its amax costs no
+    // wait; that buffer's last readers finished before this tile's barrier)
+    if (new_slice) {
+      tables(gam_next, nx.first, tb ^ 1);
+      tb ^= 1;
     }
     cur = nx;
   }
