@@ -27,6 +27,34 @@ inline FastDiv make_fastdiv(uint32_t d) {
   return f;
 }
 
+// Where the tile of a one-tile-per-CTA kernel lies: tiles numbered slice by
+// slice, row of tiles by row of tiles, column tiles fastest. The divisions by
+// the tile counts are FastDiv multiplies (the grid holds < 2^31 tiles), and
+// the slice size is precomputed, so no CTA runs a 64-bit division.
+struct TileGeom {
+  FastDiv by_tiles_c, by_tiles_slice;
+  uint32_t tiles_c, tiles_slice;
+  int64_t slice_elems;  // R * C
+};
+inline TileGeom make_tile_geom(int64_t R, int64_t C, int64_t TR, int64_t TC) {
+  TileGeom g;
+  const int64_t tc = (C + TC - 1) / TC, tr = (R + TR - 1) / TR;
+  g.tiles_c = (uint32_t)tc;
+  g.tiles_slice = (uint32_t)(tc * tr);
+  g.by_tiles_c = make_fastdiv(g.tiles_c);
+  g.by_tiles_slice = make_fastdiv(g.tiles_slice);
+  g.slice_elems = R * C;
+  return g;
+}
+// Slice, tile row and tile column of tile t.
+__device__ __forceinline__ void tile_of(uint32_t t, const TileGeom& g, uint32_t& s, uint32_t& tr,
+                                        uint32_t& tc) {
+  s = fastdiv(t, g.by_tiles_slice);
+  const uint32_t u = t - s * g.tiles_slice;
+  tr = fastdiv(u, g.by_tiles_c);
+  tc = u - tr * g.tiles_c;
+}
+
 // CTAs of `kernel` (with `threads` threads and `smem` dynamic shared memory)
 // that fit on one SM at once, at least 1: sizes persistent grids to a single
 // wave.

@@ -60,8 +60,9 @@ __device__ __forceinline__ uint2 e4m3x8_sr_mag(const float* y, const uint4& rb) 
 // exponents ex[k]; writes codes and (one lane of four) the scale byte.
 template <bool SR>
 __device__ __forceinline__ void encode_rows(const MxParams& p, const uint4 (&v)[4],
-                                            const int (&ex)[4], const int64_t (&e)[4],
+                                            const int (&ex)[4], int64_t e0, int64_t step,
                                             const bool (&ok)[4], int lane) {
+  const int64_t e[4] = {e0, e0 + step, e0 + 2 * step, e0 + 3 * step};
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const f2 sc = make_float2(exp2_neg(ex[k]), exp2_neg(ex[k]));
@@ -84,7 +85,7 @@ __device__ __forceinline__ void encode_rows(const MxParams& p, const uint4 (&v)[
     }
     if (ok[k]) {
       __stcs(reinterpret_cast<uint2*>(p.r_codes + e[k]), codes);
-      if ((lane & 3) == 0) p.r_scales[e[k] / 32] = (uint8_t)(ex[k] + 127);
+      if ((lane & 3) == 0) p.r_scales[e[k] >> 5] = (uint8_t)(ex[k] + 127);
     }
   }
 }
@@ -132,42 +133,41 @@ __device__ __forceinline__ void encode_cols(const MxParams& p, const uint32_t (&
     }
     if (h ? ok1 : ok0) {
       __stcs(reinterpret_cast<uint4*>(p.c_codes + e), make_uint4(a.x, a.y, b.x, b.y));
-      if (write_scale) p.c_scales[e / 32] = (uint8_t)(ex[h] + 127);
+      if (write_scale) p.c_scales[e >> 5] = (uint8_t)(ex[h] + 127);
     }
   }
 }
 
 template <bool SR, bool ROWS, bool COLS>
-__device__ __forceinline__ void mx_quant_tile(const MxParams& p, int64_t tiles_r,
-                                              int64_t tiles_c) {
+__device__ __forceinline__ void mx_quant_tile(const MxParams& p, const TileGeom& geo) {
   __shared__ __align__(16) uint32_t tile[COLS ? TR * kWords : 4];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t R = p.R, C = p.C;
-  const int64_t bid = blockIdx.x;
-  const int64_t tc = bid % tiles_c, tr = (bid / tiles_c) % tiles_r, s = bid / (tiles_c * tiles_r);
-  const int64_t r0 = tr * TR, c0 = tc * TC;
-  const uint16_t* xs = p.x + s * R * C;
+  uint32_t s32, tr32, tc32;
+  tile_of(blockIdx.x, geo, s32, tr32, tc32);
+  const int64_t s = s32, r0 = (int64_t)tr32 * TR, c0 = (int64_t)tc32 * TC;
+  const int64_t slice0 = s * geo.slice_elems;
   const bool vec = (C % 8) == 0;
 
   // ---- 1: load, flag non-finite values, encode the row blocks ------------
+  // chunk k of this thread: row 16 k + t / 16, columns 8 (t % 16) .. of the tile
+  const int lr0 = threadIdx.x / kChunksPerRow, lc = (threadIdx.x % kChunksPerRow) * 8;
+  const int64_t e0 = slice0 + (r0 + lr0) * C + c0 + lc, step = (int64_t)(kThreads / kChunksPerRow) * C;
+  const bool c_ok = c0 + lc < C;
   uint4 v[4];
   bool ok[4];
-  int64_t e[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const int chunk = k * kThreads + threadIdx.x;
-    const int lr = chunk / kChunksPerRow, lc = (chunk % kChunksPerRow) * 8;
-    const int64_t r = r0 + lr, c = c0 + lc;
-    ok[k] = r < R && c < C;
-    e[k] = (s * R + r) * C + c;  // flat row-layout index
+    ok[k] = r0 + lr0 + 16 * k < R && c_ok;
+    const int64_t ek = e0 + k * step;  // flat row-layout index
     v[k] = make_uint4(0, 0, 0, 0);
     if (ok[k]) {
       if (vec) {
-        v[k] = __ldcs(reinterpret_cast<const uint4*>(xs + r * C + c));
+        v[k] = __ldcs(reinterpret_cast<const uint4*>(p.x + ek));
       } else {  // column-only encoding of a tensor whose rows are not 16 B multiples
         uint32_t h[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) h[i] = (c + i < C) ? xs[r * C + c + i] : 0u;
+        for (int i = 0; i < 8; ++i) h[i] = (c0 + lc + i < C) ? p.x[ek + i] : 0u;
         v[k] = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
                           h[6] | (h[7] << 16));
       }
@@ -183,7 +183,7 @@ __device__ __forceinline__ void mx_quant_tile(const MxParams& p, int64_t tiles_r
       m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
       ex[k] = mx_shared_exp(__uint_as_float(m << 16));
     }
-    encode_rows<SR>(p, v, ex, e, ok, lane);
+    encode_rows<SR>(p, v, ex, e0, step, ok, lane);
   } else {
 #pragma unroll
     for (int k = 0; k < 4; ++k)
@@ -213,7 +213,7 @@ __device__ __forceinline__ void mx_quant_tile(const MxParams& p, int64_t tiles_r
     int ex[2];
     ex[0] = mx_shared_exp(__uint_as_float(mm << 16));
     ex[1] = mx_shared_exp(__uint_as_float(mm & 0xFFFF0000u));
-    const int64_t ce = (s * C + cg) * R + r0 + 16 * q;  // flat column-layout index
+    const int64_t ce = (int64_t)s32 * geo.slice_elems + cg * R + r0 + 16 * q;  // column layout
     const bool ok0 = row_ok && cg < C, ok1 = row_ok && cg + 1 < C;
     encode_cols<SR>(p, w, ex, ce, ok0, ok1, (q & 1) == 0);
   }
@@ -226,15 +226,14 @@ __device__ __forceinline__ void mx_quant_tile(const MxParams& p, int64_t tiles_r
 // 4 % slower).
 template <bool ROWS, bool COLS>
 __global__ void __launch_bounds__(kThreads, 6) mx_quant_rne_kernel(const MxParams p,
-                                                                   int64_t tiles_r,
-                                                                   int64_t tiles_c) {
+                                                                   const TileGeom geo) {
   pdl_begin();
-  mx_quant_tile<false, ROWS, COLS>(p, tiles_r, tiles_c);
+  mx_quant_tile<false, ROWS, COLS>(p, geo);
 }
 template <bool ROWS, bool COLS>
-__global__ void mx_quant_sr_kernel(const MxParams p, int64_t tiles_r, int64_t tiles_c) {
+__global__ void mx_quant_sr_kernel(const MxParams p, const TileGeom geo) {
   pdl_begin();
-  mx_quant_tile<true, ROWS, COLS>(p, tiles_r, tiles_c);
+  mx_quant_tile<true, ROWS, COLS>(p, geo);
 }
 
 template <bool SR, bool ROWS, bool COLS>
@@ -242,12 +241,13 @@ cudaError_t launch_t(const MxParams& p, cudaStream_t st) {
   const int64_t tiles_r = (p.R + TR - 1) / TR, tiles_c = (p.C + TC - 1) / TC;
   const int64_t n = p.S * tiles_r * tiles_c;
   if (n > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
+  const TileGeom geo = make_tile_geom(p.R, p.C, TR, TC);
   if constexpr (SR)
     return launch_pdl(mx_quant_sr_kernel<ROWS, COLS>, dim3((unsigned)n), dim3(kThreads), st, p,
-                      tiles_r, tiles_c);
+                      geo);
   else
     return launch_pdl(mx_quant_rne_kernel<ROWS, COLS>, dim3((unsigned)n), dim3(kThreads), st, p,
-                      tiles_r, tiles_c);
+                      geo);
 }
 
 }  // namespace

@@ -51,32 +51,33 @@ __device__ __forceinline__ uint32_t nibbles4(uint32_t B, int j) {
 // (E4M3 with SR: 101.1 vs 103.6 us on a 14336 x 4096 weight).
 template <int FMT, bool SR>
 __global__ void __launch_bounds__(kThreads, 6) quant_tile16_kernel(const Tile16Params p,
-                                                                int64_t tiles_r, int64_t tiles_c) {
+                                                                const TileGeom geo) {
   pdl_begin();
   __shared__ uint32_t s_codes[TR * kChunksPerRow];
   __shared__ uint32_t s_tmax[4][8];  // bf16 bits of each scale tile's amax
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t R = p.R, C = p.C;
-  const int64_t bid = blockIdx.x;
-  const int64_t tc = bid % tiles_c, tr = (bid / tiles_c) % tiles_r, s = bid / (tiles_c * tiles_r);
-  const int64_t r0 = tr * TR, c0 = tc * TC;
+  uint32_t s32, tr32, tc32;
+  tile_of(blockIdx.x, geo, s32, tr32, tc32);
+  const int64_t s = s32, r0 = (int64_t)tr32 * TR, c0 = (int64_t)tc32 * TC;
+  const int64_t slice0 = s * geo.slice_elems;
 
   // ---- 1: loads (thread t's chunk k lies in band k, tile column (t % 16) / 2)
+  // chunk k of thread t: row 16 k + t / 16, columns 8 (t % 16) .. of the region
+  const int lr0 = tid / kChunksPerRow, lc = (tid % kChunksPerRow) * 8;
+  const int64_t e0 = slice0 + (r0 + lr0) * C + c0 + lc, step = (int64_t)(kThreads / kChunksPerRow) * C;
   uint4 v[4];
   bool ok[4];
   int64_t e[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const int chunk = k * kThreads + tid;
-    const int lr = chunk / kChunksPerRow, lc = (chunk % kChunksPerRow) * 8;
-    const int64_t r = r0 + lr, c = c0 + lc;
-    ok[k] = r < R && c < C;
-    e[k] = (s * R + r) * C + c;  // flat row-layout index
-    v[k] = ok[k] ? __ldcs(p.x + e[k] / 8) : make_uint4(0, 0, 0, 0);
+    ok[k] = r0 + lr0 + 16 * k < R && c0 + lc < C;
+    e[k] = e0 + k * step;  // flat row-layout index
+    v[k] = ok[k] ? __ldcs(p.x + (e[k] >> 3)) : make_uint4(0, 0, 0, 0);
   }
   if (tid < 32) (&s_tmax[0][0])[tid] = 0u;
   const SliceScale ss = slice_scale(p.gamax[s], p.M);
-  if (ss.bad && tid == 0 && tr == 0 && tc == 0) flag(p.status, NVFP4_DEV_BAD_AMAX_BIT);
+  if (ss.bad && tid == 0 && tr32 == 0 && tc32 == 0) flag(p.status, NVFP4_DEV_BAD_AMAX_BIT);
   __syncthreads();  // s_tmax zeroed
   const int tcol = (tid % kChunksPerRow) >> 1;
 #pragma unroll
@@ -105,12 +106,12 @@ __global__ void __launch_bounds__(kThreads, 6) quant_tile16_kernel(const Tile16P
     unpack8(v[k], x);
     const uint32_t w = round8<SR>(x, inv, rb);
     if (ok[k]) {
-      p.r_codes[e[k] / 8] = w;
-      if ((c16 & 1) == 0) p.r_scales[e[k] / 16] = (uint8_t)code;
+      p.r_codes[e[k] >> 3] = w;
+      if ((c16 & 1) == 0) p.r_scales[e[k] >> 4] = (uint8_t)code;
       if (want_dq) {
         f2 qv[4];
         e2m1x8_to_f2(w, qv);
-        __stcs(p.r_dq + e[k] / 8, dequant8(qv, d));
+        __stcs(p.r_dq + (e[k] >> 3), dequant8(qv, d));
       }
     }
     if (want_cols) s_codes[code_of(lr, c16)] = w;
@@ -140,16 +141,16 @@ __global__ void __launch_bounds__(kThreads, 6) quant_tile16_kernel(const Tile16P
   for (int j = 0; j < 2; ++j) {
     const uint32_t cw0 = nibbles4(B[0], j) | (nibbles4(B[1], j) << 16);
     const uint32_t cw1 = nibbles4(B[2], j) | (nibbles4(B[3], j) << 16);
-    const int64_t ce = (s * C + cc + j) * R + rr;
+    const int64_t ce = slice0 + (cc + j) * R + rr;
     if (rr < R && cc + j < C) {
-      *reinterpret_cast<uint2*>(p.c_codes + ce / 8) = make_uint2(cw0, cw1);
-      p.c_scales[ce / 16] = (uint8_t)code;
+      *reinterpret_cast<uint2*>(p.c_codes + (ce >> 3)) = make_uint2(cw0, cw1);
+      p.c_scales[ce >> 4] = (uint8_t)code;
       if (col_dq) {
         f2 qv[4];
         e2m1x8_to_f2(cw0, qv);
-        __stcs(p.c_dq + ce / 8, dequant8(qv, d));
+        __stcs(p.c_dq + (ce >> 3), dequant8(qv, d));
         e2m1x8_to_f2(cw1, qv);
-        __stcs(p.c_dq + ce / 8 + 1, dequant8(qv, d));
+        __stcs(p.c_dq + (ce >> 3) + 1, dequant8(qv, d));
       }
     }
   }
@@ -161,7 +162,7 @@ cudaError_t launch_t(const Tile16Params& p, cudaStream_t st) {
   const int64_t n = p.S * tiles_r * tiles_c;
   if (n > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
   return launch_pdl(quant_tile16_kernel<FMT, SR>, dim3((unsigned)n), dim3(kThreads), st, p,
-                    tiles_r, tiles_c);
+                    make_tile_geom(p.R, p.C, TR, TC));
 }
 
 }  // namespace

@@ -122,8 +122,8 @@ __device__ __forceinline__ void load_src(const RequantParams& p, bool valid, con
     for (int k = 0; k < 2; ++k) {
       if (r0 + L.row0 + 32 * k < p.R) {
         const int64_t e = base + L.off0 + k * 32 * p.C;  // flat element index, e % 16 == 0
-        v.codes[k] = __ldcs(reinterpret_cast<const uint2*>(p.codes + e / 2));
-        v.scale[k] = __ldcs(p.scales + e / 16);
+        v.codes[k] = __ldcs(reinterpret_cast<const uint2*>(p.codes + (e >> 1)));
+        v.scale[k] = __ldcs(p.scales + (e >> 4));
       }
     }
   }
@@ -194,6 +194,10 @@ __global__ void __launch_bounds__(kThreads, min_blocks(TARGET, SR, FOS)) requant
   SrcRegs v;
   load_src(p, ntiles > 0, ti, L, v);
   int64_t cur_slice = -1;
+  // 4/6 bitmap of the current slice, and the flat index of its first block
+  const int64_t W = (R * C / 16 + 31) / 32;
+  uint32_t* words = p.out_choice;
+  int64_t slice_b0 = 0;
   SliceScale ss_dst{};
   for (int64_t it = 0; it < ntiles; ++it) {  // block-uniform
     ti = tn;
@@ -201,6 +205,10 @@ __global__ void __launch_bounds__(kThreads, min_blocks(TARGET, SR, FOS)) requant
     if (ti.s != cur_slice) {  // block-uniform; the previous tile ended with a barrier
       build_tables<DFMT, NV>(p, ti.s, s_src, s_d, s_inv, ss_dst);
       cur_slice = ti.s;
+      if constexpr (NV && FOS != 0) {
+        words = p.out_choice + ti.s * W;
+        slice_b0 = ti.s * (R * C / 16);
+      }
       __syncthreads();
     }
     // ---- 1: de-quantise this thread's two blocks into the tile ---------
@@ -277,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, min_blocks(TARGET, SR, FOS)) requant
         }
         if (ok) {
           __stcs(reinterpret_cast<uint4*>(p.out_codes + e0), w);
-          if ((q & 1) == 0) p.out_scales[e0 / 32] = (uint8_t)((h ? ex1 : ex0) + 127);
+          if ((q & 1) == 0) p.out_scales[e0 >> 5] = (uint8_t)((h ? ex1 : ex0) + 127);
         }
       }
     } else {
@@ -302,17 +310,15 @@ __global__ void __launch_bounds__(kThreads, min_blocks(TARGET, SR, FOS)) requant
             lo, hi, amax, ss_dst, TableScales{s_d, s_inv}, sr_bits_or_zero<SR>(p, (uint64_t)e0),
             sr_bits_or_zero<SR>(p, (uint64_t)e0 + 8), false, FOS == 2 ? p.rule : 0);
         if (ok) {
-          __stcs(reinterpret_cast<uint2*>(p.out_codes + e0 / 2), make_uint2(r.codes[0], r.codes[1]));
-          p.out_scales[e0 / 16] = (uint8_t)r.scale;
+          __stcs(reinterpret_cast<uint2*>(p.out_codes + (e0 >> 1)), make_uint2(r.codes[0], r.codes[1]));
+          p.out_scales[e0 >> 4] = (uint8_t)r.scale;
         }
         if constexpr (FOS != 0) {
           // bits of this column's 4 blocks: lanes 4 cp .. 4 cp + 3
           const uint32_t bits =
               (__ballot_sync(0xFFFFFFFFu, ok && r.pick4) >> (4 * cp)) & 0xFu;
           if (q == 0 && bits) {
-            const int64_t b0 = ((c0 + c) * R + r0) / 16;  // block index within the slice
-            const int64_t W = (R * C / 16 + 31) / 32;
-            uint32_t* words = p.out_choice + ti.s * W;
+            const int64_t b0 = (e0 >> 4) - slice_b0;  // block index within the slice
             const int off = (int)(b0 & 31);
             atomicOr(words + (b0 >> 5), bits << off);
             if (off > 28 && (bits >> (32 - off))) atomicOr(words + (b0 >> 5) + 1, bits >> (32 - off));
