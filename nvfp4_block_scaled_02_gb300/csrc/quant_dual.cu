@@ -3,13 +3,14 @@
 // (End-to-End 4-Bit Training, "Block-scaled backward passes": the transposed
 // operand groups each value with the 15 values above/below it instead).
 //
-// One CTA (256 threads) per 64 x 128 tile of one slice:
-//  1. every thread loads 4 chunks of 8 bf16 (128-bit loads; a warp covers two
-//     full 256 B tile rows) and stores them into a 16 KiB shared tile of
-//     32-bit words (two columns each), word w of row r kept at
-//     w ^ (((r >> 4) & 3) << 3);
-//  2. in BOTH mode the row blocks are encoded straight from the registers,
-//     lanes 2m and 2m+1 holding the two halves of a block (encode_half8);
+// A CTA (256 threads) takes a run of consecutive 64 x 128 tiles; for each:
+//  1. the tile arrives by cp.async, while the previous one is encoded, into
+//     one of two 16 KiB shared buffers of 32-bit words (two columns each),
+//     every thread copying 4 chunks of 8 bf16 (a warp covers two full 256 B
+//     tile rows); word w of row r is kept at w ^ (((r >> 4) & 3) << 3);
+//  2. in BOTH mode the row blocks are read back as 128-bit chunks and
+//     encoded with lanes 2m and 2m+1 holding the two halves of a block
+//     (encode_half8);
 //  3. lane (cp, q) = (lane >> 2, lane & 3) of warp w takes column pair
 //     8 w + cp in the 16-row band q: it reads one word per row (with the
 //     swizzle the 32 lanes hit 32 distinct banks) and encodes the two column
@@ -17,9 +18,9 @@
 //     of a column are adjacent lanes, so each column's 64 rows of codes
 //     (32 B), scales (4 B) and dequant (128 B, two instructions) leave from
 //     one store instruction.
-// The 4/6 bits of the tile are gathered in shared memory (one ballot per warp
-// and half-block) and OR-ed into the pre-zeroed bitmaps once per tile: a
-// tile's bits share words with other tiles. Non-finite inputs are gathered
+// The 4/6 bits of a tile are gathered in shared memory (one ballot per warp
+// and half-block) and OR-ed into the pre-zeroed bitmaps during the next tile:
+// a tile's bits share words with other tiles. Non-finite inputs are gathered
 // per thread and flagged once.
 #include "encode.cuh"
 #include "launch.h"
