@@ -168,10 +168,6 @@ class Workload:
         raise NotImplementedError
 
 
-def _alloc_like(shape, dtype, device):
-    return torch.empty(shape, dtype=dtype, device=device)
-
-
 class Activation(Workload):
     """Activations [S x H] = [8192 x 4096]: amax + row quantise with 4/6."""
 
