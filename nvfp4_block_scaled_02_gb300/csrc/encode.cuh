@@ -23,20 +23,6 @@ __device__ __forceinline__ uint32_t round8(const f2 (&x)[4], float inv, const ui
   if constexpr (!SR) return e2m1x8_rn(y);
   else return sr8(y, rb);
 }
-// The same with the codes' sign bits given (sign = e2m1_signs(x)): x * inv
-// has the sign of x for every inv >= 0 (zeros included), so the two 4/6
-// candidates of one block share them.
-template <bool SR>
-__device__ __forceinline__ uint32_t round8s(const f2 (&x)[4], float inv, const uint4& rb,
-                                            uint32_t sign) {
-  f2 y[4];
-  const f2 iv = make_float2(inv, inv);
-#pragma unroll
-  for (int k = 0; k < 4; ++k) y[k] = f2_mul(x[k], iv);
-  if constexpr (!SR) return e2m1x8_rn(y);
-  else return sr8_signed(y, rb, sign);
-}
-
 // Sum over 8 values of (x - q d)^2 in the fixed order: even and odd positions
 // accumulate separately with fma from +0 (one f32x2 accumulator), then
 // even + odd. Also returns the decoded code values.
@@ -82,11 +68,6 @@ __device__ __forceinline__ float half_metric_q(const f2 (&x)[4], const f2 (&q)[4
     acc = make_float2(fmaxf(acc.x, fabsf(e.x)), fmaxf(acc.y, fabsf(e.y)));
   }
   return fmaxf(acc.x, acc.y);
-}
-__device__ __forceinline__ float half_metric(const f2 (&x)[4], uint32_t codes, float d, int rule) {
-  f2 q[4];
-  e2m1x8_to_f2(codes, q);
-  return half_metric_q(x, q, d, rule);
 }
 __device__ __forceinline__ float combine_halves(float h0, float h1, int rule) {
   return rule == 2 ? fmaxf(h0, h1) : __fadd_rn(h0, h1);
@@ -335,18 +316,6 @@ __device__ __forceinline__ HalfOut encode_half8(const f2 (&x)[4], uint32_t amax_
     if (want_dq) r.dq = dequant8_pick(v4, v6, r.pick4, e4.x, e6.x);
   }
   return r;
-}
-
-// Per-slice block-scale table in shared memory: for every code c of the
-// format, d = dec(c) * g and inv = 1/d. Built by the first 256 threads.
-template <int FMT>
-__device__ __forceinline__ void build_scale_table(float* s_d, float* s_inv, float g) {
-  for (int c = threadIdx.x; c < 256; c += blockDim.x) {
-    float d, inv;
-    scale_entry<FMT>((uint32_t)c, g, d, inv);
-    s_d[c] = d;
-    s_inv[c] = inv;
-  }
 }
 
 }  // namespace nvfp4
