@@ -145,3 +145,16 @@ def test_sweep_candidate_count_edges(bench):
     v = np.full((1, 16), 0.75, np.float32)
     assert bench.sweep_candidates_per_block((v.view(np.uint32) >> 16).astype(np.uint16),
                                             2688.0 * 0.75) < 60
+
+
+def test_committed_counts_match_the_sources(bench):
+    """Every instruction count and traffic figure under profiles/ was taken
+    from the sources the kernels are built from now (a kernel changed since
+    its capture would report no issue or traffic figure)."""
+    import json
+    for fname in ("inst.json", "traffic.json"):
+        with open(os.path.join(ROOT, "profiles", fname)) as f:
+            d = json.load(f)
+        for cfg, kernels in d["workloads"].items():
+            for kernel, e in kernels.items():
+                assert e["source_sha"] == bench.kernel_source_hash(kernel), (fname, cfg, kernel)
