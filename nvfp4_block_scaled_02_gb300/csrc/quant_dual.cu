@@ -81,7 +81,7 @@ struct DualGeom {
 };
 
 template <int FMT, bool SR, int FOS, bool ROWS>
-__global__ void __launch_bounds__(kThreads, SR ? (FOS != 0 ? 2 : 3) : (FOS != 0 ? 3 : 4))
+__global__ void __launch_bounds__(kThreads, SR ? (FOS != 0 ? 2 : 3) : (FOS == 2 ? 3 : 4))
     quant_dual_kernel(const DualParams p, const DualGeom geo) {
   pdl_begin();
   __shared__ __align__(16) uint32_t tile[2][TR * kWords];
