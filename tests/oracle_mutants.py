@@ -130,6 +130,7 @@ MUTANTS = [
     ("rq_transpose", "for (int64_t c = 0; c < C; ++c) xt[s * R * C + c * R + r] = xh[s * R * C + r * C + c];", "for (int64_t c = 0; c < C; ++c) xt[s * R * C + c * R + r] = xh[s * R * C + r * C + (C - 1 - c)];"),
     ("mx_scale_sign", "float y = ldexpf(vb[i], -e);", "float y = ldexpf(vb[i], e);"),
     ("tile_sr_idx", "if (rounding) v16[i] = orc_sr_bits(seed, step, 0, (uint64_t)(e0 + i));", "if (rounding) v16[i] = orc_sr_bits(seed, step, 0, (uint64_t)(e0 + 15 - i));"),
+    ("tile_amax_row", "for (int rr = 0; rr < 16; ++rr)\n          for (int cc = 0; cc < 16; ++cc)", "for (int rr = 0; rr < 1; ++rr)\n          for (int cc = 0; cc < 16; ++cc)"),
 ]
 
 EXPECTED_SURVIVORS = {"block_sum_order"}
