@@ -1230,7 +1230,7 @@ def time_ours(wl, args, world, local):
     return statistics.median(passes), stats, per_kernel, clk, wall
 
 
-def time_e2e(wl, steps, device, sets=None):
+def time_e2e(wl, steps, device, sets=None, passes=3):
     """The same metric through the C ABI with host buffers, as a user streaming
     tensors through it would run it: every step copies its inputs from pinned
     host memory to the device (copy-in stream), runs the kernels (the
@@ -1239,7 +1239,9 @@ def time_e2e(wl, steps, device, sets=None):
     the workload's e2e_sets, else 2, or 1 when the workload holds a single
     set); events order each buffer's reuse, so
     one step's copies overlap its neighbours' compute and copies. Events
-    bracket the whole run on all three streams. Afterwards the inputs' and
+    bracket each pass of `steps` steps on all three streams; the median of
+    `passes` passes is the figure (the host and its memory are shared, so one
+    pass can catch a transient slowdown). Afterwards the inputs' and
     outputs' copies are timed alone, each direction by itself, for the host
     link's rates in the same run. Returns (ms, bytes in, bytes out, link)."""
     B = sets or getattr(wl, "e2e_sets", 1 if wl.nsets == 1 else 2)
@@ -1288,20 +1290,23 @@ def time_e2e(wl, steps, device, sets=None):
     for k in range(2):
         step(k)
     torch.cuda.synchronize()
-    in_free[:] = [None] * B
-    out_free[:] = [None] * B
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
-    a.record(comp)
-    cin.wait_event(a)
-    cout.wait_event(a)
-    last = None
-    for k in range(steps):
-        last = step(k)
-    comp.wait_event(last)
-    b.record(comp)
-    torch.cuda.synchronize()
-    ms = a.elapsed_time(b)
+    pass_ms = []
+    for _ in range(max(1, passes)):
+        in_free[:] = [None] * B
+        out_free[:] = [None] * B
+        a.record(comp)
+        cin.wait_event(a)
+        cout.wait_event(a)
+        last = None
+        for k in range(steps):
+            last = step(k)
+        comp.wait_event(last)
+        b.record(comp)
+        torch.cuda.synchronize()
+        pass_ms.append(a.elapsed_time(b))
+    ms = statistics.median(pass_ms)
     # the host link's rates at this moment, each direction alone, on the same
     # buffers (best of 3): the bound the e2e figure is read against
     ins, outs = wl.e2e_io(0, 0)
@@ -1319,7 +1324,7 @@ def time_e2e(wl, steps, device, sets=None):
         return best
     link = {"copy_in_gbs": round(bi / (copy_ms(list(zip(ins, h_in))) * 1e-3) / 1e9, 1),
             "copy_out_gbs": round(bo / (copy_ms(list(zip(h_out[0], outs))) * 1e-3) / 1e9, 1),
-            "device_sets": B}
+            "device_sets": B, "passes_ms": [round(t, 3) for t in pass_ms]}
     return ms, bi, bo, link
 
 
@@ -1552,6 +1557,8 @@ def main():
     ap.add_argument("--config", type=int, default=5, choices=sorted(WORKLOADS) + [FOS_OVERHEAD])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--e2e-passes", type=int, default=3,
+                    help="timed end-to-end passes; the median is reported")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-rows", type=int, default=512)
     ap.add_argument("--no-cpu", action="store_true")
@@ -1660,7 +1667,8 @@ def main():
         "host_wall_s": round(wall, 3),
     }
     if rank == 0 and not args.no_e2e:
-        ms, bi, bo, link = time_e2e(wl, args.e2e_steps, device, args.e2e_sets)
+        ms, bi, bo, link = time_e2e(wl, args.e2e_steps, device, args.e2e_sets,
+                                       args.e2e_passes)
         per_step_bytes = alg_bytes / world / args.steps
         # no step can take less than its larger copy at that direction's rate
         bound_s = max(bi / (link["copy_in_gbs"] * 1e9), bo / (link["copy_out_gbs"] * 1e9))
