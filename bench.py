@@ -1346,6 +1346,15 @@ def time_e2e(wl, steps, device, sets=None, passes=3):
     return ms, bi, bo, link
 
 
+def link_bound_gbs(step_bytes: float, bytes_in: float, bytes_out: float, link: dict) -> float:
+    """The end-to-end figure's ceiling in GB/s of algorithmic bytes: no step
+    can take less than its larger copy at that direction's rate, nor less
+    than both copies at the rate the two directions reach together."""
+    step_s = max(bytes_in / (link["copy_in_gbs"] * 1e9), bytes_out / (link["copy_out_gbs"] * 1e9),
+                 (bytes_in + bytes_out) / (link["copy_both_gbs"] * 1e9))
+    return step_bytes / step_s / 1e9
+
+
 def cpu_model() -> str:
     """The host CPU's model name (Linux /proc/cpuinfo; the Arm machines give a
     part number instead)."""
@@ -1698,11 +1707,7 @@ def main():
             if best is None or e2e > best[0]:
                 best = (e2e, bi, bo, link)
         e2e, bi, bo, link = best
-        # no step can take less than its larger copy at that direction's rate,
-        # nor less than both copies at the rate the two directions reach together
-        bound_s = max(bi / (link["copy_in_gbs"] * 1e9), bo / (link["copy_out_gbs"] * 1e9),
-                      (bi + bo) / (link["copy_both_gbs"] * 1e9))
-        link["bound_gbs"] = round(per_step_bytes / bound_s / 1e9, 1)
+        link["bound_gbs"] = round(link_bound_gbs(per_step_bytes, bi, bo, link), 1)
         link["frac_of_bound"] = round(e2e / link["bound_gbs"], 3)
         link["by_device_sets"] = by_sets
         line["e2e"] = {"value": round(e2e, 2), "unit": "GB/s", "h2d_bytes_per_step": int(bi),

@@ -158,3 +158,18 @@ def test_committed_counts_match_the_sources(bench):
         for cfg, kernels in d["workloads"].items():
             for kernel, e in kernels.items():
                 assert e["source_sha"] == bench.kernel_source_hash(kernel), (fname, cfg, kernel)
+
+
+def test_link_bound_takes_the_slowest_copy_arrangement(bench):
+    """The end-to-end ceiling: the larger one-way copy, or both copies at the
+    rate the two directions reach together, whichever takes longer (the MoE
+    step's 1.9 GB in and 4.8 GB out on a 211 / 193 GB/s link)."""
+    bi, bo, step = 1879048192, 4829741056, 8.592e9
+    duplex = {"copy_in_gbs": 211.2, "copy_out_gbs": 193.4, "copy_both_gbs": 342.0}
+    half = dict(duplex, copy_both_gbs=255.3)
+    # full duplex: the copy-out alone sets the step (24.97 ms)
+    assert abs(bench.link_bound_gbs(step, bi, bo, duplex) - step / (bo / 193.4e9) / 1e9) < 1e-6
+    # both directions at 255.3 GB/s together: 26.28 ms, longer than the copy-out alone
+    want = step / ((bi + bo) / 255.3e9) / 1e9
+    assert abs(bench.link_bound_gbs(step, bi, bo, half) - want) < 1e-6
+    assert bench.link_bound_gbs(step, bi, bo, half) < bench.link_bound_gbs(step, bi, bo, duplex)
