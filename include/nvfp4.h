@@ -51,7 +51,8 @@ extern "C" {
 typedef enum {
   NVFP4_OK = 0,
   NVFP4_ERR_NULL = 1,  /* a required pointer is NULL                          */
-  NVFP4_ERR_SHAPE = 2, /* negative size, or a blocked dim not a multiple of 16 */
+  NVFP4_ERR_SHAPE = 2, /* negative size, a size or element count above 2^60 - 1,
+                          or a blocked dim not a multiple of 16 */
   NVFP4_ERR_ALIGN = 3, /* a pointer is not aligned as required                 */
   NVFP4_ERR_ENUM = 4,  /* a configuration field is out of range                */
   NVFP4_ERR_CUDA = 6   /* a CUDA launch failed                                 */

@@ -30,6 +30,18 @@ namespace {
 
 bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
 
+// Non-negative dimensions, each and their element count small enough for the
+// byte offsets derived from them to fit in int64 (at most 8 bytes per
+// element): a product that wrapped would size grids and checks from a wrong
+// count.
+constexpr int64_t kMaxElems = INT64_MAX >> 3;
+bool dims_ok(int64_t s, int64_t r, int64_t c) {
+  int64_t n = 0;
+  return s >= 0 && r >= 0 && c >= 0 && s <= kMaxElems && r <= kMaxElems && c <= kMaxElems &&
+         !__builtin_mul_overflow(r, c, &n) && !__builtin_mul_overflow(n, s, &n) &&
+         n <= kMaxElems;
+}
+
 // 0 = 4/6 off, 1 = on with the MSE rule (compiled in), 2 = on, rule read at run time
 int fos_mode(const nvfp4_config* cfg) {
   if (!cfg->four_over_six) return 0;
@@ -100,7 +112,7 @@ const char* nvfp4_status_string(nvfp4_status s) {
 
 nvfp4_status nvfp4_amax(const void* x, int64_t slices, int64_t rows, int64_t cols, float* amax,
                         int32_t* status, void* stream) {
-  if (slices < 0 || rows < 0 || cols < 0) return NVFP4_ERR_SHAPE;
+  if (!dims_ok(slices, rows, cols)) return NVFP4_ERR_SHAPE;
   if (slices == 0) return NVFP4_OK;
   if (!amax) return NVFP4_ERR_NULL;
   if (rows * cols != 0 && !x) return NVFP4_ERR_NULL;
@@ -115,7 +127,7 @@ size_t nvfp4_amax_ws_bytes(int64_t slices) {
 
 nvfp4_status nvfp4_amax_ws(const void* x, int64_t slices, int64_t rows, int64_t cols, float* amax,
                            void* workspace, size_t ws_bytes, int32_t* status, void* stream) {
-  if (slices < 0 || rows < 0 || cols < 0) return NVFP4_ERR_SHAPE;
+  if (!dims_ok(slices, rows, cols)) return NVFP4_ERR_SHAPE;
   if (slices == 0) return NVFP4_OK;
   if (!amax || !workspace) return NVFP4_ERR_NULL;
   if (rows * cols != 0 && !x) return NVFP4_ERR_NULL;
@@ -130,7 +142,7 @@ nvfp4_status nvfp4_amax_ws(const void* x, int64_t slices, int64_t rows, int64_t 
 
 nvfp4_status nvfp4_amax_noalloc(const void* x, int64_t slices, int64_t rows, int64_t cols,
                                 float* amax, int32_t* status, void* stream) {
-  if (slices < 0 || rows < 0 || cols < 0) return NVFP4_ERR_SHAPE;
+  if (!dims_ok(slices, rows, cols)) return NVFP4_ERR_SHAPE;
   if (slices > NVFP4_AMAX_NOALLOC_MAX_SLICES) return NVFP4_ERR_SHAPE;
   if (slices == 0) return NVFP4_OK;
   if (!amax) return NVFP4_ERR_NULL;
@@ -150,7 +162,7 @@ nvfp4_status nvfp4_quantize(const nvfp4_config* cfg, const void* x, int64_t slic
       cfg->rounding < 0 || cfg->rounding > 1 || cfg->four_over_six < 0 || cfg->four_over_six > 1 ||
       !(cfg->scale_max >= 0.0f) || !(cfg->scale_max <= 3.402823466e+38f))
     return NVFP4_ERR_ENUM;
-  if (slices < 0 || rows < 0 || cols < 0) return NVFP4_ERR_SHAPE;
+  if (!dims_ok(slices, rows, cols)) return NVFP4_ERR_SHAPE;
   if (cfg->blocks == NVFP4_BLOCKS_TILE16) return quantize_tile16(cfg, x, slices, rows, cols,
                                                                  global_amax, row, col, status,
                                                                  stream);
@@ -230,7 +242,7 @@ nvfp4_status nvfp4_quantize_per_token(const nvfp4_config* cfg, const void* x, in
       cfg->rounding < 0 || cfg->rounding > 1 || cfg->four_over_six < 0 ||
       cfg->four_over_six > 1 || !(cfg->scale_max >= 0.0f) || !(cfg->scale_max <= 3.402823466e+38f))
     return NVFP4_ERR_ENUM;
-  if (rows < 0 || cols < 0 || cols % 16 != 0) return NVFP4_ERR_SHAPE;
+  if (!dims_ok(1, rows, cols) || cols % 16 != 0) return NVFP4_ERR_SHAPE;
   if (rows == 0 || cols == 0) return NVFP4_OK;
   if (!x || !row_amax) return NVFP4_ERR_NULL;
   if (!aligned(x, 16) || !aligned(row_amax, 4) || !aligned(status, 4)) return NVFP4_ERR_ALIGN;
@@ -272,7 +284,7 @@ nvfp4_status nvfp4_requant_transpose(const nvfp4_config* src, const nvfp4_config
              dst->four_over_six_rule > 2 || !(dst->scale_max >= 0.0f) ||
              !(dst->scale_max <= 3.402823466e+38f)))
     return NVFP4_ERR_ENUM;
-  if (slices < 0 || rows < 0 || cols < 0 || cols % 16 != 0 || rows % (nv ? 16 : 32) != 0)
+  if (!dims_ok(slices, rows, cols) || cols % 16 != 0 || rows % (nv ? 16 : 32) != 0)
     return NVFP4_ERR_SHAPE;
   if (slices == 0 || rows == 0 || cols == 0) return NVFP4_OK;
   if (!codes || !scales || !global_amax || !out || !out->codes || !out->scales)
@@ -317,7 +329,7 @@ nvfp4_status nvfp4_mx_quantize(const nvfp4_config* cfg, const void* x, int64_t s
   if (cfg->blocks < 1 || cfg->blocks > 3 || cfg->rounding < 0 || cfg->rounding > 1)
     return NVFP4_ERR_ENUM;
   const bool do_row = cfg->blocks & 1, do_col = cfg->blocks & 2;
-  if (slices < 0 || rows < 0 || cols < 0 || (do_row && cols % 32 != 0) ||
+  if (!dims_ok(slices, rows, cols) || (do_row && cols % 32 != 0) ||
       (do_col && rows % 32 != 0))
     return NVFP4_ERR_SHAPE;
   if (slices == 0 || rows == 0 || cols == 0) return NVFP4_OK;
@@ -350,7 +362,7 @@ nvfp4_status nvfp4_mx_quantize(const nvfp4_config* cfg, const void* x, int64_t s
 }
 
 static nvfp4_status ste_common(const void* x, int64_t rows, int64_t cols, const float* s_pre) {
-  if (rows < 0 || cols < 0 || cols % 16 != 0) return NVFP4_ERR_SHAPE;
+  if (!dims_ok(1, rows, cols) || cols % 16 != 0) return NVFP4_ERR_SHAPE;
   if (rows == 0 || cols == 0) return NVFP4_OK;
   if (!x || !s_pre) return NVFP4_ERR_NULL;
   if (!aligned(x, 16) || !aligned(s_pre, 4)) return NVFP4_ERR_ALIGN;
@@ -453,7 +465,7 @@ nvfp4_status nvfp4_scale_grad_bwd_fp8scale(const void* x, const void* gq, int64_
 nvfp4_status nvfp4_scale_init_mse(const void* x, int64_t rows, int64_t cols,
                                   const float* global_amax, uint8_t* scale_codes, float* s,
                                   int32_t* status, void* stream) {
-  if (rows < 0 || cols < 0 || cols % 16 != 0) return NVFP4_ERR_SHAPE;
+  if (!dims_ok(1, rows, cols) || cols % 16 != 0) return NVFP4_ERR_SHAPE;
   if (rows == 0 || cols == 0) return NVFP4_OK;
   if (!x || (!scale_codes && !s)) return NVFP4_ERR_NULL;
   nvfp4_status e = fp8_common(global_amax, status);
@@ -494,7 +506,7 @@ nvfp4_status nvfp4_export_scales(const void* x, int64_t rows, int64_t cols, cons
 nvfp4_status nvfp4_codec_probe(int32_t op, const float* in, const uint32_t* aux, int64_t n,
                                uint8_t* out, void* stream) {
   if (op < 0 || op > 7) return NVFP4_ERR_ENUM;
-  if (n < 0) return NVFP4_ERR_SHAPE;
+  if (n < 0 || n > kMaxElems) return NVFP4_ERR_SHAPE;
   if (n == 0) return NVFP4_OK;
   if (!in || !out || ((op == 3 || op == 5 || op == 7) && !aux)) return NVFP4_ERR_NULL;
   if (!aligned(in, 4) || !aligned(aux, 4)) return NVFP4_ERR_ALIGN;
@@ -504,7 +516,7 @@ nvfp4_status nvfp4_codec_probe(int32_t op, const float* in, const uint32_t* aux,
 
 nvfp4_status nvfp4_sr_bits(uint32_t seed, uint32_t step, uint32_t direction, uint64_t idx0,
                            int64_t n, uint32_t* out, void* stream) {
-  if (n < 0) return NVFP4_ERR_SHAPE;
+  if (n < 0 || n > kMaxElems) return NVFP4_ERR_SHAPE;
   if (n == 0) return NVFP4_OK;
   if (!out) return NVFP4_ERR_NULL;
   if (!aligned(out, 4)) return NVFP4_ERR_ALIGN;

@@ -285,3 +285,25 @@ def test_binding_refuses_cpu_tensors():
     x = torch.zeros((16, 32), dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         nv.nvfp4_amax(x)
+
+
+def test_sizes_whose_element_count_overflows_are_shape_errors(L):
+    """A dimension or element count above 2^60 - 1 (byte offsets of up to 8
+    bytes per element would no longer fit in int64) is refused before any
+    pointer is read, including products that would wrap around to a small
+    or negative count."""
+    big = 1 << 40
+    assert q(L, _cfg(blocks=1), R=big, Cc=big, row=_out()) == 2          # 2^80 elements
+    assert q(L, _cfg(blocks=3), S=1 << 21, R=1 << 20, Cc=1 << 20, row=_out(), col=_out()) == 2
+    assert q(L, _cfg(blocks=4), R=big, Cc=big, row=_out(), col=_out()) == 2
+    assert q(L, _cfg(blocks=1), S=1 << 62, R=0, row=_out()) == 2        # one dimension alone
+    assert L.nvfp4_amax(FAKE, 1, 1 << 32, 1 << 32, FAKE, None, None) == 2  # 2^64 wraps to 0
+    assert L.nvfp4_amax(FAKE, 1 << 61, 0, 4, FAKE, None, None) == 2
+    pt = L.nvfp4_quantize_per_token
+    assert pt(C.byref(_cfg()), FAKE, big, big, FAKE, C.byref(_out()), None, None) == 2
+    assert L.nvfp4_fakequant_fwd(FAKE, big, big, FAKE, None, FAKE, None, None) == 2
+    assert L.nvfp4_codec_probe(0, FAKE, None, 1 << 61, FAKE, None) == 2
+    assert L.nvfp4_sr_bits(0, 0, 0, 0, 1 << 61, FAKE, None) == 2
+    # the largest accepted count still gets past the shape check (to the null check)
+    assert L.nvfp4_amax(None, 1, 1 << 30, (1 << 30) - 1, FAKE, None, None) == 1
+    assert L.nvfp4_amax(None, 1, 1 << 30, 1 << 30, FAKE, None, None) == 2   # 2^60
