@@ -102,7 +102,9 @@ const char* nvfp4_status_string(nvfp4_status s) {
   switch (s) {
     case NVFP4_OK: return "ok";
     case NVFP4_ERR_NULL: return "a required pointer is NULL";
-    case NVFP4_ERR_SHAPE: return "invalid shape (negative, or a blocked dimension not a multiple of 16)";
+    case NVFP4_ERR_SHAPE:
+      return "invalid shape (negative, a size or element count above 2^60 - 1, or a blocked "
+             "dimension not a multiple of 16)";
     case NVFP4_ERR_ALIGN: return "a pointer is not aligned as required";
     case NVFP4_ERR_ENUM: return "a configuration field is out of range";
     case NVFP4_ERR_CUDA: return "a CUDA launch failed";
